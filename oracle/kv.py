@@ -1,0 +1,123 @@
+"""Paged KV-cache commit/rollback, restated on block tables (test infrastructure only).
+
+Sources: "aiengineeringfromscratch.com - Speculative decoding and EAGLE-3",
+sections "Rolling back the KV cache" (write drafts to a scratch area and commit
+on accept; the rollback cost is bytes per layer per head) and "Step 4: KV
+rollback accounting" (the logical length after a step is prefix + j + 1);
+"sglang_spec_decode" README, provisional-layer section (provisional blocks are
+committed or freed at once; no block may be leaked or freed twice).
+
+Reading used here: each row holds K+1 provisional slots whose KV covers
+[last committed token, d_0 .. d_{K-1}]. With n accepted drafts, slots 0..n are
+copied to logical positions seq_len .. seq_len + n of the row's own paged
+cache, new blocks are taken from the top of the free stack (rows in ascending
+order, all pops before any push), then every provisional block is pushed back
+in row order and the row's length becomes seq_len + n + 1.
+
+The whole call is all-or-nothing: if any row is invalid, or the free stack
+cannot cover every row, nothing changes and error bits are returned.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# error bits shared in meaning (not in code) with the library's device error word
+ERR_BAD_ACCEPT = 1 << 2     # num_accepted outside [0, K]
+ERR_BAD_LENGTH = 1 << 3     # negative seq_len, or the row outgrows its block table
+ERR_NO_SPACE = 1 << 4       # the free stack cannot supply every new block
+ERR_BAD_BLOCK = 1 << 5      # a block id outside [0, num_blocks) where one is needed
+
+
+def _cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def kv_commit(block_table, seq_lens, num_accepted, prov_blocks, free_stack, free_top: int,
+              *, block_size: int, K: int, num_blocks: int) -> dict:
+    """One commit/rollback of every row. Returns the new state, the copy list and error bits.
+
+    copies: list of (row, slot, src_block, src_offset, dst_block, dst_offset); each
+    entry moves one token's KV (all layers, K and V) from provisional slot `slot`.
+    """
+    bt = np.array(block_table, np.int64, copy=True)
+    sl = np.array(seq_lens, np.int64, copy=True)
+    na = np.asarray(num_accepted, np.int64)
+    pb = np.array(prov_blocks, np.int64, copy=True)
+    fs = np.array(free_stack, np.int64, copy=True)
+    top = int(free_top)
+    B, max_blocks = bt.shape
+    P = pb.shape[1]
+    err = 0
+
+    def ok_block(x):
+        return 0 <= x < num_blocks
+
+    # validation of every row before anything changes
+    need = np.zeros(B, np.int64)
+    for b in range(B):
+        n, L = int(na[b]), int(sl[b])
+        if not 0 <= n <= K:
+            err |= ERR_BAD_ACCEPT
+            continue
+        if L < 0 or _cdiv(L + n + 1, block_size) > max_blocks:
+            err |= ERR_BAD_LENGTH
+            continue
+        have = _cdiv(L, block_size)
+        total = _cdiv(L + n + 1, block_size)
+        if not all(ok_block(int(x)) for x in bt[b, :have]):
+            err |= ERR_BAD_BLOCK
+        if any(int(x) != -1 for x in bt[b, have:total]):
+            err |= ERR_BAD_BLOCK        # a slot the commit must fill is already taken
+        if n // block_size >= P or not all(ok_block(int(pb[b, s // block_size]))
+                                           for s in range(n + 1)):
+            err |= ERR_BAD_BLOCK
+        need[b] = total - have
+    if err == 0 and int(need.sum()) > top:
+        err |= ERR_NO_SPACE
+    if err:
+        return dict(block_table=np.asarray(block_table, np.int64).copy(),
+                    seq_lens=np.asarray(seq_lens, np.int64).copy(),
+                    prov_blocks=np.asarray(prov_blocks, np.int64).copy(),
+                    free_stack=np.asarray(free_stack, np.int64).copy(), free_top=int(free_top),
+                    copies=[], err=err)
+
+    # 1. allocation: pop from the top of the stack, rows ascending
+    for b in range(B):
+        have = _cdiv(int(sl[b]), block_size)
+        for k in range(int(need[b])):
+            top -= 1
+            bt[b, have + k] = fs[top]
+            fs[top] = -1
+    # 2. copies of the accepted slots 0..n into logical positions L..L+n
+    copies = []
+    for b in range(B):
+        L, n = int(sl[b]), int(na[b])
+        for s in range(n + 1):
+            src_b, src_o = int(pb[b, s // block_size]), s % block_size
+            p = L + s
+            dst_b, dst_o = int(bt[b, p // block_size]), p % block_size
+            copies.append((b, s, src_b, src_o, dst_b, dst_o))
+    # 3. every provisional block goes back on the stack, rows ascending
+    for b in range(B):
+        for k in range(P):
+            if pb[b, k] >= 0:
+                fs[top] = pb[b, k]
+                top += 1
+                pb[b, k] = -1
+    # 4. new logical lengths: prefix + n + 1
+    sl = sl + na + 1
+    return dict(block_table=bt, seq_lens=sl, prov_blocks=pb, free_stack=fs, free_top=top,
+                copies=copies, err=0)
+
+
+def pool_invariant_ok(block_table, prov_blocks, free_stack, free_top: int, num_blocks: int,
+                      seq_lens=None, block_size: int | None = None) -> bool:
+    """No leak, no double free: the live free-stack entries, the block-table entries
+    and the provisional blocks together hold every block id exactly once."""
+    bt = np.asarray(block_table).ravel()
+    pb = np.asarray(prov_blocks).ravel()
+    fs = np.asarray(free_stack)[: int(free_top)]
+    ids = np.concatenate([bt[bt >= 0], pb[pb >= 0], fs])
+    if ids.size != num_blocks:
+        return False
+    return bool(np.array_equal(np.sort(ids), np.arange(num_blocks)))

@@ -1,0 +1,142 @@
+"""Pins for the KV commit/rollback oracle (CPU only).
+
+The oracle works on block tables and returns a copy list. These tests check it
+against a brute-force model that never looks at block tables the way the
+oracle does: a dict from (block, offset) to the token-slot label it holds,
+walked through each row's logical positions after the commit. Sources: the
+lesson's exercise of two sequences (one accepts everything, one rejects at
+position 2) and "Step 4: KV rollback accounting"; the sglang_spec_decode README
+requirement that no block is leaked or freed twice across all rejection
+patterns.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import kv as okv
+import synth
+
+
+def _apply_and_read(case, res):
+    """Brute force: label every slot, apply the copy list, read logical sequences."""
+    bs = case.block_size
+    mem = {}
+    for b in range(case.B):
+        for pos in range(int(case.seq_lens[b])):
+            blk = int(case.block_table[b, pos // bs])
+            mem[(blk, pos % bs)] = ("prefix", b, pos)
+        for s in range(case.K + 1):
+            blk = int(case.prov_blocks[b, s // bs])
+            mem[(blk, s % bs)] = ("prov", b, s)
+    snapshot = dict(mem)
+    for (b, s, sb, so, db, do) in res["copies"]:
+        mem[(db, do)] = snapshot[(sb, so)]
+    seqs = []
+    for b in range(case.B):
+        L = int(res["seq_lens"][b])
+        seqs.append([mem.get((int(res["block_table"][b, p // bs]), p % bs)) for p in range(L)])
+    return seqs
+
+
+def _commit(case):
+    return oracle.kv_commit(case.block_table, case.seq_lens, case.num_accepted, case.prov_blocks,
+                            case.free_stack, case.free_top, block_size=case.block_size, K=case.K,
+                            num_blocks=case.num_blocks)
+
+
+def _expected_seq(case, b):
+    L, n = int(case.seq_lens[b]), int(case.num_accepted[b])
+    return [("prefix", b, p) for p in range(L)] + [("prov", b, s) for s in range(n + 1)]
+
+
+def test_two_sequences_exercise():
+    """Row A accepts all K = 4 drafts, row B rejects at position 2 (n = 2):
+    new lengths prefix + 5 and prefix + 3."""
+    c = synth.kv_case(2, 4, seq_lens=np.array([37, 64]), num_accepted=np.array([4, 2]), seed=1)
+    res = _commit(c)
+    assert res["err"] == 0
+    assert res["seq_lens"].tolist() == [37 + 5, 64 + 3]
+    seqs = _apply_and_read(c, res)
+    for b in range(2):
+        assert seqs[b] == _expected_seq(c, b)
+    assert oracle.pool_invariant_ok(res["block_table"], res["prov_blocks"], res["free_stack"],
+                                    res["free_top"], c.num_blocks)
+
+
+@pytest.mark.parametrize("K,bs", [(4, 16), (7, 16), (15, 16), (5, 4), (9, 8)])
+def test_every_rejection_pattern(K, bs):
+    """Every n in 0..K at prefix lengths straddling block boundaries."""
+    lens = [bs * 3 - 1, bs * 3, bs * 3 + 1, bs * 4 - K, bs * 4 - K - 1, 0, 1]
+    rows = list(itertools.product(lens, range(K + 1)))
+    sl = np.array([r[0] for r in rows])
+    na = np.array([r[1] for r in rows])
+    c = synth.kv_case(len(rows), K, block_size=bs, seq_lens=sl, num_accepted=na, seed=K * 31 + bs)
+    res = _commit(c)
+    assert res["err"] == 0
+    seqs = _apply_and_read(c, res)
+    for b in range(c.B):
+        assert seqs[b] == _expected_seq(c, b), b
+        assert res["seq_lens"][b] == sl[b] + na[b] + 1
+    assert oracle.pool_invariant_ok(res["block_table"], res["prov_blocks"], res["free_stack"],
+                                    res["free_top"], c.num_blocks)
+    assert oracle.pool_invariant_ok(c.block_table, c.prov_blocks, c.free_stack, c.free_top,
+                                    c.num_blocks)
+    # exactly the blocks the new lengths need are in use, and no provisional block remains
+    used = sum(-(-int(L) // bs) for L in res["seq_lens"])
+    assert (res["block_table"] >= 0).sum() == used
+    assert (res["prov_blocks"] == -1).all()
+
+
+def test_allocation_order_is_rows_ascending_pop_before_push():
+    c = synth.kv_case(3, 4, seq_lens=np.array([16, 15, 32]), num_accepted=np.array([0, 4, 1]),
+                      seed=2)
+    top0 = c.free_top
+    stack0 = c.free_stack.copy()
+    res = _commit(c)
+    # row 0 (16 -> 17) needs a block, row 1 (15 -> 20) needs one, row 2 (32 -> 34) needs one
+    assert res["block_table"][0, 1] == stack0[top0 - 1]
+    assert res["block_table"][1, 1] == stack0[top0 - 2]
+    assert res["block_table"][2, 2] == stack0[top0 - 3]
+    # then the three provisional blocks are pushed in row order
+    assert res["free_top"] == top0 - 3 + 3
+    assert res["free_stack"][top0 - 3: top0].tolist() == c.prov_blocks[:, 0].tolist()
+
+
+@pytest.mark.parametrize("mutate,bit", [
+    ("accept_high", okv.ERR_BAD_ACCEPT),
+    ("accept_neg", okv.ERR_BAD_ACCEPT),
+    ("len_neg", okv.ERR_BAD_LENGTH),
+    ("table_small", okv.ERR_BAD_LENGTH),
+    ("no_space", okv.ERR_NO_SPACE),
+    ("bad_table_block", okv.ERR_BAD_BLOCK),
+    ("bad_prov_block", okv.ERR_BAD_BLOCK),
+    ("slot_taken", okv.ERR_BAD_BLOCK),
+])
+def test_errors_leave_state_unchanged(mutate, bit):
+    c = synth.kv_case(4, 4, seq_lens=np.array([16, 20, 31, 47]), num_accepted=np.array([1, 2, 4, 0]),
+                      seed=4)
+    if mutate == "accept_high":
+        c.num_accepted[2] = 5
+    elif mutate == "accept_neg":
+        c.num_accepted[1] = -1
+    elif mutate == "len_neg":
+        c.seq_lens[0] = -3
+    elif mutate == "table_small":
+        c.block_table = c.block_table[:, :2].copy()
+    elif mutate == "no_space":
+        c.free_top = 1
+    elif mutate == "bad_table_block":
+        c.block_table[3, 1] = c.num_blocks
+    elif mutate == "bad_prov_block":
+        c.prov_blocks[1, 0] = -1
+    elif mutate == "slot_taken":
+        c.block_table[0, 1] = c.free_stack[0]
+    res = _commit(c)
+    assert res["err"] & bit
+    assert res["copies"] == []
+    assert np.array_equal(res["block_table"], c.block_table)
+    assert np.array_equal(res["seq_lens"], c.seq_lens)
+    assert np.array_equal(res["prov_blocks"], c.prov_blocks)
+    assert res["free_top"] == c.free_top
