@@ -1,0 +1,442 @@
+"""Benchmark of the speculative-decoding verification step on GB300.
+
+One step = one pass of the whole hot path over one batch:
+  spec_verify_sample  (accept/reject, first rejection, residual or bonus draw)
+  kv_commit_rollback  (commit of the accepted slots in the paged KV cache)
+on B=256 rows, K=4 drafts, V=151936 bf16 logits, T=1.0, draft = target + N(0, 0.5^2),
+paged KV of 32 layers x 8 KV heads x head_dim 128 bf16, block 16, prefixes U[512, 4096].
+
+Metric: verified draft positions per second (B*K per step), whole job over all ranks.
+Inputs rotate over 3 pre-generated batches (3 x 622 MB of logits, larger than the
+129 MB L2) so no step finds its logits in L2. Each step also restores the small KV
+tables (so every step commits the same rows); that copy is inside the timed region.
+
+Prints one JSON line (rank 0). `--impl reference` times the fp64 CPU oracle on the
+same workload instead (a bounded sample of rows per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "positions/s"
+WORKLOAD = dict(B=256, K=4, V=151936, T=1.0, sigma=0.5, target_std=3.0, logits="bf16",
+                kv_layers=32, kv_heads=8, head_dim=128, kv_dtype="bf16", block_size=16,
+                prefix_lo=512, prefix_hi=4096)
+PROFILE_JSON = os.path.join(ROOT, "profiles", "verify_sample_kernel_b256_k4_v151936.json")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--temperature", type=float, default=WORKLOAD["T"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--mode", default="step", choices=["step", "verify", "greedy"],
+                   help="step: verify + KV commit (the benchmark); verify / greedy: that kernel "
+                        "alone on the same logits, no KV pool (small footprint, for profiling)")
+    p.add_argument("--batches", type=int, default=3, help="input batches to rotate over")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_name(T):
+    w = WORKLOAD
+    return (f"sampling verify + paged-KV commit: B={w['B']}, K={w['K']}, V={w['V']} bf16 logits, "
+            f"T={T}, draft = target + N(0, {w['sigma']}^2), target ~ N(0, {w['target_std']}^2); "
+            f"KV {w['kv_layers']}L x {w['kv_heads']}H x {w['head_dim']}D bf16, block "
+            f"{w['block_size']}, prefix U[{w['prefix_lo']}, {w['prefix_hi']}]")
+
+
+# ------------------------------------------------------------------ inputs
+def gen_batch(torch, seed, T):
+    """Synthetic verifier inputs on the GPU (the draft token is the draft model's
+    own Gumbel-max sample; the verifier never sees how it was drawn)."""
+    import numpy as np
+    import synth
+    w = WORKLOAD
+    B, K, V = w["B"], w["K"], w["V"]
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    zt = (torch.randn((B, K + 1, V), device="cuda", generator=g) * w["target_std"]).to(torch.bfloat16)
+    zd = (zt[:, :K].float() + torch.randn((B, K, V), device="cuda", generator=g) * w["sigma"]
+          ).to(torch.bfloat16)
+    gum = -torch.log(-torch.log(torch.rand((B, K, V), device="cuda", generator=g)
+                                .clamp_(1e-20, 1.0 - 1e-7)))
+    tok = torch.argmax(zd.float() / float(np.float32(T)) + gum, dim=-1).to(torch.int32)
+    del gum
+    u = torch.from_numpy(synth.philox_uniforms((B, K + 1), seed)).cuda()
+    return dict(target=zt.contiguous(), draft=zd.contiguous(), tokens=tok.contiguous(), uniforms=u)
+
+
+def kv_state(torch, na):
+    import numpy as np
+    import synth
+    w = WORKLOAD
+    c = synth.kv_case(w["B"], w["K"], block_size=w["block_size"], prefix_lo=w["prefix_lo"],
+                      prefix_hi=w["prefix_hi"], num_accepted=na, seed=44)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()  # noqa: E731
+    d = dict(bt=t(c.block_table), sl=t(c.seq_lens), pb=t(c.prov_blocks), fs=t(c.free_stack),
+             ft=t([c.free_top]), st=t([0]))
+    saved = {k: v.clone() for k, v in d.items()}
+    pool = torch.empty((c.num_blocks, w["kv_layers"], 2, w["block_size"], w["kv_heads"],
+                        w["head_dim"]), dtype=torch.bfloat16, device="cuda")
+    return c, d, saved, pool
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.p = None
+        self.gpu = gpu_index
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_sample_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    try:
+        with open(PROFILE_JSON) as f:
+            p = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if p.get("source_hash") != source_hash():
+        return None
+    return p.get("dram_bytes_per_launch")
+
+
+def algorithmic_verify_bytes(na, K, V, e=2):
+    """Bytes the verify launch must move: all 2K logit rows of every batch row, the
+    bonus row of fully accepted rows, and the per-row inputs/outputs."""
+    import numpy as np
+    B = len(na)
+    full = int(np.sum(np.asarray(na) == K))
+    meta = B * (4 * K + 4 * (K + 1) + 4 * (K + 1) + 4)
+    return B * 2 * K * V * e + full * V * e + meta
+
+
+def kv_bytes(na, w):
+    import numpy as np
+    slot = w["kv_layers"] * 2 * w["kv_heads"] * w["head_dim"] * 2  # bytes of one token's KV
+    return int(np.sum(np.asarray(na) + 1)) * slot * 2              # read + write
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def oracle_sample_rate(rows: int, T: float, budget_s: float):
+    """Times the fp64 oracle (verify + KV bookkeeping) on `rows` rows of the workload
+    until `budget_s` seconds; returns positions/s and a description."""
+    import numpy as np
+    import oracle
+    import synth
+    w = WORKLOAD
+    c = synth.sampling_case(rows, w["K"], w["V"], temperature=T, target_std=w["target_std"],
+                            draft_noise_std=w["sigma"], seed=99, uniform_seed=99)
+    t_vals, d_vals = c.target_values(), c.draft_values()
+    kc = synth.kv_case(rows, w["K"], block_size=w["block_size"], prefix_lo=w["prefix_lo"],
+                       prefix_hi=w["prefix_hi"], seed=45)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        r = oracle.verify_sample(t_vals, d_vals, c.tokens, c.uniforms, T)
+        oracle.kv_commit(kc.block_table, kc.seq_lens, r["num_accepted"], kc.prov_blocks,
+                         kc.free_stack, kc.free_top, block_size=w["block_size"], K=w["K"],
+                         num_blocks=kc.num_blocks)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    rate = done * rows * w["K"] / el
+    return rate, el, done
+
+
+# ------------------------------------------------------------------ main
+def main():
+    a = parse()
+    rank, world, local = dist_env()
+    T = a.temperature
+    if a.impl == "reference":
+        return run_reference(a, rank, world, T)
+    import numpy as np
+    import torch
+    import speculative_decoding_verification_sample_gb300 as sv
+    from speculative_decoding_verification_sample_gb300 import build
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    build.build()
+    sv.lib()
+    w = WORKLOAD
+    B, K, V = w["B"], w["K"], w["V"]
+    stream = torch.cuda.current_stream()
+    nb = max(1, a.batches)
+    batches = [gen_batch(torch, 1000 * rank + i, T) for i in range(nb)]
+    out = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
+    n = torch.empty((B,), dtype=torch.int32, device="cuda")
+    info = torch.empty((B,), dtype=torch.int32, device="cuda")
+    # accepted counts of each batch (fixed for the run) to build the KV state and byte counts
+    na_list = []
+    for bt in batches:
+        sv.spec_verify_sample(bt["target"], bt["draft"], bt["tokens"], bt["uniforms"], T, out, n,
+                              row_info=info)
+        torch.cuda.synchronize()
+        na_list.append((n.cpu().numpy().copy(), info.cpu().numpy().copy()))
+    if a.mode == "step":
+        kc, kd, saved, pool = kv_state(torch, np.max([x[0] for x in na_list], axis=0))
+
+    def step(i, ev=None):
+        bt = batches[i % nb]
+        if a.mode == "step":
+            for k in ("bt", "sl", "pb", "fs", "ft"):
+                kd[k].copy_(saved[k], non_blocking=True)
+        if ev is not None:
+            ev[0].record(stream)
+        if a.mode == "greedy":
+            sv.spec_verify_greedy(bt["target"], bt["tokens"], out, n)
+        else:
+            sv.spec_verify_sample(bt["target"], bt["draft"], bt["tokens"], bt["uniforms"], T,
+                                  out, n)
+        if ev is not None:
+            ev[1].record(stream)
+        if a.mode == "step":
+            sv.kv_commit_rollback(kd["bt"], kd["sl"], n, kd["pb"], pool, kd["fs"], kd["ft"],
+                                  kd["st"], K=K, block_size=w["block_size"])
+
+    for i in range(max(3, a.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    if a.mode == "step" and int(kd["st"].item()) != 0:
+        raise RuntimeError(f"kv commit status {int(kd['st'].item())}")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(a.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    time.sleep(0.2)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(a.steps):
+        step(i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    verify_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
+    if world > 1:
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / a.steps
+    value = world * B * K / (ms_per_step / 1e3)
+
+    # roofline of the dominant kernel (spec_verify_sample), live CUDA-event durations
+    if a.mode == "greedy":
+        # greedy reads target rows 0..K-1, plus row K for rows that accept everything
+        alg = statistics.mean(B * K * V * 2 + B * 8 * K for _ in range(nb))
+    else:
+        alg = statistics.mean(algorithmic_verify_bytes(x[0], K, V) for x in na_list)
+    v_ms = statistics.mean(verify_ms)
+    peak, peak_kind = peaks()
+    achieved = alg / (v_ms / 1e3) / 1e9
+    refined = float(np.mean([np.mean(x[1] != 0) for x in na_list]))
+    kvb = statistics.mean(kv_bytes(x[0], w) for x in na_list)
+
+    # end-to-end through the public API with host buffers
+    e2e = None
+    if a.e2e_steps > 0 and a.mode == "step" and nb >= 2:
+        host = [{k: v.cpu().pin_memory() for k, v in bt.items()} for bt in batches]
+        h2d = sum(v.numel() * v.element_size() for v in host[0].values())
+        d2h = out.numel() * 4 + n.numel() * 4
+        out_h = torch.empty_like(out, device="cpu").pin_memory()
+        n_h = torch.empty_like(n, device="cpu").pin_memory()
+
+        def e2e_step(i):
+            hb = host[i % nb]
+            db = batches[(i + 1) % nb]   # device buffers that receive the copy
+            for k in ("target", "draft", "tokens", "uniforms"):
+                db[k].copy_(hb[k], non_blocking=True)
+            for k in ("bt", "sl", "pb", "fs", "ft"):
+                kd[k].copy_(saved[k], non_blocking=True)
+            sv.spec_verify_sample(db["target"], db["draft"], db["tokens"], db["uniforms"], T, out, n)
+            sv.kv_commit_rollback(kd["bt"], kd["sl"], n, kd["pb"], pool, kd["fs"], kd["ft"],
+                                  kd["st"], K=K, block_size=w["block_size"])
+            out_h.copy_(out, non_blocking=True)
+            n_h.copy_(n, non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(a.e2e_steps):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / a.e2e_steps
+        if world > 1:
+            tt = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        e2e = {"value": world * B * K / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline and a.mode == "step":
+        rate, el, reps = oracle_sample_rate(4, T, 12.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"4 rows of the workload (B=4, K=4, V=151936, T={T}) verify + KV "
+                         f"bookkeeping, {reps} repetitions in {el:.1f} s, single-threaded NumPy fp64"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+            "warmup": max(3, a.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_name(T), "global_batch": world * B, "B_per_gpu": B,
+                       "K": K, "V": V, "logits_dtype": "bf16", "temperature": T,
+                       "parallelism": f"replicas x{world} (batch rows sharded, no collective)",
+                       "mode": a.mode,
+                       "l2": f"inputs rotate over {nb} batch(es) of 622 MB logits (> 129 MB L2)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(),
+                         "kernel": "verify_sample_kernel<bf16>", "peak_kind": peak_kind,
+                         "algorithmic_bytes_per_launch": alg, "avg_launch_ms": v_ms},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": (3 if a.mode == "step" else 1) * a.steps,
+            "clocks": clk,
+            "extra": {"verify_ms": v_ms, "kv_commit_and_table_restore_ms": ms_per_step - v_ms,
+                      "kv_bytes_per_step": kvb, "refined_row_fraction": refined,
+                      "mean_accepted": float(np.mean([x[0].mean() for x in na_list])),
+                      "hbm_frac_of_nominal_8TBs": achieved / 8000.0},
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(a, rank, world, T):
+    """Reference arm: the fp64 CPU oracle on a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import synth
+    w = WORKLOAD
+    rows = 1
+    c = synth.sampling_case(rows, w["K"], w["V"], temperature=T, target_std=w["target_std"],
+                            draft_noise_std=w["sigma"], seed=99, uniform_seed=99)
+    tv, dv = c.target_values(), c.draft_values()
+    kc = synth.kv_case(rows, w["K"], block_size=w["block_size"], prefix_lo=w["prefix_lo"],
+                       prefix_hi=w["prefix_hi"], seed=45)
+
+    def step():
+        r = oracle.verify_sample(tv, dv, c.tokens, c.uniforms, T)
+        oracle.kv_commit(kc.block_table, kc.seq_lens, r["num_accepted"], kc.prov_blocks,
+                         kc.free_stack, kc.free_top, block_size=w["block_size"], K=w["K"],
+                         num_blocks=kc.num_blocks)
+
+    for _ in range(max(3, a.warmup)):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(a.steps):
+        step()
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / a.steps
+    value = rows * w["K"] / (el / a.steps)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": a.steps, "warmup": max(3, a.warmup), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": workload_name(T) + " (oracle: 1 row per step)",
+                       "global_batch": rows, "K": w["K"], "V": w["V"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "1 batch row per step (verify + KV bookkeeping), "
+                                       "single-threaded NumPy fp64"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

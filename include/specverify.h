@@ -1,0 +1,192 @@
+/*
+ * specverify.h - C ABI of the GB300 speculative-decoding verification library.
+ *
+ * The library implements the verifier-side step of speculative decoding:
+ *   - spec_verify_sample: temperature softmax of target and draft logits,
+ *     the accept/reject test of each draft token, the first rejection, and the
+ *     correction (residual) or bonus draw;
+ *   - spec_verify_greedy: the argmax-match variant;
+ *   - kv_commit_rollback: commit of the accepted provisional KV slots into a
+ *     paged cache and release of the provisional blocks.
+ *
+ * Sources (page title, section):
+ *   [L] aiengineeringfromscratch.com, "Speculative decoding and EAGLE-3":
+ *       "Variant: Leviathan rejection sampling" (accept d ~ p with probability
+ *       min(1, q(d)/p(d)); on rejection sample (q - p)+ / ||(q - p)+||_1; the
+ *       verifier returns q_1..q_{N+1}; first rejection at j samples the
+ *       residual of row j, full acceptance samples a bonus token from
+ *       q_{N+1}); "Step 1: the rejection rule" (p(d) <= 0 accepts; strict
+ *       u < min(1, q/p)); "Step 2: residual distribution" (zero residual mass
+ *       falls back to q); "Rolling back the KV cache" and "Step 4: KV rollback
+ *       accounting" (logical length prefix + j + 1).
+ *   [P] devpost.com, "phoenix", section "What it does": greedy verification
+ *       keeps tokens up to the first disagreement and writes the target's token
+ *       there; output identical to the target alone.
+ *   [S] "sglang_spec_decode" README, provisional KV layer: provisional blocks
+ *       are committed or freed immediately; no block leaked or freed twice.
+ *
+ * Notation: q = target (verifier) distribution, p = draft distribution.
+ * Positions are 0-based: draft positions 0..K-1, bonus row K.
+ *
+ * Conventions for every entry point:
+ *   - All array arguments are DEVICE pointers owned by the caller. The library
+ *     allocates no device or host memory and keeps no state between calls
+ *     (its only static data is a read-only constant table).
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *     the legacy default stream). Nothing synchronises; outputs are valid once
+ *     the stream reaches the call.
+ *   - Arguments are validated on the host before any launch. A host-side
+ *     failure returns a negative status and launches nothing.
+ *   - Problems only visible on the device (a token id out of range, non-finite
+ *     logits, an exhausted free-block stack) are reported by OR-ing bits into
+ *     the optional device word *err_flag; the affected batch row is written
+ *     as -1 (verify) or the whole call leaves its state unchanged (KV commit).
+ *     No device-side trap or assert is ever raised.
+ *   - Arrays are C-contiguous. Logit arrays must start on a 16-byte boundary.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (return values) ---- */
+#define SPEC_OK 0
+#define SPEC_EINVAL (-1)   /* null pointer, bad size, bad dtype, misaligned logits */
+#define SPEC_ECUDA (-2)    /* a CUDA launch or attribute call failed */
+#define SPEC_ENOTSUP (-3)  /* valid request this build does not handle */
+
+/* ---- logit dtypes ---- */
+#define SPEC_BF16 0 /* bfloat16, passed as raw 16-bit words */
+#define SPEC_F32 1  /* IEEE float32 */
+
+/* ---- device error bits OR-ed into *err_flag ---- */
+#define SPEC_DERR_TOKEN 1        /* a draft token outside [0, V); that row's outputs are -1 */
+#define SPEC_DERR_LOGITS 2       /* a row needed by the step has NaN/+inf logits or only -inf */
+#define SPEC_DERR_BAD_ACCEPT 4   /* kv: num_accepted outside [0, K] */
+#define SPEC_DERR_BAD_LENGTH 8   /* kv: negative seq_len, or the row outgrows max_blocks */
+#define SPEC_DERR_NO_SPACE 16    /* kv: the free stack cannot supply every new block */
+#define SPEC_DERR_BAD_BLOCK 32   /* kv: a block id out of range, or a target slot already taken */
+#define SPEC_DERR_TIMEOUT 64     /* an internal bounded wait gave up (should never happen) */
+
+/* ---- per-row diagnostic bits written to row_info[b] (optional) ---- */
+#define SPEC_ROW_ACCEPT_REFINED 1 /* an accept test fell inside the fp32 error bound and was
+                                     decided by the double-float path */
+#define SPEC_ROW_SAMPLE_REFINED 2 /* the final draw fell inside the fp32 error bound and was
+                                     decided by the double-float path */
+#define SPEC_ROW_UNCERTIFIED 4    /* the double-float path could not certify its decision either
+                                     (its result is still returned) */
+#define SPEC_ROW_ZERO_RESIDUAL 8  /* the residual mass was exactly zero; q_j was used */
+
+/*
+ * spec_verify_sample - accept/reject with temperature softmax ([L] Leviathan
+ * rejection sampling, Steps 1-3).
+ *
+ *   target_logits  [B, K+1, V]  dtype  target row i is q_i before softmax; row K is q_{K+1}
+ *   draft_logits   [B, K,   V]  dtype  draft row i is p_i before softmax
+ *   draft_tokens   [B, K]       int32  d_i, expected in [0, V)
+ *   uniforms       [B, K+1]     float  in [0, 1): u[i] decides test i, u[K] is the single
+ *                                      uniform of the correction or bonus draw
+ *   temperature    > 0 applies softmax(z / T) to both tensors; == 0 behaves exactly as
+ *                  spec_verify_greedy (draft_logits and uniforms are then unused);
+ *                  negative or NaN -> SPEC_EINVAL
+ *   B >= 1, 1 <= K <= 31, V >= 1
+ *   out_tokens       [B, K+1] int32  d_0..d_{n-1}, then the correction or bonus token, then -1
+ *   out_num_accepted [B]      int32  n in [0, K] (-1 for a row with a device error)
+ *   stream         cudaStream_t
+ *   dtype          SPEC_BF16 or SPEC_F32 (both logit tensors)
+ *   err_flag       optional [1] int32, device error bits are OR-ed in (never cleared)
+ *   row_info       optional [B] int32, SPEC_ROW_* bits of each row (overwritten)
+ *   q_at_d, p_at_d optional [B, K] float, q_i(d_i) and p_i(d_i) (for inspection)
+ *
+ * Semantics: for i = 0..K-1, d_i is accepted iff p_i(d_i) <= 0 or
+ * u[i] < min(1, q_i(d_i)/p_i(d_i)); at the first rejection j the token is the
+ * smallest v with u[K] * sum(r) < sum_{w<=v} r_w for r = max(0, q_j - p_j) (r = q_j if
+ * that sum is 0); if all K are accepted the same draw is made from q_K. Every
+ * decision is certified against a proven error bound of the fp32 arithmetic; the
+ * rare decisions inside the bound are recomputed in double-float arithmetic.
+ * Logit arrays must be 16-byte aligned and V * sizeof(dtype) a multiple of 16.
+ */
+int spec_verify_sample(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const float* uniforms, float temperature,
+                       int B, int K, int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                       void* stream, int dtype, int32_t* err_flag, int32_t* row_info,
+                       float* q_at_d, float* p_at_d);
+
+/*
+ * spec_verify_greedy - greedy verification ([P] "What it does").
+ *
+ *   target_logits [B, K+1, V] dtype; draft_tokens [B, K] int32.
+ *   g_i = argmax_v target[b, i, v] over raw logits, ties to the lowest index.
+ *   n = number of leading i with d_i == g_i; out_tokens[b] = d_0..d_{n-1}, g_n, -1...;
+ *   out_num_accepted[b] = n. Same pointer, alignment and error conventions as
+ *   spec_verify_sample; a row with NaN logits is reported as SPEC_DERR_LOGITS.
+ */
+int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int K,
+                       int V, int32_t* out_tokens, int32_t* out_num_accepted, void* stream,
+                       int dtype, int32_t* err_flag);
+
+/*
+ * kv_commit_rollback - commit the accepted provisional KV slots and free the
+ * provisional blocks ([L] "Rolling back the KV cache", "Step 4"; [S] provisional layer).
+ *
+ *   block_table  [B, max_blocks] int32  committed blocks of each row, -1 = unused;
+ *                                       entries [0, ceil(seq_len/bs)) must be valid
+ *   seq_lens     [B] int32              committed length L_b; becomes L_b + n_b + 1
+ *   num_accepted [B] int32              n_b from the verify call (same stream -> ordered)
+ *   prov_blocks  [B, P] int32           blocks holding provisional slots 0..K
+ *                                       (slot s in block prov[b][s / bs], offset s % bs);
+ *                                       all are pushed to the free stack and set to -1
+ *   kv_pool      [num_blocks][num_layers][2][block_size][num_kv_heads][head_dim]
+ *                elements of kv_elem_bytes bytes (K and V planes per layer)
+ *   free_stack   [num_blocks] int32, free_top [1] int32: a stack of free block ids,
+ *                live entries free_stack[0 .. *free_top)
+ *   status       REQUIRED [1] int32, overwritten on the device with 0 when the call
+ *                committed, else with the SPEC_DERR_* bits that stopped it
+ *   K            0 <= K <= 31; P (provisional blocks per row) in [1, 512];
+ *                num_kv_heads * head_dim * kv_elem_bytes a multiple of 16, kv_pool
+ *                16-byte aligned
+ *
+ * For every row, provisional slots 0..n (n + 1 tokens: the KV of the last committed
+ * token and of d_0..d_{n-1}) are copied, for all layers and both K and V, to logical
+ * positions L..L+n of the row's own blocks. New blocks come from the top of the free
+ * stack, rows in ascending order, before any block is pushed; then every provisional
+ * block is pushed back in row order. All-or-nothing: if any row is invalid or the
+ * stack is short, nothing changes and *status receives the error bits. Validation
+ * checks, per row: n in [0, K]; L >= 0 and ceil((L+n+1)/bs) <= max_blocks; the
+ * partly filled tail block (index L/bs when L % bs != 0) is a valid id; the
+ * entries the commit fills are -1; the provisional blocks of slots 0..n are valid
+ * and every provisional id >= 0 is < num_blocks. Globally: 0 <= *free_top <=
+ * num_blocks and covers the new blocks, the popped ids are valid, and the pushes fit.
+ * Only the accepted bytes move. Blocks freed by the call must not be reused until
+ * the stream passes it.
+ */
+int kv_commit_rollback(int32_t* block_table, int32_t* seq_lens, const int32_t* num_accepted,
+                       int32_t* prov_blocks, void* kv_pool, int num_blocks, int num_layers,
+                       int num_kv_heads, int head_dim, int kv_elem_bytes, int block_size, int B,
+                       int K, int max_blocks, int P, int32_t* free_stack, int32_t* free_top,
+                       int32_t* status, void* stream);
+
+/*
+ * spec_selftest_ex2 - diagnostic: the maximum relative error of the hardware
+ * base-2 exponential over every fp32 argument in [lo, hi] (-126 <= lo <= hi <= 64),
+ * measured against fp64 exp2 and written to the device double *out_max_rel.
+ * The sampler's certification assumes this maximum stays below its built-in
+ * bound on [-126, 1]; tests re-measure it on the GPU in use.
+ */
+int spec_selftest_ex2(float lo, float hi, double* out_max_rel, void* stream);
+
+/* Human-readable text of a status code (static string). */
+const char* spec_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int spec_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

@@ -54,7 +54,14 @@ def kv_commit(block_table, seq_lens, num_accepted, prov_blocks, free_stack, free
 
     # validation of every row before anything changes
     need = np.zeros(B, np.int64)
+    push_total = 0
     for b in range(B):
+        for k in range(P):                      # every provisional block goes back on the stack
+            x = int(pb[b, k])
+            if x >= 0:
+                push_total += 1
+                if x >= num_blocks:
+                    err |= ERR_BAD_BLOCK
         n, L = int(na[b]), int(sl[b])
         if not 0 <= n <= K:
             err |= ERR_BAD_ACCEPT
@@ -64,16 +71,24 @@ def kv_commit(block_table, seq_lens, num_accepted, prov_blocks, free_stack, free
             continue
         have = _cdiv(L, block_size)
         total = _cdiv(L + n + 1, block_size)
-        if not all(ok_block(int(x)) for x in bt[b, :have]):
-            err |= ERR_BAD_BLOCK
-        if any(int(x) != -1 for x in bt[b, have:total]):
-            err |= ERR_BAD_BLOCK        # a slot the commit must fill is already taken
-        if n // block_size >= P or not all(ok_block(int(pb[b, s // block_size]))
-                                           for s in range(n + 1)):
+        for j in range(L // block_size, total):  # the blocks the commit writes into
+            x = int(bt[b, j])
+            if j < have:
+                if not ok_block(x):
+                    err |= ERR_BAD_BLOCK        # the partly filled tail block
+            elif x != -1:
+                err |= ERR_BAD_BLOCK            # a slot the commit must fill is already taken
+        if n // block_size >= P or not all(ok_block(int(pb[b, k]))
+                                           for k in range(n // block_size + 1)):
             err |= ERR_BAD_BLOCK
         need[b] = total - have
-    if err == 0 and int(need.sum()) > top:
+    need_total = int(need.sum())
+    if err == 0 and (top < 0 or top > num_blocks or need_total > top):
         err |= ERR_NO_SPACE
+    if err == 0 and top - need_total + push_total > num_blocks:
+        err |= ERR_BAD_BLOCK                    # the pushes would overflow the stack
+    if err == 0 and not all(ok_block(int(x)) for x in fs[top - need_total: top]):
+        err |= ERR_BAD_BLOCK                    # a block about to be popped is not a valid id
     if err:
         return dict(block_table=np.asarray(block_table, np.int64).copy(),
                     seq_lens=np.asarray(seq_lens, np.int64).copy(),

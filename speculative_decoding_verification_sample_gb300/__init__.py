@@ -1,0 +1,209 @@
+"""GB300 speculative-decoding verification (sm_103a).
+
+Thin ctypes binding of the in-tree C-ABI library `libspecverify.so`: argument
+marshalling only. Every step of the verification runs in the library's CUDA
+kernels; PyTorch supplies device memory and the current stream. There is no
+CPU fallback: without the built library (or without a GPU) these calls raise.
+
+The entry points carry the C names:
+  spec_verify_sample(...)   accept/reject with temperature softmax, residual or bonus draw
+  spec_verify_greedy(...)   argmax-match verification
+  kv_commit_rollback(...)   commit accepted provisional KV slots, free provisional blocks
+See include/specverify.h for layouts, ownership and error behaviour.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+
+SPEC_OK, SPEC_EINVAL, SPEC_ECUDA, SPEC_ENOTSUP = 0, -1, -2, -3
+SPEC_BF16, SPEC_F32 = 0, 1
+SPEC_DERR_TOKEN, SPEC_DERR_LOGITS = 1, 2
+SPEC_DERR_BAD_ACCEPT, SPEC_DERR_BAD_LENGTH, SPEC_DERR_NO_SPACE, SPEC_DERR_BAD_BLOCK = 4, 8, 16, 32
+SPEC_DERR_TIMEOUT = 64
+SPEC_ROW_ACCEPT_REFINED, SPEC_ROW_SAMPLE_REFINED = 1, 2
+SPEC_ROW_UNCERTIFIED, SPEC_ROW_ZERO_RESIDUAL = 4, 8
+
+EXPORTED = ("spec_verify_sample", "spec_verify_greedy", "kv_commit_rollback",
+            "spec_selftest_ex2", "spec_status_string", "spec_version")
+
+_lib = None
+
+
+class SpecError(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, fn: str, status: int):
+        msg = lib().spec_status_string(status).decode() if _lib else str(status)
+        super().__init__(f"{fn}: status {status} ({msg})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libspecverify.so (built by `build.build()`); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built; run "
+                               "speculative_decoding_verification_sample_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.spec_verify_sample.argtypes = [P, P, P, P, F, I, I, I, P, P, P, I, P, P, P, P]
+        L.spec_verify_sample.restype = I
+        L.spec_verify_greedy.argtypes = [P, P, I, I, I, P, P, P, I, P]
+        L.spec_verify_greedy.restype = I
+        L.kv_commit_rollback.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P, P, P, P]
+        L.kv_commit_rollback.restype = I
+        L.spec_selftest_ex2.argtypes = [F, F, P, P]
+        L.spec_selftest_ex2.restype = I
+        L.spec_status_string.argtypes = [I]
+        L.spec_status_string.restype = ctypes.c_char_p
+        L.spec_version.argtypes = []
+        L.spec_version.restype = I
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _check(t, name, ndim=None, dtype=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature: float,
+                       out_tokens, out_num_accepted, *, stream=None, err_flag=None,
+                       row_info=None, q_at_d=None, p_at_d=None) -> None:
+    """Sampling-mode verification; shapes [B,K+1,V], [B,K,V], [B,K], [B,K+1] -> [B,K+1], [B]."""
+    import torch
+    _check(target_logits, "target_logits", 3)
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    if float(temperature) != 0.0:
+        _check(draft_logits, "draft_logits", 3, target_logits.dtype)
+        _check(uniforms, "uniforms", 2, torch.float32)
+    _check(draft_tokens, "draft_tokens", 2, torch.int32)
+    _check(out_tokens, "out_tokens", 2, torch.int32)
+    _check(out_num_accepted, "out_num_accepted", 1, torch.int32)
+    st = lib().spec_verify_sample(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(uniforms),
+        ctypes.c_float(temperature), B, K, V, _ptr(out_tokens), _ptr(out_num_accepted),
+        _stream(stream), _dtype_code(target_logits), _ptr(err_flag), _ptr(row_info),
+        _ptr(q_at_d), _ptr(p_at_d))
+    if st != SPEC_OK:
+        raise SpecError("spec_verify_sample", st)
+
+
+def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted, *,
+                       stream=None, err_flag=None) -> None:
+    """Greedy verification; target [B,K+1,V], tokens [B,K] -> [B,K+1], [B]."""
+    import torch
+    _check(target_logits, "target_logits", 3)
+    _check(draft_tokens, "draft_tokens", 2, torch.int32)
+    _check(out_tokens, "out_tokens", 2, torch.int32)
+    _check(out_num_accepted, "out_num_accepted", 1, torch.int32)
+    B, K1, V = target_logits.shape
+    st = lib().spec_verify_greedy(_ptr(target_logits), _ptr(draft_tokens), B, K1 - 1, V,
+                                  _ptr(out_tokens), _ptr(out_num_accepted), _stream(stream),
+                                  _dtype_code(target_logits), _ptr(err_flag))
+    if st != SPEC_OK:
+        raise SpecError("spec_verify_greedy", st)
+
+
+def kv_commit_rollback(block_table, seq_lens, num_accepted, prov_blocks, kv_pool, free_stack,
+                       free_top, status, *, K: int, block_size: int, stream=None) -> None:
+    """Commit the accepted provisional slots. kv_pool: [num_blocks, layers, 2, block_size,
+    heads, head_dim] (any element type); tables int32 as in include/specverify.h."""
+    import torch
+    for t, n in ((block_table, "block_table"), (prov_blocks, "prov_blocks")):
+        _check(t, n, 2, torch.int32)
+    for t, n in ((seq_lens, "seq_lens"), (num_accepted, "num_accepted"),
+                 (free_stack, "free_stack"), (free_top, "free_top"), (status, "status")):
+        _check(t, n, 1, torch.int32)
+    _check(kv_pool, "kv_pool", 6)
+    NB, NL, two, bs, H, D = kv_pool.shape
+    if two != 2 or bs != block_size:
+        raise ValueError("kv_pool must be [num_blocks, layers, 2, block_size, heads, head_dim]")
+    B, MB = block_table.shape
+    P = prov_blocks.shape[1]
+    st = lib().kv_commit_rollback(
+        _ptr(block_table), _ptr(seq_lens), _ptr(num_accepted), _ptr(prov_blocks), _ptr(kv_pool),
+        NB, NL, H, D, kv_pool.element_size(), block_size, B, K, MB, P, _ptr(free_stack),
+        _ptr(free_top), _ptr(status), _stream(stream))
+    if st != SPEC_OK:
+        raise SpecError("kv_commit_rollback", st)
+
+
+def spec_selftest_ex2(lo: float, hi: float, *, stream=None) -> float:
+    """Maximum relative error of the hardware exp2 over all fp32 arguments in [lo, hi]."""
+    import torch
+    out = torch.zeros(1, dtype=torch.float64, device="cuda")
+    st = lib().spec_selftest_ex2(ctypes.c_float(lo), ctypes.c_float(hi), _ptr(out),
+                                 _stream(stream))
+    if st != SPEC_OK:
+        raise SpecError("spec_selftest_ex2", st)
+    return float(out.item())
+
+
+# ------------------------------------------------------------------ conveniences
+def verify(target_logits, draft_logits, draft_tokens, uniforms, temperature: float, *,
+           stream=None, with_info: bool = False):
+    """Allocates the outputs on the logits' device and runs spec_verify_sample.
+    Returns (out_tokens [B,K+1], num_accepted [B]) (+ (row_info, err) if with_info)."""
+    import torch
+    B, K1, _ = target_logits.shape
+    dev = target_logits.device
+    out = torch.empty((B, K1), dtype=torch.int32, device=dev)
+    n = torch.empty((B,), dtype=torch.int32, device=dev)
+    info = torch.empty((B,), dtype=torch.int32, device=dev) if with_info else None
+    err = torch.zeros((1,), dtype=torch.int32, device=dev) if with_info else None
+    spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature, out, n,
+                       stream=stream, err_flag=err, row_info=info)
+    return (out, n, info, err) if with_info else (out, n)
+
+
+def verify_host(target_logits, draft_logits, draft_tokens, uniforms, temperature: float, *,
+                device="cuda", stream=None):
+    """End-to-end call on HOST (CPU, ideally pinned) tensors: copies the inputs to the
+    device, verifies, and copies (out_tokens, num_accepted) back to the host."""
+    import torch
+    s = stream or torch.cuda.current_stream()
+    with torch.cuda.stream(s):
+        t = target_logits.to(device, non_blocking=True)
+        d = draft_logits.to(device, non_blocking=True) if draft_logits is not None else None
+        k = draft_tokens.to(device, non_blocking=True)
+        u = uniforms.to(device, non_blocking=True)
+        out, n = verify(t, d, k, u, temperature, stream=s)
+        out_h = out.to("cpu", non_blocking=False)
+        n_h = n.to("cpu", non_blocking=False)
+    return out_h, n_h

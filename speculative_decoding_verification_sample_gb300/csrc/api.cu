@@ -1,0 +1,101 @@
+// C-ABI entry points: host-side argument validation, then asynchronous launch
+// on the caller's stream. No allocation, no synchronisation.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/specverify.h"
+#include "launch.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(int dtype) { return dtype == SPEC_BF16 ? 2 : (dtype == SPEC_F32 ? 4 : 0); }
+
+}  // namespace
+
+extern "C" {
+
+int spec_version(void) { return 100; }
+
+const char* spec_status_string(int status) {
+  switch (status) {
+    case SPEC_OK:
+      return "ok";
+    case SPEC_EINVAL:
+      return "invalid argument";
+    case SPEC_ECUDA:
+      return "CUDA launch failed";
+    case SPEC_ENOTSUP:
+      return "unsupported configuration";
+    default:
+      return "unknown status";
+  }
+}
+
+int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int K,
+                       int V, int32_t* out_tokens, int32_t* out_num_accepted, void* stream,
+                       int dtype, int32_t* err_flag) {
+  const int eb = elem_bytes(dtype);
+  if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SPEC_EINVAL;
+  if (eb == 0 || B < 1 || K < 1 || K > 31 || V < 1) return SPEC_EINVAL;
+  if (!aligned16(target_logits)) return SPEC_EINVAL;
+  if ((int64_t(V) * eb) % 16 != 0) return SPEC_ENOTSUP;
+  if (int64_t(B) * 16 > INT32_MAX) return SPEC_EINVAL;
+  sv::GreedyLaunch g{target_logits, draft_tokens, B, K, V, dtype, out_tokens, out_num_accepted,
+                     err_flag, stream};
+  return sv::launch_verify_greedy(g);
+}
+
+int spec_verify_sample(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const float* uniforms, float temperature,
+                       int B, int K, int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                       void* stream, int dtype, int32_t* err_flag, int32_t* row_info,
+                       float* q_at_d, float* p_at_d) {
+  if (std::isnan(temperature) || temperature < 0.0f || std::isinf(temperature)) return SPEC_EINVAL;
+  if (temperature == 0.0f) {
+    const int st = spec_verify_greedy(target_logits, draft_tokens, B, K, V, out_tokens,
+                                      out_num_accepted, stream, dtype, err_flag);
+    if (st == SPEC_OK && row_info)
+      if (cudaMemsetAsync(row_info, 0, size_t(B) * sizeof(int32_t),
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SPEC_ECUDA;
+    return st;
+  }
+  const int eb = elem_bytes(dtype);
+  if (!target_logits || !draft_logits || !draft_tokens || !uniforms || !out_tokens ||
+      !out_num_accepted)
+    return SPEC_EINVAL;
+  if ((q_at_d == nullptr) != (p_at_d == nullptr)) return SPEC_EINVAL;
+  if (eb == 0 || B < 1 || K < 1 || K > 31 || V < 1) return SPEC_EINVAL;
+  if (!aligned16(target_logits) || !aligned16(draft_logits)) return SPEC_EINVAL;
+  if ((int64_t(V) * eb) % 16 != 0) return SPEC_ENOTSUP;
+  if (int64_t(B) * 16 > INT32_MAX) return SPEC_EINVAL;
+  sv::SampleLaunch s{target_logits, draft_logits, draft_tokens, uniforms, temperature, B, K, V,
+                     dtype, out_tokens, out_num_accepted, err_flag, row_info, q_at_d, p_at_d,
+                     stream};
+  return sv::launch_verify_sample(s);
+}
+
+int kv_commit_rollback(int32_t* block_table, int32_t* seq_lens, const int32_t* num_accepted,
+                       int32_t* prov_blocks, void* kv_pool, int num_blocks, int num_layers,
+                       int num_kv_heads, int head_dim, int kv_elem_bytes, int block_size, int B,
+                       int K, int max_blocks, int P, int32_t* free_stack, int32_t* free_top,
+                       int32_t* status, void* stream) {
+  if (!block_table || !seq_lens || !num_accepted || !prov_blocks || !kv_pool || !free_stack ||
+      !free_top || !status)
+    return SPEC_EINVAL;
+  if (num_blocks < 1 || num_layers < 1 || num_kv_heads < 1 || head_dim < 1 || kv_elem_bytes < 1 ||
+      block_size < 1 || B < 1 || K < 0 || K > 31 || max_blocks < 1 || P < 1 || P > 512)
+    return SPEC_EINVAL;
+  const int64_t slot = int64_t(num_kv_heads) * head_dim * kv_elem_bytes;
+  if (slot % 16 != 0 || !aligned16(kv_pool)) return SPEC_ENOTSUP;
+  sv::KvLaunch k{block_table, seq_lens, num_accepted, prov_blocks, kv_pool, num_blocks,
+                 num_layers,  num_kv_heads, head_dim, kv_elem_bytes, block_size, B, K,
+                 max_blocks,  P, free_stack, free_top, status, stream};
+  return sv::launch_kv_commit(k);
+}
+
+}  // extern "C"

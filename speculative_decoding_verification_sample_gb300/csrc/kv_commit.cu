@@ -1,0 +1,275 @@
+// Paged KV-cache commit/rollback of the accepted provisional slots.
+//
+// Method: "aiengineeringfromscratch.com - Speculative decoding and EAGLE-3",
+// "Rolling back the KV cache" (drafts are written to a scratch area and
+// committed on acceptance; rollback costs bytes per layer per head) and
+// "Step 4: KV rollback accounting" (new logical length prefix + j + 1);
+// "sglang_spec_decode" README, provisional layer (provisional blocks are freed
+// at once; no block leaked or freed twice).
+//
+// Two launches on the caller's stream:
+//   kv_plan_kernel   one CTA: validates every row (all-or-nothing), pops the
+//                    new tail blocks from the free stack (rows ascending),
+//                    then pushes every provisional block (rows ascending) and
+//                    writes the call's status word;
+//   kv_copy_kernel   one CTA per row: if the status is 0, copies slots 0..n of
+//                    the row's provisional blocks, for every layer and both K
+//                    and V planes, to logical positions L..L+n, then sets the
+//                    new length and clears the provisional entries.
+// Only the accepted bytes move: 2 * (n + 1) * layers * heads * head_dim * elem
+// bytes read and written per row.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/specverify.h"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace sv {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kCopyThreads = 512;
+
+struct KvArgs {
+  int32_t* bt;
+  int32_t* sl;
+  const int32_t* na;
+  int32_t* pb;
+  uint8_t* pool;
+  int NB, NL, H, D, eb, bs;
+  int B, K, MB, P;
+  int32_t* fs;
+  int32_t* ftop;
+  int32_t* status;
+  int64_t slot_bytes;  // H * D * eb
+};
+
+__device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Block-wide exclusive scan of one int per thread (kPlanThreads threads).
+__device__ int block_excl_scan(int v, int* sh, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < kPlanThreads / 32 ? sh[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    sh[32 + lane] = wi - w;
+    if (lane == 31) sh[64] = wi;
+  }
+  __syncthreads();
+  const int res = sh[32 + warp] + inc - v;
+  total = sh[64];
+  __syncthreads();
+  return res;
+}
+
+// Validation of one row; returns error bits, the number of new blocks and of
+// provisional blocks to push.
+__device__ int validate_row(const KvArgs& a, int b, int& need, int& npush) {
+  int e = 0;
+  need = 0;
+  npush = 0;
+  const int n = a.na[b], L = a.sl[b];
+  for (int k = 0; k < a.P; ++k) {
+    const int x = a.pb[size_t(b) * a.P + k];
+    if (x >= 0) {
+      ++npush;
+      if (x >= a.NB) e |= SPEC_DERR_BAD_BLOCK;
+    }
+  }
+  if (n < 0 || n > a.K) return e | SPEC_DERR_BAD_ACCEPT;
+  if (L < 0 || cdiv(L + n + 1, a.bs) > a.MB) return e | SPEC_DERR_BAD_LENGTH;
+  const int have = cdiv(L, a.bs), tot = cdiv(L + n + 1, a.bs);
+  for (int j = L / a.bs; j < tot; ++j) {
+    const int x = a.bt[size_t(b) * a.MB + j];
+    if (j < have) {
+      if (x < 0 || x >= a.NB) e |= SPEC_DERR_BAD_BLOCK;  // the partly filled tail block
+    } else if (x != -1) {
+      e |= SPEC_DERR_BAD_BLOCK;  // a slot the commit must fill is already taken
+    }
+  }
+  if (n / a.bs >= a.P) {
+    e |= SPEC_DERR_BAD_BLOCK;
+  } else {
+    for (int k = 0; k <= n / a.bs; ++k) {
+      const int x = a.pb[size_t(b) * a.P + k];
+      if (x < 0 || x >= a.NB) e |= SPEC_DERR_BAD_BLOCK;
+    }
+  }
+  need = tot - have;
+  return e;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) kv_plan_kernel(const KvArgs a) {
+  __shared__ int sh[96];
+  __shared__ int s_err, s_need, s_push;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_err = 0;
+    s_need = 0;
+    s_push = 0;
+  }
+  __syncthreads();
+  // 1. validation and totals
+  int e = 0, need_sum = 0, push_sum = 0;
+  for (int b = tid; b < a.B; b += kPlanThreads) {
+    int need, np;
+    e |= validate_row(a, b, need, np);
+    need_sum += need;
+    push_sum += np;
+  }
+  atomicOr(&s_err, e);
+  atomicAdd(&s_need, need_sum);
+  atomicAdd(&s_push, push_sum);
+  __syncthreads();
+  const int top = *a.ftop;
+  int err = s_err;
+  const int need_total = s_need, push_total = s_push;
+  if (err == 0 && (top < 0 || top > a.NB || need_total > top)) err |= SPEC_DERR_NO_SPACE;
+  if (err == 0 && top - need_total + push_total > a.NB) err |= SPEC_DERR_BAD_BLOCK;
+  if (err == 0) {
+    // every block about to be popped must be a valid id
+    int pe = 0;
+    for (int i = top - need_total + tid; i < top; i += kPlanThreads) {
+      const int x = a.fs[i];
+      if (x < 0 || x >= a.NB) pe = 1;
+    }
+    if (pe) atomicOr(&s_err, SPEC_DERR_BAD_BLOCK);
+    __syncthreads();
+    err |= s_err;
+  }
+  if (err != 0) {
+    if (tid == 0) *a.status = err;
+    return;
+  }
+  // 2. pops: row b takes free_stack[top-1-(prefix_b+k)], rows ascending
+  int carry = 0;
+  for (int b0 = 0; b0 < a.B; b0 += kPlanThreads) {
+    const int b = b0 + tid;
+    int need = 0, np = 0;
+    if (b < a.B) validate_row(a, b, need, np);
+    int chunk_total;
+    const int pre = block_excl_scan(need, sh, chunk_total) + carry;
+    if (b < a.B) {
+      const int have = cdiv(a.sl[b], a.bs);
+      for (int k = 0; k < need; ++k)
+        a.bt[size_t(b) * a.MB + have + k] = a.fs[top - 1 - (pre + k)];
+    }
+    carry += chunk_total;
+  }
+  __syncthreads();  // all pops have read the stack before any push writes it
+  // 3. pushes: provisional blocks, rows ascending, from the new top
+  const int base = top - need_total;
+  carry = 0;
+  for (int b0 = 0; b0 < a.B; b0 += kPlanThreads) {
+    const int b = b0 + tid;
+    int np = 0;
+    if (b < a.B)
+      for (int k = 0; k < a.P; ++k) np += a.pb[size_t(b) * a.P + k] >= 0;
+    int chunk_total;
+    const int pre = block_excl_scan(np, sh, chunk_total) + carry;
+    if (b < a.B) {
+      int w = 0;
+      for (int k = 0; k < a.P; ++k) {
+        const int x = a.pb[size_t(b) * a.P + k];
+        if (x >= 0) a.fs[base + pre + (w++)] = x;
+      }
+    }
+    carry += chunk_total;
+  }
+  if (tid == 0) {
+    *a.ftop = base + push_total;
+    *a.status = 0;
+  }
+}
+
+__global__ void __launch_bounds__(kCopyThreads) kv_copy_kernel(const KvArgs a) {
+  __shared__ int64_t s_src[32 + 1], s_dst[32 + 1];
+  const int b = blockIdx.x;
+  if (*a.status != 0) return;
+  const int n = a.na[b], L = a.sl[b];
+  const int64_t layer_stride = int64_t(2) * a.bs * a.slot_bytes;  // one layer: K and V planes
+  const int64_t block_stride = int64_t(a.NL) * layer_stride;
+  if (threadIdx.x <= n) {
+    const int s = threadIdx.x;
+    const int sb = a.pb[size_t(b) * a.P + s / a.bs];
+    const int pos = L + s;
+    const int db = a.bt[size_t(b) * a.MB + pos / a.bs];
+    s_src[s] = int64_t(sb) * block_stride + int64_t(s % a.bs) * a.slot_bytes;
+    s_dst[s] = int64_t(db) * block_stride + int64_t(pos % a.bs) * a.slot_bytes;
+  }
+  __syncthreads();
+  const int vpu = int(a.slot_bytes / 16);          // 16-byte vectors per (slot, layer, plane)
+  const int64_t units = int64_t(n + 1) * a.NL * 2;  // (slot, layer, plane) units
+  const int64_t total = units * vpu;
+  const int64_t step = kCopyThreads;
+  constexpr int kUnroll = 4;
+  for (int64_t g0 = threadIdx.x; g0 < total; g0 += step * kUnroll) {
+    uint4 v[kUnroll];
+    int64_t dsto[kUnroll];
+#pragma unroll
+    for (int i = 0; i < kUnroll; ++i) {
+      const int64_t g = g0 + i * step;
+      dsto[i] = -1;
+      if (g < total) {
+        const int64_t u = g / vpu;
+        const int w = int(g - u * vpu);
+        const int s = int(u / (2 * a.NL));
+        const int rem = int(u - int64_t(s) * 2 * a.NL);  // layer * 2 + plane
+        const int64_t within = int64_t(rem) * a.bs * a.slot_bytes + int64_t(w) * 16;
+        v[i] = ldg_nc_v4(a.pool + s_src[s] + within);
+        dsto[i] = s_dst[s] + within;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kUnroll; ++i)
+      if (dsto[i] >= 0) *reinterpret_cast<uint4*>(a.pool + dsto[i]) = v[i];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) a.sl[b] = L + n + 1;
+  if (threadIdx.x < a.P) a.pb[size_t(b) * a.P + threadIdx.x] = -1;
+}
+
+int launch_kv_commit(const KvLaunch& k) {
+  KvArgs a;
+  a.bt = k.block_table;
+  a.sl = k.seq_lens;
+  a.na = k.num_accepted;
+  a.pb = k.prov_blocks;
+  a.pool = static_cast<uint8_t*>(k.kv_pool);
+  a.NB = k.num_blocks;
+  a.NL = k.num_layers;
+  a.H = k.num_kv_heads;
+  a.D = k.head_dim;
+  a.eb = k.elem_bytes;
+  a.bs = k.block_size;
+  a.B = k.B;
+  a.K = k.K;
+  a.MB = k.max_blocks;
+  a.P = k.P;
+  a.fs = k.free_stack;
+  a.ftop = k.free_top;
+  a.status = k.status;
+  a.slot_bytes = int64_t(k.num_kv_heads) * k.head_dim * k.elem_bytes;
+  cudaStream_t st = static_cast<cudaStream_t>(k.stream);
+  kv_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ECUDA;
+  kv_copy_kernel<<<k.B, kCopyThreads, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ECUDA;
+  return SPEC_OK;
+}
+
+}  // namespace sv

@@ -113,6 +113,9 @@ def test_allocation_order_is_rows_ascending_pop_before_push():
     ("bad_table_block", okv.ERR_BAD_BLOCK),
     ("bad_prov_block", okv.ERR_BAD_BLOCK),
     ("slot_taken", okv.ERR_BAD_BLOCK),
+    ("top_too_big", okv.ERR_NO_SPACE),
+    ("bad_free_entry", okv.ERR_BAD_BLOCK),
+    ("prov_out_of_range", okv.ERR_BAD_BLOCK),
 ])
 def test_errors_leave_state_unchanged(mutate, bit):
     c = synth.kv_case(4, 4, seq_lens=np.array([16, 20, 31, 47]), num_accepted=np.array([1, 2, 4, 0]),
@@ -128,11 +131,17 @@ def test_errors_leave_state_unchanged(mutate, bit):
     elif mutate == "no_space":
         c.free_top = 1
     elif mutate == "bad_table_block":
-        c.block_table[3, 1] = c.num_blocks
+        c.block_table[3, 2] = c.num_blocks       # row 3 (L = 47) has its tail in block 2
     elif mutate == "bad_prov_block":
         c.prov_blocks[1, 0] = -1
     elif mutate == "slot_taken":
         c.block_table[0, 1] = c.free_stack[0]
+    elif mutate == "top_too_big":
+        c.free_top = c.num_blocks + 1
+    elif mutate == "bad_free_entry":
+        c.free_stack[c.free_top - 1] = -5
+    elif mutate == "prov_out_of_range":
+        c.prov_blocks[2, 0] = c.num_blocks + 3
     res = _commit(c)
     assert res["err"] & bit
     assert res["copies"] == []
