@@ -56,7 +56,45 @@ __device__ __forceinline__ df df_mul(df x, df y) {
   return fast_two_sum(p.hi, e);
 }
 
-__device__ __forceinline__ double df_to_double(df x) { return (double)x.hi + (double)x.lo; }
+__device__ __forceinline__ df df_add_f(df x, float y) {
+  df s = two_sum(x.hi, y);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, x.lo));
+}
+
+__device__ __forceinline__ df df_mul_f(df x, float y) {
+  df p = two_prod(x.hi, y);
+  return fast_two_sum(p.hi, __fmaf_rn(x.lo, y, p.lo));
+}
+
+// 1/x for x > 0: float reciprocal refined by one Newton step in pair arithmetic.
+__device__ __forceinline__ df df_recip(df x) {
+  const float r0 = __frcp_rn(x.hi);
+  // e = 1 - x*r0 formed from the exact residual of x.hi*r0
+  const float e = __fsub_rn(-__fmaf_rn(x.hi, r0, -1.0f), __fmul_rn(x.lo, r0));
+  return fast_two_sum(r0, __fmul_rn(r0, e));
+}
+
+__device__ __forceinline__ bool df_gt(df a, df b) {
+  return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+
+__device__ __forceinline__ df df_shfl_xor(df x, int o) {
+  return {__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)};
+}
+__device__ __forceinline__ df df_shfl_up(df x, int o) {
+  return {__shfl_up_sync(0xffffffffu, x.hi, o), __shfl_up_sync(0xffffffffu, x.lo, o)};
+}
+__device__ __forceinline__ df df_shfl(df x, int l) {
+  return {__shfl_sync(0xffffffffu, x.hi, l), __shfl_sync(0xffffffffu, x.lo, l)};
+}
+
+// Warp sum in pair arithmetic; df_add is commutative bit for bit (the error of
+// TwoSum is exact), so every lane ends with the same value.
+__device__ __forceinline__ df df_warp_sum(df v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = df_add(v, df_shfl_xor(v, o));
+  return v;
+}
 
 // ---------------------------------------------------------------- 2^(j/256)
 // Values computed at compile time in double precision from the exponential
@@ -95,10 +133,10 @@ __constant__ Exp2Table kExp2Tab = make_exp2_table();
 constexpr float kLn2Hi = 0.693147182464599609375f;               // fl32(ln 2)
 constexpr float kLn2Lo = static_cast<float>(kLn2d - 0.693147182464599609375);
 
-// 2^(xh + xl) as hi + lo, for xh + xl in [-149, 127). Values below 2^-149
-// return 0 (their absolute size is below every error budget used here).
+// 2^(xh + xl) as hi + lo, for xh + xl in [-126, 127). Smaller values return 0
+// (an absolute error below 2^-126 per term, far below every error budget here).
 //   m + j/256 = round(256 xh) / 256, g = xh - (m + j/256) is exact because
-//   |xh| < 2^8 makes xh a multiple of 2^-15 and |g| <= 2^-9;
+//   xh is a multiple of ulp(xh) <= 2^-16 (|xh| < 2^8), so is g, and |g| <= 2^-9;
 //   t = (g + xl) ln2 is formed as a float pair (error < 2^-46 |t|);
 //   exp(t) = 1 + t + t^2/2 + t^3/6 + t^4/24 with |t| < 1.36e-3: truncation
 //   < 3e-17, the t^2.. part (< 9.3e-7) evaluated in fp32 (error < 2.2e-13);
@@ -108,7 +146,7 @@ constexpr double kDfExpRelErr = 4e-13;
 
 __device__ __forceinline__ df df_exp2(float xh, float xl, const float* tab_hi,
                                       const float* tab_lo) {
-  if (xh < -149.0f) return {0.0f, 0.0f};
+  if (!(xh >= -126.0f)) return {0.0f, 0.0f};  // below 2^-126 (or -inf): flushed
   float k = rintf(__fmul_rn(xh, 256.0f));
   float g = __fmaf_rn(k, -1.0f / 256.0f, xh);  // exact
   int ki = static_cast<int>(k);
@@ -135,13 +173,8 @@ __device__ __forceinline__ df df_exp2(float xh, float xl, const float* tab_hi,
   rl = __fmaf_rn(Th, e.lo, rl);
   rl = __fmaf_rn(Tl, e.hi, rl);
   df r = fast_two_sum(rh, rl);
-  // scale by 2^m (exact while the result stays normal; tiny results flush)
-  if (m < -126) {
-    // two-step scaling keeps intermediate values normal
-    float s1 = __int_as_float((m + 126 + 127) << 23);
-    float s2 = __int_as_float(1 << 23);  // 2^-126
-    return {__fmul_rn(__fmul_rn(r.hi, s1), s2), __fmul_rn(__fmul_rn(r.lo, s1), s2)};
-  }
+  // scale by 2^m (exact: m >= -127 and the result stays normal or is flushed)
+  if (m < -126) return {0.0f, 0.0f};
   float s = __int_as_float((m + 127) << 23);
   return {__fmul_rn(r.hi, s), __fmul_rn(r.lo, s)};
 }
