@@ -31,7 +31,12 @@
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers owned by the caller. The library
  *     allocates no device or host memory and keeps no state between calls
- *     (its only static data is a read-only constant table).
+ *     (its only static data is a read-only constant table and a per-process
+ *     cache of occupancy queries). The verify calls take a caller-allocated
+ *     device workspace of spec_verify_workspace_bytes(B, K, V, dtype) bytes
+ *     (256-byte aligned) that holds per-slice partial sums and the work queue;
+ *     its contents need no initialisation, and calls that share one workspace
+ *     must not overlap on the device (one stream, or ordered streams).
  *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
  *     the legacy default stream). Nothing synchronises; outputs are valid once
  *     the stream reaches the call.
@@ -110,12 +115,13 @@ extern "C" {
  * decision is certified against a proven error bound of the fp32 arithmetic; the
  * rare decisions inside the bound are recomputed in double-float arithmetic.
  * Logit arrays must be 16-byte aligned and V * sizeof(dtype) a multiple of 16.
+ * workspace / workspace_bytes: see the conventions above (SPEC_EINVAL if too small).
  */
 int spec_verify_sample(const void* target_logits, const void* draft_logits,
                        const int32_t* draft_tokens, const float* uniforms, float temperature,
                        int B, int K, int V, int32_t* out_tokens, int32_t* out_num_accepted,
                        void* stream, int dtype, int32_t* err_flag, int32_t* row_info,
-                       float* q_at_d, float* p_at_d);
+                       float* q_at_d, float* p_at_d, void* workspace, size_t workspace_bytes);
 
 /*
  * spec_verify_greedy - greedy verification ([P] "What it does").
@@ -128,7 +134,14 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
  */
 int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int K,
                        int V, int32_t* out_tokens, int32_t* out_num_accepted, void* stream,
-                       int dtype, int32_t* err_flag);
+                       int dtype, int32_t* err_flag, void* workspace, size_t workspace_bytes);
+
+/*
+ * spec_verify_workspace_bytes - size of the device workspace that
+ * spec_verify_sample and spec_verify_greedy need for (B, K, V, dtype); 0 for
+ * arguments those calls would reject. One workspace serves both calls.
+ */
+size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype);
 
 /*
  * kv_commit_rollback - commit the accepted provisional KV slots and free the

@@ -27,8 +27,8 @@ SPEC_DERR_TIMEOUT = 64
 SPEC_ROW_ACCEPT_REFINED, SPEC_ROW_SAMPLE_REFINED = 1, 2
 SPEC_ROW_UNCERTIFIED, SPEC_ROW_ZERO_RESIDUAL = 4, 8
 
-EXPORTED = ("spec_verify_sample", "spec_verify_greedy", "kv_commit_rollback",
-            "spec_selftest_ex2", "spec_status_string", "spec_version")
+EXPORTED = ("spec_verify_sample", "spec_verify_greedy", "spec_verify_workspace_bytes",
+            "kv_commit_rollback", "spec_selftest_ex2", "spec_status_string", "spec_version")
 
 _lib = None
 
@@ -51,10 +51,13 @@ def lib() -> ctypes.CDLL:
                                "speculative_decoding_verification_sample_gb300.build.build()")
         L = ctypes.CDLL(LIB_PATH)
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
-        L.spec_verify_sample.argtypes = [P, P, P, P, F, I, I, I, P, P, P, I, P, P, P, P]
+        Z = ctypes.c_size_t
+        L.spec_verify_sample.argtypes = [P, P, P, P, F, I, I, I, P, P, P, I, P, P, P, P, P, Z]
         L.spec_verify_sample.restype = I
-        L.spec_verify_greedy.argtypes = [P, P, I, I, I, P, P, P, I, P]
+        L.spec_verify_greedy.argtypes = [P, P, I, I, I, P, P, P, I, P, P, Z]
         L.spec_verify_greedy.restype = I
+        L.spec_verify_workspace_bytes.argtypes = [I, I, I, I]
+        L.spec_verify_workspace_bytes.restype = Z
         L.kv_commit_rollback.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P, P, P, P]
         L.kv_commit_rollback.restype = I
         L.spec_selftest_ex2.argtypes = [F, F, P, P]
@@ -101,9 +104,43 @@ def _check(t, name, ndim=None, dtype=None):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+_workspaces = {}
+
+
+def spec_verify_workspace_bytes(B: int, K: int, V: int, dtype_code: int) -> int:
+    """Device workspace bytes the verify calls need for (B, K, V, dtype)."""
+    return int(lib().spec_verify_workspace_bytes(B, K, V, dtype_code))
+
+
+def workspace_for(B: int, K: int, V: int, dtype_code: int, device):
+    """A cached device workspace (uint8 tensor) large enough for (B, K, V, dtype)
+    on `device`. Calls sharing it must be ordered on the device."""
+    import torch
+    need = spec_verify_workspace_bytes(B, K, V, dtype_code)
+    if need == 0:
+        raise SpecError("spec_verify_workspace_bytes", SPEC_EINVAL)
+    dev = torch.device(device)
+    key = (dev.type, dev.index if dev.index is not None else torch.cuda.current_device())
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(need + 256, dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
+    return ws
+
+
+def _ws_args(ws, B, K, V, code, device):
+    if ws is None:
+        if spec_verify_workspace_bytes(B, K, V, code) == 0:
+            # unsupported shape: the library call itself reports why
+            return ctypes.c_void_p(0), ctypes.c_size_t(0)
+        ws = workspace_for(B, K, V, code, device)
+    off = (-ws.data_ptr()) % 256
+    return ctypes.c_void_p(ws.data_ptr() + off), ctypes.c_size_t(ws.numel() - off)
+
+
 def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature: float,
                        out_tokens, out_num_accepted, *, stream=None, err_flag=None,
-                       row_info=None, q_at_d=None, p_at_d=None) -> None:
+                       row_info=None, q_at_d=None, p_at_d=None, workspace=None) -> None:
     """Sampling-mode verification; shapes [B,K+1,V], [B,K,V], [B,K], [B,K+1] -> [B,K+1], [B]."""
     import torch
     _check(target_logits, "target_logits", 3)
@@ -115,17 +152,19 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temp
     _check(draft_tokens, "draft_tokens", 2, torch.int32)
     _check(out_tokens, "out_tokens", 2, torch.int32)
     _check(out_num_accepted, "out_num_accepted", 1, torch.int32)
+    code = _dtype_code(target_logits)
+    wsp, wsn = _ws_args(workspace, B, K, V, code, target_logits.device)
     st = lib().spec_verify_sample(
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(uniforms),
         ctypes.c_float(temperature), B, K, V, _ptr(out_tokens), _ptr(out_num_accepted),
-        _stream(stream), _dtype_code(target_logits), _ptr(err_flag), _ptr(row_info),
-        _ptr(q_at_d), _ptr(p_at_d))
+        _stream(stream), code, _ptr(err_flag), _ptr(row_info),
+        _ptr(q_at_d), _ptr(p_at_d), wsp, wsn)
     if st != SPEC_OK:
         raise SpecError("spec_verify_sample", st)
 
 
 def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted, *,
-                       stream=None, err_flag=None) -> None:
+                       stream=None, err_flag=None, workspace=None) -> None:
     """Greedy verification; target [B,K+1,V], tokens [B,K] -> [B,K+1], [B]."""
     import torch
     _check(target_logits, "target_logits", 3)
@@ -133,9 +172,11 @@ def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted
     _check(out_tokens, "out_tokens", 2, torch.int32)
     _check(out_num_accepted, "out_num_accepted", 1, torch.int32)
     B, K1, V = target_logits.shape
+    code = _dtype_code(target_logits)
+    wsp, wsn = _ws_args(workspace, B, K1 - 1, V, code, target_logits.device)
     st = lib().spec_verify_greedy(_ptr(target_logits), _ptr(draft_tokens), B, K1 - 1, V,
                                   _ptr(out_tokens), _ptr(out_num_accepted), _stream(stream),
-                                  _dtype_code(target_logits), _ptr(err_flag))
+                                  code, _ptr(err_flag), wsp, wsn)
     if st != SPEC_OK:
         raise SpecError("spec_verify_greedy", st)
 

@@ -35,17 +35,32 @@ const char* spec_status_string(int status) {
   }
 }
 
+size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype) {
+  const int eb = elem_bytes(dtype);
+  if (eb == 0 || B < 1 || K < 1 || K > 31 || V < 1 || (int64_t(V) * eb) % 16 != 0) return 0;
+  const size_t a = sv::sample_workspace_bytes(B, K, V, dtype);
+  const size_t g = sv::greedy_workspace_bytes(B, K, V, dtype);
+  return a > g ? a : g;
+}
+
+static int check_workspace(void* ws, size_t bytes, int B, int K, int V, int dtype) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPEC_EINVAL;
+  if (bytes < spec_verify_workspace_bytes(B, K, V, dtype)) return SPEC_EINVAL;
+  return SPEC_OK;
+}
+
 int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int K,
                        int V, int32_t* out_tokens, int32_t* out_num_accepted, void* stream,
-                       int dtype, int32_t* err_flag) {
+                       int dtype, int32_t* err_flag, void* workspace, size_t workspace_bytes) {
   const int eb = elem_bytes(dtype);
   if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SPEC_EINVAL;
   if (eb == 0 || B < 1 || K < 1 || K > 31 || V < 1) return SPEC_EINVAL;
   if (!aligned16(target_logits)) return SPEC_EINVAL;
   if ((int64_t(V) * eb) % 16 != 0) return SPEC_ENOTSUP;
-  if (int64_t(B) * 16 > INT32_MAX) return SPEC_EINVAL;
+  if (int64_t(B) * (V / (16 / eb)) > INT32_MAX) return SPEC_EINVAL;
+  if (check_workspace(workspace, workspace_bytes, B, K, V, dtype) != SPEC_OK) return SPEC_EINVAL;
   sv::GreedyLaunch g{target_logits, draft_tokens, B, K, V, dtype, out_tokens, out_num_accepted,
-                     err_flag, stream};
+                     err_flag, stream, workspace};
   return sv::launch_verify_greedy(g);
 }
 
@@ -53,11 +68,12 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
                        const int32_t* draft_tokens, const float* uniforms, float temperature,
                        int B, int K, int V, int32_t* out_tokens, int32_t* out_num_accepted,
                        void* stream, int dtype, int32_t* err_flag, int32_t* row_info,
-                       float* q_at_d, float* p_at_d) {
+                       float* q_at_d, float* p_at_d, void* workspace, size_t workspace_bytes) {
   if (std::isnan(temperature) || temperature < 0.0f || std::isinf(temperature)) return SPEC_EINVAL;
   if (temperature == 0.0f) {
     const int st = spec_verify_greedy(target_logits, draft_tokens, B, K, V, out_tokens,
-                                      out_num_accepted, stream, dtype, err_flag);
+                                      out_num_accepted, stream, dtype, err_flag, workspace,
+                                      workspace_bytes);
     if (st == SPEC_OK && row_info)
       if (cudaMemsetAsync(row_info, 0, size_t(B) * sizeof(int32_t),
                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -72,10 +88,11 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
   if (eb == 0 || B < 1 || K < 1 || K > 31 || V < 1) return SPEC_EINVAL;
   if (!aligned16(target_logits) || !aligned16(draft_logits)) return SPEC_EINVAL;
   if ((int64_t(V) * eb) % 16 != 0) return SPEC_ENOTSUP;
-  if (int64_t(B) * 16 > INT32_MAX) return SPEC_EINVAL;
+  if (int64_t(B) * (V / (16 / eb)) > INT32_MAX) return SPEC_EINVAL;
+  if (check_workspace(workspace, workspace_bytes, B, K, V, dtype) != SPEC_OK) return SPEC_EINVAL;
   sv::SampleLaunch s{target_logits, draft_logits, draft_tokens, uniforms, temperature, B, K, V,
                      dtype, out_tokens, out_num_accepted, err_flag, row_info, q_at_d, p_at_d,
-                     stream};
+                     stream, workspace};
   return sv::launch_verify_sample(s);
 }
 

@@ -13,15 +13,12 @@ namespace sv {
 constexpr int kCW = 8;                 // consumer warps per CTA
 constexpr int kCons = kCW * 32;        // consumer threads
 constexpr int kThreads = kCons + 32;   // + one producer warp (bulk-copy issue)
-constexpr int kStages = 5;             // ring depth (5 x 16 KB: two CTAs per SM)
+constexpr int kStages = 6;             // ring depth (6 x 16 KB: two CTAs per SM)
 constexpr int kChunk = 16384;          // bytes per ring stage
-constexpr int kMaxCluster = 16;        // CTAs per batch row (non-portable maximum)
 constexpr int kMaxK = 31;              // draft positions (fits a warp ballot)
 constexpr int kMaxRows = 2 * kMaxK + 1;
 
 constexpr float kU = 5.9604644775390625e-8f;  // fp32 unit roundoff 2^-24
-constexpr double kUd = 5.9604644775390625e-8;
-constexpr double kLn2 = 0.693147180559945309417232121458176568;
 constexpr float kLn2f = 0.693147180559945309417232121458176568f;
 
 // max that returns NaN when either input is NaN (PTX max.NaN).
@@ -79,11 +76,6 @@ struct EF32 {
 };
 
 // ----------------------------------------------------------------- warp ops
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
 __device__ __forceinline__ float warp_sum_f(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -25,6 +25,7 @@ struct SampleLaunch {
   float* q_at_d;
   float* p_at_d;
   void* stream;
+  void* workspace;
 };
 
 struct GreedyLaunch {
@@ -35,6 +36,7 @@ struct GreedyLaunch {
   int32_t* out_n;
   int32_t* err;
   void* stream;
+  void* workspace;
 };
 
 struct KvLaunch {
@@ -52,6 +54,8 @@ struct KvLaunch {
 };
 
 int launch_verify_sample(const SampleLaunch& s);
+size_t sample_workspace_bytes(int B, int K, int V, int dtype);
+size_t greedy_workspace_bytes(int B, int K, int V, int dtype);
 int launch_verify_greedy(const GreedyLaunch& g);
 int launch_kv_commit(const KvLaunch& k);
 int verify_cluster_size(int B, int V, int dtype);

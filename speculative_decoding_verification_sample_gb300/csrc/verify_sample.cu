@@ -7,33 +7,29 @@
 // zero); after K acceptances a bonus token is drawn from q_K. The draw is the
 // inverse CDF in token-index order with the single uniform u_K.
 //
-// GB300 mapping. Persistent thread-block clusters; cluster c verifies batch
-// rows c, c + ncl, ... The C CTAs of a cluster split the vocabulary into C
-// contiguous slices. Per row:
-//   1. pass 1: each CTA consumes its slice of the 2K logit rows (target and
-//      draft, positions 0..K-1) from the bulk-copy ring (stream.cuh), keeping
-//      per-thread running (max, sum of exp2); the producer thread is already
-//      streaming the next row behind it;
-//   2. per-CTA partials are all-gathered over distributed shared memory, so
-//      every CTA holds the softmax statistics of all 2K rows and evaluates the
-//      K accept tests; a warp ballot gives the first rejection j;
-//   3. the final draw re-reads only row j of both tensors (hot in L2), or
-//      target row K for a bonus (its statistics first): each CTA sums its
-//      slice, keeping the sum of every 16-byte vector in shared memory; the
-//      CTA sums are all-gathered and the CTA holding u_K * total mass finds
-//      the token by a block scan over its vector sums;
-//   4. CTA 0 writes the row's outputs.
-// No global scratch memory is used.
+// GB300 mapping (dataflow engine, engine.cuh). Each batch row is cut into S
+// vocabulary slices and goes through these stages, each a set of S slice
+// tasks whose last finisher continues the row:
+//   P1  softmax statistics (max, sum of exp2) of the slice of all 2K logit
+//       rows (target and draft, positions 0..K-1), streamed from HBM;
+//       finish: combine -> K accept tests -> first rejection j (warp ballot)
+//   BS  (only when all K are accepted) statistics of target row K
+//   SW  fp32 residual (q_j - p_j)+ (or q_K) over the slice of row j, re-read
+//       while hot in L2; per 32-vector unit sums kept in the workspace;
+//       finish: locate u_K * total mass slice -> unit -> entry, certify
+//   FA  (rare) double-float row sums of the draw's rows
+//   FB  (rare) double-float residual and unit sums; finish: certified search
+// Only row j of the draft/target pair is ever re-read for the draw.
 //
 // Arithmetic. No fp64 arithmetic (GB300 runs fp64 at a small fraction of its
 // fp32 rate): logits are widened to fp32, exponentials use the MUFU exp2 with
-// an integer offset ceil(max * log2(e)/T), and every sum a decision depends on
-// is a float pair (df.cuh). A decision (an accept test, or the boundary of the
-// drawn token) is taken from the fp32 path only when the uniform is farther
-// from the threshold than twice a proven bound on that path's error;
-// otherwise the row is recomputed with double-float exponentials (relative
-// error < 4e-12 per term) and flagged in row_info. The result equals an
-// exact-arithmetic evaluation except for rows flagged SPEC_ROW_UNCERTIFIED.
+// an integer offset ceil(max * log2(e)/T), and sums a decision depends on are
+// float pairs (df.cuh). A decision is taken from the fp32 path only when the
+// uniform is farther from the threshold than twice a proven bound on that
+// path's error; otherwise the FA/FB stages recompute it with double-float
+// exponentials (relative error < 4e-12 per term) and the row is flagged in
+// row_info. The output equals an exact-arithmetic evaluation except for rows
+// flagged SPEC_ROW_UNCERTIFIED.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -41,122 +37,134 @@
 #include <cstdint>
 
 #include "../../include/specverify.h"
-#include "cluster_launch.cuh"
 #include "common.cuh"
 #include "df.cuh"
+#include "engine.cuh"
+#include "launch_util.cuh"
 #include "launch.h"
 #include "ptx.cuh"
-#include "stream.cuh"
 
 namespace sv {
 namespace {
 
-constexpr int kVsCap = 2048;  // vector sums kept per CTA (slice <= kVsCap vectors)
-constexpr int kUnroll = 4;    // vectors in flight per thread in the direct-load sweeps
+enum TaskType { kP1 = 1, kBS = 2, kSW = 3, kFA = 4, kFB = 5 };
+enum { kAccept = 0, kReject = 1, kAmbiguous = 2, kInvalid = 3 };
+constexpr int kModeResidual = 0, kModeQ = 1;  // RowState.mode
 
-// ------------------------------------------------------------------ layout
-struct Misc {
-  int tok[kMaxK];
-  float zt_d[kMaxK];  // target logit of the draft token, per position
-  float zd_d[kMaxK];  // draft logit of the draft token
-  float u[kMaxK + 1];
-  int bad_token;
-  int abort;
-  int acc_state[kMaxK];
-  float qd[kMaxK], pd[kMaxK];
-  float src[16];  // this CTA's small exchange payload
-  df wR[kCW];
-  float wQ[kCW], wP[kCW], wAq[kCW], wAp[kCW];
-  df scan[kCW];
-  // scalars computed by one thread, read by all consumers
-  int go;      // a sample point exists
-  int cs;      // CTA holding the sample point
-  df base;     // mass before CTA cs
-  df tstar;    // u_K * total mass
-  float E;     // error bound of the draw
-  int zero_res;
-  int token, cert, found;
+// ------------------------------------------------------------------ arguments
+struct Bounds {
+  float ex2;     // relative error bound of ex2.approx.ftz.f32 on [-126, 1]
+  float gamma1;  // relative error bound of the per-thread fp32 summation of row sums
+  float xbar;    // bound on sum_v q_v |x_v| used by the accept tests (log2 V + 2)
 };
 
-struct Layout {
+struct SampleArgs {
+  const void* target;
+  const void* draft;
+  const int32_t* tokens;
+  const float* uniforms;
+  int B, K, V, S, nvec;
+  float c;         // fl32(log2(e) / T)
+  float Chi, Clo;  // log2(e) / T as a float pair
+  Bounds bd;
+  int32_t* out_tokens;
+  int32_t* out_n;
+  int32_t* err;
+  int32_t* row_info;
+  float* q_at_d;
+  float* p_at_d;
+  Ws ws;
+};
+
+// ------------------------------------------------------------------ shared memory
+struct Misc {
+  int abort;
+  int last;  // this CTA completed the stage of the current task's row
+  int tok[kMaxK];
+  float zt_d[kMaxK], zd_d[kMaxK], u[kMaxK + 1];
+  int bad_token;
+  int acc_state[kMaxK];
+  float qd[kMaxK], pd[kMaxK];
+  df wR[kCW];
+  float wF[4][kCW];
+  df wA[kCW], wB[kCW];
+  int token, cert, found;
+  df tstar, base;
+  float E;
+};
+
+struct Smem {
   Ring ring;
-  Xc xc;
   Misc* misc;
-  float* wM;  // [R][kCW]
-  df* wS;     // [R][kCW]
-  int* wBad;  // [R][kCW]
-  float* rowM;
+  float* wM;  // [2K+1][kCW]
+  df* wS;     // [2K+1][kCW]
+  int* wBad;  // [2K+1][kCW]
   float* rowKc;
   df* rowS;
   df* rowInv;
   int* rowOK;
-  df* vsd;  // [kVsCap]
   float* tab_hi;
   float* tab_lo;
 };
 
-__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-__host__ __device__ inline int xc_floats(int R) { return 4 * R > 16 ? 4 * R : 16; }
+__host__ __device__ inline size_t al(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 template <class F>
 __host__ __device__ inline size_t carve(int R, F&& put) {
-  size_t o = size_t(kStages) * kChunk;  // ring at offset 0
-  auto take = [&](size_t bytes, size_t al) {
-    o = align_up(o, al);
+  size_t o = size_t(kStages) * kChunk;
+  auto take = [&](size_t bytes, size_t a) {
+    o = al(o, a);
     const size_t at = o;
     o += bytes;
     return at;
   };
-  put(0, take((2 * kStages + 2) * 8, 8));                          // ring + exchange barriers
-  put(1, take(sizeof(Misc), 16));                                  // misc
-  put(2, take(size_t(R) * kCW * sizeof(df), 8));                   // wS
-  put(3, take(size_t(R) * sizeof(df) * 2, 8));                     // rowS, rowInv
-  put(4, take(size_t(kVsCap) * sizeof(df), 16));                   // vector sums
-  put(5, take(size_t(2) * kMaxCluster * xc_floats(R) * 4, 16));    // exchange slots
-  put(6, take(size_t(R) * kCW * 4 * 2, 4));                        // wM, wBad
-  put(7, take(size_t(R) * 4 * 3, 4));                              // rowM, rowKc, rowOK
-  put(8, take(256 * 4 * 2, 4));                                    // exp2 table
-  return align_up(o, 128);
+  put(0, take(2 * kStages * 8, 8));
+  put(1, take(kStages * sizeof(ChunkMeta), 16));
+  put(2, take(kStages * sizeof(QTask), 16));
+  put(3, take(sizeof(Misc), 16));
+  put(4, take(size_t(R) * kCW * sizeof(df), 8));
+  put(5, take(size_t(R) * sizeof(df) * 2, 8));
+  put(6, take(size_t(R) * kCW * 8, 4));
+  put(7, take(size_t(R) * 8, 4));
+  put(8, take(256 * 8, 4));
+  return al(o, 128);
 }
 
 __host__ __device__ inline size_t sample_smem_bytes(int R) { return carve(R, [](int, size_t) {}); }
 
-__device__ inline Layout make_layout(uint8_t* base, int R) {
-  Layout L;
+__device__ inline Smem make_smem(uint8_t* base, int R) {
+  Smem L;
   L.ring.buf = base;
-  L.xc.slot = xc_floats(R);
   carve(R, [&](int id, size_t at) {
     uint8_t* p = base + at;
     switch (id) {
       case 0:
         L.ring.full = reinterpret_cast<uint64_t*>(p);
         L.ring.empty = L.ring.full + kStages;
-        L.xc.bar = L.ring.empty + kStages;
         break;
       case 1:
+        L.ring.meta = reinterpret_cast<ChunkMeta*>(p);
+        break;
+      case 2:
+        L.ring.ttab = reinterpret_cast<QTask*>(p);
+        break;
+      case 3:
         L.misc = reinterpret_cast<Misc*>(p);
         L.ring.abort = &L.misc->abort;
         break;
-      case 2:
+      case 4:
         L.wS = reinterpret_cast<df*>(p);
         break;
-      case 3:
+      case 5:
         L.rowS = reinterpret_cast<df*>(p);
         L.rowInv = L.rowS + R;
-        break;
-      case 4:
-        L.vsd = reinterpret_cast<df*>(p);
-        break;
-      case 5:
-        L.xc.buf = reinterpret_cast<float*>(p);
         break;
       case 6:
         L.wM = reinterpret_cast<float*>(p);
         L.wBad = reinterpret_cast<int*>(L.wM + R * kCW);
         break;
       case 7:
-        L.rowM = reinterpret_cast<float*>(p);
-        L.rowKc = L.rowM + R;
+        L.rowKc = reinterpret_cast<float*>(p);
         L.rowOK = reinterpret_cast<int*>(L.rowKc + R);
         break;
       case 8:
@@ -168,49 +176,32 @@ __device__ inline Layout make_layout(uint8_t* base, int R) {
   return L;
 }
 
-// ------------------------------------------------------------------ arguments
-struct Bounds {
-  float ex2;     // relative error bound of ex2.approx.ftz.f32 on [-126, 1]
-  float gamma1;  // relative error bound of the pass-1 fp32 summation
-  float xbar;    // bound on sum_v q_v |x_v| before the row is swept (log2 V + 2)
-};
-
-struct SampleArgs {
-  const void* target;
-  const void* draft;
-  const int32_t* tokens;
-  const float* uniforms;
-  int B, K, V;
-  float c;         // fl32(log2(e) / T)
-  float Chi, Clo;  // log2(e) / T as a float pair
-  Bounds bd;
-  int32_t* out_tokens;
-  int32_t* out_n;
-  int32_t* err;
-  int32_t* row_info;
-  float* q_at_d;
-  float* p_at_d;
-};
-
-enum { kAccept = 0, kReject = 1, kAmbiguous = 2, kInvalid = 3 };
-
-// ------------------------------------------------------------------ pass-1 statistics
+// ------------------------------------------------------------------ statistics
 // Per-thread running max M, integer offset Kc = ceil(M c) and S = sum exp2(z c - Kc).
 template <class E>
 struct StatOp {
-  float c;
-  float M, Kc, S;
+  float c, M, Kc, S;
   int bad;
-  int row_base;
-  const Layout* L;
-  __device__ void begin_row(int) {
+  __device__ __forceinline__ void begin() {
     M = -INFINITY;
     Kc = -INFINITY;
     S = 0.0f;
     bad = 0;
   }
-  __device__ __forceinline__ void vec(const uint4& v, int) {
-    const float vm = E::vmax(v);
+  // The vectors i = tid, tid + kCons, ... < cnt of one ring stage (at most
+  // kPer per thread): loaded together, one running-maximum update per stage,
+  // then the exponentials, so the loads and MUFU operations overlap.
+  __device__ __forceinline__ void chunk(const uint4* buf, int cnt, int tid) {
+    constexpr int kPer = kChunk / 16 / kCons;
+    uint4 v[kPer];
+    float vm = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      if (tid + k * kCons < cnt) {
+        v[k] = buf[tid + k * kCons];
+        vm = max_nan(vm, E::vmax(v[k]));
+      }
+    }
     if (vm != vm) {
       bad = 1;
       return;
@@ -222,18 +213,24 @@ struct StatOp {
       Kc = Kn;
     }
     if (Kc == -INFINITY) return;  // only -inf logits so far
-    float z[E::kVec];
-    E::unpack(v, z);
-    float e[E::kVec];
 #pragma unroll
-    for (int k = 0; k < E::kVec; ++k) e[k] = ex2_approx(__fmaf_rn(z[k], c, -Kc));
+    for (int k = 0; k < kPer; ++k) {
+      if (tid + k * kCons < cnt) {
+        float z[E::kVec];
+        E::unpack(v[k], z);
+        float e[E::kVec];
 #pragma unroll
-    for (int w = 1; w < E::kVec; w <<= 1)
+        for (int j = 0; j < E::kVec; ++j) e[j] = ex2_approx(__fmaf_rn(z[j], c, -Kc));
 #pragma unroll
-      for (int k = 0; k < E::kVec; k += 2 * w) e[k] = __fadd_rn(e[k], e[k + w]);
-    S = __fadd_rn(S, e[0]);
+        for (int w = 1; w < E::kVec; w <<= 1)
+#pragma unroll
+          for (int j = 0; j < E::kVec; j += 2 * w) e[j] = __fadd_rn(e[j], e[j + w]);
+        S = __fadd_rn(S, e[0]);
+      }
+    }
   }
-  __device__ void end_row(int r) {
+  // warp partial of row r into smem
+  __device__ void end_row(const Smem& L, int r) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float Mw = warp_max_f(M);
     df s{0.f, 0.f};
@@ -241,19 +238,17 @@ struct StatOp {
     s = df_warp_sum(s);
     const int anybad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-      const int rr = row_base + r;
-      L->wM[rr * kCW + warp] = Mw;
-      L->wS[rr * kCW + warp] = s;
-      L->wBad[rr * kCW + warp] = anybad;
+      L.wM[r * kCW + warp] = Mw;
+      L.wS[r * kCW + warp] = s;
+      L.wBad[r * kCW + warp] = anybad;
     }
   }
 };
 
-// Consumers: the CTA partial (M, S.hi, S.lo, bad) of rows [r0, r1) into the
-// exchange payload at float offset 4*(r - r0).
-__device__ void stats_payload(const Layout& L, int r0, int r1, float c, float* out) {
+// CTA partial (M, S.hi, S.lo, bad) of rows [0, nrows) into out[4r..4r+3].
+__device__ void stats_to_global(const Smem& L, int nrows, float c, float* out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = r0 + warp; r < r1; r += kCW) {
+  for (int r = warp; r < nrows; r += kCW) {
     const float m = lane < kCW ? L.wM[r * kCW + lane] : -INFINITY;
     df s = lane < kCW ? L.wS[r * kCW + lane] : df{0.f, 0.f};
     const int bw = lane < kCW ? L.wBad[r * kCW + lane] : 0;
@@ -265,7 +260,7 @@ __device__ void stats_payload(const Layout& L, int r0, int r1, float c, float* o
     s = df_warp_sum(s);
     const int bad = __any_sync(0xffffffffu, bw);
     if (lane == 0) {
-      float* o = out + 4 * (r - r0);
+      float* o = out + 4 * r;
       o[0] = Mc;
       o[1] = s.hi;
       o[2] = s.lo;
@@ -274,64 +269,31 @@ __device__ void stats_payload(const Layout& L, int r0, int r1, float c, float* o
   }
 }
 
-// Final statistics of rows [r0, r1) from the gathered payloads of exchange e
-// (same values, same order in every CTA: bit-identical results everywhere).
-__device__ void stats_final(const Layout& L, uint32_t e, int r0, int r1, float c, int csize) {
-  for (int r = r0 + int(threadIdx.x); r < r1; r += kCons) {
-    const int o = 4 * (r - r0);
-    float M = -INFINITY;
-    int bad = 0;
-    for (int q = 0; q < csize; ++q) {
-      const float* s = xc_slot(L.xc, e, q) + o;
-      M = fmaxf(M, s[0]);
-      bad |= __float_as_int(s[3]);
-    }
-    const float Kc = offset_of(M, c);
-    df S{0.f, 0.f};
-    for (int q = 0; q < csize; ++q) {
-      const float* s = xc_slot(L.xc, e, q) + o;
-      if (s[1] != 0.0f) {
-        const float sc = pow2i(__fsub_rn(offset_of(s[0], c), Kc));
-        S = df_add(S, df{__fmul_rn(s[1], sc), __fmul_rn(s[2], sc)});
-      }
-    }
-    const bool ok = !bad && isfinite(M) && fabsf(Kc) < 4194304.0f && S.hi > 0.0f && isfinite(S.hi);
-    L.rowM[r] = M;
-    L.rowKc[r] = Kc;
-    L.rowS[r] = S;
-    L.rowInv[r] = ok ? df_recip(S) : df{0.f, 0.f};
-    L.rowOK[r] = ok ? 1 : 0;
+// Row statistics (into smem slot rs) from the S slice partials of row r at
+// float offset 4r of each slice's part block; same order everywhere.
+__device__ void stats_combine(const SampleArgs& a, const Smem& L, int b, int r, int rs) {
+  float M = -INFINITY;
+  int bad = 0;
+  for (int s = 0; s < a.S; ++s) {
+    const float* p = a.ws.part(b, s) + 4 * r;
+    M = fmaxf(M, ld_cg_f(p));
+    bad |= __float_as_int(ld_cg_f(p + 3));
   }
-}
-
-// Full statistics exchange of rows [r0, r1): payload, all-gather, final.
-__device__ bool stats_exchange(const Layout& L, uint32_t& e, int r0, int r1, float c, int crank,
-                               int csize, float* scratch) {
-  stats_payload(L, r0, r1, c, scratch);
-  consumers_sync();
-  if (threadIdx.x < 32) xc_push(L.xc, e, scratch, 4 * (r1 - r0), crank, csize);
-  const bool ok = xc_wait(L.xc, e, L.ring.abort);
-  if (ok) stats_final(L, e, r0, r1, c, csize);
-  ++e;
-  consumers_sync();
-  return ok;
-}
-
-// Statistics of one row slice read directly from global memory (bonus row).
-template <class E>
-__device__ void stats_direct(const typename E::T* row, int vbeg, int vend, StatOp<E>& op) {
-  const uint4* p = reinterpret_cast<const uint4*>(row);
-  op.begin_row(0);
-  for (int v0 = vbeg + int(threadIdx.x); v0 < vend; v0 += kCons * kUnroll) {
-    uint4 buf[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (v0 + u * kCons < vend) buf[u] = ldg_nc_v4(p + v0 + u * kCons);
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-      if (v0 + u * kCons < vend) op.vec(buf[u], v0 + u * kCons);
+  const float Kc = offset_of(M, a.c);
+  df S{0.f, 0.f};
+  for (int s = 0; s < a.S; ++s) {
+    const float* p = a.ws.part(b, s) + 4 * r;
+    const float sh = ld_cg_f(p + 1);
+    if (sh != 0.0f) {
+      const float sc = pow2i(__fsub_rn(offset_of(ld_cg_f(p), a.c), Kc));
+      S = df_add(S, df{__fmul_rn(sh, sc), __fmul_rn(ld_cg_f(p + 2), sc)});
+    }
   }
-  op.end_row(0);
+  const bool ok = !bad && isfinite(M) && fabsf(Kc) < 4194304.0f && S.hi > 0.0f && isfinite(S.hi);
+  L.rowKc[rs] = Kc;
+  L.rowS[rs] = S;
+  L.rowInv[rs] = ok ? df_recip(S) : df{0.f, 0.f};
+  L.rowOK[rs] = ok ? 1 : 0;
 }
 
 // ------------------------------------------------------------------ accurate path
@@ -344,88 +306,33 @@ __device__ __forceinline__ df acc_elem(float z, float Chi, float Clo, float Kc, 
   return df_exp2(s.hi, __fadd_rn(s.lo, pl), th, tl);
 }
 
-// Relative error bound of one normalised double-float term q_v or p_v: the
-// exponential (< 4e-13), its argument (< 2^-46 (|z C| + |Kc|) < 1e-12 for
-// offsets below 2^22, the row check), the normaliser sum and reciprocal
-// (< 1e-12); kept above their total.
+// Relative error bound of one normalised double-float term: the exponential
+// (< 4e-13), its argument (< 2^-46 (|z C| + |Kc|), offsets below 2^22 by the
+// row checks), the normaliser sum and reciprocal; kept above their total.
 constexpr float kAccRho = 4e-12f;
 
-__device__ inline void load_table(const Layout& L) {
+// Upper bound on the sum of the computed fp32 probabilities of a row.
+constexpr float kQmax = 1.001f;
+
+__device__ inline void load_table(const Smem& L) {
   for (int i = threadIdx.x; i < 256; i += kCons) {
     L.tab_hi[i] = kExp2Tab.hi[i];
     L.tab_lo[i] = kExp2Tab.lo[i];
   }
 }
 
-// Accurate sum_v 2^(z_v C - Kc) over the whole row for up to two rows (row1
-// may be null). Consumers only; every CTA returns the same pairs.
-template <class E>
-__device__ bool acc_norms(const Layout& L, uint32_t& e, const typename E::T* row0, float Kc0,
-                          const typename E::T* row1, float Kc1, int vbeg, int vend,
-                          const SampleArgs& a, int crank, int csize, df* out) {
-  Misc& ms = *L.misc;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  df a0{0.f, 0.f}, a1{0.f, 0.f};
-  const uint4* p0 = reinterpret_cast<const uint4*>(row0);
-  const uint4* p1 = reinterpret_cast<const uint4*>(row1);
-  for (int vi = vbeg + tid; vi < vend; vi += kCons) {
-    float z[E::kVec];
-    E::unpack(ldg_nc_v4(p0 + vi), z);
-#pragma unroll
-    for (int k = 0; k < E::kVec; ++k)
-      a0 = df_add(a0, acc_elem(z[k], a.Chi, a.Clo, Kc0, L.tab_hi, L.tab_lo));
-    if (row1) {
-      E::unpack(ldg_nc_v4(p1 + vi), z);
-#pragma unroll
-      for (int k = 0; k < E::kVec; ++k)
-        a1 = df_add(a1, acc_elem(z[k], a.Chi, a.Clo, Kc1, L.tab_hi, L.tab_lo));
-    }
-  }
-  a0 = df_warp_sum(a0);
-  a1 = df_warp_sum(a1);
-  if (lane == 0) {
-    ms.scan[warp] = a0;
-    ms.wR[warp] = a1;
-  }
-  consumers_sync();
-  if (tid == 0) {
-    df s0{0.f, 0.f}, s1{0.f, 0.f};
-    for (int w = 0; w < kCW; ++w) {
-      s0 = df_add(s0, ms.scan[w]);
-      s1 = df_add(s1, ms.wR[w]);
-    }
-    ms.src[0] = s0.hi;
-    ms.src[1] = s0.lo;
-    ms.src[2] = s1.hi;
-    ms.src[3] = s1.lo;
-  }
-  consumers_sync();
-  if (tid < 32) xc_push(L.xc, e, ms.src, 4, crank, csize);
-  const bool ok = xc_wait(L.xc, e, L.ring.abort);
-  df t0{0.f, 0.f}, t1{0.f, 0.f};
-  for (int q = 0; q < csize; ++q) {
-    const float* s = xc_slot(L.xc, e, q);
-    t0 = df_add(t0, df{s[0], s[1]});
-    t1 = df_add(t1, df{s[2], s[3]});
-  }
-  out[0] = t0;
-  out[1] = t1;
-  ++e;
-  consumers_sync();
-  return ok;
-}
-
-// ------------------------------------------------------------------ final draw entries
-// fp32 path: r = max(0, q - p) with q = exp2(z c - Kc_q) / S_q (or r = q).
+// ------------------------------------------------------------------ draw entries
+// fp32 path: r = max(0, q - p), q = exp2(z c - Kq) * Rq (r = q when tp is
+// null). aq / ap accumulate sum q x and sum p x (x the exponent argument,
+// clamped at -1e4 so that masked logits add 0), from which the error bound
+// of the sweep follows.
 template <class E>
 struct FastEntries {
   const uint4* tq;
-  const uint4* tp;  // null: draw from q
+  const uint4* tp;
   float c, Kq, Rq, Kp, Rp;
-  // r[k] from loaded vectors; returns their pairwise fp32 sum and accumulates
-  // sum q, sum p, sum q|x|, sum p|x|.
   __device__ __forceinline__ float run(const uint4& vq, const uint4& vp, float (&r)[E::kVec],
-                                       float& qs, float& ps, float& aq, float& ap) const {
+                                       float& aq, float& ap) const {
     float zq[E::kVec], zp[E::kVec];
     E::unpack(vq, zq);
     if (tp) E::unpack(vp, zp);
@@ -433,13 +340,11 @@ struct FastEntries {
     for (int k = 0; k < E::kVec; ++k) {
       const float xa = __fmaf_rn(zq[k], c, -Kq);
       const float q = __fmul_rn(ex2_approx(xa), Rq);
-      qs = __fadd_rn(qs, q);
-      aq = __fmaf_rn(q, fminf(fabsf(xa), 1.0e4f), aq);
+      aq = __fmaf_rn(q, fmaxf(xa, -1.0e4f), aq);
       if (tp) {
         const float xb = __fmaf_rn(zp[k], c, -Kp);
         const float p = __fmul_rn(ex2_approx(xb), Rp);
-        ps = __fadd_rn(ps, p);
-        ap = __fmaf_rn(p, fminf(fabsf(xb), 1.0e4f), ap);
+        ap = __fmaf_rn(p, fmaxf(xb, -1.0e4f), ap);
         r[k] = fmaxf(__fsub_rn(q, p), 0.0f);
       } else {
         r[k] = q;
@@ -454,13 +359,12 @@ struct FastEntries {
       for (int k = 0; k < E::kVec; k += 2 * w) t[k] = __fadd_rn(t[k], t[k + w]);
     return t[0];
   }
-  // entries of vector vi as pairs, and the vector sum the sweep recorded
   __device__ __forceinline__ df entries(int vi, df (&rd)[E::kVec]) const {
     float r[E::kVec];
-    float a = 0.f, b = 0.f, cc = 0.f, d = 0.f;
+    float a0 = 0.f, a1 = 0.f;
     const uint4 vq = ldg_nc_v4(tq + vi);
     const uint4 vp = tp ? ldg_nc_v4(tp + vi) : vq;
-    const float vs = run(vq, vp, r, a, b, cc, d);
+    const float vs = run(vq, vp, r, a0, a1);
 #pragma unroll
     for (int k = 0; k < E::kVec; ++k) rd[k] = {r[k], 0.f};
     return {vs, 0.f};
@@ -473,7 +377,7 @@ struct AccEntries {
   const uint4* tq;
   const uint4* tp;
   float Chi, Clo, Kq, Kp;
-  df Iq, Ip;  // accurate 1/S of the two rows
+  df Iq, Ip;
   const float* th;
   const float* tl;
   __device__ __forceinline__ df run(const uint4& vq, const uint4& vp, df (&r)[E::kVec], float& qs,
@@ -499,255 +403,238 @@ struct AccEntries {
     return vs;
   }
   __device__ __forceinline__ df entries(int vi, df (&rd)[E::kVec]) const {
-    float a = 0.f, b = 0.f;
+    float a0 = 0.f, a1 = 0.f;
     const uint4 vq = ldg_nc_v4(tq + vi);
     const uint4 vp = tp ? ldg_nc_v4(tp + vi) : vq;
-    return run(vq, vp, rd, a, b);
+    return run(vq, vp, rd, a0, a1);
   }
 };
 
-// ------------------------------------------------------------------ draw search
-// Block-wide exclusive scan of one pair per consumer thread (in thread order).
-__device__ df block_excl_scan_df(Misc& ms, df v, df& total) {
+// ------------------------------------------------------------------ helpers
+template <class E>
+struct RowPtrs {
+  const typename E::T* tgt;
+  const typename E::T* drf;
+};
+
+template <class E>
+__device__ __forceinline__ RowPtrs<E> row_ptrs(const SampleArgs& a, int b) {
+  using T = typename E::T;
+  return {static_cast<const T*>(a.target) + size_t(b) * (a.K + 1) * a.V,
+          static_cast<const T*>(a.draft) + size_t(b) * a.K * a.V};
+}
+
+// Consumers: block sum of a per-thread pair and four floats (thread 0 gets
+// the totals).
+__device__ void cta_reduce(Misc& ms, df& r, float (&f)[4]) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  df inc = v;
+  r = df_warp_sum(r);
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const df y = df_shfl_up(inc, o);
-    if (lane >= o) inc = df_add(inc, y);
-  }
-  if (lane == 31) ms.scan[warp] = inc;
-  consumers_sync();
-  df pre{0.f, 0.f};
-  total = {0.f, 0.f};
-  for (int w = 0; w < kCW; ++w) {
-    if (w == warp) pre = total;
-    total = df_add(total, ms.scan[w]);
+  for (int j = 0; j < 4; ++j) f[j] = warp_sum_f(f[j]);
+  if (lane == 0) {
+    ms.wR[warp] = r;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) ms.wF[j][warp] = f[j];
   }
   consumers_sync();
-  return df_add(pre, df_sub(inc, v));
+  if (threadIdx.x == 0) {
+    r = {0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f[j] = 0.f;
+    for (int w = 0; w < kCW; ++w) {
+      r = df_add(r, ms.wR[w]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) f[j] += ms.wF[j][w];
+    }
+  }
 }
 
-// CTA ms.cs: find the entry holding t = ms.tstar, using the per-vector sums in
-// L.vsd (nv <= kVsCap) and recomputing only the vector that holds it. Thread
-// 0..kCons-1 call; the result lands in ms.token / ms.cert (certified iff both
-// boundaries are farther than 2E from t).
-template <int kVec, class Entries>
-__device__ void block_search(const Layout& L, int vbeg, int vend, const Entries& ent) {
-  Misc& ms = *L.misc;
-  const int tid = threadIdx.x;
-  const int nv = vend - vbeg;
-  const int seg = (nv + kCons - 1) / kCons;
-  const int s0 = min(nv, tid * seg), s1 = min(nv, s0 + seg);
-  df s{0.f, 0.f};
-  for (int i = s0; i < s1; ++i) s = df_add(s, L.vsd[i]);
-  df total;
-  const df excl = block_excl_scan_df(ms, s, total);
-  const df lo = df_add(ms.base, excl);
-  const df hi = df_add(lo, s);
-  const df t = ms.tstar;
-  // first thread whose segment ends past t; else the last thread with mass
-  if (tid == 0) ms.found = INT_MAX;
+// Consumers: publish the task's partials (already stored) and arrive on the
+// row's stage counter. Returns true in every thread when this CTA completed
+// the stage (then it must continue the row).
+__device__ bool arrive_row(const SampleArgs& a, Misc& ms, int b) {
+  __threadfence();
   consumers_sync();
-  if (s.hi > 0.0f && df_gt(hi, t)) atomicMin(&ms.found, tid);
-  consumers_sync();
-  if (ms.found == INT_MAX) {
-    if (tid == 0) ms.found = -1;
-    consumers_sync();
-    if (s.hi > 0.0f) atomicMax(&ms.found, tid);
-    consumers_sync();
-  }
-  if (tid == ms.found) {
-    // walk this segment's vectors, then the entries of the vector holding t
-    df cum = lo;
-    int vsel = -1, vlast = -1;
-    df vlo = lo, vlast_lo = lo;
-    for (int i = s0; i < s1; ++i) {
-      const df nx = df_add(cum, L.vsd[i]);
-      if (L.vsd[i].hi > 0.0f) {
-        vlast = i;
-        vlast_lo = cum;
-        if (df_gt(nx, t)) {
-          vsel = i;
-          vlo = cum;
-          break;
-        }
-      }
-      cum = nx;
+  if (threadIdx.x == 0) {
+    const uint32_t old = atomicAdd(&a.ws.row_cnt()[b], 1u);
+    const int last = (old == uint32_t(a.S) - 1);
+    if (last) {
+      a.ws.row_cnt()[b] = 0;  // the next stage counts from zero
+      __threadfence();
     }
-    if (vsel < 0) {
-      vsel = vlast;
-      vlo = vlast_lo;
-    }
-    int token = -1;
-    df tlo = vlo, thi = vlo;
-    if (vsel >= 0) {
-      df r[kVec];
-      ent.entries(vbeg + vsel, r);
-      df c0 = vlo;
-      int lastk = -1;
-      df llo = vlo, lhi = vlo;
-      for (int k = 0; k < kVec; ++k) {
-        const df c1 = df_add(c0, r[k]);
-        if (r[k].hi > 0.0f) {
-          lastk = k;
-          llo = c0;
-          lhi = c1;
-          if (token < 0 && df_gt(c1, t)) {
-            token = (vbeg + vsel) * kVec + k;
-            tlo = c0;
-            thi = c1;
-          }
-        }
-        c0 = c1;
-      }
-      if (token < 0 && lastk >= 0) {
-        token = (vbeg + vsel) * kVec + lastk;
-        tlo = llo;
-        thi = lhi;
-      }
-    }
-    const float m1 = df_sub(t, tlo).hi, m2 = df_sub(thi, t).hi;
-    ms.token = token;
-    ms.cert = (token >= 0 && fminf(m1, m2) > 2.02f * ms.E) ? 1 : 0;
+    ms.last = last;
   }
   consumers_sync();
+  return ms.last != 0;
 }
 
-// CTA ms.cs when its slice exceeds the vector-sum buffer: warp 0 walks the
-// whole slice (lanes on consecutive vectors) for the entry holding t.
-template <int kVec, class Entries>
-__device__ void warp_walk_search(const Layout& L, int vbeg, int vend, const Entries& ent) {
-  Misc& ms = *L.misc;
+__device__ void write_outputs(const SampleArgs& a, const Misc& ms, int b, int n, int token,
+                              int flags, bool error) {
+  const int K = a.K;
+  for (int i = threadIdx.x; i <= K; i += kCons) {
+    int32_t v;
+    if (error) v = -1;
+    else if (i < n) v = ms.tok[i];
+    else if (i == n) v = token;
+    else v = -1;
+    a.out_tokens[size_t(b) * (K + 1) + i] = v;
+  }
+  if (threadIdx.x == 0) {
+    a.out_n[b] = error ? -1 : n;
+    if (a.row_info) a.row_info[b] = flags;
+  }
+  __threadfence();
+  consumers_sync();
+  if (threadIdx.x == 0) atomicAdd(&a.ws.hdr()->rows_done, 1u);
+}
+
+// Locate the slice, then the 32-vector unit, holding t, then the entry (warp 0
+// walks the unit). ms.token / ms.cert receive the result; certified iff both
+// boundaries of the drawn entry are farther than 2E from t.
+template <class E, class Entries>
+__device__ void search_draw(const SampleArgs& a, Misc& ms, int b, const Entries& ent) {
   const int lane = threadIdx.x & 31;
   if (threadIdx.x < 32) {
     const df t = ms.tstar;
-    df base = ms.base;
-    int tokn = -1, lastk = -1;
-    df tlo = base, thi = base, llo = base, lhi = base;
-    for (int v0 = vbeg; v0 < vend && tokn < 0; v0 += 32) {
-      const int vi = v0 + lane;
-      df r[kVec];
-      df vs{0.f, 0.f};
-      if (vi < vend) {
-        vs = ent.entries(vi, r);
-      } else {
-#pragma unroll
-        for (int k = 0; k < kVec; ++k) r[k] = {0.f, 0.f};
-      }
-      df inc = vs;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const df y = df_shfl_up(inc, o);
-        if (lane >= o) inc = df_add(inc, y);
-      }
-      df c0 = df_add(base, df_sub(inc, vs));
-      int tk = -1, lk = -1;
-      df lo{0.f, 0.f}, hi{0.f, 0.f}, l0{0.f, 0.f}, l1{0.f, 0.f};
-#pragma unroll
-      for (int k = 0; k < kVec; ++k) {
-        const df c1 = df_add(c0, r[k]);
-        if (r[k].hi > 0.0f) {
-          lk = vi * kVec + k;
-          l0 = c0;
-          l1 = c1;
-          if (tk < 0 && df_gt(c1, t)) {
-            tk = vi * kVec + k;
-            lo = c0;
-            hi = c1;
-          }
+    // slice: lanes scan 32 slices at a time; the first slice with mass whose
+    // end passes t, else the last slice with mass (rounding fallback)
+    int ss = -1;
+    df pre_s{0.f, 0.f};
+    {
+      df sbase{0.f, 0.f};
+      for (int s0 = 0; s0 < a.S; s0 += 32) {
+        const int s = s0 + lane;
+        df x{0.f, 0.f};
+        if (s < a.S) {
+          const float* p = a.ws.part(b, s);
+          x = df{ld_cg_f(p), ld_cg_f(p + 1)};
         }
-        c0 = c1;
+        df inc = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const df y = df_shfl_up(inc, o);
+          if (lane >= o) inc = df_add(inc, y);
+        }
+        const df lo = df_add(sbase, df_sub(inc, x));
+        const unsigned hm = __ballot_sync(0xffffffffu, x.hi > 0.0f && df_gt(df_add(lo, x), t));
+        const unsigned pm = __ballot_sync(0xffffffffu, x.hi > 0.0f);
+        if (hm) {
+          const int l = __ffs(int(hm)) - 1;
+          ss = s0 + l;
+          pre_s = df_shfl(lo, l);
+          break;
+        }
+        if (pm) {
+          const int l = 31 - __clz(int(pm));
+          ss = s0 + l;
+          pre_s = df_shfl(lo, l);
+        }
+        sbase = df_add(sbase, df_shfl(inc, 31));
       }
-      const unsigned hit = __ballot_sync(0xffffffffu, tk >= 0);
-      if (hit) {
-        const int l = __ffs(int(hit)) - 1;
-        tokn = __shfl_sync(0xffffffffu, tk, l);
-        tlo = df_shfl(lo, l);
-        thi = df_shfl(hi, l);
-      }
-      const unsigned has = __ballot_sync(0xffffffffu, lk >= 0);
-      if (has) {
-        const int l = 31 - __clz(int(has));
-        lastk = __shfl_sync(0xffffffffu, lk, l);
-        llo = df_shfl(l0, l);
-        lhi = df_shfl(l1, l);
-      }
-      base = df_add(base, df_shfl(inc, 31));
     }
-    if (tokn < 0) {
-      tokn = lastk;
-      tlo = llo;
-      thi = lhi;
+    int token = -1;
+    df tlo = pre_s, thi = pre_s;
+    if (ss >= 0) {
+      int v0, v1;
+      slice_range(a.nvec, a.S, ss, v0, v1);
+      const int nu = (v1 - v0 + 31) / 32;
+      // unit: lanes scan 32 units at a time
+      const float2* up = a.ws.units(b, ss);
+      int us = -1;
+      df ubase = pre_s, ubase_s = pre_s;
+      for (int u0 = 0; u0 < nu && us < 0; u0 += 32) {
+        const int u = u0 + lane;
+        df x{0.f, 0.f};
+        if (u < nu) x = df{__ldcg(&up[u].x), __ldcg(&up[u].y)};
+        df inc = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const df y = df_shfl_up(inc, o);
+          if (lane >= o) inc = df_add(inc, y);
+        }
+        const df lo = df_add(ubase, df_sub(inc, x));
+        const bool hit = x.hi > 0.0f && df_gt(df_add(lo, x), t);
+        const unsigned hm = __ballot_sync(0xffffffffu, hit);
+        const unsigned pm = __ballot_sync(0xffffffffu, u < nu && x.hi > 0.0f);
+        if (hm) {
+          const int l = __ffs(int(hm)) - 1;
+          us = u0 + l;
+          ubase_s = df_shfl(lo, l);
+        } else if (pm) {
+          const int l = 31 - __clz(int(pm));
+          ubase_s = df_shfl(lo, l);  // last unit with mass so far (rounding fallback)
+          us = -(u0 + l) - 2;
+        }
+        ubase = df_add(ubase, df_shfl(inc, 31));
+      }
+      if (us < -1) us = -us - 2;
+      if (us >= 0) {
+        // entries of the unit's 32 vectors, lane-minor
+        const int vi = v0 + us * 32 + lane;
+        df r[E::kVec];
+        df vs{0.f, 0.f};
+        if (vi < v1) {
+          vs = ent.entries(vi, r);
+        } else {
+#pragma unroll
+          for (int k = 0; k < E::kVec; ++k) r[k] = {0.f, 0.f};
+        }
+        df inc = vs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const df y = df_shfl_up(inc, o);
+          if (lane >= o) inc = df_add(inc, y);
+        }
+        df c0 = df_add(ubase_s, df_sub(inc, vs));
+        int tk = -1, lk = -1;
+        df lo{0.f, 0.f}, hi{0.f, 0.f}, l0{0.f, 0.f}, l1{0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < E::kVec; ++k) {
+          const df c1 = df_add(c0, r[k]);
+          if (r[k].hi > 0.0f) {
+            lk = vi * E::kVec + k;
+            l0 = c0;
+            l1 = c1;
+            if (tk < 0 && df_gt(c1, t)) {
+              tk = vi * E::kVec + k;
+              lo = c0;
+              hi = c1;
+            }
+          }
+          c0 = c1;
+        }
+        const unsigned hm = __ballot_sync(0xffffffffu, tk >= 0);
+        const unsigned pm = __ballot_sync(0xffffffffu, lk >= 0);
+        if (hm) {
+          const int l = __ffs(int(hm)) - 1;
+          token = __shfl_sync(0xffffffffu, tk, l);
+          tlo = df_shfl(lo, l);
+          thi = df_shfl(hi, l);
+        } else if (pm) {
+          const int l = 31 - __clz(int(pm));
+          token = __shfl_sync(0xffffffffu, lk, l);
+          tlo = df_shfl(l0, l);
+          thi = df_shfl(l1, l);
+        }
+      }
     }
     if (lane == 0) {
       const float m1 = df_sub(t, tlo).hi, m2 = df_sub(thi, t).hi;
-      ms.token = tokn;
-      ms.cert = (tokn >= 0 && fminf(m1, m2) > 2.02f * ms.E) ? 1 : 0;
+      ms.token = token;
+      ms.cert = (token >= 0 && fminf(m1, m2) > 2.02f * ms.E) ? 1 : 0;
     }
   }
   consumers_sync();
 }
 
-// Thread 0: locate the CTA holding t among the gathered CTA sums of exchange e
-// (floats 0, 1 of each slot).
-__device__ void locate_cta(const Layout& L, uint32_t e, int csize) {
-  Misc& ms = *L.misc;
-  int cs = -1;
-  df pre{0.f, 0.f}, pre_cs{0.f, 0.f};
-  for (int q = 0; q < csize; ++q) {
-    const float* s = xc_slot(L.xc, e, q);
-    const df x{s[0], s[1]};
-    const df nx = df_add(pre, x);
-    if (x.hi > 0.0f) {
-      cs = q;
-      pre_cs = pre;
-      if (df_gt(nx, ms.tstar)) break;
-    }
-    pre = nx;
-  }
-  ms.cs = cs;
-  ms.base = pre_cs;
-}
-
-// After a search: every CTA learns the token and its certification.
-__device__ bool publish_draw(const Layout& L, uint32_t& e, int crank, int csize, int& token,
-                             int& cert) {
-  Misc& ms = *L.misc;
-  if (threadIdx.x == 0) {
-    const bool mine = ms.go && ms.cs == crank;
-    ms.src[0] = __int_as_float(mine ? ms.token : -2);
-    ms.src[1] = __int_as_float(mine ? ms.cert : 0);
-  }
-  consumers_sync();
-  if (threadIdx.x < 32) xc_push(L.xc, e, ms.src, 2, crank, csize);
-  const bool ok = xc_wait(L.xc, e, L.ring.abort);
-  token = -1;
-  cert = 0;
-  for (int q = 0; q < csize; ++q) {
-    const float* s = xc_slot(L.xc, e, q);
-    if (__float_as_int(s[0]) != -2) {
-      token = __float_as_int(s[0]);
-      cert = __float_as_int(s[1]);
-    }
-  }
-  ++e;
-  consumers_sync();
-  return ok;
-}
-
-// ------------------------------------------------------------------ one row
+// ------------------------------------------------------------------ stage finishers
+// P1 complete: statistics of the 2K rows, accept tests, first rejection.
 template <class E>
-__device__ void verify_row(const SampleArgs& a, const Layout& L, int b, int vbeg, int vend,
-                           int crank, int csize, uint32_t& it, uint32_t& e) {
-  using T = typename E::T;
+__device__ void finish_p1(const SampleArgs& a, const Smem& L, int b) {
   Misc& ms = *L.misc;
-  const int K = a.K, V = a.V;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const T* tgt = static_cast<const T*>(a.target) + size_t(b) * (K + 1) * V;
-  const T* drf = static_cast<const T*>(a.draft) + size_t(b) * K * V;
-  const float c = a.c;
-
+  const int K = a.K, V = a.V, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const RowPtrs<E> rp = row_ptrs<E>(a, b);
+  for (int r = tid; r < 2 * K; r += kCons) stats_combine(a, L, b, r, r);
   if (warp == 1) {
     int bad = 0;
     if (lane < K) {
@@ -758,26 +645,16 @@ __device__ void verify_row(const SampleArgs& a, const Layout& L, int b, int vbeg
         ms.zt_d[lane] = 0.f;
         ms.zd_d[lane] = 0.f;
       } else {
-        ms.zt_d[lane] = E::load(tgt + size_t(lane) * V, d);
-        ms.zd_d[lane] = E::load(drf + size_t(lane) * V, d);
+        ms.zt_d[lane] = E::load(rp.tgt + size_t(lane) * V, d);
+        ms.zd_d[lane] = E::load(rp.drf + size_t(lane) * V, d);
       }
     }
     if (lane <= K) ms.u[lane] = a.uniforms[size_t(b) * (K + 1) + lane];
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) ms.bad_token = bad;
   }
-
-  // ---------------------------------------------------------------- pass 1
-  StatOp<E> op;
-  op.c = c;
-  op.row_base = 0;
-  op.L = &L;
-  it = consume_rows(L.ring, it, 2 * K, vbeg, vend, op);
   consumers_sync();
-  float* scratch = reinterpret_cast<float*>(L.vsd);  // payload staging (vsd is free here)
-  bool alive = stats_exchange(L, e, 0, 2 * K, c, crank, csize, scratch);
-
-  // ---------------------------------------------------------------- accept tests
+  const float c = a.c;
   if (warp == 0 && lane < K) {
     const int i = lane, rt = 2 * i, rd = 2 * i + 1;
     int st;
@@ -798,7 +675,7 @@ __device__ void verify_row(const SampleArgs& a, const Layout& L, int b, int vbeg
         st = kAccept;  // 0 < q(d)/p(d) whenever q(d) > 0
       } else {
         // ratio = 2^(xt - xd) * S_d / S_t; relative error bound: exp2, the
-        // arguments (with the fp32 temperature constant), both row sums, and
+        // arguments (with the fp32 temperature constant), both row sums and
         // five roundings
         const float ar = __fsub_rn(xt, xd);
         const float ratio = __fmul_rn(__fmul_rn(ex2_approx(ar), L.rowS[rd].hi), L.rowInv[rt].hi);
@@ -819,39 +696,64 @@ __device__ void verify_row(const SampleArgs& a, const Layout& L, int b, int vbeg
     ms.acc_state[i] = st;
     ms.qd[i] = qd;
     ms.pd[i] = pd;
+    if (a.q_at_d) {
+      a.q_at_d[size_t(b) * K + i] = qd;
+      a.p_at_d[size_t(b) * K + i] = pd;
+    }
   }
   consumers_sync();
 
   int flags = 0, n = 0;
-  bool error = ms.bad_token != 0 || !alive;
+  bool error = ms.bad_token != 0;
   while (!error) {
     int i = n;
     while (i < K && ms.acc_state[i] == kAccept) ++i;
-    if (i == K) {
-      n = K;
-      break;
-    }
-    const int st = ms.acc_state[i];
     n = i;
+    if (i == K) break;
+    const int st = ms.acc_state[i];
     if (st == kInvalid) {
       error = true;
       break;
     }
     if (st == kReject) break;
-    // ambiguous: decide with accurate row sums of target and draft row i
+    // ambiguous: decide with accurate sums of target and draft row i over the
+    // whole vocabulary (this CTA alone; probability ~1e-6 per test)
     flags |= SPEC_ROW_ACCEPT_REFINED;
     load_table(L);
     consumers_sync();
-    df S2[2];
-    alive = acc_norms<E>(L, e, tgt + size_t(i) * V, L.rowKc[2 * i], drf + size_t(i) * V,
-                         L.rowKc[2 * i + 1], vbeg, vend, a, crank, csize, S2);
-    if (!alive) {
-      error = true;
-      break;
+    df s0{0.f, 0.f}, s1{0.f, 0.f};
+    {
+      const uint4* p0 = reinterpret_cast<const uint4*>(rp.tgt + size_t(i) * V);
+      const uint4* p1 = reinterpret_cast<const uint4*>(rp.drf + size_t(i) * V);
+      const float K0 = L.rowKc[2 * i], K1 = L.rowKc[2 * i + 1];
+      for (int vi = tid; vi < a.nvec; vi += kCons) {
+        float z[E::kVec];
+        E::unpack(ldg_nc_v4(p0 + vi), z);
+#pragma unroll
+        for (int k = 0; k < E::kVec; ++k)
+          s0 = df_add(s0, acc_elem(z[k], a.Chi, a.Clo, K0, L.tab_hi, L.tab_lo));
+        E::unpack(ldg_nc_v4(p1 + vi), z);
+#pragma unroll
+        for (int k = 0; k < E::kVec; ++k)
+          s1 = df_add(s1, acc_elem(z[k], a.Chi, a.Clo, K1, L.tab_hi, L.tab_lo));
+      }
+      s0 = df_warp_sum(s0);
+      s1 = df_warp_sum(s1);
+      if (lane == 0) {
+        ms.wA[warp] = s0;
+        ms.wB[warp] = s1;
+      }
+      consumers_sync();
+      s0 = s1 = {0.f, 0.f};
+      for (int w = 0; w < kCW; ++w) {
+        s0 = df_add(s0, ms.wA[w]);
+        s1 = df_add(s1, ms.wB[w]);
+      }
     }
     // ratio = 2^((zt C - Kt) - (zd C - Kd)) * S_d / S_t in pair arithmetic
     const float zt = ms.zt_d[i], zd = ms.zd_d[i], u = ms.u[i];
-    const df xt = df_add_f(df_add(two_prod(zt, a.Chi), df{__fmul_rn(zt, a.Clo), 0.f}), -L.rowKc[2 * i]);
+    const df xt =
+        df_add_f(df_add(two_prod(zt, a.Chi), df{__fmul_rn(zt, a.Clo), 0.f}), -L.rowKc[2 * i]);
     const df xd =
         df_add_f(df_add(two_prod(zd, a.Chi), df{__fmul_rn(zd, a.Clo), 0.f}), -L.rowKc[2 * i + 1]);
     const df ar = df_sub(xt, xd);
@@ -861,317 +763,457 @@ __device__ void verify_row(const SampleArgs& a, const Layout& L, int b, int vbeg
     } else if (ar.hi < -126.0f) {
       acc = false;  // ratio < 2^-100 < u (u > 0 here)
     } else {
-      const df ratio =
-          df_mul(df_mul(df_exp2(ar.hi, ar.lo, L.tab_hi, L.tab_lo), S2[1]), df_recip(S2[0]));
+      const df ratio = df_mul(df_mul(df_exp2(ar.hi, ar.lo, L.tab_hi, L.tab_lo), s1), df_recip(s0));
       acc = (ratio.hi >= 1.0f) || df_gt(ratio, df{u, 0.f});
       if (fabsf(__fsub_rn(u, fminf(1.0f, ratio.hi))) <= 1e-10f * ratio.hi) flags |= SPEC_ROW_UNCERTIFIED;
     }
+    consumers_sync();
     if (!acc) break;
     if (tid == 0) ms.acc_state[i] = kAccept;
     consumers_sync();
     n = i + 1;
   }
-
-  // ---------------------------------------------------------------- final draw
-  int token = -1;
-  if (!error) {
-    const bool bonus = (n == K);
-    const int rq = bonus ? 2 * K : 2 * n;
-    const int rpd = bonus ? -1 : 2 * n + 1;
-    if (bonus) {
-      StatOp<E> opk;
-      opk.c = c;
-      opk.row_base = 2 * K;
-      opk.L = &L;
-      stats_direct<E>(tgt + size_t(K) * V, vbeg, vend, opk);
-      consumers_sync();
-      alive = stats_exchange(L, e, 2 * K, 2 * K + 1, c, crank, csize, scratch);
-      if (!alive || !L.rowOK[2 * K]) error = true;
-    }
-    if (!error) {
-      const int jrow = bonus ? K : n;
-      const uint4* vq = reinterpret_cast<const uint4*>(tgt + size_t(jrow) * V);
-      const uint4* vp = bonus ? nullptr : reinterpret_cast<const uint4*>(drf + size_t(n) * V);
-      const float uK = ms.u[K];
-      const int nv = vend - vbeg;
-      const bool keep = nv <= kVsCap;
-
-      // ---------------- fp32 sweep, per-vector sums kept for the search
-      FastEntries<E> fe;
-      fe.tq = vq;
-      fe.tp = vp;
-      fe.c = c;
-      fe.Kq = L.rowKc[rq];
-      fe.Rq = L.rowInv[rq].hi;
-      fe.Kp = bonus ? 0.f : L.rowKc[rpd];
-      fe.Rp = bonus ? 0.f : L.rowInv[rpd].hi;
-      {
-        df acc{0.f, 0.f};
-        float Q = 0.f, P = 0.f, Aq = 0.f, Ap = 0.f;
-        for (int v0 = vbeg + tid; v0 < vend; v0 += kCons * kUnroll) {
-          uint4 bq[kUnroll], bp[kUnroll];
-#pragma unroll
-          for (int u = 0; u < kUnroll; ++u) {
-            const int vi = v0 + u * kCons;
-            if (vi < vend) {
-              bq[u] = ldg_nc_v4(vq + vi);
-              bp[u] = vp ? ldg_nc_v4(vp + vi) : bq[u];
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < kUnroll; ++u) {
-            const int vi = v0 + u * kCons;
-            if (vi < vend) {
-              float r[E::kVec];
-              const float vs = fe.run(bq[u], bp[u], r, Q, P, Aq, Ap);
-              if (keep) L.vsd[vi - vbeg] = {vs, 0.f};
-              acc = df_add_f(acc, vs);
-            }
-          }
-        }
-        acc = df_warp_sum(acc);
-        Q = warp_sum_f(Q);
-        P = warp_sum_f(P);
-        Aq = warp_sum_f(Aq);
-        Ap = warp_sum_f(Ap);
-        if (lane == 0) {
-          ms.wR[warp] = acc;
-          ms.wQ[warp] = Q;
-          ms.wP[warp] = P;
-          ms.wAq[warp] = Aq;
-          ms.wAp[warp] = Ap;
-        }
-      }
-      consumers_sync();
-      if (tid == 0) {
-        df Rc{0.f, 0.f};
-        float Qc = 0.f, Pc = 0.f, Aqc = 0.f, Apc = 0.f;
-        for (int w = 0; w < kCW; ++w) {
-          Rc = df_add(Rc, ms.wR[w]);
-          Qc += ms.wQ[w];
-          Pc += ms.wP[w];
-          Aqc += ms.wAq[w];
-          Apc += ms.wAp[w];
-        }
-        ms.src[0] = Rc.hi;
-        ms.src[1] = Rc.lo;
-        ms.src[2] = Qc;
-        ms.src[3] = Pc;
-        ms.src[4] = Aqc;
-        ms.src[5] = Apc;
-      }
-      consumers_sync();
-      if (tid < 32) xc_push(L.xc, e, ms.src, 6, crank, csize);
-      alive = xc_wait(L.xc, e, L.ring.abort);
-      if (tid == 0) {
-        df Sr{0.f, 0.f};
-        float Qt = 0.f, Pt = 0.f, Aqt = 0.f, Apt = 0.f;
-        for (int q = 0; q < csize; ++q) {
-          const float* s = xc_slot(L.xc, e, q);
-          Sr = df_add(Sr, df{s[0], s[1]});
-          Qt += s[2];
-          Pt += s[3];
-          Aqt += s[4];
-          Apt += s[5];
-        }
-        // Error bound (probability units) of the fp32 sweep. Per term,
-        // relative: exp2 (ex2), argument rounding and the fp32 temperature
-        // constant (ln2 u |x| each), 1/S and the product (3u), and the row sum
-        // behind 1/S (ex2 + ln2 u sum q|x| + gamma1); weights q (resp. p).
-        auto side = [&](float Qs, float A) {
-          const float xb = A / fmaxf(Qs, 1e-30f) + 1.0f;
-          return 1.05f * fmaxf(Qs, 1.0f) *
-                 (2.0f * a.bd.ex2 + 3.0f * kU + a.bd.gamma1 + kLn2f * kU * 4.0f * xb);
-        };
-        const float E = side(Qt, Aqt) + (bonus ? 0.f : side(Pt, Apt)) + 5.0f * kU * Sr.hi + 1e-30f;
-        ms.E = E;
-        ms.tstar = df_mul_f(Sr, uK);
-        ms.go = (alive && Sr.hi > 2.0f * E) ? 1 : 0;
-        if (ms.go) locate_cta(L, e, csize);
-      }
-      ++e;
-      consumers_sync();
-      if (ms.go && ms.cs == crank) {
-        if (keep) block_search<E::kVec>(L, vbeg, vend, fe);
-        else warp_walk_search<E::kVec>(L, vbeg, vend, fe);
-      }
-      consumers_sync();
-      int cert = 0;
-      alive = publish_draw(L, e, crank, csize, token, cert) && alive;
-      if (!alive) error = true;
-
-      if (!error && !cert) {
-        // ---------------- double-float path
-        flags |= SPEC_ROW_SAMPLE_REFINED;
-        load_table(L);
-        consumers_sync();
-        df S2[2];
-        alive = acc_norms<E>(L, e, tgt + size_t(jrow) * V, L.rowKc[rq],
-                             bonus ? nullptr : drf + size_t(n) * V, bonus ? 0.f : L.rowKc[rpd],
-                             vbeg, vend, a, crank, csize, S2);
-        AccEntries<E> ae;
-        ae.tq = vq;
-        ae.tp = vp;
-        ae.Chi = a.Chi;
-        ae.Clo = a.Clo;
-        ae.Kq = L.rowKc[rq];
-        ae.Kp = bonus ? 0.f : L.rowKc[rpd];
-        ae.Iq = df_recip(S2[0]);
-        ae.Ip = bonus ? df{0.f, 0.f} : df_recip(S2[1]);
-        ae.th = L.tab_hi;
-        ae.tl = L.tab_lo;
-        for (int pass = 0; pass < 2 && alive; ++pass) {
-          df acc{0.f, 0.f};
-          float Q = 0.f, P = 0.f;
-          for (int v0 = vbeg + tid; v0 < vend; v0 += kCons * kUnroll) {
-            uint4 bq[kUnroll], bp[kUnroll];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-              const int vi = v0 + u * kCons;
-              if (vi < vend) {
-                bq[u] = ldg_nc_v4(vq + vi);
-                bp[u] = ae.tp ? ldg_nc_v4(vp + vi) : bq[u];
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-              const int vi = v0 + u * kCons;
-              if (vi < vend) {
-                df r[E::kVec];
-                const df vs = ae.run(bq[u], bp[u], r, Q, P);
-                if (keep) L.vsd[vi - vbeg] = vs;
-                acc = df_add(acc, vs);
-              }
-            }
-          }
-          acc = df_warp_sum(acc);
-          Q = warp_sum_f(Q);
-          P = warp_sum_f(P);
-          if (lane == 0) {
-            ms.wR[warp] = acc;
-            ms.wQ[warp] = Q;
-            ms.wP[warp] = P;
-          }
-          consumers_sync();
-          if (tid == 0) {
-            df Rc{0.f, 0.f};
-            float Qc = 0.f, Pc = 0.f;
-            for (int w = 0; w < kCW; ++w) {
-              Rc = df_add(Rc, ms.wR[w]);
-              Qc += ms.wQ[w];
-              Pc += ms.wP[w];
-            }
-            ms.src[0] = Rc.hi;
-            ms.src[1] = Rc.lo;
-            ms.src[2] = Qc;
-            ms.src[3] = Pc;
-          }
-          consumers_sync();
-          if (tid < 32) xc_push(L.xc, e, ms.src, 4, crank, csize);
-          alive = xc_wait(L.xc, e, L.ring.abort);
-          if (tid == 0) {
-            df Sr{0.f, 0.f};
-            float Qt = 0.f, Pt = 0.f;
-            for (int q = 0; q < csize; ++q) {
-              const float* s = xc_slot(L.xc, e, q);
-              Sr = df_add(Sr, df{s[0], s[1]});
-              Qt += s[2];
-              Pt += s[3];
-            }
-            ms.zero_res = (Sr.hi == 0.0f && ae.tp != nullptr) ? 1 : 0;
-            ms.E = kAccRho * (Qt + Pt) + 1e-14f * Sr.hi + 1e-36f;
-            ms.tstar = df_mul_f(Sr, uK);
-            ms.go = (alive && Sr.hi > 0.0f) ? 1 : 0;
-            if (ms.go) locate_cta(L, e, csize);
-          }
-          ++e;
-          consumers_sync();
-          if (ms.zero_res) {
-            // zero residual mass: the draw uses q_j itself
-            flags |= SPEC_ROW_ZERO_RESIDUAL;
-            ae.tp = nullptr;
-            continue;
-          }
-          if (ms.go && ms.cs == crank) {
-            if (keep) block_search<E::kVec>(L, vbeg, vend, ae);
-            else warp_walk_search<E::kVec>(L, vbeg, vend, ae);
-          }
-          consumers_sync();
-          alive = publish_draw(L, e, crank, csize, token, cert) && alive;
-          if (!ms.go || !cert) flags |= SPEC_ROW_UNCERTIFIED;
-          break;
-        }
-        if (token < 0 || !alive) error = true;
-      }
-    }
+  if (error) {
+    if (tid == 0 && a.err) atomicOr(a.err, ms.bad_token ? SPEC_DERR_TOKEN : SPEC_DERR_LOGITS);
+    write_outputs(a, ms, b, n, -1, flags, true);
+    return;
   }
-
-  // ---------------------------------------------------------------- outputs
-  if (crank == 0) {
-    if (tid <= K) {
-      int32_t v;
-      if (error) v = -1;
-      else if (tid < n) v = ms.tok[tid];
-      else if (tid == n) v = token;
-      else v = -1;
-      a.out_tokens[size_t(b) * (K + 1) + tid] = v;
+  if (tid == 0) {
+    RowState* st = a.ws.rowstate(b);
+    st->n = n;
+    st->flags = flags;
+    st->err = 0;
+    if (n < K) {
+      st->mode = kModeResidual;
+      st->Kq = L.rowKc[2 * n];
+      st->Rq = L.rowInv[2 * n].hi;
+      st->Kp = L.rowKc[2 * n + 1];
+      st->Rp = L.rowInv[2 * n + 1].hi;
+    } else {
+      st->mode = kModeQ;
     }
-    if (tid == 0) {
-      a.out_n[b] = error ? -1 : n;
-      if (a.row_info) a.row_info[b] = flags;
-      if (error && a.err) {
-        const int bit = *L.ring.abort ? SPEC_DERR_TIMEOUT
-                        : ms.bad_token ? SPEC_DERR_TOKEN
-                                       : SPEC_DERR_LOGITS;
-        atomicOr(a.err, bit);
-      }
-    }
-    if (warp == 0 && lane < K && a.q_at_d) {
-      a.q_at_d[size_t(b) * K + lane] = ms.qd[lane];
-      a.p_at_d[size_t(b) * K + lane] = ms.pd[lane];
-    }
+    __threadfence();
+    enqueue_row_stage(a.ws, n < K ? kSW : kBS, b, a.S, n);
   }
-  consumers_sync();  // the next row reuses every per-row buffer
 }
 
 // ------------------------------------------------------------------ kernel
 template <class E>
-__global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const SampleArgs a, int ncl) {
+__global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const SampleArgs a) {
   using T = typename E::T;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  const int K = a.K, V = a.V, R = 2 * K + 1;
-  const Layout L = make_layout(smem_raw, R);
-  const int crank = int(cluster_ctarank()), csize = int(cluster_nctarank());
-  const int cid = blockIdx.x / csize;
-  int vbeg, vend;
-  cta_slice(V / E::kVec, crank, csize, vbeg, vend);
-
-  ring_xc_init(L.ring, L.xc, csize);
+  const int K = a.K, R = 2 * K + 1;
+  const Smem L = make_smem(smem_raw, R);
+  Misc& ms = *L.misc;
+  ring_init(L.ring);
   __syncthreads();
-  cluster_sync();  // every CTA's barriers are initialised before any remote arrive
 
   if (threadIdx.x >= kCons) {
+    // ------------------------------------------------ producer
     if (threadIdx.x == kCons) {
-      uint32_t it = 0;
-      for (int b = cid; b < a.B; b += ncl) {
-        const T* tgt = static_cast<const T*>(a.target) + size_t(b) * (K + 1) * V;
-        const T* drf = static_cast<const T*>(a.draft) + size_t(b) * K * V;
-        auto rp = [&](int r) -> const T* {
-          const int i = r >> 1;
-          return (r & 1) ? drf + size_t(i) * V : tgt + size_t(i) * V;
-        };
-        it = produce_rows(L.ring, it, 2 * K, rp, vbeg, vend);
+      uint32_t it = 0, nt = 0;
+      uint64_t idle_t0 = 0;
+      int64_t pending = -1;
+      WsHeader* h = a.ws.hdr();
+      while (!*L.ring.abort && !ld_volatile_u32(&h->abort)) {
+        QTask t;
+        bool exhausted;
+        if (!fetch_task(a.ws, kP1, t, exhausted, pending)) {
+          if (!producer_idle(a.ws, exhausted, idle_t0)) break;
+          continue;
+        }
+        idle_t0 = 0;
+        const RowPtrs<E> rp = row_ptrs<E>(a, t.b);
+        int v0, v1;
+        slice_range(a.nvec, a.S, t.s, v0, v1);
+        const char* rows[2 * kMaxK];
+        int nrows = 0;
+        bool paired = false;
+        if (t.type == kP1) {
+          for (int i = 0; i < K; ++i) {
+            rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(i) * a.V);
+            rows[nrows++] = reinterpret_cast<const char*>(rp.drf + size_t(i) * a.V);
+          }
+        } else if (t.type == kBS) {
+          rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(K) * a.V);
+        } else {
+          const int n = t.aux & 0xff, mode = t.aux >> 8;
+          const int j = n;  // row j (j = K for the bonus draw)
+          rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(j) * a.V);
+          if (mode == kModeResidual && n < K) {
+            rows[nrows++] = reinterpret_cast<const char*>(rp.drf + size_t(j) * a.V);
+            paired = true;
+          }
+        }
+        if (!produce_task(L.ring, it, nt, t, rows, nrows, paired, v0, v1)) break;
       }
+      produce_end(L.ring, it);
     }
   } else {
-    uint32_t it = 0, e = 0;
-    for (int b = cid; b < a.B; b += ncl) verify_row<E>(a, L, b, vbeg, vend, crank, csize, it, e);
+    // ------------------------------------------------ consumers
+    uint32_t it = 0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    while (true) {
+      if (!wait_stage(L.ring, it)) break;
+      const ChunkMeta m0 = L.ring.meta[it % kStages];
+      if (m0.slot < 0) break;
+      const QTask t = L.ring.ttab[m0.slot];
+      const int b = t.b, s = t.s;
+      const RowPtrs<E> rp = row_ptrs<E>(a, b);
+      int v0, v1;
+      slice_range(a.nvec, a.S, s, v0, v1);
+      if (t.type == kP1 || t.type == kBS) {
+        // ---------------- statistics of the slice of every row of the task
+        StatOp<E> op;
+        op.c = a.c;
+        op.begin();
+        for (;;) {
+          const ChunkMeta m = L.ring.meta[it % kStages];
+          const uint4* buf = stage_data(L.ring, it);
+          op.chunk(buf, m.c1 - m.c0, tid);
+          release_stage(L.ring, it);
+          ++it;
+          if (m.last_k) {
+            op.end_row(L, m.r);
+            op.begin();
+          }
+          if (m.last) break;
+          if (!wait_stage(L.ring, it)) break;
+        }
+        consumers_sync();
+        const int nrows = (t.type == kP1) ? 2 * K : 1;
+        stats_to_global(L, nrows, a.c, a.ws.part(b, s));
+        if (arrive_row(a, ms, b)) {
+          if (t.type == kP1) {
+            finish_p1<E>(a, L, b);
+          } else {
+            // bonus statistics of target row K -> its draw
+            if (tid == 0) {
+              stats_combine(a, L, b, 0, 2 * K);
+              RowState* st = a.ws.rowstate(b);
+              if (!L.rowOK[2 * K]) {
+                st->err = 1;
+              } else {
+                st->Kq = L.rowKc[2 * K];
+                st->Rq = L.rowInv[2 * K].hi;
+              }
+            }
+            consumers_sync();
+            const RowState* st = a.ws.rowstate(b);
+            if (ld_cg_i(&st->err)) {
+              if (warp == 1 && lane < K) ms.tok[lane] = a.tokens[size_t(b) * K + lane];
+              consumers_sync();
+              if (tid == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
+              write_outputs(a, ms, b, K, -1, ld_cg_i(&st->flags), true);
+            } else if (tid == 0) {
+              __threadfence();
+              enqueue_row_stage(a.ws, kSW, b, a.S, K | (kModeQ << 8));
+            }
+          }
+        }
+        consumers_sync();
+        continue;
+      }
+      // ------------------------------------------------ draw stages
+      const RowState* stp = a.ws.rowstate(b);
+      const int n = t.aux & 0xff, mode = t.aux >> 8;
+      const bool pair = (mode == kModeResidual && n < K);
+      const int jrow = n;
+      const uint4* vq = reinterpret_cast<const uint4*>(rp.tgt + size_t(jrow) * a.V);
+      const uint4* vp = pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(jrow) * a.V) : nullptr;
+      if (t.type == kSW) {
+        FastEntries<E> fe;
+        fe.tq = vq;
+        fe.tp = vp;
+        fe.c = a.c;
+        fe.Kq = ld_cg_f(&stp->Kq);
+        fe.Rq = ld_cg_f(&stp->Rq);
+        fe.Kp = pair ? ld_cg_f(&stp->Kp) : 0.f;
+        fe.Rp = pair ? ld_cg_f(&stp->Rp) : 0.f;
+        constexpr int kPer = kChunk / 16 / kCons;
+        float accf = 0.f, Aq = 0.f, Ap = 0.f;
+        float2* units = a.ws.units(b, s);
+        for (;;) {
+          const ChunkMeta m = L.ring.meta[it % kStages];
+          const uint4* bq = stage_data(L.ring, it);
+          const uint4* bp = bq;
+          uint32_t it2 = it;
+          if (pair) {
+            if (!wait_stage(L.ring, it + 1)) break;
+            bp = stage_data(L.ring, it + 1);
+            it2 = it + 1;
+          }
+          const int cnt = m.c1 - m.c0;
+          // unit u of this stage = vectors [32u, 32u + 32): warp w takes units
+          // w, w + 8, ...; every lane one vector pair of each
+          float vs[kPer];
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            const int i = warp * 32 + k * kCons + lane;
+            vs[k] = 0.f;
+            if (i < cnt) {
+              float r[E::kVec];
+              vs[k] = fe.run(bq[i], bp[i], r, Aq, Ap);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < kPer; ++k) {
+            const int i0 = warp * 32 + k * kCons;
+            if (i0 < cnt) {
+              const float us = warp_sum_f(vs[k]);
+              if (lane == 0) units[(m.c0 - v0 + i0) / 32] = make_float2(us, 0.f);
+            }
+            accf = __fadd_rn(accf, vs[k]);
+          }
+          const bool lastc = L.ring.meta[it2 % kStages].last != 0;
+          release_stage(L.ring, it);
+          if (pair) release_stage(L.ring, it2);
+          it = it2 + 1;
+          if (lastc) break;
+          if (!wait_stage(L.ring, it)) break;
+        }
+        df acc{accf, 0.f};
+        float f4[4] = {Aq, Ap, 0.f, 0.f};
+        cta_reduce(ms, acc, f4);
+        if (tid == 0) {
+          float* o = a.ws.part(b, s);
+          o[0] = acc.hi;
+          o[1] = acc.lo;
+          o[2] = f4[0];
+          o[3] = f4[1];
+        }
+        if (arrive_row(a, ms, b)) {
+          // ---------------- fp32 draw: bound, locate, certify
+          if (tid == 0) {
+            df Sr{0.f, 0.f};
+            float Aqt = 0.f, Apt = 0.f;
+            for (int q = 0; q < a.S; ++q) {
+              const float* p = a.ws.part(b, q);
+              Sr = df_add(Sr, df{ld_cg_f(p), ld_cg_f(p + 1)});
+              Aqt += ld_cg_f(p + 2);
+              Apt += ld_cg_f(p + 3);
+            }
+            // Error bound (probability units) of the fp32 sweep. Per term,
+            // relative: exp2 (ex2), argument rounding and the fp32
+            // temperature constant (ln2 u |x| each), 1/S and the product
+            // (3u), and the row sum behind 1/S (ex2 + ln2 u sum q|x| +
+            // gamma1); summed with weights q (resp. p), whose sum is at most
+            // kQmax. sum q|x| <= kQmax/2 - sum q x, since x <= 1/4 (the offset
+            // is ceil of the rounded max * c, below 2^22 in magnitude).
+            // Rounding of the unit, slice and row sums adds 16 u Sr.
+            auto side = [&](float A) {
+              const float absx = 1.01f * fmaxf(0.0f, -A) + 0.5f * kQmax;
+              return 1.05f * (kQmax * (2.0f * a.bd.ex2 + 3.0f * kU + a.bd.gamma1 + 4.0f * kLn2f * kU) +
+                              4.0f * kLn2f * kU * absx);
+            };
+            const float E = side(Aqt) + (pair ? side(Apt) : 0.f) + 16.0f * kU * Sr.hi + 1e-30f;
+            ms.E = E;
+            ms.tstar = df_mul_f(Sr, a.uniforms[size_t(b) * (K + 1) + K]);
+            ms.found = (Sr.hi > 2.0f * E) ? 1 : 0;
+          }
+          consumers_sync();
+          if (ms.found) search_draw<E>(a, ms, b, fe);
+          const int flags = ld_cg_i(&stp->flags);
+          if (ms.found && ms.cert) {
+            if (warp == 1 && lane < K) ms.tok[lane] = a.tokens[size_t(b) * K + lane];
+            consumers_sync();
+            write_outputs(a, ms, b, n, ms.token, flags, false);
+          } else if (tid == 0) {
+            RowState* st = a.ws.rowstate(b);
+            st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
+            __threadfence();
+            enqueue_row_stage(a.ws, kFA, b, a.S, t.aux);
+          }
+        }
+        consumers_sync();
+        continue;
+      }
+      // ---------------- double-float stages (rare)
+      load_table(L);
+      consumers_sync();
+      if (t.type == kFA) {
+        df s0{0.f, 0.f}, s1{0.f, 0.f};
+        const float K0 = ld_cg_f(&stp->Kq), K1 = pair ? ld_cg_f(&stp->Kp) : 0.f;
+        for (;;) {
+          const ChunkMeta m = L.ring.meta[it % kStages];
+          const uint4* buf = stage_data(L.ring, it);
+          const float Kr = (m.r == 0) ? K0 : K1;
+          df acc{0.f, 0.f};
+          for (int i = tid; i < m.c1 - m.c0; i += kCons) {
+            float z[E::kVec];
+            E::unpack(buf[i], z);
+#pragma unroll
+            for (int k = 0; k < E::kVec; ++k)
+              acc = df_add(acc, acc_elem(z[k], a.Chi, a.Clo, Kr, L.tab_hi, L.tab_lo));
+          }
+          if (m.r == 0) s0 = df_add(s0, acc);
+          else s1 = df_add(s1, acc);
+          release_stage(L.ring, it);
+          ++it;
+          if (m.last) break;
+          if (!wait_stage(L.ring, it)) break;
+        }
+        s0 = df_warp_sum(s0);
+        s1 = df_warp_sum(s1);
+        if (lane == 0) {
+          ms.wA[warp] = s0;
+          ms.wB[warp] = s1;
+        }
+        consumers_sync();
+        if (tid == 0) {
+          df t0{0.f, 0.f}, t1{0.f, 0.f};
+          for (int w = 0; w < kCW; ++w) {
+            t0 = df_add(t0, ms.wA[w]);
+            t1 = df_add(t1, ms.wB[w]);
+          }
+          float* o = a.ws.part(b, s);
+          o[0] = t0.hi;
+          o[1] = t0.lo;
+          o[2] = t1.hi;
+          o[3] = t1.lo;
+        }
+        if (arrive_row(a, ms, b) && tid == 0) {
+          df S0{0.f, 0.f}, S1{0.f, 0.f};
+          for (int q = 0; q < a.S; ++q) {
+            const float* p = a.ws.part(b, q);
+            S0 = df_add(S0, df{ld_cg_f(p), ld_cg_f(p + 1)});
+            S1 = df_add(S1, df{ld_cg_f(p + 2), ld_cg_f(p + 3)});
+          }
+          RowState* st = a.ws.rowstate(b);
+          const df I0 = df_recip(S0);
+          st->Iq_hi = I0.hi;
+          st->Iq_lo = I0.lo;
+          if (pair) {
+            const df I1 = df_recip(S1);
+            st->Ip_hi = I1.hi;
+            st->Ip_lo = I1.lo;
+          }
+          __threadfence();
+          enqueue_row_stage(a.ws, kFB, b, a.S, t.aux);
+        }
+        consumers_sync();
+        continue;
+      }
+      // kFB: double-float residual sums and unit sums
+      AccEntries<E> ae;
+      ae.tq = vq;
+      ae.tp = vp;
+      ae.Chi = a.Chi;
+      ae.Clo = a.Clo;
+      ae.Kq = ld_cg_f(&stp->Kq);
+      ae.Kp = pair ? ld_cg_f(&stp->Kp) : 0.f;
+      ae.Iq = df{ld_cg_f(&stp->Iq_hi), ld_cg_f(&stp->Iq_lo)};
+      ae.Ip = pair ? df{ld_cg_f(&stp->Ip_hi), ld_cg_f(&stp->Ip_lo)} : df{0.f, 0.f};
+      ae.th = L.tab_hi;
+      ae.tl = L.tab_lo;
+      {
+        df acc{0.f, 0.f};
+        float Q = 0.f, P = 0.f;
+        float2* units = a.ws.units(b, s);
+        for (;;) {
+          const ChunkMeta m = L.ring.meta[it % kStages];
+          const uint4* bq = stage_data(L.ring, it);
+          const uint4* bp = bq;
+          uint32_t it2 = it;
+          if (pair) {
+            if (!wait_stage(L.ring, it + 1)) break;
+            bp = stage_data(L.ring, it + 1);
+            it2 = it + 1;
+          }
+          const int cnt = m.c1 - m.c0;
+          for (int i0 = warp * 32; i0 < cnt; i0 += kCons) {
+            const int i = i0 + lane;
+            df vs{0.f, 0.f};
+            if (i < cnt) {
+              df r[E::kVec];
+              vs = ae.run(bq[i], bp[i], r, Q, P);
+              acc = df_add(acc, vs);
+            }
+            const df us = df_warp_sum(vs);
+            if (lane == 0) units[(m.c0 - v0 + i0) / 32] = make_float2(us.hi, us.lo);
+          }
+          const bool lastc = L.ring.meta[it2 % kStages].last != 0;
+          release_stage(L.ring, it);
+          if (pair) release_stage(L.ring, it2);
+          it = it2 + 1;
+          if (lastc) break;
+          if (!wait_stage(L.ring, it)) break;
+        }
+        float f4[4] = {Q, P, 0.f, 0.f};
+        cta_reduce(ms, acc, f4);
+        if (tid == 0) {
+          float* o = a.ws.part(b, s);
+          o[0] = acc.hi;
+          o[1] = acc.lo;
+          o[2] = f4[0];
+          o[3] = f4[1];
+        }
+      }
+      if (arrive_row(a, ms, b)) {
+        if (tid == 0) {
+          df Sr{0.f, 0.f};
+          float Qt = 0.f, Pt = 0.f;
+          for (int q = 0; q < a.S; ++q) {
+            const float* p = a.ws.part(b, q);
+            Sr = df_add(Sr, df{ld_cg_f(p), ld_cg_f(p + 1)});
+            Qt += ld_cg_f(p + 2);
+            Pt += ld_cg_f(p + 3);
+          }
+          ms.E = kAccRho * (Qt + Pt) + 1e-14f * Sr.hi + 1e-36f;
+          ms.tstar = df_mul_f(Sr, a.uniforms[size_t(b) * (K + 1) + K]);
+          ms.found = (Sr.hi > 0.0f) ? 1 : (pair ? 2 : 0);  // 2: zero residual mass
+        }
+        consumers_sync();
+        const int flags = ld_cg_i(&stp->flags);
+        if (ms.found == 2) {
+          // zero residual mass: the draw uses q_j itself
+          if (tid == 0) {
+            RowState* st = a.ws.rowstate(b);
+            st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;
+            __threadfence();
+            enqueue_row_stage(a.ws, kFB, b, a.S, n | (kModeQ << 8));
+          }
+        } else {
+          if (ms.found == 1) search_draw<E>(a, ms, b, ae);
+          if (warp == 1 && lane < K) ms.tok[lane] = a.tokens[size_t(b) * K + lane];
+          consumers_sync();
+          const int tokn = ms.found == 1 ? ms.token : -1;
+          int fl = flags;
+          if (!(ms.found == 1 && ms.cert)) fl |= SPEC_ROW_UNCERTIFIED;
+          if (tokn < 0 && tid == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
+          write_outputs(a, ms, b, n, tokn, fl, tokn < 0);
+        }
+      }
+      consumers_sync();
+    }
   }
   __syncthreads();
-  cluster_sync();  // no CTA leaves while another may still address its shared memory
+  if (threadIdx.x == 0 && (*L.ring.abort || ld_volatile_u32(&a.ws.hdr()->abort))) {
+    atomicExch(&a.ws.hdr()->abort, 1u);
+    if (a.err) atomicOr(a.err, SPEC_DERR_TIMEOUT);
+  }
 }
 
 }  // namespace
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+WsLayout sample_layout(int B, int K, int V, int dtype) {
+  const int kvec = (dtype == SPEC_BF16) ? 8 : 4;
+  const int nvec = V / kvec;
+  const int S = slices_for(nvec, B);
+  const int maxslice = (nvec + S - 1) / S;
+  const int ustride = (maxslice + 31) / 32 + 1;
+  const int part = (8 * K > 8) ? 8 * K : 8;
+  return ws_layout(B, S, part, ustride, 5);
+}
+
+}  // namespace
+
+size_t sample_workspace_bytes(int B, int K, int V, int dtype) {
+  return sample_layout(B, K, V, dtype).total;
+}
 
 int launch_verify_sample(const SampleLaunch& s) {
   SampleArgs a;
@@ -1182,14 +1224,18 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.B = s.B;
   a.K = s.K;
   a.V = s.V;
+  const int kvec = (s.dtype == SPEC_BF16) ? 8 : 4;
+  a.nvec = s.V / kvec;
+  const WsLayout wl = sample_layout(s.B, s.K, s.V, s.dtype);
+  a.S = wl.S;
+  a.ws.base = static_cast<uint8_t*>(s.workspace);
+  a.ws.L = wl;
   const double C = 1.4426950408889634073599246810018921 / double(s.temperature);  // log2(e)/T
   a.c = float(C);
   a.Chi = float(C);
   a.Clo = float(C - double(a.Chi));
-  const int kvec = (s.dtype == SPEC_BF16) ? 8 : 4;
-  const int nvec = s.V / kvec;
-  const int csize = pick_cluster(s.B, nvec);
-  const int run = (nvec / csize) / kCons + 2;  // running-sum length per thread per row slice
+  const int maxslice = (a.nvec + a.S - 1) / a.S;
+  const int run = maxslice / kCons + 2;  // running-sum length per thread per row slice
   a.bd.ex2 = float(kEx2RelErrBound);
   a.bd.gamma1 = float((3.0 + run) * 5.9604644775390625e-8 * 1.01);
   a.bd.xbar = float(std::log2(double(s.V)) + 2.0);
@@ -1199,11 +1245,11 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.row_info = s.row_info;
   a.q_at_d = s.q_at_d;
   a.p_at_d = s.p_at_d;
-  const size_t smem = sample_smem_bytes(2 * s.K + 1);
   cudaStream_t st = static_cast<cudaStream_t>(s.stream);
-  if (s.dtype == SPEC_BF16)
-    return launch_persistent(verify_sample_kernel<EBf16>, a, s.B, csize, smem, st);
-  return launch_persistent(verify_sample_kernel<EF32>, a, s.B, csize, smem, st);
+  if (cudaMemsetAsync(s.workspace, 0, wl.zero_bytes, st) != cudaSuccess) return SPEC_ECUDA;
+  const size_t smem = sample_smem_bytes(2 * s.K + 1);
+  if (s.dtype == SPEC_BF16) return launch_dataflow(verify_sample_kernel<EBf16>, a, smem, st);
+  return launch_dataflow(verify_sample_kernel<EF32>, a, smem, st);
 }
 
 }  // namespace sv

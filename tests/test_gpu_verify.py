@@ -291,8 +291,16 @@ def test_host_validation(sv):
     # misaligned base
     buf = torch.zeros((2 * 3 * 64 + 1,), dtype=torch.bfloat16, device="cuda")
     mis = buf[1:].view(2, 3, 64)
+    ws = m.workspace_for(2, 2, 64, m.SPEC_BF16, "cuda")
     st = m.lib().spec_verify_greedy(mis.data_ptr(), dv["tokens"].data_ptr(), 2, 2, 64,
-                                    out.data_ptr(), n.data_ptr(), None, m.SPEC_BF16, None)
+                                    out.data_ptr(), n.data_ptr(), None, m.SPEC_BF16, None,
+                                    ws.data_ptr(), ws.numel())
+    assert st == m.SPEC_EINVAL
+    # workspace too small
+    import ctypes
+    st = m.lib().spec_verify_greedy(dv["target"].data_ptr(), dv["tokens"].data_ptr(), 2, 2, 64,
+                                    out.data_ptr(), n.data_ptr(), None, m.SPEC_BF16, None,
+                                    ws.data_ptr(), ctypes.c_size_t(16))
     assert st == m.SPEC_EINVAL
 
 
