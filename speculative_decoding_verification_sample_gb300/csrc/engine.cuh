@@ -1,18 +1,22 @@
 // Dataflow engine of the verification kernels.
 //
 // The batch is cut into tasks: task (b, s) works on vocabulary slice s of
-// batch row b. Every kernel is persistent (one or two CTAs per SM, no
-// clusters). In each CTA one producer thread fetches tasks and streams their
-// logit slices from global memory into a ring of shared-memory stages with
-// 1-D bulk async copies (completion on mbarriers); eight consumer warps
-// process the stages in order. A task leaves its partial results (per-slice
-// sums) in an L2-resident workspace and arrives on an atomic counter of its
-// row; the CTA whose arrival completes the row's stage combines the partials
-// and continues the row: it decides, writes outputs, or enqueues the row's
-// next stage as new tasks. No CTA ever waits for another one, so the HBM
-// stream never stalls behind a row's serial steps.
+// batch row b. The kernels are persistent (two CTAs per SM, no clusters) and
+// every CTA has three roles:
+//   * one producer thread fetches tasks and streams their logit slices from
+//     global memory into a ring of shared-memory stages with 1-D bulk async
+//     copies (completion on mbarriers);
+//   * eight consumer warps process the stages in order and leave per-warp
+//     partial results of each task in a hand-off slot;
+//   * one finisher warp combines a task's per-warp partials, stores them in
+//     an L2-resident workspace and arrives on an atomic counter of the row;
+//     when its arrival completes the row's stage it continues the row: it
+//     decides, writes outputs, or enqueues the row's next stage as new tasks.
+// Consumers never wait on global memory round trips, and no CTA ever waits
+// for another one, so the HBM stream does not stall behind a row's serial
+// steps.
 //
-// Task sources, in priority order: the dynamic queue (later stages of rows
+// Task sources, in priority order: the work queue (later stages of rows
 // already started, which keeps their data hot in L2), then the static list of
 // first-stage tasks (b, s) in row order. Every wait is bounded; a timeout sets
 // the workspace abort word, the kernel drains, and unfinished rows keep the -1
@@ -49,10 +53,10 @@ __host__ __device__ inline int slices_for(int nvec, int B) {
 // ------------------------------------------------------------------ workspace
 struct WsHeader {           // zeroed by the host before every launch
   uint32_t p1_next;         // next first-stage task
-  uint32_t dq_tail;         // dynamic-queue reservations
-  uint32_t dq_head;         // dynamic-queue claims
+  uint32_t dq_tail;         // queue reservations
+  uint32_t dq_head;         // queue tickets handed out
   uint32_t rows_done;       // rows whose outputs are written
-  uint32_t abort;           // set on any timeout
+  uint32_t abort;           // set on any timeout or overflow
   uint32_t pad[3];
 };
 
@@ -60,26 +64,32 @@ struct QTask {
   int type, b, s, aux;
 };
 
+// A queued task in one 64-bit word (written and read as a whole):
+// bits 0-7 type (>= 1, so a written entry is never 0), 8-15 slice, 16-31 aux,
+// 32-63 batch row.
+__device__ __forceinline__ uint64_t pack_task(int type, int b, int s, int aux) {
+  return uint64_t(uint32_t(type) & 0xffu) | (uint64_t(uint32_t(s) & 0xffu) << 8) |
+         (uint64_t(uint32_t(aux) & 0xffffu) << 16) | (uint64_t(uint32_t(b)) << 32);
+}
+__device__ __forceinline__ QTask unpack_task(uint64_t w) {
+  return QTask{int(w & 0xffu), int(uint32_t(w >> 32)), int((w >> 8) & 0xffu),
+               int((w >> 16) & 0xffffu)};
+}
+
 // Offsets (bytes) of the workspace regions; computed identically on host and device.
 struct WsLayout {
-  size_t header, row_cnt, ready, entries, part, units, rowstate, total, zero_bytes;
-  int B, S, qcap, part_floats, ustride;
-};
-
-// per-row state written by the row's finishers
-struct RowState {
-  int n, flags, mode, err;  // mode: 0 residual (q_j, p_j), 1 draw from q alone
-  float Kq, Kp, Rq, Rp;     // integer offsets and fp32 1/S of the draw's rows
-  float Iq_hi, Iq_lo, Ip_hi, Ip_lo;  // accurate 1/S (double-float path)
-  float pad[4];
+  size_t header, row_cnt, entries, part, units, rowstate, total, zero_bytes;
+  int B, S, qcap, part_floats, ustride, rowstate_bytes;
 };
 
 __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) / 256 * 256; }
 
-// part_floats: floats of partial results per (row, slice); ustride: unit slots per slice.
+// part_floats: floats of partial results per (row, slice); ustride: unit
+// slots per slice; rowstate_bytes: per-row state of the kernel's finishers.
 __host__ __device__ inline WsLayout ws_layout(int B, int S, int part_floats, int ustride,
-                                              int stages_per_row) {
+                                              int stages_per_row, int rowstate_bytes) {
   WsLayout w;
+  w.rowstate_bytes = rowstate_bytes;
   w.B = B;
   w.S = S;
   w.qcap = B * S * stages_per_row;
@@ -90,17 +100,15 @@ __host__ __device__ inline WsLayout ws_layout(int B, int S, int part_floats, int
   o += ws_align(sizeof(WsHeader));
   w.row_cnt = o;
   o += ws_align(size_t(B) * 4);
-  w.ready = o;
-  o += ws_align(size_t(w.qcap) * 4);
-  w.zero_bytes = o;  // everything above is zeroed per call
   w.entries = o;
-  o += ws_align(size_t(w.qcap) * sizeof(QTask));
+  o += ws_align(size_t(w.qcap) * 8);
+  w.zero_bytes = o;  // everything above is zeroed per call
   w.part = o;
   o += ws_align(size_t(B) * S * part_floats * 4);
   w.units = o;
   o += ws_align(size_t(B) * S * ustride * 8);
   w.rowstate = o;
-  o += ws_align(size_t(B) * sizeof(RowState));
+  o += ws_align(size_t(B) * rowstate_bytes);
   w.total = o;
   return w;
 }
@@ -110,91 +118,118 @@ struct Ws {
   WsLayout L;
   __device__ WsHeader* hdr() const { return reinterpret_cast<WsHeader*>(base + L.header); }
   __device__ uint32_t* row_cnt() const { return reinterpret_cast<uint32_t*>(base + L.row_cnt); }
-  __device__ uint32_t* ready() const { return reinterpret_cast<uint32_t*>(base + L.ready); }
-  __device__ QTask* entries() const { return reinterpret_cast<QTask*>(base + L.entries); }
+  __device__ uint64_t* entries() const { return reinterpret_cast<uint64_t*>(base + L.entries); }
   __device__ float* part(int b, int s) const {
     return reinterpret_cast<float*>(base + L.part) + (size_t(b) * L.S + s) * L.part_floats;
   }
   __device__ float2* units(int b, int s) const {
     return reinterpret_cast<float2*>(base + L.units) + (size_t(b) * L.S + s) * L.ustride;
   }
-  __device__ RowState* rowstate(int b) const {
-    return reinterpret_cast<RowState*>(base + L.rowstate) + b;
+  __device__ uint8_t* rowstate(int b) const {
+    return base + L.rowstate + size_t(b) * L.rowstate_bytes;
   }
 };
 
 // ------------------------------------------------------------------ memory helpers
 __device__ __forceinline__ float ld_cg_f(const float* p) { return __ldcg(p); }
 __device__ __forceinline__ int ld_cg_i(const int* p) { return __ldcg(p); }
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
   return *reinterpret_cast<const volatile uint32_t*>(p);
 }
 
 // ------------------------------------------------------------------ queue
-// Appends n tasks (type, b, s = 0..n-1, aux). One calling thread. A queue
-// overflow (more later-stage tasks than the layout provides) aborts the launch.
+// Appends the n tasks (type, b, s = 0..n-1, aux); called by one lane. A
+// fence between the caller's earlier writes (row state) and the entries,
+// paired with the fence the reader issues after seeing an entry, makes those
+// writes visible to the task. A queue overflow (more later-stage tasks than
+// the layout provides) aborts the launch.
 __device__ inline void enqueue_row_stage(const Ws& ws, int type, int b, int n, int aux) {
   const uint32_t base = atomicAdd(&ws.hdr()->dq_tail, uint32_t(n));
+  __threadfence();  // the caller's writes before any entry (the reader fences after its load)
   if (base + uint32_t(n) > uint32_t(ws.L.qcap)) {
     atomicExch(&ws.hdr()->abort, 1u);
     return;
   }
-  QTask* e = ws.entries();
-  for (int s = 0; s < n; ++s) e[base + s] = QTask{type, b, s, aux};
-  __threadfence();
-  for (int s = 0; s < n; ++s) st_release_u32(&ws.ready()[base + s], 1u);
+  uint64_t* e = ws.entries();
+  for (int s = 0; s < n; ++s) st_relaxed_u64(&e[base + s], pack_task(type, b, s, aux));
 }
 
-// The producer's fetch. Queued tasks are claimed by ticket: a producer that
-// sees the queue non-empty takes the next ticket with one atomicAdd (no
-// compare-and-swap retries, which serialise hundreds of producers on one
-// word) and from then on polls only that entry's ready flag. A ticket can
-// outrun the queue (several producers saw the same last entry); its holder
-// keeps taking first-stage tasks until the entry appears, and once every row
-// is done the ticket is simply dropped. `pending` is the held ticket (-1:
-// none). Returns false when nothing is runnable now; `exhausted` then says
-// that no first-stage task is left.
-__device__ inline bool fetch_task(const Ws& ws, int first_type, QTask& t, bool& exhausted,
-                                  int64_t& pending) {
-  WsHeader* h = ws.hdr();
-  exhausted = false;
-  if (pending < 0) {
-    const uint32_t head = ld_volatile_u32(&h->dq_head);
-    const uint32_t tail = ld_volatile_u32(&h->dq_tail);
-    if (head < tail) pending = int64_t(atomicAdd(&h->dq_head, 1u));
-  }
-  if (pending >= 0 && pending < int64_t(ws.L.qcap) &&
-      ld_acquire_u32(&ws.ready()[pending])) {
-    const QTask* e = ws.entries() + pending;
-    t = QTask{__ldcg(&e->type), __ldcg(&e->b), __ldcg(&e->s), __ldcg(&e->aux)};
-    pending = -1;
-    return true;
-  }
-  const uint32_t total = uint32_t(ws.L.B) * uint32_t(ws.L.S);
-  if (ld_volatile_u32(&h->p1_next) < total) {
-    const uint32_t k = atomicAdd(&h->p1_next, 1u);
-    if (k < total) {
-      t = QTask{first_type, int(k / ws.L.S), int(k % ws.L.S), 0};
-      return true;
-    }
-  }
-  exhausted = true;
-  return false;
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
 }
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// The producer's task source. Queued tasks are claimed by ticket: every
+// producer holds one ticket (dq_head, one atomicAdd, no compare-and-swap
+// retries, which serialise hundreds of producers on one word) and runs the
+// queue entry of that number once it is written. Tickets run ahead of the
+// queue; a ticket whose entry never comes is dropped when every row is done.
+// First-stage tasks are reserved one at a time (p1_next).
+//
+// The round trips are pipelined behind the streaming: prepare(), called once
+// the first stage of a task is issued, takes the next ticket, loads the held
+// ticket's entry and reserves the next first-stage task, all without waiting;
+// next(), called at the task boundary, uses what prepare() found. Only when
+// nothing was prepared does next() wait on memory itself. Entries are read
+// with relaxed loads and acquired with a fence once seen.
+struct Fetcher {
+  static constexpr uint32_t kNone = 0xffffffffu;
+  int64_t ticket = -1;   // held queue ticket
+  uint64_t word = 0;     // its entry as last loaded (0: not written yet)
+  uint32_t kres = kNone; // reserved first-stage index
+  bool first_left = true;
+
+  __device__ __forceinline__ void prepare(const Ws& ws) {
+    WsHeader* h = ws.hdr();
+    if (ticket < 0) ticket = int64_t(atomicAdd(&h->dq_head, 1u));
+    else if (word == 0 && ticket < int64_t(ws.L.qcap)) word = ld_relaxed_u64(&ws.entries()[ticket]);
+    if (kres == kNone && first_left) kres = atomicAdd(&h->p1_next, 1u);
+  }
+
+  // 1: task in t; 0: nothing runnable now; the caller backs off and retries.
+  __device__ __forceinline__ int next(const Ws& ws, int first_type, QTask& t) {
+    WsHeader* h = ws.hdr();
+    const uint32_t total = uint32_t(ws.L.B) * uint32_t(ws.L.S);
+    for (int pass = 0; pass < 2; ++pass) {
+      if (ticket >= 0 && word != 0) {
+        fence_acq_rel_gpu();
+        t = unpack_task(word);
+        ticket = -1;
+        word = 0;
+        return 1;
+      }
+      if (kres != kNone) {
+        const uint32_t k = kres;
+        kres = kNone;
+        if (k < total) {
+          t = QTask{first_type, int(k / ws.L.S), int(k % ws.L.S), 0};
+          return 1;
+        }
+        first_left = false;
+      }
+      if (pass == 1) break;
+      // nothing prepared: fetch now
+      if (ticket < 0) ticket = int64_t(atomicAdd(&h->dq_head, 1u));
+      if (ticket < int64_t(ws.L.qcap)) word = ld_relaxed_u64(&ws.entries()[ticket]);
+      if (word == 0 && first_left) kres = atomicAdd(&h->p1_next, 1u);
+    }
+    return 0;
+  }
+};
 
 // Producer back-off when no task is runnable. Returns false when production
 // should stop: every row is done, the launch aborted, or nothing became
 // runnable for kWaitNs (then the launch is aborted). `idle_t0` is the global
 // time at which the current idle stretch began (0: not idle).
 __device__ inline bool producer_idle(const Ws& ws, bool exhausted, uint64_t& idle_t0) {
+  // (exhausted: no first-stage task is left)
   WsHeader* h = ws.hdr();
   if (ld_volatile_u32(&h->abort)) return false;
   if (exhausted && ld_volatile_u32(&h->rows_done) >= uint32_t(ws.L.B)) return false;
@@ -230,8 +265,6 @@ struct Ring {
   volatile int* abort;  // CTA-local abort flag
 };
 
-__device__ __forceinline__ void consumers_sync() { named_bar_sync(1, kCons); }
-
 __device__ inline void ring_init(const Ring& r) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -259,7 +292,7 @@ __device__ __forceinline__ void chunking(int nv, int& nchunk, int& cv) {
   if (nchunk > 0) nchunk = (nv + cv - 1) / cv;
 }
 
-// Producer: waits for stage `it` to be free, then fills its metadata.
+// Producer: waits for stage `it` to be free.
 __device__ __forceinline__ bool claim_stage(const Ring& ring, uint32_t it) {
   const int stage = it % kStages;
   if (it >= kStages && !mbar_wait(&ring.empty[stage], ((it / kStages) - 1) & 1)) {
@@ -271,9 +304,13 @@ __device__ __forceinline__ bool claim_stage(const Ring& ring, uint32_t it) {
 
 // Producer: streams the rows of one task (rows[] are row base pointers,
 // `paired` interleaves chunk k of every row: r0k0, r1k0, r0k1, r1k1, ...).
+// `after_first` runs once the first stage is issued: the producer fetches its
+// next task there, so the fetch's memory round trips overlap the streaming
+// instead of leaving the ring to drain between tasks.
+template <class AfterFirst>
 __device__ inline bool produce_task(const Ring& ring, uint32_t& it, uint32_t& nt, const QTask& t,
                                     const char* const* rows, int nrows, bool paired, int v0,
-                                    int v1) {
+                                    int v1, AfterFirst&& after_first) {
   // The table entry of task nt is reused by task nt + kStages; it is written
   // only once the task's first stage is claimed, i.e. after every consumer
   // warp released the stage kStages earlier and so has read the entry of every
@@ -305,6 +342,7 @@ __device__ inline bool produce_task(const Ring& ring, uint32_t& it, uint32_t& nt
     mbar_arrive_expect_tx(&ring.full[stage], bytes);
     bulk_g2s(ring.buf + size_t(stage) * kChunk, rows[r] + size_t(c0) * 16, bytes,
              &ring.full[stage]);
+    if (q == 0) after_first();
   }
   return true;
 }
@@ -335,6 +373,101 @@ __device__ __forceinline__ void release_stage(const Ring& ring, uint32_t it) {
 
 __device__ __forceinline__ const uint4* stage_data(const Ring& ring, uint32_t it) {
   return reinterpret_cast<const uint4*>(ring.buf + size_t(it % kStages) * kChunk);
+}
+
+// ------------------------------------------------------------------ hand-off
+// Consumers -> finisher: kSlots slots in rotation. Task n of a CTA uses slot
+// n % kSlots; `done` completes when all consumer warps stored their partials
+// (count kCW), `freed` when the finisher has read them (count 1).
+constexpr int kSlots = 8;
+
+struct Handoff {
+  uint64_t* done;   // [kSlots]
+  uint64_t* freed;  // [kSlots]
+  uint8_t* data;    // [kSlots][slot_bytes]
+  int slot_bytes;
+  __device__ uint8_t* slot(uint32_t n) const { return data + size_t(n % kSlots) * slot_bytes; }
+};
+
+__device__ inline void handoff_init(const Handoff& h) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&h.done[s], kCW);
+      mbar_init(&h.freed[s], 1);
+    }
+    fence_mbar_init();
+  }
+}
+
+// Consumers: wait until the slot of task n is free (the finisher has read
+// task n - kSlots).
+__device__ __forceinline__ bool handoff_acquire(const Handoff& h, uint32_t n) {
+  if (n < kSlots) return true;
+  return mbar_wait(&h.freed[n % kSlots], ((n / kSlots) - 1) & 1);
+}
+
+// Consumers: this warp's partials of task n are stored.
+__device__ __forceinline__ void handoff_post(const Handoff& h, uint32_t n) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&h.done[n % kSlots]);
+}
+
+// The finisher warp's loop. It takes the finished tasks in order, in batches
+// of those already complete: per batch it combines each task's per-warp
+// partials into the task's slice partials (`combine(t, slot)`, plain stores),
+// issues one fence, frees the slots, arrives on every task's row counter
+// (lanes in parallel, one atomicAdd each), and then runs the continuation
+// (`cont(t)`) of every row whose stage that arrival completed. One memory
+// round trip per batch instead of two per task.
+template <class Combine, class Continue>
+__device__ inline void finisher_loop(const Ws& ws, const Handoff& ho, volatile int* abort,
+                                     Combine&& combine, Continue&& cont) {
+  const int lane = threadIdx.x & 31;
+  for (uint32_t n = 0;;) {
+    if (!mbar_wait(&ho.done[n % kSlots], (n / kSlots) & 1)) {
+      *abort = 1;
+      return;
+    }
+    uint32_t m = n + 1;
+    while (m < n + kSlots && mbar_test_wait(&ho.done[m % kSlots], (m / kSlots) & 1)) ++m;
+    const int avail = int(m - n);
+    QTask mine{0, 0, 0, 0};
+    if (lane < avail) mine = *reinterpret_cast<const QTask*>(ho.slot(n + lane));
+    const unsigned endm = __ballot_sync(0xffffffffu, lane < avail && mine.type == 0);
+    const int cnt = endm ? __ffs(int(endm)) - 1 : avail;
+    for (int k = 0; k < cnt; ++k) {
+      QTask t;
+      t.type = __shfl_sync(0xffffffffu, mine.type, k);
+      t.b = __shfl_sync(0xffffffffu, mine.b, k);
+      t.s = __shfl_sync(0xffffffffu, mine.s, k);
+      t.aux = __shfl_sync(0xffffffffu, mine.aux, k);
+      combine(t, ho.slot(n + k));
+    }
+    __syncwarp();
+    __threadfence();
+    if (lane == 0)
+      for (int k = 0; k < cnt; ++k) mbar_arrive(&ho.freed[(n + k) % kSlots]);
+    int last = 0;
+    if (lane < cnt) {
+      const uint32_t old = atomicAdd(&ws.row_cnt()[mine.b], 1u);
+      last = (old == uint32_t(ws.L.S) - 1);
+      if (last) ws.row_cnt()[mine.b] = 0;  // the row's next stage counts from zero
+    }
+    unsigned lm = __ballot_sync(0xffffffffu, last);
+    if (lm) __threadfence();
+    while (lm) {
+      const int k = __ffs(int(lm)) - 1;
+      lm &= lm - 1;
+      QTask t;
+      t.type = __shfl_sync(0xffffffffu, mine.type, k);
+      t.b = __shfl_sync(0xffffffffu, mine.b, k);
+      t.s = __shfl_sync(0xffffffffu, mine.s, k);
+      t.aux = __shfl_sync(0xffffffffu, mine.aux, k);
+      cont(t);
+    }
+    n += uint32_t(cnt);
+    if (endm) return;
+  }
 }
 
 }  // namespace sv

@@ -6,11 +6,13 @@
 // alone. Ties in the argmax go to the lowest vocabulary index.
 //
 // GB300 mapping (dataflow engine, engine.cuh): task (b, s) streams slice s of
-// target rows 0..K-1 and leaves each row's (max, first index) in the
-// workspace; the CTA completing row b combines the S partials, finds the first
-// mismatch with a warp ballot, and either writes the row or (all K accepted)
-// enqueues the slices of target row K, whose completing CTA writes the bonus
-// token. Raw logits are compared exactly (no temperature).
+// target rows 0..K-1; the consumer warps leave per-warp (max, first index)
+// pairs in a hand-off slot, the finisher warp combines them into the slice's
+// partials and arrives on the row's counter. The finisher completing row b
+// combines the S partials, finds the first mismatch with a warp ballot, and
+// either writes the row or (all K accepted) enqueues the slices of target row
+// K, whose completing finisher writes the bonus token. Raw logits are compared
+// exactly (no temperature).
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -27,6 +29,7 @@ namespace sv {
 namespace {
 
 enum { kG1 = 1, kGB = 2 };
+constexpr int kFinWarp = kCW + 1;  // warp index of the finisher
 
 struct GreedyArgs {
   const void* target;
@@ -38,28 +41,23 @@ struct GreedyArgs {
   Ws ws;
 };
 
-struct Misc {
-  int abort;
-  int last;
-  int tok[kMaxK];
-  int best[kMaxK + 1];
-  int first_mismatch;
-  int bad_token;
-};
+// Hand-off slot: the task (16 bytes), then float wM[R][kCW], int wI[R][kCW]
+// (index -2: a NaN was seen).
+__host__ __device__ inline int slot_bytes(int R) { return (16 + R * kCW * 8 + 15) / 16 * 16; }
 
 struct Smem {
   Ring ring;
-  Misc* misc;
-  float* wM;  // [K+1][kCW]
-  int* wI;    // [K+1][kCW]  (-2: NaN seen)
+  Handoff ho;
+  float2* item;  // [256] finisher scratch: slice partials being combined
 };
 
 __host__ __device__ inline size_t greedy_smem_bytes(int R) {
   size_t o = size_t(kStages) * kChunk;
   o += 2 * kStages * 8;
   o += kStages * sizeof(ChunkMeta) + kStages * sizeof(QTask);
-  o += (sizeof(Misc) + 15) / 16 * 16;
-  o += size_t(R) * kCW * 8;
+  o += 2 * kSlots * 8 + 16;
+  o += 256 * 8;
+  o += size_t(kSlots) * slot_bytes(R);
   return (o + 127) / 128 * 128;
 }
 
@@ -74,11 +72,15 @@ __device__ inline Smem make_smem(uint8_t* base, int R) {
   o += kStages * sizeof(ChunkMeta);
   L.ring.ttab = reinterpret_cast<QTask*>(base + o);
   o += kStages * sizeof(QTask);
-  L.misc = reinterpret_cast<Misc*>(base + o);
-  L.ring.abort = &L.misc->abort;
-  o += (sizeof(Misc) + 15) / 16 * 16;
-  L.wM = reinterpret_cast<float*>(base + o);
-  L.wI = reinterpret_cast<int*>(L.wM + R * kCW);
+  L.ho.done = reinterpret_cast<uint64_t*>(base + o);
+  L.ho.freed = L.ho.done + kSlots;
+  o += 2 * kSlots * 8;
+  L.ring.abort = reinterpret_cast<volatile int*>(base + o);
+  o += 16;
+  L.item = reinterpret_cast<float2*>(base + o);
+  o += 256 * 8;
+  L.ho.data = base + o;
+  L.ho.slot_bytes = slot_bytes(R);
   return L;
 }
 
@@ -129,7 +131,8 @@ struct ArgmaxOp {
       }
     }
   }
-  __device__ void end_row(const Smem& L, int r) {
+  // Warp partial of row r into the hand-off slot.
+  __device__ __forceinline__ void end_row(uint8_t* slot, int R, int r) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -142,90 +145,123 @@ struct ArgmaxOp {
     }
     const int anybad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-      L.wM[r * kCW + warp] = best;
-      L.wI[r * kCW + warp] = anybad ? -2 : idx;
+      float* wM = reinterpret_cast<float*>(slot + 16);
+      int* wI = reinterpret_cast<int*>(wM + R * kCW);
+      wM[r * kCW + warp] = best;
+      wI[r * kCW + warp] = anybad ? -2 : idx;
     }
   }
 };
 
-// CTA (value, index) of rows [0, nrows) into out[2r], out[2r+1].
-__device__ void argmax_to_global(const Smem& L, int nrows, float* out) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < nrows; r += kCW) {
-    float best = lane < kCW ? L.wM[r * kCW + lane] : -INFINITY;
-    int idx = lane < kCW ? L.wI[r * kCW + lane] : INT_MAX;
-    int bad = (idx == -2);
-    if (bad) idx = INT_MAX;
+// Finisher: slice partial (value, index) of the task's rows into out[2r], out[2r+1].
+__device__ void combine_task(const GreedyArgs& a, const QTask& t, const uint8_t* slot) {
+  const int lane = threadIdx.x & 31;
+  const int R = a.K, nrows = (t.type == kG1) ? a.K : 1;
+  const float* wM = reinterpret_cast<const float*>(slot + 16);
+  const int* wI = reinterpret_cast<const int*>(wM + R * kCW);
+  float* out = a.ws.part(t.b, t.s);
+  for (int r = lane; r < nrows; r += 32) {
+    float best = -INFINITY;
+    int idx = INT_MAX, bad = 0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-      if (better(ob, oi, best, idx)) {
-        best = ob;
-        idx = oi;
+    for (int q = 0; q < kCW; ++q) {
+      const float v = wM[r * kCW + q];
+      const int i = wI[r * kCW + q];
+      if (i == -2) bad = 1;
+      else if (better(v, i, best, idx)) {
+        best = v;
+        idx = i;
       }
     }
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) {
-      out[2 * r] = best;
-      out[2 * r + 1] = __int_as_float(bad ? -2 : idx);
-    }
+    out[2 * r] = best;
+    out[2 * r + 1] = __int_as_float(bad ? -2 : idx);
   }
+  __syncwarp();
 }
 
-// Row argmax (-1 for a NaN row) from the S slice partials at float offset 2r.
-__device__ int argmax_combine(const GreedyArgs& a, int b, int r) {
-  float best = -INFINITY;
-  int idx = INT_MAX, bad = 0;
-  for (int s = 0; s < a.S; ++s) {
-    const float* p = a.ws.part(b, s) + 2 * r;
-    const float v = ld_cg_f(p);
-    const int i = __float_as_int(ld_cg_f(p + 1));
-    if (i == -2) {
-      bad = 1;
-      continue;
+// Row argmax (-1 for a NaN row) of rows [0, nrows) from the S slice
+// partials (float offset 2r: value, index or -2 for NaN); the partials of a
+// group of rows are loaded by all lanes at once, then lane r combines row r.
+// The result of row r ends in lane r (r < 32).
+__device__ int argmax_rows(const GreedyArgs& a, const Smem& L, int b, int nrows) {
+  const int lane = threadIdx.x & 31, S = a.S;
+  const int per_group = 256 / S > 0 ? 256 / S : 1;
+  int res = -1;
+  for (int r0 = 0; r0 < nrows; r0 += per_group) {
+    const int rg = min(per_group, nrows - r0), items = rg * S;
+#pragma unroll 8
+    for (int i = lane; i < items; i += 32) {
+      const int r = r0 + i / S, sl = i % S;
+      L.item[i] = __ldcg(reinterpret_cast<const float2*>(a.ws.part(b, sl) + 2 * r));
     }
-    if (better(v, i, best, idx)) {
-      best = v;
-      idx = i;
+    __syncwarp();
+    for (int rr = lane - r0; rr >= 0 && rr < rg; rr += 32) {
+      float best = -INFINITY;
+      int idx = INT_MAX, bad = 0;
+      for (int sl = 0; sl < S; ++sl) {
+        const float2 v = L.item[rr * S + sl];
+        const int i = __float_as_int(v.y);
+        if (i == -2) bad = 1;
+        else if (better(v.x, i, best, idx)) {
+          best = v.x;
+          idx = i;
+        }
+      }
+      res = (bad || idx == INT_MAX) ? -1 : idx;
     }
+    __syncwarp();
   }
-  return (bad || idx == INT_MAX) ? -1 : idx;
+  return res;
 }
 
-__device__ bool arrive_row(const GreedyArgs& a, Misc& ms, int b) {
-  __threadfence();
-  consumers_sync();
-  if (threadIdx.x == 0) {
-    const uint32_t old = atomicAdd(&a.ws.row_cnt()[b], 1u);
-    const int last = (old == uint32_t(a.S) - 1);
-    if (last) {
-      a.ws.row_cnt()[b] = 0;
-      __threadfence();
-    }
-    ms.last = last;
-  }
-  consumers_sync();
-  return ms.last != 0;
-}
-
-__device__ void write_row(const GreedyArgs& a, const Misc& ms, int b, int n, int token, bool error) {
-  const int K = a.K;
-  for (int i = threadIdx.x; i <= K; i += kCons) {
+__device__ void write_row(const GreedyArgs& a, int b, int n, int token, bool error, int errbits) {
+  const int lane = threadIdx.x & 31, K = a.K;
+  for (int i = lane; i <= K; i += 32) {
     int32_t v;
     if (error) v = -1;
-    else if (i < n) v = ms.tok[i];
+    else if (i < n) v = a.tokens[size_t(b) * K + i];
     else if (i == n) v = token;
     else v = -1;
     a.out_tokens[size_t(b) * (K + 1) + i] = v;
   }
-  if (threadIdx.x == 0) {
+  if (lane == 0) {
     a.out_n[b] = error ? -1 : n;
-    if (error && a.err) atomicOr(a.err, ms.bad_token ? SPEC_DERR_TOKEN : SPEC_DERR_LOGITS);
+    if (error && a.err) atomicOr(a.err, errbits);
+    atomicAdd(&a.ws.hdr()->rows_done, 1u);  // lets the producers stop; no ordering needed
   }
-  __threadfence();
-  consumers_sync();
-  if (threadIdx.x == 0) atomicAdd(&a.ws.hdr()->rows_done, 1u);
+  __syncwarp();
+}
+
+// G1 complete: first mismatch between draft tokens and the target argmaxes.
+__device__ void finish_g1(const GreedyArgs& a, const Smem& L, int b) {
+  const int lane = threadIdx.x & 31, K = a.K;
+  int d = 0, badtok = 0;
+  if (lane < K) {
+    d = a.tokens[size_t(b) * K + lane];
+    badtok = (d < 0 || d >= a.V);
+  }
+  const int g = argmax_rows(a, L, b, K);
+  badtok = __any_sync(0xffffffffu, badtok);
+  const unsigned mism = __ballot_sync(0xffffffffu, lane < K && g != d);
+  const int n = mism ? (__ffs(int(mism)) - 1) : K;
+  // a NaN row up to the first mismatch is an error
+  const int nan_row = __any_sync(0xffffffffu, lane < K && lane <= n && g < 0);
+  if (badtok || nan_row) {
+    write_row(a, b, n, -1, true, badtok ? SPEC_DERR_TOKEN : SPEC_DERR_LOGITS);
+    return;
+  }
+  if (n < K) {
+    write_row(a, b, n, __shfl_sync(0xffffffffu, g, n), false, 0);
+    return;
+  }
+  if (lane == 0) enqueue_row_stage(a.ws, kGB, b, a.S, K);
+  __syncwarp();
+}
+
+// GB complete: the bonus token is the argmax of target row K.
+__device__ void finish_gb(const GreedyArgs& a, const Smem& L, int b) {
+  const int tok = __shfl_sync(0xffffffffu, argmax_rows(a, L, b, 1), 0);
+  write_row(a, b, a.K, tok, tok < 0, SPEC_DERR_LOGITS);
 }
 
 template <class E>
@@ -233,21 +269,23 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
   using T = typename E::T;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int K = a.K;
-  const Smem L = make_smem(smem_raw, K + 1);
-  Misc& ms = *L.misc;
+  const Smem L = make_smem(smem_raw, K);
   ring_init(L.ring);
+  handoff_init(L.ho);
   __syncthreads();
-  if (threadIdx.x >= kCons) {
-    if (threadIdx.x == kCons) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WsHeader* h = a.ws.hdr();
+
+  if (warp == kCW) {
+    // ------------------------------------------------ producer
+    if (lane == 0) {
       uint32_t it = 0, nt = 0;
       uint64_t idle_t0 = 0;
-      int64_t pending = -1;
-      WsHeader* h = a.ws.hdr();
+      Fetcher fx;
       while (!*L.ring.abort && !ld_volatile_u32(&h->abort)) {
         QTask t;
-        bool exhausted;
-        if (!fetch_task(a.ws, kG1, t, exhausted, pending)) {
-          if (!producer_idle(a.ws, exhausted, idle_t0)) break;
+        if (!fx.next(a.ws, kG1, t)) {
+          if (!producer_idle(a.ws, !fx.first_left, idle_t0)) break;
           continue;
         }
         idle_t0 = 0;
@@ -261,79 +299,70 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
         } else {
           rows[nrows++] = reinterpret_cast<const char*>(tgt + size_t(K) * a.V);
         }
-        if (!produce_task(L.ring, it, nt, t, rows, nrows, false, v0, v1)) break;
+        auto prefetch = [&]() { fx.prepare(a.ws); };
+        if (!produce_task(L.ring, it, nt, t, rows, nrows, false, v0, v1, prefetch)) break;
       }
       produce_end(L.ring, it);
     }
+  } else if (warp == kFinWarp) {
+    // ------------------------------------------------ finisher
+    finisher_loop(
+        a.ws, L.ho, L.ring.abort,
+        [&](const QTask& t, const uint8_t* slot) { combine_task(a, t, slot); },
+        [&](const QTask& t) {
+          if (t.type == kG1) finish_g1(a, L, t.b);
+          else finish_gb(a, L, t.b);
+        });
   } else {
-    uint32_t it = 0;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    while (true) {
+    // ------------------------------------------------ consumers
+    const int tid = threadIdx.x;
+    uint32_t it = 0, n = 0;
+    for (;; ++n) {
       if (!wait_stage(L.ring, it)) break;
       const ChunkMeta m0 = L.ring.meta[it % kStages];
       if (m0.slot < 0) break;
       const QTask t = L.ring.ttab[m0.slot];
-      const int b = t.b, s = t.s;
+      if (!handoff_acquire(L.ho, n)) {
+        *L.ring.abort = 1;
+        break;
+      }
+      uint8_t* slot = L.ho.slot(n);
+      if (tid == 0) *reinterpret_cast<QTask*>(slot) = t;
       ArgmaxOp<E> op;
       op.begin();
+      bool ok = true;
       for (;;) {
         const ChunkMeta m = L.ring.meta[it % kStages];
-        const uint4* buf = stage_data(L.ring, it);
-        op.chunk(buf, m.c1 - m.c0, m.c0, tid);
+        op.chunk(stage_data(L.ring, it), m.c1 - m.c0, m.c0, tid);
         release_stage(L.ring, it);
         ++it;
         if (m.last_k) {
-          op.end_row(L, m.r);
+          op.end_row(slot, K, m.r);
           op.begin();
         }
         if (m.last) break;
-        if (!wait_stage(L.ring, it)) break;
-      }
-      consumers_sync();
-      const int nrows = (t.type == kG1) ? K : 1;
-      argmax_to_global(L, nrows, a.ws.part(b, s));
-      if (arrive_row(a, ms, b)) {
-        if (warp == 1) {
-          int bad = 0;
-          if (lane < K) {
-            const int d = a.tokens[size_t(b) * K + lane];
-            ms.tok[lane] = d;
-            bad = (d < 0 || d >= a.V);
-          }
-          bad = __any_sync(0xffffffffu, bad);
-          if (lane == 0) ms.bad_token = bad;
-        }
-        if (t.type == kG1) {
-          for (int r = tid; r < K; r += kCons) ms.best[r] = argmax_combine(a, b, r);
-          consumers_sync();
-          if (warp == 0) {
-            const int g = lane < K ? ms.best[lane] : 0;
-            const unsigned mism = __ballot_sync(0xffffffffu, lane < K && g != ms.tok[lane]);
-            if (lane == 0) ms.first_mismatch = mism ? (__ffs(int(mism)) - 1) : K;
-          }
-          consumers_sync();
-          const int n = ms.first_mismatch;
-          bool error = ms.bad_token != 0;
-          for (int i = 0; i <= min(n, K - 1); ++i)
-            if (ms.best[i] < 0) error = true;  // a NaN row up to the first mismatch
-          if (error || n < K) {
-            write_row(a, ms, b, n, error ? -1 : ms.best[n], error);
-          } else if (tid == 0) {
-            enqueue_row_stage(a.ws, kGB, b, a.S, K);
-          }
-        } else {
-          if (tid == 0) ms.best[K] = argmax_combine(a, b, 0);
-          consumers_sync();
-          const int tok = ms.best[K];
-          write_row(a, ms, b, K, tok, tok < 0 || ms.bad_token != 0);
+        if (!wait_stage(L.ring, it)) {
+          ok = false;
+          break;
         }
       }
-      consumers_sync();
+      handoff_post(L.ho, n);
+      if (!ok) {
+        ++n;
+        break;
+      }
+    }
+    // end of stream for the finisher
+    if (handoff_acquire(L.ho, n)) {
+      if (tid == 0) *reinterpret_cast<QTask*>(L.ho.slot(n)) = QTask{0, 0, 0, 0};
+      handoff_post(L.ho, n);
+    } else {
+      *L.ring.abort = 1;
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0 && (*L.ring.abort || ld_volatile_u32(&a.ws.hdr()->abort))) {
-    atomicExch(&a.ws.hdr()->abort, 1u);
+  if (threadIdx.x == 0 && (*L.ring.abort || ld_volatile_u32(&h->abort))) {
+    atomicExch(&h->abort, 1u);
     if (a.err) atomicOr(a.err, SPEC_DERR_TIMEOUT);
   }
 }
@@ -341,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
 WsLayout greedy_layout(int B, int K, int V, int dtype) {
   const int kvec = (dtype == SPEC_BF16) ? 8 : 4;
   const int nvec = V / kvec;
-  return ws_layout(B, slices_for(nvec, B), 2 * K + 2, 1, 2);
+  return ws_layout(B, slices_for(nvec, B), 2 * K + 2, 1, 2, 16);
 }
 
 }  // namespace
@@ -368,7 +397,7 @@ int launch_verify_greedy(const GreedyLaunch& g) {
   a.err = g.err;
   cudaStream_t st = static_cast<cudaStream_t>(g.stream);
   if (cudaMemsetAsync(g.workspace, 0, wl.zero_bytes, st) != cudaSuccess) return SPEC_ECUDA;
-  const size_t smem = greedy_smem_bytes(g.K + 1);
+  const size_t smem = greedy_smem_bytes(g.K);
   if (g.dtype == SPEC_BF16) return launch_dataflow(verify_greedy_kernel<EBf16>, a, smem, st);
   return launch_dataflow(verify_greedy_kernel<EF32>, a, smem, st);
 }

@@ -12,7 +12,9 @@
 // tasks whose last finisher continues the row:
 //   P1  softmax statistics (max, sum of exp2) of the slice of all 2K logit
 //       rows (target and draft, positions 0..K-1), streamed from HBM;
-//       finish: combine -> K accept tests -> first rejection j (warp ballot)
+//       finish: combine -> K accept tests -> first rejection j
+//   AR  (rare) double-float sums of target and draft row i when accept test i
+//       falls inside the fp32 error bound; finish: decide test i, go on
 //   BS  (only when all K are accepted) statistics of target row K
 //   SW  fp32 residual (q_j - p_j)+ (or q_K) over the slice of row j, re-read
 //       while hot in L2; per 32-vector unit sums kept in the workspace;
@@ -26,10 +28,10 @@
 // an integer offset ceil(max * log2(e)/T), and sums a decision depends on are
 // float pairs (df.cuh). A decision is taken from the fp32 path only when the
 // uniform is farther from the threshold than twice a proven bound on that
-// path's error; otherwise the FA/FB stages recompute it with double-float
-// exponentials (relative error < 4e-12 per term) and the row is flagged in
-// row_info. The output equals an exact-arithmetic evaluation except for rows
-// flagged SPEC_ROW_UNCERTIFIED.
+// path's error; otherwise the AR / FA / FB stages recompute it with
+// double-float exponentials (relative error < 4e-12 per term) and the row is
+// flagged in row_info. The output equals an exact-arithmetic evaluation except
+// for rows flagged SPEC_ROW_UNCERTIFIED.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -47,14 +49,15 @@
 namespace sv {
 namespace {
 
-enum TaskType { kP1 = 1, kBS = 2, kSW = 3, kFA = 4, kFB = 5 };
+enum TaskType { kP1 = 1, kBS = 2, kSW = 3, kFA = 4, kFB = 5, kAR = 6 };
 enum { kAccept = 0, kReject = 1, kAmbiguous = 2, kInvalid = 3 };
-constexpr int kModeResidual = 0, kModeQ = 1;  // RowState.mode
+constexpr int kModeResidual = 0, kModeQ = 1;  // draw modes (task aux bits 8+)
+constexpr int kFinWarp = kCW + 1;             // warp index of the finisher
 
 // ------------------------------------------------------------------ arguments
 struct Bounds {
   float ex2;     // relative error bound of ex2.approx.ftz.f32 on [-126, 1]
-  float gamma1;  // relative error bound of the per-thread fp32 summation of row sums
+  float gamma1;  // relative error bound of the fp32 summation of row sums
   float xbar;    // bound on sum_v q_v |x_v| used by the accept tests (log2 V + 2)
 };
 
@@ -76,33 +79,45 @@ struct SampleArgs {
   Ws ws;
 };
 
+// Per-row state kept in the workspace between a row's stages. Written by the
+// finisher of one stage, read (through L2) by the tasks and finisher of the
+// next.
+struct RowState {
+  int flags, pad0, pad1, pad2;       // SPEC_ROW_* bits so far
+  float Kq, Kp, Rq, Rp;              // offsets and fp32 1/S of the draw's rows
+  float Iq_hi, Iq_lo, Ip_hi, Ip_lo;  // accurate 1/S (double-float path)
+  int8_t acc[32];                    // accept-test states of positions 0..K-1
+  float rK[2 * kMaxK];  // offsets of rows 0..2K-1 (target i: 2i, draft i: 2i+1)
+  float rR[2 * kMaxK];  // fp32 1/S of those rows
+};
+
+__device__ __forceinline__ RowState* row_state(const SampleArgs& a, int b) {
+  return reinterpret_cast<RowState*>(a.ws.rowstate(b));
+}
+
 // ------------------------------------------------------------------ shared memory
-struct Misc {
-  int abort;
-  int last;  // this CTA completed the stage of the current task's row
-  int tok[kMaxK];
-  float zt_d[kMaxK], zd_d[kMaxK], u[kMaxK + 1];
-  int bad_token;
-  int acc_state[kMaxK];
-  float qd[kMaxK], pd[kMaxK];
-  df wR[kCW];
-  float wF[4][kCW];
-  df wA[kCW], wB[kCW];
-  int token, cert, found;
-  df tstar, base;
-  float E;
+// Hand-off slot: the task (16 bytes), then per-warp partials.
+//   P1 / BS: float wM[R][kCW], float wS[R][kCW], int wBad[R][kCW]
+//   SW:      float wAcc[kCW], wAq[kCW], wAp[kCW]
+//   FA / AR: df wA[kCW], wB[kCW]
+//   FB:      df wR[kCW], float wQ[kCW], wP[kCW]
+__host__ __device__ inline int slot_bytes(int R) {
+  const int body = R * kCW * 12 > 2 * kCW * 8 ? R * kCW * 12 : 2 * kCW * 8;
+  return (16 + body + 15) / 16 * 16;
+}
+
+struct Fin {  // finisher-private scratch: statistics of the 2K rows of a P1
+  float rowKc[2 * kMaxK];
+  df rowS[2 * kMaxK];
+  df rowInv[2 * kMaxK];
+  int rowOK[2 * kMaxK];
+  float4 item[256];  // slice partials being combined
 };
 
 struct Smem {
   Ring ring;
-  Misc* misc;
-  float* wM;  // [2K+1][kCW]
-  df* wS;     // [2K+1][kCW]
-  int* wBad;  // [2K+1][kCW]
-  float* rowKc;
-  df* rowS;
-  df* rowInv;
-  int* rowOK;
+  Handoff ho;
+  Fin* fin;
   float* tab_hi;
   float* tab_lo;
 };
@@ -121,12 +136,11 @@ __host__ __device__ inline size_t carve(int R, F&& put) {
   put(0, take(2 * kStages * 8, 8));
   put(1, take(kStages * sizeof(ChunkMeta), 16));
   put(2, take(kStages * sizeof(QTask), 16));
-  put(3, take(sizeof(Misc), 16));
-  put(4, take(size_t(R) * kCW * sizeof(df), 8));
-  put(5, take(size_t(R) * sizeof(df) * 2, 8));
-  put(6, take(size_t(R) * kCW * 8, 4));
-  put(7, take(size_t(R) * 8, 4));
-  put(8, take(256 * 8, 4));
+  put(3, take(2 * kSlots * 8, 8));
+  put(4, take(16, 16));
+  put(5, take(sizeof(Fin), 16));
+  put(6, take(256 * 8, 16));
+  put(7, take(size_t(kSlots) * slot_bytes(R), 16));
   return al(o, 128);
 }
 
@@ -135,6 +149,7 @@ __host__ __device__ inline size_t sample_smem_bytes(int R) { return carve(R, [](
 __device__ inline Smem make_smem(uint8_t* base, int R) {
   Smem L;
   L.ring.buf = base;
+  L.ho.slot_bytes = slot_bytes(R);
   carve(R, [&](int id, size_t at) {
     uint8_t* p = base + at;
     switch (id) {
@@ -149,27 +164,21 @@ __device__ inline Smem make_smem(uint8_t* base, int R) {
         L.ring.ttab = reinterpret_cast<QTask*>(p);
         break;
       case 3:
-        L.misc = reinterpret_cast<Misc*>(p);
-        L.ring.abort = &L.misc->abort;
+        L.ho.done = reinterpret_cast<uint64_t*>(p);
+        L.ho.freed = L.ho.done + kSlots;
         break;
       case 4:
-        L.wS = reinterpret_cast<df*>(p);
+        L.ring.abort = reinterpret_cast<volatile int*>(p);
         break;
       case 5:
-        L.rowS = reinterpret_cast<df*>(p);
-        L.rowInv = L.rowS + R;
+        L.fin = reinterpret_cast<Fin*>(p);
         break;
       case 6:
-        L.wM = reinterpret_cast<float*>(p);
-        L.wBad = reinterpret_cast<int*>(L.wM + R * kCW);
-        break;
-      case 7:
-        L.rowKc = reinterpret_cast<float*>(p);
-        L.rowOK = reinterpret_cast<int*>(L.rowKc + R);
-        break;
-      case 8:
         L.tab_hi = reinterpret_cast<float*>(p);
         L.tab_lo = L.tab_hi + 256;
+        break;
+      case 7:
+        L.ho.data = p;
         break;
     }
   });
@@ -229,72 +238,23 @@ struct StatOp {
       }
     }
   }
-  // warp partial of row r into smem
-  __device__ void end_row(const Smem& L, int r) {
+  // Warp partial (max, sum relative to the offset of the warp's max, NaN
+  // seen) of row r into the hand-off slot.
+  __device__ __forceinline__ void end_row(uint8_t* slot, int R, int r) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float Mw = warp_max_f(M);
-    df s{0.f, 0.f};
-    if (S != 0.0f) s.hi = __fmul_rn(S, pow2i(__fsub_rn(Kc, offset_of(Mw, c))));
-    s = df_warp_sum(s);
+    float s = 0.0f;
+    if (S != 0.0f) s = __fmul_rn(S, pow2i(__fsub_rn(Kc, offset_of(Mw, c))));
+    s = warp_sum_f(s);
     const int anybad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
-      L.wM[r * kCW + warp] = Mw;
-      L.wS[r * kCW + warp] = s;
-      L.wBad[r * kCW + warp] = anybad;
+      float* w = reinterpret_cast<float*>(slot + 16);
+      w[r * kCW + warp] = Mw;
+      w[(R + r) * kCW + warp] = s;
+      reinterpret_cast<int*>(w + 2 * R * kCW)[r * kCW + warp] = anybad;
     }
   }
 };
-
-// CTA partial (M, S.hi, S.lo, bad) of rows [0, nrows) into out[4r..4r+3].
-__device__ void stats_to_global(const Smem& L, int nrows, float c, float* out) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < nrows; r += kCW) {
-    const float m = lane < kCW ? L.wM[r * kCW + lane] : -INFINITY;
-    df s = lane < kCW ? L.wS[r * kCW + lane] : df{0.f, 0.f};
-    const int bw = lane < kCW ? L.wBad[r * kCW + lane] : 0;
-    const float Mc = warp_max_f(m);
-    if (s.hi != 0.0f) {
-      const float sc = pow2i(__fsub_rn(offset_of(m, c), offset_of(Mc, c)));
-      s = {__fmul_rn(s.hi, sc), __fmul_rn(s.lo, sc)};
-    }
-    s = df_warp_sum(s);
-    const int bad = __any_sync(0xffffffffu, bw);
-    if (lane == 0) {
-      float* o = out + 4 * r;
-      o[0] = Mc;
-      o[1] = s.hi;
-      o[2] = s.lo;
-      o[3] = __int_as_float(bad);
-    }
-  }
-}
-
-// Row statistics (into smem slot rs) from the S slice partials of row r at
-// float offset 4r of each slice's part block; same order everywhere.
-__device__ void stats_combine(const SampleArgs& a, const Smem& L, int b, int r, int rs) {
-  float M = -INFINITY;
-  int bad = 0;
-  for (int s = 0; s < a.S; ++s) {
-    const float* p = a.ws.part(b, s) + 4 * r;
-    M = fmaxf(M, ld_cg_f(p));
-    bad |= __float_as_int(ld_cg_f(p + 3));
-  }
-  const float Kc = offset_of(M, a.c);
-  df S{0.f, 0.f};
-  for (int s = 0; s < a.S; ++s) {
-    const float* p = a.ws.part(b, s) + 4 * r;
-    const float sh = ld_cg_f(p + 1);
-    if (sh != 0.0f) {
-      const float sc = pow2i(__fsub_rn(offset_of(ld_cg_f(p), a.c), Kc));
-      S = df_add(S, df{__fmul_rn(sh, sc), __fmul_rn(ld_cg_f(p + 2), sc)});
-    }
-  }
-  const bool ok = !bad && isfinite(M) && fabsf(Kc) < 4194304.0f && S.hi > 0.0f && isfinite(S.hi);
-  L.rowKc[rs] = Kc;
-  L.rowS[rs] = S;
-  L.rowInv[rs] = ok ? df_recip(S) : df{0.f, 0.f};
-  L.rowOK[rs] = ok ? 1 : 0;
-}
 
 // ------------------------------------------------------------------ accurate path
 // 2^(z C - Kc) in pair arithmetic (C = log2(e)/T as Chi + Clo, Kc an integer).
@@ -314,13 +274,6 @@ constexpr float kAccRho = 4e-12f;
 // Upper bound on the sum of the computed fp32 probabilities of a row.
 constexpr float kQmax = 1.001f;
 
-__device__ inline void load_table(const Smem& L) {
-  for (int i = threadIdx.x; i < 256; i += kCons) {
-    L.tab_hi[i] = kExp2Tab.hi[i];
-    L.tab_lo[i] = kExp2Tab.lo[i];
-  }
-}
-
 // ------------------------------------------------------------------ draw entries
 // fp32 path: r = max(0, q - p), q = exp2(z c - Kq) * Rq (r = q when tp is
 // null). aq / ap accumulate sum q x and sum p x (x the exponent argument,
@@ -328,20 +281,21 @@ __device__ inline void load_table(const Smem& L) {
 // of the sweep follows.
 template <class E>
 struct FastEntries {
-  const uint4* tq;
+  const uint4* tq;  // rows read by entries() (the draw's search)
   const uint4* tp;
+  bool pair;        // residual q - p (else q alone)
   float c, Kq, Rq, Kp, Rp;
   __device__ __forceinline__ float run(const uint4& vq, const uint4& vp, float (&r)[E::kVec],
                                        float& aq, float& ap) const {
     float zq[E::kVec], zp[E::kVec];
     E::unpack(vq, zq);
-    if (tp) E::unpack(vp, zp);
+    if (pair) E::unpack(vp, zp);
 #pragma unroll
     for (int k = 0; k < E::kVec; ++k) {
       const float xa = __fmaf_rn(zq[k], c, -Kq);
       const float q = __fmul_rn(ex2_approx(xa), Rq);
       aq = __fmaf_rn(q, fmaxf(xa, -1.0e4f), aq);
-      if (tp) {
+      if (pair) {
         const float xb = __fmaf_rn(zp[k], c, -Kp);
         const float p = __fmul_rn(ex2_approx(xb), Rp);
         ap = __fmaf_rn(p, fmaxf(xb, -1.0e4f), ap);
@@ -363,7 +317,7 @@ struct FastEntries {
     float r[E::kVec];
     float a0 = 0.f, a1 = 0.f;
     const uint4 vq = ldg_nc_v4(tq + vi);
-    const uint4 vp = tp ? ldg_nc_v4(tp + vi) : vq;
+    const uint4 vp = pair ? ldg_nc_v4(tp + vi) : vq;
     const float vs = run(vq, vp, r, a0, a1);
 #pragma unroll
     for (int k = 0; k < E::kVec; ++k) rd[k] = {r[k], 0.f};
@@ -374,8 +328,9 @@ struct FastEntries {
 // double-float path.
 template <class E>
 struct AccEntries {
-  const uint4* tq;
+  const uint4* tq;  // rows read by entries() (the draw's search)
   const uint4* tp;
+  bool pair;        // residual q - p (else q alone)
   float Chi, Clo, Kq, Kp;
   df Iq, Ip;
   const float* th;
@@ -384,14 +339,14 @@ struct AccEntries {
                                     float& ps) const {
     float zq[E::kVec], zp[E::kVec];
     E::unpack(vq, zq);
-    if (tp) E::unpack(vp, zp);
+    if (pair) E::unpack(vp, zp);
     df vs{0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < E::kVec; ++k) {
       const df q = df_mul(acc_elem(zq[k], Chi, Clo, Kq, th, tl), Iq);
       qs = __fadd_rn(qs, q.hi);
       df rk = q;
-      if (tp) {
+      if (pair) {
         const df p = df_mul(acc_elem(zp[k], Chi, Clo, Kp, th, tl), Ip);
         ps = __fadd_rn(ps, p.hi);
         rk = df_sub(q, p);
@@ -405,7 +360,7 @@ struct AccEntries {
   __device__ __forceinline__ df entries(int vi, df (&rd)[E::kVec]) const {
     float a0 = 0.f, a1 = 0.f;
     const uint4 vq = ldg_nc_v4(tq + vi);
-    const uint4 vp = tp ? ldg_nc_v4(tp + vi) : vq;
+    const uint4 vp = pair ? ldg_nc_v4(tp + vi) : vq;
     return run(vq, vp, rd, a0, a1);
   }
 };
@@ -424,402 +379,936 @@ __device__ __forceinline__ RowPtrs<E> row_ptrs(const SampleArgs& a, int b) {
           static_cast<const T*>(a.draft) + size_t(b) * a.K * a.V};
 }
 
-// Consumers: block sum of a per-thread pair and four floats (thread 0 gets
-// the totals).
-__device__ void cta_reduce(Misc& ms, df& r, float (&f)[4]) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  r = df_warp_sum(r);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) f[j] = warp_sum_f(f[j]);
-  if (lane == 0) {
-    ms.wR[warp] = r;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ms.wF[j][warp] = f[j];
-  }
-  consumers_sync();
-  if (threadIdx.x == 0) {
-    r = {0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) f[j] = 0.f;
-    for (int w = 0; w < kCW; ++w) {
-      r = df_add(r, ms.wR[w]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) f[j] += ms.wF[j][w];
+// Rows of a draw stage (SW, FA, FB) from the task's aux: target row j and,
+// for a residual draw before the bonus position, draft row j.
+struct DrawRows {
+  int j;
+  bool pair;
+};
+__device__ __forceinline__ DrawRows draw_rows(int K, int aux) {
+  const int j = aux & 0xff, mode = aux >> 8;
+  return {j, mode == kModeResidual && j < K};
+}
+
+// ------------------------------------------------------------------ finisher
+// Everything below runs in the finisher warp (32 lanes). Data written by
+// other CTAs (partials, unit sums, row state) is read through L2 (ld.cg).
+
+// Row statistics of rows [0, nrows) (float offset 4r of each slice's
+// partials: max, sum hi, sum lo, NaN seen) into the finisher scratch: the
+// partials of a group of rows are loaded by all lanes at once (one memory
+// round trip per group), then lane r combines row r from shared memory.
+__device__ void stats_rows(const SampleArgs& a, Fin& F, int b, int nrows) {
+  const int lane = threadIdx.x & 31, S = a.S;
+  const int per_group = 256 / S > 0 ? 256 / S : 1;
+  for (int r0 = 0; r0 < nrows; r0 += per_group) {
+    const int rg = min(per_group, nrows - r0), items = rg * S;
+#pragma unroll 8
+    for (int i = lane; i < items; i += 32) {
+      const int r = r0 + i / S, sl = i % S;
+      F.item[i] = __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, sl) + 4 * r));
     }
+    __syncwarp();
+    for (int rr = lane; rr < rg; rr += 32) {
+      const float4* it = F.item + rr * S;
+      float M = -INFINITY;
+      int bad = 0;
+      for (int sl = 0; sl < S; ++sl) {
+        M = fmaxf(M, it[sl].x);
+        bad |= __float_as_int(it[sl].w);
+      }
+      const float Kc = offset_of(M, a.c);
+      df Ssum{0.f, 0.f};
+      for (int sl = 0; sl < S; ++sl) {
+        if (it[sl].y != 0.0f) {
+          const float sc = pow2i(__fsub_rn(offset_of(it[sl].x, a.c), Kc));
+          Ssum = df_add(Ssum, df{__fmul_rn(it[sl].y, sc), __fmul_rn(it[sl].z, sc)});
+        }
+      }
+      const bool ok = !bad && isfinite(M) && fabsf(Kc) < 4194304.0f && Ssum.hi > 0.0f &&
+                      isfinite(Ssum.hi);
+      const int r = r0 + rr;
+      F.rowKc[r] = Kc;
+      F.rowS[r] = Ssum;
+      F.rowInv[r] = ok ? df_recip(Ssum) : df{0.f, 0.f};
+      F.rowOK[r] = ok ? 1 : 0;
+    }
+    __syncwarp();
   }
 }
 
-// Consumers: publish the task's partials (already stored) and arrive on the
-// row's stage counter. Returns true in every thread when this CTA completed
-// the stage (then it must continue the row).
-__device__ bool arrive_row(const SampleArgs& a, Misc& ms, int b) {
-  __threadfence();
-  consumers_sync();
-  if (threadIdx.x == 0) {
-    const uint32_t old = atomicAdd(&a.ws.row_cnt()[b], 1u);
-    const int last = (old == uint32_t(a.S) - 1);
-    if (last) {
-      a.ws.row_cnt()[b] = 0;  // the next stage counts from zero
-      __threadfence();
+// Sums over the S slices of the four floats at offset 0 of each slice's
+// partials, lanes in parallel: x0 + x1 as a pair, x2 and x3 as floats (or
+// x2 + x3 as a second pair when `pairs`). Every lane gets the totals.
+struct SliceSums {
+  df p0, p1;
+  float f2, f3;
+};
+__device__ SliceSums slice_sums(const SampleArgs& a, int b, bool pairs) {
+  const int lane = threadIdx.x & 31;
+  df p0{0.f, 0.f}, p1{0.f, 0.f};
+  float f2 = 0.f, f3 = 0.f;
+  for (int sl = lane; sl < a.S; sl += 32) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, sl)));
+    p0 = df_add(p0, df{v.x, v.y});
+    if (pairs) {
+      p1 = df_add(p1, df{v.z, v.w});
+    } else {
+      f2 += v.z;
+      f3 += v.w;
     }
-    ms.last = last;
   }
-  consumers_sync();
-  return ms.last != 0;
+  SliceSums r;
+  r.p0 = df_warp_sum(p0);
+  r.p1 = pairs ? df_warp_sum(p1) : df{0.f, 0.f};
+  r.f2 = warp_sum_f(f2);
+  r.f3 = warp_sum_f(f3);
+  return r;
 }
 
-__device__ void write_outputs(const SampleArgs& a, const Misc& ms, int b, int n, int token,
-                              int flags, bool error) {
-  const int K = a.K;
-  for (int i = threadIdx.x; i <= K; i += kCons) {
+// Writes row b's outputs: accepted tokens 0..n-1 (lane i holds draft token i
+// in `tok`), `token` at n, -1 after (all -1 on error), num_accepted and
+// row_info; counts the row done. The count only lets the producers stop, so
+// no fence orders the outputs before it (the launch's end publishes them).
+__device__ void write_outputs(const SampleArgs& a, int b, int n, int token, int flags, bool error,
+                              int tok) {
+  const int lane = threadIdx.x & 31, K = a.K;
+  if (lane <= K) {
     int32_t v;
     if (error) v = -1;
-    else if (i < n) v = ms.tok[i];
-    else if (i == n) v = token;
+    else if (lane < n) v = tok;
+    else if (lane == n) v = token;
     else v = -1;
-    a.out_tokens[size_t(b) * (K + 1) + i] = v;
+    a.out_tokens[size_t(b) * (K + 1) + lane] = v;
   }
-  if (threadIdx.x == 0) {
+  if (lane == 0) {
     a.out_n[b] = error ? -1 : n;
     if (a.row_info) a.row_info[b] = flags;
+    atomicAdd(&a.ws.hdr()->rows_done, 1u);
   }
-  __threadfence();
-  consumers_sync();
-  if (threadIdx.x == 0) atomicAdd(&a.ws.hdr()->rows_done, 1u);
+  __syncwarp();
 }
 
-// Locate the slice, then the 32-vector unit, holding t, then the entry (warp 0
-// walks the unit). ms.token / ms.cert receive the result; certified iff both
-// boundaries of the drawn entry are farther than 2E from t.
-template <class E, class Entries>
-__device__ void search_draw(const SampleArgs& a, Misc& ms, int b, const Entries& ent) {
+// Draft tokens of row b, lane i holding position i (0 past K).
+__device__ __forceinline__ int load_tokens(const SampleArgs& a, int b) {
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x < 32) {
-    const df t = ms.tstar;
-    // slice: lanes scan 32 slices at a time; the first slice with mass whose
-    // end passes t, else the last slice with mass (rounding fallback)
-    int ss = -1;
-    df pre_s{0.f, 0.f};
-    {
-      df sbase{0.f, 0.f};
-      for (int s0 = 0; s0 < a.S; s0 += 32) {
-        const int s = s0 + lane;
-        df x{0.f, 0.f};
-        if (s < a.S) {
-          const float* p = a.ws.part(b, s);
-          x = df{ld_cg_f(p), ld_cg_f(p + 1)};
-        }
-        df inc = x;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const df y = df_shfl_up(inc, o);
-          if (lane >= o) inc = df_add(inc, y);
-        }
-        const df lo = df_add(sbase, df_sub(inc, x));
-        const unsigned hm = __ballot_sync(0xffffffffu, x.hi > 0.0f && df_gt(df_add(lo, x), t));
-        const unsigned pm = __ballot_sync(0xffffffffu, x.hi > 0.0f);
-        if (hm) {
-          const int l = __ffs(int(hm)) - 1;
-          ss = s0 + l;
-          pre_s = df_shfl(lo, l);
-          break;
-        }
-        if (pm) {
-          const int l = 31 - __clz(int(pm));
-          ss = s0 + l;
-          pre_s = df_shfl(lo, l);
-        }
-        sbase = df_add(sbase, df_shfl(inc, 31));
-      }
-    }
-    int token = -1;
-    df tlo = pre_s, thi = pre_s;
-    if (ss >= 0) {
-      int v0, v1;
-      slice_range(a.nvec, a.S, ss, v0, v1);
-      const int nu = (v1 - v0 + 31) / 32;
-      // unit: lanes scan 32 units at a time
-      const float2* up = a.ws.units(b, ss);
-      int us = -1;
-      df ubase = pre_s, ubase_s = pre_s;
-      for (int u0 = 0; u0 < nu && us < 0; u0 += 32) {
-        const int u = u0 + lane;
-        df x{0.f, 0.f};
-        if (u < nu) x = df{__ldcg(&up[u].x), __ldcg(&up[u].y)};
-        df inc = x;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const df y = df_shfl_up(inc, o);
-          if (lane >= o) inc = df_add(inc, y);
-        }
-        const df lo = df_add(ubase, df_sub(inc, x));
-        const bool hit = x.hi > 0.0f && df_gt(df_add(lo, x), t);
-        const unsigned hm = __ballot_sync(0xffffffffu, hit);
-        const unsigned pm = __ballot_sync(0xffffffffu, u < nu && x.hi > 0.0f);
-        if (hm) {
-          const int l = __ffs(int(hm)) - 1;
-          us = u0 + l;
-          ubase_s = df_shfl(lo, l);
-        } else if (pm) {
-          const int l = 31 - __clz(int(pm));
-          ubase_s = df_shfl(lo, l);  // last unit with mass so far (rounding fallback)
-          us = -(u0 + l) - 2;
-        }
-        ubase = df_add(ubase, df_shfl(inc, 31));
-      }
-      if (us < -1) us = -us - 2;
-      if (us >= 0) {
-        // entries of the unit's 32 vectors, lane-minor
-        const int vi = v0 + us * 32 + lane;
-        df r[E::kVec];
-        df vs{0.f, 0.f};
-        if (vi < v1) {
-          vs = ent.entries(vi, r);
-        } else {
-#pragma unroll
-          for (int k = 0; k < E::kVec; ++k) r[k] = {0.f, 0.f};
-        }
-        df inc = vs;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const df y = df_shfl_up(inc, o);
-          if (lane >= o) inc = df_add(inc, y);
-        }
-        df c0 = df_add(ubase_s, df_sub(inc, vs));
-        int tk = -1, lk = -1;
-        df lo{0.f, 0.f}, hi{0.f, 0.f}, l0{0.f, 0.f}, l1{0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k < E::kVec; ++k) {
-          const df c1 = df_add(c0, r[k]);
-          if (r[k].hi > 0.0f) {
-            lk = vi * E::kVec + k;
-            l0 = c0;
-            l1 = c1;
-            if (tk < 0 && df_gt(c1, t)) {
-              tk = vi * E::kVec + k;
-              lo = c0;
-              hi = c1;
-            }
-          }
-          c0 = c1;
-        }
-        const unsigned hm = __ballot_sync(0xffffffffu, tk >= 0);
-        const unsigned pm = __ballot_sync(0xffffffffu, lk >= 0);
-        if (hm) {
-          const int l = __ffs(int(hm)) - 1;
-          token = __shfl_sync(0xffffffffu, tk, l);
-          tlo = df_shfl(lo, l);
-          thi = df_shfl(hi, l);
-        } else if (pm) {
-          const int l = 31 - __clz(int(pm));
-          token = __shfl_sync(0xffffffffu, lk, l);
-          tlo = df_shfl(l0, l);
-          thi = df_shfl(l1, l);
-        }
-      }
-    }
-    if (lane == 0) {
-      const float m1 = df_sub(t, tlo).hi, m2 = df_sub(thi, t).hi;
-      ms.token = token;
-      ms.cert = (token >= 0 && fminf(m1, m2) > 2.02f * ms.E) ? 1 : 0;
-    }
-  }
-  consumers_sync();
+  return lane < a.K ? a.tokens[size_t(b) * a.K + lane] : 0;
 }
 
-// ------------------------------------------------------------------ stage finishers
+// Starts the draw at position j: the residual of target / draft row j with
+// the fp32 statistics given (lane 0's values), or (j == K) the bonus
+// distribution q_K, whose statistics the BS stage supplies first.
+__device__ void start_draw(const SampleArgs& a, int b, int j, int flags, float Kq, float Rq,
+                           float Kp, float Rp) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    RowState* st = row_state(a, b);
+    st->flags = flags;
+    if (j < a.K) {
+      st->Kq = Kq;
+      st->Rq = Rq;
+      st->Kp = Kp;
+      st->Rp = Rp;
+      enqueue_row_stage(a.ws, kSW, b, a.S, j | (kModeResidual << 8));
+    } else {
+      enqueue_row_stage(a.ws, kBS, b, a.S, a.K | (kModeQ << 8));
+    }
+  }
+  __syncwarp();
+}
+
+// Continues the accept tests from position i0 given the test states (lane i
+// holds test i's state in `state`, its offsets / fp32 1/S of target and
+// draft row i in rk_t, rr_t, rk_d, rr_d): skips accepted positions and stops
+// at a rejection (draw), an invalid row (error), an ambiguous test (AR
+// stage) or the end (bonus draw).
+__device__ void continue_tests(const SampleArgs& a, int b, int i0, int flags, int state, int tok,
+                               float rk_t, float rr_t, float rk_d, float rr_d) {
+  const int lane = threadIdx.x & 31, K = a.K;
+  const unsigned pend = __ballot_sync(0xffffffffu, lane >= i0 && lane < K && state != kAccept);
+  if (!pend) {
+    start_draw(a, b, K, flags, 0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const int i = __ffs(int(pend)) - 1;
+  const int s = __shfl_sync(0xffffffffu, state, i);
+  if (s == kReject) {
+    start_draw(a, b, i, flags, __shfl_sync(0xffffffffu, rk_t, i), __shfl_sync(0xffffffffu, rr_t, i),
+               __shfl_sync(0xffffffffu, rk_d, i), __shfl_sync(0xffffffffu, rr_d, i));
+    return;
+  }
+  if (s == kInvalid) {
+    if (lane == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
+    write_outputs(a, b, i, -1, flags, true, tok);
+    return;
+  }
+  // ambiguous: double-float sums of target and draft row i (AR stage)
+  if (lane == 0) {
+    row_state(a, b)->flags = flags | SPEC_ROW_ACCEPT_REFINED;
+    enqueue_row_stage(a.ws, kAR, b, a.S, i);
+  }
+  __syncwarp();
+}
+
 // P1 complete: statistics of the 2K rows, accept tests, first rejection.
+// Memory round trips: the draft tokens, uniforms and slice partials load
+// together, then the logits at the draft tokens.
 template <class E>
 __device__ void finish_p1(const SampleArgs& a, const Smem& L, int b) {
-  Misc& ms = *L.misc;
-  const int K = a.K, V = a.V, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lane = threadIdx.x & 31, K = a.K, V = a.V;
+  Fin& F = *L.fin;
+  RowState* st = row_state(a, b);
   const RowPtrs<E> rp = row_ptrs<E>(a, b);
-  for (int r = tid; r < 2 * K; r += kCons) stats_combine(a, L, b, r, r);
-  if (warp == 1) {
-    int bad = 0;
-    if (lane < K) {
-      const int d = a.tokens[size_t(b) * K + lane];
-      ms.tok[lane] = d;
-      if (d < 0 || d >= V) {
-        bad = 1;
-        ms.zt_d[lane] = 0.f;
-        ms.zd_d[lane] = 0.f;
-      } else {
-        ms.zt_d[lane] = E::load(rp.tgt + size_t(lane) * V, d);
-        ms.zd_d[lane] = E::load(rp.drf + size_t(lane) * V, d);
-      }
-    }
-    if (lane <= K) ms.u[lane] = a.uniforms[size_t(b) * (K + 1) + lane];
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) ms.bad_token = bad;
+  const int d = load_tokens(a, b);
+  const float u = lane < K ? a.uniforms[size_t(b) * (K + 1) + lane] : 1.0f;
+  stats_rows(a, F, b, 2 * K);
+  const bool badtok_lane = lane < K && (d < 0 || d >= V);
+  float zt = 0.f, zd = 0.f;
+  if (lane < K && !badtok_lane) {
+    zt = E::load(rp.tgt + size_t(lane) * V, d);
+    zd = E::load(rp.drf + size_t(lane) * V, d);
   }
-  consumers_sync();
+  for (int r = lane; r < 2 * K; r += 32) {
+    st->rK[r] = F.rowKc[r];
+    st->rR[r] = F.rowInv[r].hi;
+  }
   const float c = a.c;
-  if (warp == 0 && lane < K) {
-    const int i = lane, rt = 2 * i, rd = 2 * i + 1;
-    int st;
+  int s = kAccept;
+  float rk_t = 0.f, rr_t = 0.f, rk_d = 0.f, rr_d = 0.f;
+  if (lane < K) {
+    const int rt = 2 * lane, rd = 2 * lane + 1;
+    rk_t = F.rowKc[rt];
+    rr_t = F.rowInv[rt].hi;
+    rk_d = F.rowKc[rd];
+    rr_d = F.rowInv[rd].hi;
     float qd = -1.f, pd = -1.f;
-    if (ms.bad_token || !L.rowOK[rt] || !L.rowOK[rd]) {
-      st = kInvalid;
+    if (badtok_lane || !F.rowOK[rt] || !F.rowOK[rd]) {
+      s = kInvalid;
     } else {
-      const float zt = ms.zt_d[i], zd = ms.zd_d[i], u = ms.u[i];
-      const float xt = __fmaf_rn(zt, c, -L.rowKc[rt]);
-      const float xd = __fmaf_rn(zd, c, -L.rowKc[rd]);
-      qd = __fmul_rn(ex2_approx(xt), L.rowInv[rt].hi);
-      pd = __fmul_rn(ex2_approx(xd), L.rowInv[rd].hi);
+      const float xt = __fmaf_rn(zt, c, -rk_t);
+      const float xd = __fmaf_rn(zd, c, -rk_d);
+      qd = __fmul_rn(ex2_approx(xt), rr_t);
+      pd = __fmul_rn(ex2_approx(xd), rr_d);
       if (zd == -INFINITY) {
-        st = kAccept;  // p(d) = 0 accepts
+        s = kAccept;  // p(d) = 0 accepts
       } else if (zt == -INFINITY) {
-        st = kReject;  // q(d) = 0: u < 0 never holds
+        s = kReject;  // q(d) = 0: u < 0 never holds
       } else if (u == 0.0f) {
-        st = kAccept;  // 0 < q(d)/p(d) whenever q(d) > 0
+        s = kAccept;  // 0 < q(d)/p(d) whenever q(d) > 0
       } else {
         // ratio = 2^(xt - xd) * S_d / S_t; relative error bound: exp2, the
         // arguments (with the fp32 temperature constant), both row sums and
         // five roundings
         const float ar = __fsub_rn(xt, xd);
-        const float ratio = __fmul_rn(__fmul_rn(ex2_approx(ar), L.rowS[rd].hi), L.rowInv[rt].hi);
+        const float ratio = __fmul_rn(__fmul_rn(ex2_approx(ar), F.rowS[rd].hi), rr_t);
         const float dS = a.bd.ex2 + kLn2f * kU * a.bd.xbar + a.bd.gamma1;
         const float beta =
             1.1f * (a.bd.ex2 + 6.0f * kU + 2.0f * dS +
                     kLn2f * kU * (2.0f * fabsf(xt) + 2.0f * fabsf(xd) + fabsf(ar) +
                                   2.0f * a.bd.xbar + 4.0f));
         if (!(ar < 126.0f) || ratio >= 1.0f / (1.0f - beta)) {
-          st = kAccept;  // ratio >= 1 for certain
+          s = kAccept;  // ratio >= 1 for certain
         } else {
           const float rlo = fminf(1.0f, __fmul_rn(ratio, 1.0f - beta));
           const float rhi = fminf(1.0f, __fmul_rn(ratio, 1.0f + beta));
-          st = (u < rlo) ? kAccept : (u >= rhi && ar > -120.0f ? kReject : kAmbiguous);
+          s = (u < rlo) ? kAccept : (u >= rhi && ar > -120.0f ? kReject : kAmbiguous);
         }
       }
     }
-    ms.acc_state[i] = st;
-    ms.qd[i] = qd;
-    ms.pd[i] = pd;
+    st->acc[lane] = int8_t(s);
     if (a.q_at_d) {
-      a.q_at_d[size_t(b) * K + i] = qd;
-      a.p_at_d[size_t(b) * K + i] = pd;
+      a.q_at_d[size_t(b) * K + lane] = qd;
+      a.p_at_d[size_t(b) * K + lane] = pd;
     }
   }
-  consumers_sync();
-
-  int flags = 0, n = 0;
-  bool error = ms.bad_token != 0;
-  while (!error) {
-    int i = n;
-    while (i < K && ms.acc_state[i] == kAccept) ++i;
-    n = i;
-    if (i == K) break;
-    const int st = ms.acc_state[i];
-    if (st == kInvalid) {
-      error = true;
-      break;
-    }
-    if (st == kReject) break;
-    // ambiguous: decide with accurate sums of target and draft row i over the
-    // whole vocabulary (this CTA alone; probability ~1e-6 per test)
-    flags |= SPEC_ROW_ACCEPT_REFINED;
-    load_table(L);
-    consumers_sync();
-    df s0{0.f, 0.f}, s1{0.f, 0.f};
-    {
-      const uint4* p0 = reinterpret_cast<const uint4*>(rp.tgt + size_t(i) * V);
-      const uint4* p1 = reinterpret_cast<const uint4*>(rp.drf + size_t(i) * V);
-      const float K0 = L.rowKc[2 * i], K1 = L.rowKc[2 * i + 1];
-      for (int vi = tid; vi < a.nvec; vi += kCons) {
-        float z[E::kVec];
-        E::unpack(ldg_nc_v4(p0 + vi), z);
-#pragma unroll
-        for (int k = 0; k < E::kVec; ++k)
-          s0 = df_add(s0, acc_elem(z[k], a.Chi, a.Clo, K0, L.tab_hi, L.tab_lo));
-        E::unpack(ldg_nc_v4(p1 + vi), z);
-#pragma unroll
-        for (int k = 0; k < E::kVec; ++k)
-          s1 = df_add(s1, acc_elem(z[k], a.Chi, a.Clo, K1, L.tab_hi, L.tab_lo));
-      }
-      s0 = df_warp_sum(s0);
-      s1 = df_warp_sum(s1);
-      if (lane == 0) {
-        ms.wA[warp] = s0;
-        ms.wB[warp] = s1;
-      }
-      consumers_sync();
-      s0 = s1 = {0.f, 0.f};
-      for (int w = 0; w < kCW; ++w) {
-        s0 = df_add(s0, ms.wA[w]);
-        s1 = df_add(s1, ms.wB[w]);
-      }
-    }
-    // ratio = 2^((zt C - Kt) - (zd C - Kd)) * S_d / S_t in pair arithmetic
-    const float zt = ms.zt_d[i], zd = ms.zd_d[i], u = ms.u[i];
-    const df xt =
-        df_add_f(df_add(two_prod(zt, a.Chi), df{__fmul_rn(zt, a.Clo), 0.f}), -L.rowKc[2 * i]);
-    const df xd =
-        df_add_f(df_add(two_prod(zd, a.Chi), df{__fmul_rn(zd, a.Clo), 0.f}), -L.rowKc[2 * i + 1]);
-    const df ar = df_sub(xt, xd);
-    bool acc;
-    if (ar.hi >= 127.0f) {
-      acc = true;
-    } else if (ar.hi < -126.0f) {
-      acc = false;  // ratio < 2^-100 < u (u > 0 here)
-    } else {
-      const df ratio = df_mul(df_mul(df_exp2(ar.hi, ar.lo, L.tab_hi, L.tab_lo), s1), df_recip(s0));
-      acc = (ratio.hi >= 1.0f) || df_gt(ratio, df{u, 0.f});
-      if (fabsf(__fsub_rn(u, fminf(1.0f, ratio.hi))) <= 1e-10f * ratio.hi) flags |= SPEC_ROW_UNCERTIFIED;
-    }
-    consumers_sync();
-    if (!acc) break;
-    if (tid == 0) ms.acc_state[i] = kAccept;
-    consumers_sync();
-    n = i + 1;
-  }
-  if (error) {
-    if (tid == 0 && a.err) atomicOr(a.err, ms.bad_token ? SPEC_DERR_TOKEN : SPEC_DERR_LOGITS);
-    write_outputs(a, ms, b, n, -1, flags, true);
+  if (__any_sync(0xffffffffu, badtok_lane)) {
+    if (lane == 0 && a.err) atomicOr(a.err, SPEC_DERR_TOKEN);
+    write_outputs(a, b, 0, -1, 0, true, d);
     return;
   }
-  if (tid == 0) {
-    RowState* st = a.ws.rowstate(b);
-    st->n = n;
-    st->flags = flags;
-    st->err = 0;
-    if (n < K) {
-      st->mode = kModeResidual;
-      st->Kq = L.rowKc[2 * n];
-      st->Rq = L.rowInv[2 * n].hi;
-      st->Kp = L.rowKc[2 * n + 1];
-      st->Rp = L.rowInv[2 * n + 1].hi;
-    } else {
-      st->mode = kModeQ;
-    }
-    __threadfence();
-    enqueue_row_stage(a.ws, n < K ? kSW : kBS, b, a.S, n);
+  continue_tests(a, b, 0, 0, s, d, rk_t, rr_t, rk_d, rr_d);
+}
+
+// AR complete: decide accept test i from double-float row sums.
+template <class E>
+__device__ void finish_ar(const SampleArgs& a, const Smem& L, int b, int i) {
+  const int lane = threadIdx.x & 31, K = a.K;
+  RowState* st = row_state(a, b);
+  const int d = load_tokens(a, b);
+  int state = kAccept;
+  float rk_t = 0.f, rr_t = 0.f, rk_d = 0.f, rr_d = 0.f;
+  if (lane < K) {
+    state = __ldcg(&st->acc[lane]);
+    rk_t = __ldcg(&st->rK[2 * lane]);
+    rr_t = __ldcg(&st->rR[2 * lane]);
+    rk_d = __ldcg(&st->rK[2 * lane + 1]);
+    rr_d = __ldcg(&st->rR[2 * lane + 1]);
   }
+  int flags = __ldcg(&st->flags);
+  const float u = a.uniforms[size_t(b) * (K + 1) + i];
+  const SliceSums ss = slice_sums(a, b, true);
+  const df S0 = ss.p0, S1 = ss.p1;
+  const RowPtrs<E> rp = row_ptrs<E>(a, b);
+  const int di = __shfl_sync(0xffffffffu, d, i);
+  const float zt = E::load(rp.tgt + size_t(i) * a.V, di);
+  const float zd = E::load(rp.drf + size_t(i) * a.V, di);
+  // ratio = 2^((zt C - Kt) - (zd C - Kd)) * S_d / S_t in pair arithmetic
+  const df xt = df_add_f(df_add(two_prod(zt, a.Chi), df{__fmul_rn(zt, a.Clo), 0.f}),
+                         -__shfl_sync(0xffffffffu, rk_t, i));
+  const df xd = df_add_f(df_add(two_prod(zd, a.Chi), df{__fmul_rn(zd, a.Clo), 0.f}),
+                         -__shfl_sync(0xffffffffu, rk_d, i));
+  const df ar = df_sub(xt, xd);
+  bool acc;
+  if (ar.hi >= 127.0f) {
+    acc = true;
+  } else if (ar.hi < -126.0f) {
+    acc = false;  // ratio < 2^-100 < u (u > 0 here)
+  } else {
+    const df ratio = df_mul(df_mul(df_exp2(ar.hi, ar.lo, L.tab_hi, L.tab_lo), S1), df_recip(S0));
+    acc = (ratio.hi >= 1.0f) || df_gt(ratio, df{u, 0.f});
+    if (fabsf(__fsub_rn(u, fminf(1.0f, ratio.hi))) <= 1e-10f * ratio.hi)
+      flags |= SPEC_ROW_UNCERTIFIED;
+  }
+  if (acc) {
+    if (lane == i) {
+      state = kAccept;
+      st->acc[i] = kAccept;
+    }
+    continue_tests(a, b, i + 1, flags, state, d, rk_t, rr_t, rk_d, rr_d);
+  } else {
+    start_draw(a, b, i, flags, __shfl_sync(0xffffffffu, rk_t, i), __shfl_sync(0xffffffffu, rr_t, i),
+               __shfl_sync(0xffffffffu, rk_d, i), __shfl_sync(0xffffffffu, rr_d, i));
+  }
+}
+
+// BS complete: statistics of target row K, then the bonus draw.
+__device__ void finish_bs(const SampleArgs& a, const Smem& L, int b) {
+  const int lane = threadIdx.x & 31;
+  Fin& F = *L.fin;
+  RowState* st = row_state(a, b);
+  const int flags = __ldcg(&st->flags);
+  stats_rows(a, F, b, 1);
+  if (!F.rowOK[0]) {
+    const int d = load_tokens(a, b);
+    if (lane == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
+    write_outputs(a, b, a.K, -1, flags, true, d);
+    return;
+  }
+  if (lane == 0) {
+    st->Kq = F.rowKc[0];
+    st->Rq = F.rowInv[0].hi;
+    enqueue_row_stage(a.ws, kSW, b, a.S, a.K | (kModeQ << 8));
+  }
+  __syncwarp();
+}
+
+// The slice sums of a draw stage, lanes in parallel: lane l holds slices l
+// and l + 32 (x0 + x1 as a pair in xa / xb, the other two floats in f2 / f3),
+// and the row totals (every lane).
+struct DrawSlices {
+  df xa, xb;  // this lane's slices
+  df total;
+  float f2, f3;
+};
+__device__ DrawSlices draw_slices(const SampleArgs& a, int b) {
+  const int lane = threadIdx.x & 31;
+  DrawSlices r;
+  r.xa = r.xb = df{0.f, 0.f};
+  float f2 = 0.f, f3 = 0.f;
+  if (lane < a.S) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, lane)));
+    r.xa = df{v.x, v.y};
+    f2 = v.z;
+    f3 = v.w;
+  }
+  if (lane + 32 < a.S) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, lane + 32)));
+    r.xb = df{v.x, v.y};
+    f2 += v.z;
+    f3 += v.w;
+  }
+  r.total = df_warp_sum(df_add(r.xa, r.xb));
+  r.f2 = warp_sum_f(f2);
+  r.f3 = warp_sum_f(f3);
+  return r;
+}
+
+// Locates t in the row's draw entries: the slice (from the lanes' slice
+// sums), then the 32-vector unit, then the entry (the warp walks the unit).
+// Returns the token (-1 if none) and whether it is certified: both
+// boundaries of the drawn entry farther than 2.02 E from t.
+template <class E, class Entries>
+__device__ int search_draw(const SampleArgs& a, int b, const Entries& ent, const DrawSlices& sl,
+                           df t, float Eb, bool& cert) {
+  const int lane = threadIdx.x & 31;
+  // slice: lanes scan 32 slices at a time; the first slice with mass whose
+  // end passes t, else the last slice with mass (rounding fallback)
+  int ss = -1;
+  df pre_s{0.f, 0.f};
+  {
+    df sbase{0.f, 0.f};
+    for (int s0 = 0; s0 < a.S; s0 += 32) {
+      const df x = (s0 == 0) ? sl.xa : sl.xb;
+      df inc = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const df y = df_shfl_up(inc, o);
+        if (lane >= o) inc = df_add(inc, y);
+      }
+      const df lo = df_add(sbase, df_sub(inc, x));
+      const unsigned hm = __ballot_sync(0xffffffffu, x.hi > 0.0f && df_gt(df_add(lo, x), t));
+      const unsigned pm = __ballot_sync(0xffffffffu, x.hi > 0.0f);
+      if (hm) {
+        const int l = __ffs(int(hm)) - 1;
+        ss = s0 + l;
+        pre_s = df_shfl(lo, l);
+        break;
+      }
+      if (pm) {
+        const int l = 31 - __clz(int(pm));
+        ss = s0 + l;
+        pre_s = df_shfl(lo, l);
+      }
+      sbase = df_add(sbase, df_shfl(inc, 31));
+    }
+  }
+  int token = -1;
+  df tlo = pre_s, thi = pre_s;
+  if (ss >= 0) {
+    int v0, v1;
+    slice_range(a.nvec, a.S, ss, v0, v1);
+    const int nu = (v1 - v0 + 31) / 32;
+    // unit: lanes scan 32 units at a time
+    const float2* up = a.ws.units(b, ss);
+    int us = -1;
+    df ubase = pre_s, ubase_s = pre_s;
+    for (int u0 = 0; u0 < nu && us < 0; u0 += 32) {
+      const int u = u0 + lane;
+      df x{0.f, 0.f};
+      if (u < nu) {
+        const float2 w = __ldcg(&up[u]);
+        x = df{w.x, w.y};
+      }
+      df inc = x;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const df y = df_shfl_up(inc, o);
+        if (lane >= o) inc = df_add(inc, y);
+      }
+      const df lo = df_add(ubase, df_sub(inc, x));
+      const bool hit = x.hi > 0.0f && df_gt(df_add(lo, x), t);
+      const unsigned hm = __ballot_sync(0xffffffffu, hit);
+      const unsigned pm = __ballot_sync(0xffffffffu, u < nu && x.hi > 0.0f);
+      if (hm) {
+        const int l = __ffs(int(hm)) - 1;
+        us = u0 + l;
+        ubase_s = df_shfl(lo, l);
+      } else if (pm) {
+        const int l = 31 - __clz(int(pm));
+        ubase_s = df_shfl(lo, l);  // last unit with mass so far (rounding fallback)
+        us = -(u0 + l) - 2;
+      }
+      ubase = df_add(ubase, df_shfl(inc, 31));
+    }
+    if (us < -1) us = -us - 2;
+    if (us >= 0) {
+      // entries of the unit's 32 vectors, lane-minor
+      const int vi = v0 + us * 32 + lane;
+      df r[E::kVec];
+      df vs{0.f, 0.f};
+      if (vi < v1) {
+        vs = ent.entries(vi, r);
+      } else {
+#pragma unroll
+        for (int k = 0; k < E::kVec; ++k) r[k] = {0.f, 0.f};
+      }
+      df inc = vs;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const df y = df_shfl_up(inc, o);
+        if (lane >= o) inc = df_add(inc, y);
+      }
+      df c0 = df_add(ubase_s, df_sub(inc, vs));
+      int tk = -1, lk = -1;
+      df lo{0.f, 0.f}, hi{0.f, 0.f}, l0{0.f, 0.f}, l1{0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < E::kVec; ++k) {
+        const df c1 = df_add(c0, r[k]);
+        if (r[k].hi > 0.0f) {
+          lk = vi * E::kVec + k;
+          l0 = c0;
+          l1 = c1;
+          if (tk < 0 && df_gt(c1, t)) {
+            tk = vi * E::kVec + k;
+            lo = c0;
+            hi = c1;
+          }
+        }
+        c0 = c1;
+      }
+      const unsigned hm = __ballot_sync(0xffffffffu, tk >= 0);
+      const unsigned pm = __ballot_sync(0xffffffffu, lk >= 0);
+      if (hm) {
+        const int l = __ffs(int(hm)) - 1;
+        token = __shfl_sync(0xffffffffu, tk, l);
+        tlo = df_shfl(lo, l);
+        thi = df_shfl(hi, l);
+      } else if (pm) {
+        const int l = 31 - __clz(int(pm));
+        token = __shfl_sync(0xffffffffu, lk, l);
+        tlo = df_shfl(l0, l);
+        thi = df_shfl(l1, l);
+      }
+    }
+  }
+  const float m1 = df_sub(t, tlo).hi, m2 = df_sub(thi, t).hi;
+  cert = token >= 0 && fminf(m1, m2) > 2.02f * Eb;
+  return token;
+}
+
+// SW complete: fp32 draw with its error bound; certified, or on to FA.
+template <class E>
+__device__ void finish_sw(const SampleArgs& a, int b, int aux) {
+  const int lane = threadIdx.x & 31;
+  RowState* st = row_state(a, b);
+  const DrawRows dr = draw_rows(a.K, aux);
+  const int d = load_tokens(a, b);
+  const int flags = __ldcg(&st->flags);
+  const float Kq = __ldcg(&st->Kq), Rq = __ldcg(&st->Rq);
+  const float Kp = dr.pair ? __ldcg(&st->Kp) : 0.f, Rp = dr.pair ? __ldcg(&st->Rp) : 0.f;
+  const float uK = a.uniforms[size_t(b) * (a.K + 1) + a.K];
+  const DrawSlices sl = draw_slices(a, b);
+  const df Sr = sl.total;
+  // Error bound (probability units) of the fp32 sweep. Per term, relative:
+  // exp2 (ex2), argument rounding and the fp32 temperature constant (ln2 u |x|
+  // each), 1/S and the product (3u), and the row sum behind 1/S (ex2 + ln2 u
+  // sum q|x| + gamma1); summed with weights q (resp. p), whose sum is at most
+  // kQmax. sum q|x| <= kQmax/2 - sum q x, since x <= 1/4 (the offset is the
+  // ceiling of the rounded max * c, below 2^22 in magnitude). Rounding of the
+  // unit, slice and row sums adds 16 u Sr.
+  auto side = [&](float A) {
+    const float absx = 1.01f * fmaxf(0.0f, -A) + 0.5f * kQmax;
+    return 1.05f * (kQmax * (2.0f * a.bd.ex2 + 3.0f * kU + a.bd.gamma1 + 4.0f * kLn2f * kU) +
+                    4.0f * kLn2f * kU * absx);
+  };
+  const float Eb = side(sl.f2) + (dr.pair ? side(sl.f3) : 0.f) + 16.0f * kU * Sr.hi + 1e-30f;
+  const df t = df_mul_f(Sr, uK);
+  int token = -1;
+  bool cert = false;
+  if (Sr.hi > 2.0f * Eb) {
+    const RowPtrs<E> rp = row_ptrs<E>(a, b);
+    FastEntries<E> fe;
+    fe.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
+    fe.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
+    fe.pair = dr.pair;
+    fe.c = a.c;
+    fe.Kq = Kq;
+    fe.Rq = Rq;
+    fe.Kp = Kp;
+    fe.Rp = Rp;
+    token = search_draw<E>(a, b, fe, sl, t, Eb, cert);
+  }
+  if (token >= 0 && cert) {
+    write_outputs(a, b, dr.j, token, flags, false, d);
+    return;
+  }
+  if (lane == 0) {
+    st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
+    enqueue_row_stage(a.ws, kFA, b, a.S, aux);
+  }
+  __syncwarp();
+}
+
+// FA complete: accurate normalisers of the draw's rows, then FB.
+__device__ void finish_fa(const SampleArgs& a, int b, int aux) {
+  const int lane = threadIdx.x & 31;
+  const DrawRows dr = draw_rows(a.K, aux);
+  const SliceSums ss = slice_sums(a, b, true);
+  if (lane == 0) {
+    RowState* st = row_state(a, b);
+    const df I0 = df_recip(ss.p0);
+    st->Iq_hi = I0.hi;
+    st->Iq_lo = I0.lo;
+    if (dr.pair) {
+      const df I1 = df_recip(ss.p1);
+      st->Ip_hi = I1.hi;
+      st->Ip_lo = I1.lo;
+    }
+    enqueue_row_stage(a.ws, kFB, b, a.S, aux);
+  }
+  __syncwarp();
+}
+
+// FB complete: certified double-float draw (or the zero-residual rerun on q_j).
+template <class E>
+__device__ void finish_fb(const SampleArgs& a, const Smem& L, int b, int aux) {
+  const int lane = threadIdx.x & 31;
+  RowState* st = row_state(a, b);
+  const DrawRows dr = draw_rows(a.K, aux);
+  const int d = load_tokens(a, b);
+  const int flags = __ldcg(&st->flags);
+  const float Kq = __ldcg(&st->Kq), Kp = dr.pair ? __ldcg(&st->Kp) : 0.f;
+  const df Iq{__ldcg(&st->Iq_hi), __ldcg(&st->Iq_lo)};
+  const df Ip = dr.pair ? df{__ldcg(&st->Ip_hi), __ldcg(&st->Ip_lo)} : df{0.f, 0.f};
+  const float uK = a.uniforms[size_t(b) * (a.K + 1) + a.K];
+  const DrawSlices sl = draw_slices(a, b);
+  const df Sr = sl.total;
+  const float Eb = kAccRho * (sl.f2 + sl.f3) + 1e-14f * Sr.hi + 1e-36f;
+  if (!(Sr.hi > 0.0f) && dr.pair) {
+    // zero residual mass: the draw uses q_j itself
+    if (lane == 0) {
+      st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;
+      enqueue_row_stage(a.ws, kFB, b, a.S, dr.j | (kModeQ << 8));
+    }
+    __syncwarp();
+    return;
+  }
+  int token = -1;
+  bool cert = false;
+  if (Sr.hi > 0.0f) {
+    const RowPtrs<E> rp = row_ptrs<E>(a, b);
+    AccEntries<E> ae;
+    ae.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
+    ae.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
+    ae.pair = dr.pair;
+    ae.Chi = a.Chi;
+    ae.Clo = a.Clo;
+    ae.Kq = Kq;
+    ae.Kp = Kp;
+    ae.Iq = Iq;
+    ae.Ip = Ip;
+    ae.th = L.tab_hi;
+    ae.tl = L.tab_lo;
+    token = search_draw<E>(a, b, ae, sl, df_mul_f(Sr, uK), Eb, cert);
+  }
+  const int fl = flags | (cert ? 0 : SPEC_ROW_UNCERTIFIED);
+  if (token < 0 && lane == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
+  write_outputs(a, b, dr.j, token, fl, token < 0, d);
+}
+
+// Combines the per-warp partials of a finished task and stores them as the
+// task's slice partials in the workspace.
+__device__ void combine_task(const SampleArgs& a, const QTask& t, const uint8_t* slot) {
+  const int lane = threadIdx.x & 31;
+  float* o = a.ws.part(t.b, t.s);
+  if (t.type == kP1 || t.type == kBS) {
+    const int R = 2 * a.K, nrows = (t.type == kP1) ? 2 * a.K : 1;
+    const float* w = reinterpret_cast<const float*>(slot + 16);
+    const int* wb = reinterpret_cast<const int*>(w + 2 * R * kCW);
+    for (int r = lane; r < nrows; r += 32) {
+      float M = -INFINITY;
+      int bad = 0;
+#pragma unroll
+      for (int q = 0; q < kCW; ++q) {
+        M = fmaxf(M, w[r * kCW + q]);
+        bad |= wb[r * kCW + q];
+      }
+      const float Kc = offset_of(M, a.c);
+      df S{0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < kCW; ++q) {
+        const float s = w[(R + r) * kCW + q];
+        if (s != 0.0f)
+          S = df_add_f(S, __fmul_rn(s, pow2i(__fsub_rn(offset_of(w[r * kCW + q], a.c), Kc))));
+      }
+      o[4 * r] = M;
+      o[4 * r + 1] = S.hi;
+      o[4 * r + 2] = S.lo;
+      o[4 * r + 3] = __int_as_float(bad);
+    }
+  } else if (lane == 0) {
+    if (t.type == kSW) {
+      const float* w = reinterpret_cast<const float*>(slot + 16);
+      df acc{0.f, 0.f};
+      float aq = 0.f, ap = 0.f;
+      for (int q = 0; q < kCW; ++q) {
+        acc = df_add_f(acc, w[q]);
+        aq += w[kCW + q];
+        ap += w[2 * kCW + q];
+      }
+      o[0] = acc.hi;
+      o[1] = acc.lo;
+      o[2] = aq;
+      o[3] = ap;
+    } else if (t.type == kFA || t.type == kAR) {
+      const df* w = reinterpret_cast<const df*>(slot + 16);
+      df s0{0.f, 0.f}, s1{0.f, 0.f};
+      for (int q = 0; q < kCW; ++q) {
+        s0 = df_add(s0, w[q]);
+        s1 = df_add(s1, w[kCW + q]);
+      }
+      o[0] = s0.hi;
+      o[1] = s0.lo;
+      o[2] = s1.hi;
+      o[3] = s1.lo;
+    } else {  // kFB
+      const df* w = reinterpret_cast<const df*>(slot + 16);
+      const float* f = reinterpret_cast<const float*>(w + kCW);
+      df acc{0.f, 0.f};
+      float qs = 0.f, ps = 0.f;
+      for (int q = 0; q < kCW; ++q) {
+        acc = df_add(acc, w[q]);
+        qs += f[q];
+        ps += f[kCW + q];
+      }
+      o[0] = acc.hi;
+      o[1] = acc.lo;
+      o[2] = qs;
+      o[3] = ps;
+    }
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ consumers
+// Each returns false on a timeout; `it` advances past the task's stages.
+
+template <class E>
+__device__ bool consume_stats(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot) {
+  const int tid = threadIdx.x;
+  StatOp<E> op;
+  op.c = a.c;
+  op.begin();
+  for (;;) {
+    const ChunkMeta m = L.ring.meta[it % kStages];
+    op.chunk(stage_data(L.ring, it), m.c1 - m.c0, tid);
+    release_stage(L.ring, it);
+    ++it;
+    if (m.last_k) {
+      op.end_row(slot, 2 * a.K, m.r);
+      op.begin();
+    }
+    if (m.last) return true;
+    if (!wait_stage(L.ring, it)) return false;
+  }
+}
+
+template <class E>
+__device__ bool consume_sw(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot,
+                           const QTask& t) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const DrawRows dr = draw_rows(a.K, t.aux);
+  const RowState* st = row_state(a, t.b);
+  FastEntries<E> fe;
+  fe.tq = nullptr;  // the sweep reads the ring stages
+  fe.tp = nullptr;
+  fe.pair = dr.pair;
+  fe.c = a.c;
+  fe.Kq = __ldcg(&st->Kq);
+  fe.Rq = __ldcg(&st->Rq);
+  fe.Kp = dr.pair ? __ldcg(&st->Kp) : 0.f;
+  fe.Rp = dr.pair ? __ldcg(&st->Rp) : 0.f;
+  int v0, v1;
+  slice_range(a.nvec, a.S, t.s, v0, v1);
+  constexpr int kPer = kChunk / 16 / kCons;
+  float accf = 0.f, Aq = 0.f, Ap = 0.f;
+  float2* units = a.ws.units(t.b, t.s);
+  bool ok = true;
+  for (;;) {
+    const ChunkMeta m = L.ring.meta[it % kStages];
+    const uint4* bq = stage_data(L.ring, it);
+    const uint4* bp = bq;
+    uint32_t it2 = it;
+    if (dr.pair) {
+      if (!wait_stage(L.ring, it + 1)) {
+        ok = false;
+        break;
+      }
+      bp = stage_data(L.ring, it + 1);
+      it2 = it + 1;
+    }
+    const int cnt = m.c1 - m.c0;
+    // unit u of this stage = vectors [32u, 32u + 32): warp w takes units
+    // w, w + 8, ...; every lane one vector (pair) of each
+    float vs[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = warp * 32 + k * kCons + lane;
+      vs[k] = 0.f;
+      if (i < cnt) {
+        float r[E::kVec];
+        vs[k] = fe.run(bq[i], bp[i], r, Aq, Ap);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i0 = warp * 32 + k * kCons;
+      if (i0 < cnt) {
+        const float us = warp_sum_f(vs[k]);
+        if (lane == 0) units[(m.c0 - v0 + i0) / 32] = make_float2(us, 0.f);
+      }
+      accf = __fadd_rn(accf, vs[k]);
+    }
+    const bool lastc = L.ring.meta[it2 % kStages].last != 0;
+    release_stage(L.ring, it);
+    if (dr.pair) release_stage(L.ring, it2);
+    it = it2 + 1;
+    if (lastc) break;
+    if (!wait_stage(L.ring, it)) {
+      ok = false;
+      break;
+    }
+  }
+  accf = warp_sum_f(accf);
+  Aq = warp_sum_f(Aq);
+  Ap = warp_sum_f(Ap);
+  if (lane == 0) {
+    float* w = reinterpret_cast<float*>(slot + 16);
+    w[warp] = accf;
+    w[kCW + warp] = Aq;
+    w[2 * kCW + warp] = Ap;
+  }
+  return ok;
+}
+
+// FA / AR: double-float sums of the task's rows (row 0 with offset K0, row 1
+// with K1).
+template <class E>
+__device__ bool consume_rowsums(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot,
+                                const QTask& t) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const RowState* st = row_state(a, t.b);
+  float K0, K1;
+  if (t.type == kAR) {
+    K0 = __ldcg(&st->rK[2 * t.aux]);
+    K1 = __ldcg(&st->rK[2 * t.aux + 1]);
+  } else {
+    K0 = __ldcg(&st->Kq);
+    K1 = draw_rows(a.K, t.aux).pair ? __ldcg(&st->Kp) : 0.f;
+  }
+  df s0{0.f, 0.f}, s1{0.f, 0.f};
+  bool ok = true;
+  for (;;) {
+    const ChunkMeta m = L.ring.meta[it % kStages];
+    const uint4* buf = stage_data(L.ring, it);
+    const float Kr = (m.r == 0) ? K0 : K1;
+    df acc{0.f, 0.f};
+    for (int i = tid; i < m.c1 - m.c0; i += kCons) {
+      float z[E::kVec];
+      E::unpack(buf[i], z);
+#pragma unroll
+      for (int k = 0; k < E::kVec; ++k)
+        acc = df_add(acc, acc_elem(z[k], a.Chi, a.Clo, Kr, L.tab_hi, L.tab_lo));
+    }
+    if (m.r == 0) s0 = df_add(s0, acc);
+    else s1 = df_add(s1, acc);
+    release_stage(L.ring, it);
+    ++it;
+    if (m.last) break;
+    if (!wait_stage(L.ring, it)) {
+      ok = false;
+      break;
+    }
+  }
+  s0 = df_warp_sum(s0);
+  s1 = df_warp_sum(s1);
+  if (lane == 0) {
+    df* w = reinterpret_cast<df*>(slot + 16);
+    w[warp] = s0;
+    w[kCW + warp] = s1;
+  }
+  return ok;
+}
+
+// FB: double-float residual, unit sums and sums of q and p.
+template <class E>
+__device__ bool consume_fb(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot,
+                           const QTask& t) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const DrawRows dr = draw_rows(a.K, t.aux);
+  const RowState* st = row_state(a, t.b);
+  AccEntries<E> ae;
+  ae.tq = nullptr;  // the sweep reads the ring stages
+  ae.tp = nullptr;
+  ae.pair = dr.pair;
+  ae.Chi = a.Chi;
+  ae.Clo = a.Clo;
+  ae.Kq = __ldcg(&st->Kq);
+  ae.Kp = dr.pair ? __ldcg(&st->Kp) : 0.f;
+  ae.Iq = df{__ldcg(&st->Iq_hi), __ldcg(&st->Iq_lo)};
+  ae.Ip = dr.pair ? df{__ldcg(&st->Ip_hi), __ldcg(&st->Ip_lo)} : df{0.f, 0.f};
+  ae.th = L.tab_hi;
+  ae.tl = L.tab_lo;
+  int v0, v1;
+  slice_range(a.nvec, a.S, t.s, v0, v1);
+  df acc{0.f, 0.f};
+  float Q = 0.f, P = 0.f;
+  float2* units = a.ws.units(t.b, t.s);
+  bool ok = true;
+  for (;;) {
+    const ChunkMeta m = L.ring.meta[it % kStages];
+    const uint4* bq = stage_data(L.ring, it);
+    const uint4* bp = bq;
+    uint32_t it2 = it;
+    if (dr.pair) {
+      if (!wait_stage(L.ring, it + 1)) {
+        ok = false;
+        break;
+      }
+      bp = stage_data(L.ring, it + 1);
+      it2 = it + 1;
+    }
+    const int cnt = m.c1 - m.c0;
+    for (int i0 = warp * 32; i0 < cnt; i0 += kCons) {
+      const int i = i0 + lane;
+      df vs{0.f, 0.f};
+      if (i < cnt) {
+        df r[E::kVec];
+        vs = ae.run(bq[i], bp[i], r, Q, P);
+        acc = df_add(acc, vs);
+      }
+      const df us = df_warp_sum(vs);
+      if (lane == 0) units[(m.c0 - v0 + i0) / 32] = make_float2(us.hi, us.lo);
+    }
+    const bool lastc = L.ring.meta[it2 % kStages].last != 0;
+    release_stage(L.ring, it);
+    if (dr.pair) release_stage(L.ring, it2);
+    it = it2 + 1;
+    if (lastc) break;
+    if (!wait_stage(L.ring, it)) {
+      ok = false;
+      break;
+    }
+  }
+  acc = df_warp_sum(acc);
+  Q = warp_sum_f(Q);
+  P = warp_sum_f(P);
+  if (lane == 0) {
+    df* w = reinterpret_cast<df*>(slot + 16);
+    w[warp] = acc;
+    float* f = reinterpret_cast<float*>(w + kCW);
+    f[warp] = Q;
+    f[kCW + warp] = P;
+  }
+  return ok;
 }
 
 // ------------------------------------------------------------------ kernel
 template <class E>
 __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const SampleArgs a) {
-  using T = typename E::T;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  const int K = a.K, R = 2 * K + 1;
-  const Smem L = make_smem(smem_raw, R);
-  Misc& ms = *L.misc;
+  const int K = a.K;
+  const Smem L = make_smem(smem_raw, 2 * K);
   ring_init(L.ring);
+  handoff_init(L.ho);
+  for (int i = threadIdx.x; i < 256; i += kThreads) {
+    L.tab_hi[i] = kExp2Tab.hi[i];
+    L.tab_lo[i] = kExp2Tab.lo[i];
+  }
   __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  WsHeader* h = a.ws.hdr();
 
-  if (threadIdx.x >= kCons) {
+  if (warp == kCW) {
     // ------------------------------------------------ producer
-    if (threadIdx.x == kCons) {
+    if (lane == 0) {
       uint32_t it = 0, nt = 0;
       uint64_t idle_t0 = 0;
-      int64_t pending = -1;
-      WsHeader* h = a.ws.hdr();
+      Fetcher fx;
       while (!*L.ring.abort && !ld_volatile_u32(&h->abort)) {
         QTask t;
-        bool exhausted;
-        if (!fetch_task(a.ws, kP1, t, exhausted, pending)) {
-          if (!producer_idle(a.ws, exhausted, idle_t0)) break;
+        if (!fx.next(a.ws, kP1, t)) {
+          if (!producer_idle(a.ws, !fx.first_left, idle_t0)) break;
           continue;
         }
         idle_t0 = 0;
@@ -836,360 +1325,86 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
           }
         } else if (t.type == kBS) {
           rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(K) * a.V);
+        } else if (t.type == kAR) {
+          rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(t.aux) * a.V);
+          rows[nrows++] = reinterpret_cast<const char*>(rp.drf + size_t(t.aux) * a.V);
         } else {
-          const int n = t.aux & 0xff, mode = t.aux >> 8;
-          const int j = n;  // row j (j = K for the bonus draw)
-          rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(j) * a.V);
-          if (mode == kModeResidual && n < K) {
-            rows[nrows++] = reinterpret_cast<const char*>(rp.drf + size_t(j) * a.V);
-            paired = true;
+          const DrawRows dr = draw_rows(K, t.aux);
+          rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(dr.j) * a.V);
+          if (dr.pair) {
+            rows[nrows++] = reinterpret_cast<const char*>(rp.drf + size_t(dr.j) * a.V);
+            paired = (t.type != kFA);
           }
         }
-        if (!produce_task(L.ring, it, nt, t, rows, nrows, paired, v0, v1)) break;
+        auto prefetch = [&]() { fx.prepare(a.ws); };
+        if (!produce_task(L.ring, it, nt, t, rows, nrows, paired, v0, v1, prefetch)) break;
       }
       produce_end(L.ring, it);
     }
+  } else if (warp == kFinWarp) {
+    // ------------------------------------------------ finisher
+    finisher_loop(
+        a.ws, L.ho, L.ring.abort,
+        [&](const QTask& t, const uint8_t* slot) { combine_task(a, t, slot); },
+        [&](const QTask& t) {
+          switch (t.type) {
+            case kP1:
+              finish_p1<E>(a, L, t.b);
+              break;
+            case kAR:
+              finish_ar<E>(a, L, t.b, t.aux);
+              break;
+            case kBS:
+              finish_bs(a, L, t.b);
+              break;
+            case kSW:
+              finish_sw<E>(a, t.b, t.aux);
+              break;
+            case kFA:
+              finish_fa(a, t.b, t.aux);
+              break;
+            default:
+              finish_fb<E>(a, L, t.b, t.aux);
+              break;
+          }
+        });
   } else {
     // ------------------------------------------------ consumers
-    uint32_t it = 0;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    while (true) {
+    const int tid = threadIdx.x;
+    uint32_t it = 0, n = 0;
+    for (;; ++n) {
       if (!wait_stage(L.ring, it)) break;
       const ChunkMeta m0 = L.ring.meta[it % kStages];
       if (m0.slot < 0) break;
       const QTask t = L.ring.ttab[m0.slot];
-      const int b = t.b, s = t.s;
-      const RowPtrs<E> rp = row_ptrs<E>(a, b);
-      int v0, v1;
-      slice_range(a.nvec, a.S, s, v0, v1);
-      if (t.type == kP1 || t.type == kBS) {
-        // ---------------- statistics of the slice of every row of the task
-        StatOp<E> op;
-        op.c = a.c;
-        op.begin();
-        for (;;) {
-          const ChunkMeta m = L.ring.meta[it % kStages];
-          const uint4* buf = stage_data(L.ring, it);
-          op.chunk(buf, m.c1 - m.c0, tid);
-          release_stage(L.ring, it);
-          ++it;
-          if (m.last_k) {
-            op.end_row(L, m.r);
-            op.begin();
-          }
-          if (m.last) break;
-          if (!wait_stage(L.ring, it)) break;
-        }
-        consumers_sync();
-        const int nrows = (t.type == kP1) ? 2 * K : 1;
-        stats_to_global(L, nrows, a.c, a.ws.part(b, s));
-        if (arrive_row(a, ms, b)) {
-          if (t.type == kP1) {
-            finish_p1<E>(a, L, b);
-          } else {
-            // bonus statistics of target row K -> its draw
-            if (tid == 0) {
-              stats_combine(a, L, b, 0, 2 * K);
-              RowState* st = a.ws.rowstate(b);
-              if (!L.rowOK[2 * K]) {
-                st->err = 1;
-              } else {
-                st->Kq = L.rowKc[2 * K];
-                st->Rq = L.rowInv[2 * K].hi;
-              }
-            }
-            consumers_sync();
-            const RowState* st = a.ws.rowstate(b);
-            if (ld_cg_i(&st->err)) {
-              if (warp == 1 && lane < K) ms.tok[lane] = a.tokens[size_t(b) * K + lane];
-              consumers_sync();
-              if (tid == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
-              write_outputs(a, ms, b, K, -1, ld_cg_i(&st->flags), true);
-            } else if (tid == 0) {
-              __threadfence();
-              enqueue_row_stage(a.ws, kSW, b, a.S, K | (kModeQ << 8));
-            }
-          }
-        }
-        consumers_sync();
-        continue;
+      if (!handoff_acquire(L.ho, n)) {
+        *L.ring.abort = 1;
+        break;
       }
-      // ------------------------------------------------ draw stages
-      const RowState* stp = a.ws.rowstate(b);
-      const int n = t.aux & 0xff, mode = t.aux >> 8;
-      const bool pair = (mode == kModeResidual && n < K);
-      const int jrow = n;
-      const uint4* vq = reinterpret_cast<const uint4*>(rp.tgt + size_t(jrow) * a.V);
-      const uint4* vp = pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(jrow) * a.V) : nullptr;
-      if (t.type == kSW) {
-        FastEntries<E> fe;
-        fe.tq = vq;
-        fe.tp = vp;
-        fe.c = a.c;
-        fe.Kq = ld_cg_f(&stp->Kq);
-        fe.Rq = ld_cg_f(&stp->Rq);
-        fe.Kp = pair ? ld_cg_f(&stp->Kp) : 0.f;
-        fe.Rp = pair ? ld_cg_f(&stp->Rp) : 0.f;
-        constexpr int kPer = kChunk / 16 / kCons;
-        float accf = 0.f, Aq = 0.f, Ap = 0.f;
-        float2* units = a.ws.units(b, s);
-        for (;;) {
-          const ChunkMeta m = L.ring.meta[it % kStages];
-          const uint4* bq = stage_data(L.ring, it);
-          const uint4* bp = bq;
-          uint32_t it2 = it;
-          if (pair) {
-            if (!wait_stage(L.ring, it + 1)) break;
-            bp = stage_data(L.ring, it + 1);
-            it2 = it + 1;
-          }
-          const int cnt = m.c1 - m.c0;
-          // unit u of this stage = vectors [32u, 32u + 32): warp w takes units
-          // w, w + 8, ...; every lane one vector pair of each
-          float vs[kPer];
-#pragma unroll
-          for (int k = 0; k < kPer; ++k) {
-            const int i = warp * 32 + k * kCons + lane;
-            vs[k] = 0.f;
-            if (i < cnt) {
-              float r[E::kVec];
-              vs[k] = fe.run(bq[i], bp[i], r, Aq, Ap);
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < kPer; ++k) {
-            const int i0 = warp * 32 + k * kCons;
-            if (i0 < cnt) {
-              const float us = warp_sum_f(vs[k]);
-              if (lane == 0) units[(m.c0 - v0 + i0) / 32] = make_float2(us, 0.f);
-            }
-            accf = __fadd_rn(accf, vs[k]);
-          }
-          const bool lastc = L.ring.meta[it2 % kStages].last != 0;
-          release_stage(L.ring, it);
-          if (pair) release_stage(L.ring, it2);
-          it = it2 + 1;
-          if (lastc) break;
-          if (!wait_stage(L.ring, it)) break;
-        }
-        df acc{accf, 0.f};
-        float f4[4] = {Aq, Ap, 0.f, 0.f};
-        cta_reduce(ms, acc, f4);
-        if (tid == 0) {
-          float* o = a.ws.part(b, s);
-          o[0] = acc.hi;
-          o[1] = acc.lo;
-          o[2] = f4[0];
-          o[3] = f4[1];
-        }
-        if (arrive_row(a, ms, b)) {
-          // ---------------- fp32 draw: bound, locate, certify
-          if (tid == 0) {
-            df Sr{0.f, 0.f};
-            float Aqt = 0.f, Apt = 0.f;
-            for (int q = 0; q < a.S; ++q) {
-              const float* p = a.ws.part(b, q);
-              Sr = df_add(Sr, df{ld_cg_f(p), ld_cg_f(p + 1)});
-              Aqt += ld_cg_f(p + 2);
-              Apt += ld_cg_f(p + 3);
-            }
-            // Error bound (probability units) of the fp32 sweep. Per term,
-            // relative: exp2 (ex2), argument rounding and the fp32
-            // temperature constant (ln2 u |x| each), 1/S and the product
-            // (3u), and the row sum behind 1/S (ex2 + ln2 u sum q|x| +
-            // gamma1); summed with weights q (resp. p), whose sum is at most
-            // kQmax. sum q|x| <= kQmax/2 - sum q x, since x <= 1/4 (the offset
-            // is ceil of the rounded max * c, below 2^22 in magnitude).
-            // Rounding of the unit, slice and row sums adds 16 u Sr.
-            auto side = [&](float A) {
-              const float absx = 1.01f * fmaxf(0.0f, -A) + 0.5f * kQmax;
-              return 1.05f * (kQmax * (2.0f * a.bd.ex2 + 3.0f * kU + a.bd.gamma1 + 4.0f * kLn2f * kU) +
-                              4.0f * kLn2f * kU * absx);
-            };
-            const float E = side(Aqt) + (pair ? side(Apt) : 0.f) + 16.0f * kU * Sr.hi + 1e-30f;
-            ms.E = E;
-            ms.tstar = df_mul_f(Sr, a.uniforms[size_t(b) * (K + 1) + K]);
-            ms.found = (Sr.hi > 2.0f * E) ? 1 : 0;
-          }
-          consumers_sync();
-          if (ms.found) search_draw<E>(a, ms, b, fe);
-          const int flags = ld_cg_i(&stp->flags);
-          if (ms.found && ms.cert) {
-            if (warp == 1 && lane < K) ms.tok[lane] = a.tokens[size_t(b) * K + lane];
-            consumers_sync();
-            write_outputs(a, ms, b, n, ms.token, flags, false);
-          } else if (tid == 0) {
-            RowState* st = a.ws.rowstate(b);
-            st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
-            __threadfence();
-            enqueue_row_stage(a.ws, kFA, b, a.S, t.aux);
-          }
-        }
-        consumers_sync();
-        continue;
+      uint8_t* slot = L.ho.slot(n);
+      if (tid == 0) *reinterpret_cast<QTask*>(slot) = t;
+      bool ok;
+      if (t.type == kP1 || t.type == kBS) ok = consume_stats<E>(a, L, it, slot);
+      else if (t.type == kSW) ok = consume_sw<E>(a, L, it, slot, t);
+      else if (t.type == kFA || t.type == kAR) ok = consume_rowsums<E>(a, L, it, slot, t);
+      else ok = consume_fb<E>(a, L, it, slot, t);
+      handoff_post(L.ho, n);
+      if (!ok) {
+        ++n;
+        break;
       }
-      // ---------------- double-float stages (rare)
-      load_table(L);
-      consumers_sync();
-      if (t.type == kFA) {
-        df s0{0.f, 0.f}, s1{0.f, 0.f};
-        const float K0 = ld_cg_f(&stp->Kq), K1 = pair ? ld_cg_f(&stp->Kp) : 0.f;
-        for (;;) {
-          const ChunkMeta m = L.ring.meta[it % kStages];
-          const uint4* buf = stage_data(L.ring, it);
-          const float Kr = (m.r == 0) ? K0 : K1;
-          df acc{0.f, 0.f};
-          for (int i = tid; i < m.c1 - m.c0; i += kCons) {
-            float z[E::kVec];
-            E::unpack(buf[i], z);
-#pragma unroll
-            for (int k = 0; k < E::kVec; ++k)
-              acc = df_add(acc, acc_elem(z[k], a.Chi, a.Clo, Kr, L.tab_hi, L.tab_lo));
-          }
-          if (m.r == 0) s0 = df_add(s0, acc);
-          else s1 = df_add(s1, acc);
-          release_stage(L.ring, it);
-          ++it;
-          if (m.last) break;
-          if (!wait_stage(L.ring, it)) break;
-        }
-        s0 = df_warp_sum(s0);
-        s1 = df_warp_sum(s1);
-        if (lane == 0) {
-          ms.wA[warp] = s0;
-          ms.wB[warp] = s1;
-        }
-        consumers_sync();
-        if (tid == 0) {
-          df t0{0.f, 0.f}, t1{0.f, 0.f};
-          for (int w = 0; w < kCW; ++w) {
-            t0 = df_add(t0, ms.wA[w]);
-            t1 = df_add(t1, ms.wB[w]);
-          }
-          float* o = a.ws.part(b, s);
-          o[0] = t0.hi;
-          o[1] = t0.lo;
-          o[2] = t1.hi;
-          o[3] = t1.lo;
-        }
-        if (arrive_row(a, ms, b) && tid == 0) {
-          df S0{0.f, 0.f}, S1{0.f, 0.f};
-          for (int q = 0; q < a.S; ++q) {
-            const float* p = a.ws.part(b, q);
-            S0 = df_add(S0, df{ld_cg_f(p), ld_cg_f(p + 1)});
-            S1 = df_add(S1, df{ld_cg_f(p + 2), ld_cg_f(p + 3)});
-          }
-          RowState* st = a.ws.rowstate(b);
-          const df I0 = df_recip(S0);
-          st->Iq_hi = I0.hi;
-          st->Iq_lo = I0.lo;
-          if (pair) {
-            const df I1 = df_recip(S1);
-            st->Ip_hi = I1.hi;
-            st->Ip_lo = I1.lo;
-          }
-          __threadfence();
-          enqueue_row_stage(a.ws, kFB, b, a.S, t.aux);
-        }
-        consumers_sync();
-        continue;
-      }
-      // kFB: double-float residual sums and unit sums
-      AccEntries<E> ae;
-      ae.tq = vq;
-      ae.tp = vp;
-      ae.Chi = a.Chi;
-      ae.Clo = a.Clo;
-      ae.Kq = ld_cg_f(&stp->Kq);
-      ae.Kp = pair ? ld_cg_f(&stp->Kp) : 0.f;
-      ae.Iq = df{ld_cg_f(&stp->Iq_hi), ld_cg_f(&stp->Iq_lo)};
-      ae.Ip = pair ? df{ld_cg_f(&stp->Ip_hi), ld_cg_f(&stp->Ip_lo)} : df{0.f, 0.f};
-      ae.th = L.tab_hi;
-      ae.tl = L.tab_lo;
-      {
-        df acc{0.f, 0.f};
-        float Q = 0.f, P = 0.f;
-        float2* units = a.ws.units(b, s);
-        for (;;) {
-          const ChunkMeta m = L.ring.meta[it % kStages];
-          const uint4* bq = stage_data(L.ring, it);
-          const uint4* bp = bq;
-          uint32_t it2 = it;
-          if (pair) {
-            if (!wait_stage(L.ring, it + 1)) break;
-            bp = stage_data(L.ring, it + 1);
-            it2 = it + 1;
-          }
-          const int cnt = m.c1 - m.c0;
-          for (int i0 = warp * 32; i0 < cnt; i0 += kCons) {
-            const int i = i0 + lane;
-            df vs{0.f, 0.f};
-            if (i < cnt) {
-              df r[E::kVec];
-              vs = ae.run(bq[i], bp[i], r, Q, P);
-              acc = df_add(acc, vs);
-            }
-            const df us = df_warp_sum(vs);
-            if (lane == 0) units[(m.c0 - v0 + i0) / 32] = make_float2(us.hi, us.lo);
-          }
-          const bool lastc = L.ring.meta[it2 % kStages].last != 0;
-          release_stage(L.ring, it);
-          if (pair) release_stage(L.ring, it2);
-          it = it2 + 1;
-          if (lastc) break;
-          if (!wait_stage(L.ring, it)) break;
-        }
-        float f4[4] = {Q, P, 0.f, 0.f};
-        cta_reduce(ms, acc, f4);
-        if (tid == 0) {
-          float* o = a.ws.part(b, s);
-          o[0] = acc.hi;
-          o[1] = acc.lo;
-          o[2] = f4[0];
-          o[3] = f4[1];
-        }
-      }
-      if (arrive_row(a, ms, b)) {
-        if (tid == 0) {
-          df Sr{0.f, 0.f};
-          float Qt = 0.f, Pt = 0.f;
-          for (int q = 0; q < a.S; ++q) {
-            const float* p = a.ws.part(b, q);
-            Sr = df_add(Sr, df{ld_cg_f(p), ld_cg_f(p + 1)});
-            Qt += ld_cg_f(p + 2);
-            Pt += ld_cg_f(p + 3);
-          }
-          ms.E = kAccRho * (Qt + Pt) + 1e-14f * Sr.hi + 1e-36f;
-          ms.tstar = df_mul_f(Sr, a.uniforms[size_t(b) * (K + 1) + K]);
-          ms.found = (Sr.hi > 0.0f) ? 1 : (pair ? 2 : 0);  // 2: zero residual mass
-        }
-        consumers_sync();
-        const int flags = ld_cg_i(&stp->flags);
-        if (ms.found == 2) {
-          // zero residual mass: the draw uses q_j itself
-          if (tid == 0) {
-            RowState* st = a.ws.rowstate(b);
-            st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;
-            __threadfence();
-            enqueue_row_stage(a.ws, kFB, b, a.S, n | (kModeQ << 8));
-          }
-        } else {
-          if (ms.found == 1) search_draw<E>(a, ms, b, ae);
-          if (warp == 1 && lane < K) ms.tok[lane] = a.tokens[size_t(b) * K + lane];
-          consumers_sync();
-          const int tokn = ms.found == 1 ? ms.token : -1;
-          int fl = flags;
-          if (!(ms.found == 1 && ms.cert)) fl |= SPEC_ROW_UNCERTIFIED;
-          if (tokn < 0 && tid == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
-          write_outputs(a, ms, b, n, tokn, fl, tokn < 0);
-        }
-      }
-      consumers_sync();
+    }
+    // end of stream for the finisher
+    if (handoff_acquire(L.ho, n)) {
+      if (tid == 0) *reinterpret_cast<QTask*>(L.ho.slot(n)) = QTask{0, 0, 0, 0};
+      handoff_post(L.ho, n);
+    } else {
+      *L.ring.abort = 1;
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0 && (*L.ring.abort || ld_volatile_u32(&a.ws.hdr()->abort))) {
-    atomicExch(&a.ws.hdr()->abort, 1u);
+  if (threadIdx.x == 0 && (*L.ring.abort || ld_volatile_u32(&h->abort))) {
+    atomicExch(&h->abort, 1u);
     if (a.err) atomicOr(a.err, SPEC_DERR_TIMEOUT);
   }
 }
@@ -1206,7 +1421,8 @@ WsLayout sample_layout(int B, int K, int V, int dtype) {
   const int maxslice = (nvec + S - 1) / S;
   const int ustride = (maxslice + 31) / 32 + 1;
   const int part = (8 * K > 8) ? 8 * K : 8;
-  return ws_layout(B, S, part, ustride, 5);
+  // queued stages per row: BS, SW, FA, FB twice (zero residual), AR up to K times
+  return ws_layout(B, S, part, ustride, 5 + K, int(sizeof(RowState)));
 }
 
 }  // namespace
@@ -1234,10 +1450,13 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.c = float(C);
   a.Chi = float(C);
   a.Clo = float(C - double(a.Chi));
+  // fp32 additions a row sum goes through before the double-float combine:
+  // per thread at most `run` (vectors of a row slice per thread + 2), the
+  // 8-term tree of a vector (3) and the warp tree (5)
   const int maxslice = (a.nvec + a.S - 1) / a.S;
-  const int run = maxslice / kCons + 2;  // running-sum length per thread per row slice
+  const int run = maxslice / kCons + 2;
   a.bd.ex2 = float(kEx2RelErrBound);
-  a.bd.gamma1 = float((3.0 + run) * 5.9604644775390625e-8 * 1.01);
+  a.bd.gamma1 = float((3.0 + 5.0 + run) * 5.9604644775390625e-8 * 1.01);
   a.bd.xbar = float(std::log2(double(s.V)) + 2.0);
   a.out_tokens = s.out_tokens;
   a.out_n = s.out_n;
@@ -1247,7 +1466,7 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.p_at_d = s.p_at_d;
   cudaStream_t st = static_cast<cudaStream_t>(s.stream);
   if (cudaMemsetAsync(s.workspace, 0, wl.zero_bytes, st) != cudaSuccess) return SPEC_ECUDA;
-  const size_t smem = sample_smem_bytes(2 * s.K + 1);
+  const size_t smem = sample_smem_bytes(2 * s.K);
   if (s.dtype == SPEC_BF16) return launch_dataflow(verify_sample_kernel<EBf16>, a, smem, st);
   return launch_dataflow(verify_sample_kernel<EF32>, a, smem, st);
 }
