@@ -31,15 +31,17 @@
 namespace sv {
 
 // ------------------------------------------------------------------ slicing
-// Vocabulary slices per batch row. At least enough that one row slice fits
-// one ring stage (kChunk bytes); for small batches more, up to kTargetTasks
-// first-stage tasks so that every persistent CTA gets work (slices of at least
-// 64 vectors); never more than kMaxSlices (two warp-wide scans in the draw).
+// Vocabulary slices per batch row. Enough first-stage tasks that every
+// persistent CTA gets about four (kTargetTasks), and row slices of at most
+// four ring stages; otherwise as few as possible, since every task and every
+// row slice costs fixed work (a fetch, a hand-off, an arrival, per-row warp
+// reductions). Slices keep at least 64 vectors; at most kMaxSlices (two
+// warp-wide scans in the draw).
 constexpr int kMaxSlices = 64;
-constexpr int kTargetTasks = 608;  // two per CTA of a 152-SM GB300 at two CTAs per SM
+constexpr int kTargetTasks = 1216;  // four per CTA of a 152-SM GB300 at two CTAs per SM
 
 __host__ __device__ inline int slices_for(int nvec, int B) {
-  const int per = kChunk / 16;
+  const int per = 4 * (kChunk / 16);
   int s = (nvec + per - 1) / per;
   int par = (kTargetTasks + B - 1) / B;
   const int cap = nvec / 64 > 1 ? nvec / 64 : 1;
