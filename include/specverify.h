@@ -137,6 +137,33 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
                        int dtype, int32_t* err_flag, void* workspace, size_t workspace_bytes);
 
 /*
+ * spec_verify_greedy_noalloc - spec_verify_greedy without a caller workspace.
+ * The pages have no counterpart: this is a deployment variant for callers
+ * that cannot hand the library a device allocation of their own, e.g. code
+ * whose device memory is owned by another framework's pool, or plain C
+ * callers with no device allocator at hand. The call itself allocates
+ * nothing either: it uses one built-in device array of
+ * spec_verify_greedy_noalloc_max_bytes() bytes (4 MiB), located on the
+ * first call on each device with cudaGetSymbolAddress (that first call does
+ * this setup and may load the module; issue it before any stream capture).
+ *
+ *   Arguments, outputs and errors: as spec_verify_greedy, without workspace.
+ *   Returns SPEC_ENOTSUP when the step needs more scratch than the built-in
+ *   array holds (spec_verify_workspace_bytes(B, K, V, dtype) > 4 MiB; e.g.
+ *   B = 256, K = 4, V = 151936 bf16 needs about 1.6 MiB), SPEC_ECUDA when the
+ *   array's address cannot be obtained.
+ *   The scratch's counters and queue are cleared on `stream` at every call.
+ *   All calls on one device share the array: calls that can overlap on the
+ *   device race on it and must be ordered (one stream, or ordered streams).
+ */
+int spec_verify_greedy_noalloc(const void* target_logits, const int32_t* draft_tokens, int B,
+                               int K, int V, int32_t* out_tokens, int32_t* out_num_accepted,
+                               void* stream, int dtype, int32_t* err_flag);
+
+/* spec_verify_greedy_noalloc_max_bytes - size of the built-in scratch (bytes). */
+size_t spec_verify_greedy_noalloc_max_bytes(void);
+
+/*
  * spec_verify_workspace_bytes - size of the device workspace that
  * spec_verify_sample and spec_verify_greedy need for (B, K, V, dtype); 0 for
  * arguments those calls would reject. One workspace serves both calls.

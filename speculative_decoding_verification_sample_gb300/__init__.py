@@ -28,7 +28,8 @@ SPEC_ROW_ACCEPT_REFINED, SPEC_ROW_SAMPLE_REFINED = 1, 2
 SPEC_ROW_UNCERTIFIED, SPEC_ROW_ZERO_RESIDUAL = 4, 8
 
 EXPORTED = ("spec_verify_sample", "spec_verify_greedy", "spec_verify_workspace_bytes",
-            "kv_commit_rollback", "spec_selftest_ex2", "spec_status_string", "spec_version")
+            "kv_commit_rollback", "spec_selftest_ex2", "spec_status_string", "spec_version",
+            "spec_verify_greedy_noalloc", "spec_verify_greedy_noalloc_max_bytes")
 
 _lib = None
 
@@ -56,6 +57,10 @@ def lib() -> ctypes.CDLL:
         L.spec_verify_sample.restype = I
         L.spec_verify_greedy.argtypes = [P, P, I, I, I, P, P, P, I, P, P, Z]
         L.spec_verify_greedy.restype = I
+        L.spec_verify_greedy_noalloc.argtypes = [P, P, I, I, I, P, P, P, I, P]
+        L.spec_verify_greedy_noalloc.restype = I
+        L.spec_verify_greedy_noalloc_max_bytes.argtypes = []
+        L.spec_verify_greedy_noalloc_max_bytes.restype = Z
         L.spec_verify_workspace_bytes.argtypes = [I, I, I, I]
         L.spec_verify_workspace_bytes.restype = Z
         L.kv_commit_rollback.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P, P, P, P]
@@ -179,6 +184,29 @@ def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted
                                   code, _ptr(err_flag), wsp, wsn)
     if st != SPEC_OK:
         raise SpecError("spec_verify_greedy", st)
+
+
+def spec_verify_greedy_noalloc(target_logits, draft_tokens, out_tokens, out_num_accepted, *,
+                               stream=None, err_flag=None) -> None:
+    """Greedy verification on the library's built-in device scratch (no workspace
+    argument, nothing allocated). Calls on one device must not overlap."""
+    import torch
+    _check(target_logits, "target_logits", 3)
+    _check(draft_tokens, "draft_tokens", 2, torch.int32)
+    _check(out_tokens, "out_tokens", 2, torch.int32)
+    _check(out_num_accepted, "out_num_accepted", 1, torch.int32)
+    B, K1, V = target_logits.shape
+    st = lib().spec_verify_greedy_noalloc(_ptr(target_logits), _ptr(draft_tokens), B, K1 - 1, V,
+                                          _ptr(out_tokens), _ptr(out_num_accepted),
+                                          _stream(stream), _dtype_code(target_logits),
+                                          _ptr(err_flag))
+    if st != SPEC_OK:
+        raise SpecError("spec_verify_greedy_noalloc", st)
+
+
+def spec_verify_greedy_noalloc_max_bytes() -> int:
+    """Size of the built-in scratch used by spec_verify_greedy_noalloc."""
+    return int(lib().spec_verify_greedy_noalloc_max_bytes())
 
 
 def kv_commit_rollback(block_table, seq_lens, num_accepted, prov_blocks, kv_pool, free_stack,
