@@ -13,8 +13,8 @@ namespace sv {
 constexpr int kCW = 8;                 // consumer warps per CTA
 constexpr int kCons = kCW * 32;        // consumer threads
 constexpr int kThreads = kCons + 64;   // + producer warp (bulk-copy issue) + finisher warp
-constexpr int kStages = 6;             // ring depth (6 x 16 KB: two CTAs per SM)
-constexpr int kChunk = 16384;          // bytes per ring stage
+constexpr int kStages = 3;             // ring depth (3 x 32 KB: two CTAs per SM)
+constexpr int kChunk = 32768;          // bytes per ring stage
 constexpr int kMaxK = 31;              // draft positions (fits a warp ballot)
 constexpr int kMaxRows = 2 * kMaxK + 1;
 

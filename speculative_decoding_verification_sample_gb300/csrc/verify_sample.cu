@@ -266,10 +266,14 @@ __device__ __forceinline__ df acc_elem(float z, float Chi, float Clo, float Kc, 
   return df_exp2(s.hi, __fadd_rn(s.lo, pl), th, tl);
 }
 
-// Relative error bound of one normalised double-float term: the exponential
-// (< 4e-13), its argument (< 2^-46 (|z C| + |Kc|), offsets below 2^22 by the
-// row checks), the normaliser sum and reciprocal; kept above their total.
-constexpr float kAccRho = 4e-12f;
+// Relative error bound of one normalised double-float term, for a row whose
+// offset is Kc: the exponential (< 4e-13, or two table entries and their
+// product, < 1e-12), its argument (< 2^-46 (|z C| + |Kc|) with |z C| below
+// |Kc| + 127 for every term that is not flushed), the normaliser sum and
+// reciprocal; kept above their total.
+__device__ __forceinline__ float acc_rho(float Kc) {
+  return 2e-12f + 2.2e-14f * (fabsf(Kc) + 256.0f);
+}
 
 // Upper bound on the sum of the computed fp32 probabilities of a row.
 constexpr float kQmax = 1.001f;
@@ -953,7 +957,7 @@ __device__ void finish_fb(const SampleArgs& a, const Smem& L, int b, int aux) {
   const float uK = a.uniforms[size_t(b) * (a.K + 1) + a.K];
   const DrawSlices sl = draw_slices(a, b);
   const df Sr = sl.total;
-  const float Eb = kAccRho * (sl.f2 + sl.f3) + 1e-14f * Sr.hi + 1e-36f;
+  const float Eb = fmaxf(acc_rho(Kq), acc_rho(Kp)) * (sl.f2 + sl.f3) + 1e-14f * Sr.hi + 1e-36f;
   if (!(Sr.hi > 0.0f) && dr.pair) {
     // zero residual mass: the draw uses q_j itself
     if (lane == 0) {
