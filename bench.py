@@ -35,7 +35,10 @@ UNIT = "positions/s"
 WORKLOAD = dict(B=256, K=4, V=151936, T=1.0, sigma=0.5, target_std=3.0, logits="bf16",
                 kv_layers=32, kv_heads=8, head_dim=128, kv_dtype="bf16", block_size=16,
                 prefix_lo=512, prefix_hi=4096)
-PROFILE_JSON = os.path.join(ROOT, "profiles", "verify_sample_kernel_b256_k4_v151936.json")
+PROFILES = {  # committed ncu summaries of the timed kernel, per mode
+    "sample": os.path.join(ROOT, "profiles", "verify_sample_kernel_b256_k4_v151936.md"),
+    "greedy": os.path.join(ROOT, "profiles", "verify_greedy_kernel_b256_k4_v151936.md"),
+}
 
 
 def parse():
@@ -169,17 +172,24 @@ def source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
+def profiled_traffic(kind):
+    """DRAM bytes (read + write) per launch from the committed ncu summary of the
+    kernel, if it was taken on the current kernel sources (else None)."""
+    fields = {}
     try:
-        with open(PROFILE_JSON) as f:
-            p = json.load(f)
-    except (OSError, ValueError):
+        with open(PROFILES[kind]) as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip() in ("source_hash", "dram_bytes_per_launch") and v.strip():
+                    fields[k.strip()] = v.strip()
+    except OSError:
         return None
-    if p.get("source_hash") != source_hash():
+    if fields.get("source_hash") != source_hash():
         return None
-    return p.get("dram_bytes_per_launch")
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def algorithmic_verify_bytes(na, K, V, e=2):
@@ -378,8 +388,10 @@ def main():
                        "mode": a.mode,
                        "l2": f"inputs rotate over {nb} batch(es) of 622 MB logits (> 129 MB L2)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": profiled_traffic(),
-                         "kernel": "verify_sample_kernel<bf16>", "peak_kind": peak_kind,
+                         "frac": achieved / peak,
+                         "traffic": profiled_traffic("greedy" if a.mode == "greedy" else "sample"),
+                         "kernel": ("verify_greedy_kernel<bf16>" if a.mode == "greedy"
+                                    else "verify_sample_kernel<bf16>"), "peak_kind": peak_kind,
                          "algorithmic_bytes_per_launch": alg, "avg_launch_ms": v_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,
