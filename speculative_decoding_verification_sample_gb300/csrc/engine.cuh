@@ -419,11 +419,12 @@ __device__ __forceinline__ void handoff_post(const Handoff& h, uint32_t n) {
 // partials into the task's slice partials (`combine(t, slot)`, plain stores),
 // issues one fence, frees the slots, arrives on every task's row counter
 // (lanes in parallel, one atomicAdd each), and then runs the continuation
-// (`cont(t)`) of every row whose stage that arrival completed. One memory
-// round trip per batch instead of two per task.
-template <class Combine, class Continue>
+// (`cont(t)`) of every row whose stage that arrival completed (`expect(t)`:
+// the number of tasks of t's stage). One memory round trip per batch instead
+// of two per task.
+template <class Combine, class Continue, class Expect>
 __device__ inline void finisher_loop(const Ws& ws, const Handoff& ho, volatile int* abort,
-                                     Combine&& combine, Continue&& cont) {
+                                     Combine&& combine, Continue&& cont, Expect&& expect) {
   const int lane = threadIdx.x & 31;
   for (uint32_t n = 0;;) {
     if (!mbar_wait(&ho.done[n % kSlots], (n / kSlots) & 1)) {
@@ -452,7 +453,7 @@ __device__ inline void finisher_loop(const Ws& ws, const Handoff& ho, volatile i
     int last = 0;
     if (lane < cnt) {
       const uint32_t old = atomicAdd(&ws.row_cnt()[mine.b], 1u);
-      last = (old == uint32_t(ws.L.S) - 1);
+      last = (old == uint32_t(expect(mine)) - 1);  // tasks in the row's stage
       if (last) ws.row_cnt()[mine.b] = 0;  // the row's next stage counts from zero
     }
     unsigned lm = __ballot_sync(0xffffffffu, last);

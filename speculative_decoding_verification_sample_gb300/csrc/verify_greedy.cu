@@ -312,7 +312,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
         [&](const QTask& t) {
           if (t.type == kG1) finish_g1(a, L, t.b);
           else finish_gb(a, L, t.b);
-        });
+        },
+        [&](const QTask&) { return a.S; });
   } else {
     // ------------------------------------------------ consumers
     const int tid = threadIdx.x;

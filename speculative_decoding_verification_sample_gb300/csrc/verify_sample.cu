@@ -21,7 +21,9 @@
 //       finish: locate u_K * total mass slice -> unit -> entry, certify
 //   FA  (rare) double-float row sums of the draw's rows
 //   FB  (rare) double-float residual and unit sums; finish: certified search
-// Only row j of the draft/target pair is ever re-read for the draw.
+// Only row j of the draft/target pair is ever re-read for the draw. The rare
+// stages AR, FA and FB are cut finer (each slice into M pieces) so that a
+// refined row's compute-heavy passes spread over more CTAs.
 //
 // Arithmetic. No fp64 arithmetic (GB300 runs fp64 at a small fraction of its
 // fp32 rate): logits are widened to fp32, exponentials use the MUFU exp2 with
@@ -67,6 +69,7 @@ struct SampleArgs {
   const int32_t* tokens;
   const float* uniforms;
   int B, K, V, S, nvec;
+  int M, R;        // refinement pieces per slice, per row (R = S M)
   float c;         // fl32(log2(e) / T)
   float Chi, Clo;  // log2(e) / T as a float pair
   Bounds bd;
@@ -390,8 +393,60 @@ struct DrawRows {
   bool pair;
 };
 __device__ __forceinline__ DrawRows draw_rows(int K, int aux) {
-  const int j = aux & 0xff, mode = aux >> 8;
+  const int j = aux & 0xff, mode = (aux >> 8) & 1;
   return {j, mode == kModeResidual && j < K};
+}
+
+// The rare stages AR, FA and FB may run on pieces instead of slices (task aux
+// bit kPieceBit): the finisher that enqueues them chooses pieces once every
+// first-stage task is claimed, when the launch's tail has idle CTAs and few
+// runnable tasks; before that whole slices keep the task count low.
+constexpr int kPieceBit = 1 << 9;
+
+__device__ __forceinline__ bool is_piece(const QTask& t) {
+  return (t.type == kAR || t.type == kFA || t.type == kFB) && (t.aux & kPieceBit);
+}
+
+// kPieceBit if the next rare stage of a row should run on pieces.
+__device__ __forceinline__ int piece_choice(const SampleArgs& a) {
+  if (a.M == 1) return 0;
+  return ld_volatile_u32(&a.ws.hdr()->p1_next) >= uint32_t(a.B) * uint32_t(a.S) ? kPieceBit : 0;
+}
+
+__device__ __forceinline__ int stage_tasks(const SampleArgs& a, int piece_bit) {
+  return piece_bit ? a.R : a.S;
+}
+
+// Vector range [v0, v1) of the task's part of the row: slice s, or for the
+// piece stages piece s (slice s / M cut into M runs of whole 32-vector units,
+// none empty since a slice has at least M units). pv0 is the start of the
+// enclosing slice, whose unit-sum array the piece writes into.
+__device__ __forceinline__ void task_range(const SampleArgs& a, bool pieces, int s, int& v0,
+                                           int& v1, int& ps, int& pv0) {
+  if (!pieces) {
+    slice_range(a.nvec, a.S, s, v0, v1);
+    ps = s;
+    pv0 = v0;
+    return;
+  }
+  ps = s / a.M;
+  const int i = s % a.M;
+  int s0, s1;
+  slice_range(a.nvec, a.S, ps, s0, s1);
+  const int units = (s1 - s0 + 31) / 32;
+  v0 = s0 + (units * i / a.M) * 32;
+  v1 = (i == a.M - 1) ? s1 : s0 + (units * (i + 1) / a.M) * 32;
+  pv0 = s0;
+}
+
+// Partials of piece p of row b (4 floats) inside the row's partial block.
+__device__ __forceinline__ float* piece_part(const SampleArgs& a, int b, int p) {
+  return a.ws.part(b, 0) + 4 * p;
+}
+
+// Partials of a task's slice or piece.
+__device__ __forceinline__ float* task_part(const SampleArgs& a, bool pieces, int b, int s) {
+  return pieces ? piece_part(a, b, s) : a.ws.part(b, s);
 }
 
 // ------------------------------------------------------------------ finisher
@@ -441,19 +496,19 @@ __device__ void stats_rows(const SampleArgs& a, Fin& F, int b, int nrows) {
   }
 }
 
-// Sums over the S slices of the four floats at offset 0 of each slice's
-// partials, lanes in parallel: x0 + x1 as a pair, x2 and x3 as floats (or
-// x2 + x3 as a second pair when `pairs`). Every lane gets the totals.
+// Sums over the slices (or pieces) of the four floats of their partials, lanes
+// in parallel: x0 + x1 as a pair, x2 and x3 as floats (or x2 + x3 as a
+// second pair when `pairs`). Every lane gets the totals.
 struct SliceSums {
   df p0, p1;
   float f2, f3;
 };
-__device__ SliceSums slice_sums(const SampleArgs& a, int b, bool pairs) {
+__device__ SliceSums slice_sums(const SampleArgs& a, int b, bool pairs, bool pieces) {
   const int lane = threadIdx.x & 31;
   df p0{0.f, 0.f}, p1{0.f, 0.f};
   float f2 = 0.f, f3 = 0.f;
-  for (int sl = lane; sl < a.S; sl += 32) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, sl)));
+  for (int sl = lane; sl < (pieces ? a.R : a.S); sl += 32) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(task_part(a, pieces, b, sl)));
     p0 = df_add(p0, df{v.x, v.y});
     if (pairs) {
       p1 = df_add(p1, df{v.z, v.w});
@@ -549,7 +604,8 @@ __device__ void continue_tests(const SampleArgs& a, int b, int i0, int flags, in
   // ambiguous: double-float sums of target and draft row i (AR stage)
   if (lane == 0) {
     row_state(a, b)->flags = flags | SPEC_ROW_ACCEPT_REFINED;
-    enqueue_row_stage(a.ws, kAR, b, a.S, i);
+    const int pb = piece_choice(a);
+    enqueue_row_stage(a.ws, kAR, b, stage_tasks(a, pb), i | pb);
   }
   __syncwarp();
 }
@@ -635,8 +691,8 @@ __device__ void finish_p1(const SampleArgs& a, const Smem& L, int b) {
 
 // AR complete: decide accept test i from double-float row sums.
 template <class E>
-__device__ void finish_ar(const SampleArgs& a, const Smem& L, int b, int i) {
-  const int lane = threadIdx.x & 31, K = a.K;
+__device__ void finish_ar(const SampleArgs& a, const Smem& L, int b, int aux) {
+  const int lane = threadIdx.x & 31, K = a.K, i = aux & 0xff;
   RowState* st = row_state(a, b);
   const int d = load_tokens(a, b);
   int state = kAccept;
@@ -650,7 +706,7 @@ __device__ void finish_ar(const SampleArgs& a, const Smem& L, int b, int i) {
   }
   int flags = __ldcg(&st->flags);
   const float u = a.uniforms[size_t(b) * (K + 1) + i];
-  const SliceSums ss = slice_sums(a, b, true);
+  const SliceSums ss = slice_sums(a, b, true, aux & kPieceBit);
   const df S0 = ss.p0, S1 = ss.p1;
   const RowPtrs<E> rp = row_ptrs<E>(a, b);
   const int di = __shfl_sync(0xffffffffu, d, i);
@@ -706,27 +762,32 @@ __device__ void finish_bs(const SampleArgs& a, const Smem& L, int b) {
   __syncwarp();
 }
 
-// The slice sums of a draw stage, lanes in parallel: lane l holds slices l
-// and l + 32 (x0 + x1 as a pair in xa / xb, the other two floats in f2 / f3),
-// and the row totals (every lane).
+// The segment sums of a draw stage (slices after SW, pieces after FB), lanes
+// in parallel: lane l holds segments l and l + 32 (x0 + x1 as a pair in xa /
+// xb, the other two floats in f2 / f3), and the row totals (every lane).
 struct DrawSlices {
-  df xa, xb;  // this lane's slices
+  df xa, xb;  // this lane's segments
   df total;
   float f2, f3;
+  bool pieces;
+  int n;  // segments
 };
-__device__ DrawSlices draw_slices(const SampleArgs& a, int b) {
+__device__ DrawSlices draw_slices(const SampleArgs& a, int b, bool pieces) {
   const int lane = threadIdx.x & 31;
   DrawSlices r;
+  r.pieces = pieces;
+  r.n = pieces ? a.R : a.S;
   r.xa = r.xb = df{0.f, 0.f};
   float f2 = 0.f, f3 = 0.f;
-  if (lane < a.S) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, lane)));
+  auto seg = [&](int i) { return pieces ? piece_part(a, b, i) : a.ws.part(b, i); };
+  if (lane < r.n) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(seg(lane)));
     r.xa = df{v.x, v.y};
     f2 = v.z;
     f3 = v.w;
   }
-  if (lane + 32 < a.S) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, lane + 32)));
+  if (lane + 32 < r.n) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(seg(lane + 32)));
     r.xb = df{v.x, v.y};
     f2 += v.z;
     f3 += v.w;
@@ -751,7 +812,7 @@ __device__ int search_draw(const SampleArgs& a, int b, const Entries& ent, const
   df pre_s{0.f, 0.f};
   {
     df sbase{0.f, 0.f};
-    for (int s0 = 0; s0 < a.S; s0 += 32) {
+    for (int s0 = 0; s0 < sl.n; s0 += 32) {
       const df x = (s0 == 0) ? sl.xa : sl.xb;
       df inc = x;
 #pragma unroll
@@ -779,11 +840,11 @@ __device__ int search_draw(const SampleArgs& a, int b, const Entries& ent, const
   int token = -1;
   df tlo = pre_s, thi = pre_s;
   if (ss >= 0) {
-    int v0, v1;
-    slice_range(a.nvec, a.S, ss, v0, v1);
+    int v0, v1, ps, pv0;
+    task_range(a, sl.pieces, ss, v0, v1, ps, pv0);
     const int nu = (v1 - v0 + 31) / 32;
     // unit: lanes scan 32 units at a time
-    const float2* up = a.ws.units(b, ss);
+    const float2* up = a.ws.units(b, ps) + (v0 - pv0) / 32;
     int us = -1;
     df ubase = pre_s, ubase_s = pre_s;
     for (int u0 = 0; u0 < nu && us < 0; u0 += 32) {
@@ -881,7 +942,7 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
   const float Kq = __ldcg(&st->Kq), Rq = __ldcg(&st->Rq);
   const float Kp = dr.pair ? __ldcg(&st->Kp) : 0.f, Rp = dr.pair ? __ldcg(&st->Rp) : 0.f;
   const float uK = a.uniforms[size_t(b) * (a.K + 1) + a.K];
-  const DrawSlices sl = draw_slices(a, b);
+  const DrawSlices sl = draw_slices(a, b, false);
   const df Sr = sl.total;
   // Error bound (probability units) of the fp32 sweep. Per term, relative:
   // exp2 (ex2), argument rounding and the fp32 temperature constant (ln2 u |x|
@@ -918,7 +979,8 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
   }
   if (lane == 0) {
     st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
-    enqueue_row_stage(a.ws, kFA, b, a.S, aux);
+    const int pb = piece_choice(a);
+    enqueue_row_stage(a.ws, kFA, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
   }
   __syncwarp();
 }
@@ -927,7 +989,7 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
 __device__ void finish_fa(const SampleArgs& a, int b, int aux) {
   const int lane = threadIdx.x & 31;
   const DrawRows dr = draw_rows(a.K, aux);
-  const SliceSums ss = slice_sums(a, b, true);
+  const SliceSums ss = slice_sums(a, b, true, aux & kPieceBit);
   if (lane == 0) {
     RowState* st = row_state(a, b);
     const df I0 = df_recip(ss.p0);
@@ -938,7 +1000,8 @@ __device__ void finish_fa(const SampleArgs& a, int b, int aux) {
       st->Ip_hi = I1.hi;
       st->Ip_lo = I1.lo;
     }
-    enqueue_row_stage(a.ws, kFB, b, a.S, aux);
+    const int pb = piece_choice(a);
+    enqueue_row_stage(a.ws, kFB, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
   }
   __syncwarp();
 }
@@ -955,14 +1018,15 @@ __device__ void finish_fb(const SampleArgs& a, const Smem& L, int b, int aux) {
   const df Iq{__ldcg(&st->Iq_hi), __ldcg(&st->Iq_lo)};
   const df Ip = dr.pair ? df{__ldcg(&st->Ip_hi), __ldcg(&st->Ip_lo)} : df{0.f, 0.f};
   const float uK = a.uniforms[size_t(b) * (a.K + 1) + a.K];
-  const DrawSlices sl = draw_slices(a, b);
+  const DrawSlices sl = draw_slices(a, b, aux & kPieceBit);
   const df Sr = sl.total;
   const float Eb = fmaxf(acc_rho(Kq), acc_rho(Kp)) * (sl.f2 + sl.f3) + 1e-14f * Sr.hi + 1e-36f;
   if (!(Sr.hi > 0.0f) && dr.pair) {
     // zero residual mass: the draw uses q_j itself
     if (lane == 0) {
       st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;
-      enqueue_row_stage(a.ws, kFB, b, a.S, dr.j | (kModeQ << 8));
+      const int pb = piece_choice(a);
+      enqueue_row_stage(a.ws, kFB, b, stage_tasks(a, pb), dr.j | (kModeQ << 8) | pb);
     }
     __syncwarp();
     return;
@@ -994,7 +1058,7 @@ __device__ void finish_fb(const SampleArgs& a, const Smem& L, int b, int aux) {
 // task's slice partials in the workspace.
 __device__ void combine_task(const SampleArgs& a, const QTask& t, const uint8_t* slot) {
   const int lane = threadIdx.x & 31;
-  float* o = a.ws.part(t.b, t.s);
+  float* o = task_part(a, is_piece(t), t.b, t.s);
   if (t.type == kP1 || t.type == kBS) {
     const int R = 2 * a.K, nrows = (t.type == kP1) ? 2 * a.K : 1;
     const float* w = reinterpret_cast<const float*>(slot + 16);
@@ -1174,8 +1238,8 @@ __device__ bool consume_rowsums(const SampleArgs& a, const Smem& L, uint32_t& it
   const RowState* st = row_state(a, t.b);
   float K0, K1;
   if (t.type == kAR) {
-    K0 = __ldcg(&st->rK[2 * t.aux]);
-    K1 = __ldcg(&st->rK[2 * t.aux + 1]);
+    K0 = __ldcg(&st->rK[2 * (t.aux & 0xff)]);
+    K1 = __ldcg(&st->rK[2 * (t.aux & 0xff) + 1]);
   } else {
     K0 = __ldcg(&st->Kq);
     K1 = draw_rows(a.K, t.aux).pair ? __ldcg(&st->Kp) : 0.f;
@@ -1233,11 +1297,11 @@ __device__ bool consume_fb(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   ae.Ip = dr.pair ? df{__ldcg(&st->Ip_hi), __ldcg(&st->Ip_lo)} : df{0.f, 0.f};
   ae.th = L.tab_hi;
   ae.tl = L.tab_lo;
-  int v0, v1;
-  slice_range(a.nvec, a.S, t.s, v0, v1);
+  int v0, v1, ps, pv0;
+  task_range(a, is_piece(t), t.s, v0, v1, ps, pv0);
   df acc{0.f, 0.f};
   float Q = 0.f, P = 0.f;
-  float2* units = a.ws.units(t.b, t.s);
+  float2* units = a.ws.units(t.b, ps);  // the enclosing slice's unit sums
   bool ok = true;
   for (;;) {
     const ChunkMeta m = L.ring.meta[it % kStages];
@@ -1262,7 +1326,7 @@ __device__ bool consume_fb(const SampleArgs& a, const Smem& L, uint32_t& it, uin
         acc = df_add(acc, vs);
       }
       const df us = df_warp_sum(vs);
-      if (lane == 0) units[(m.c0 - v0 + i0) / 32] = make_float2(us.hi, us.lo);
+      if (lane == 0) units[(m.c0 - pv0 + i0) / 32] = make_float2(us.hi, us.lo);
     }
     const bool lastc = L.ring.meta[it2 % kStages].last != 0;
     release_stage(L.ring, it);
@@ -1317,8 +1381,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
         }
         idle_t0 = 0;
         const RowPtrs<E> rp = row_ptrs<E>(a, t.b);
-        int v0, v1;
-        slice_range(a.nvec, a.S, t.s, v0, v1);
+        int v0, v1, ps, pv0;
+        task_range(a, is_piece(t), t.s, v0, v1, ps, pv0);
         const char* rows[2 * kMaxK];
         int nrows = 0;
         bool paired = false;
@@ -1330,8 +1394,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
         } else if (t.type == kBS) {
           rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(K) * a.V);
         } else if (t.type == kAR) {
-          rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(t.aux) * a.V);
-          rows[nrows++] = reinterpret_cast<const char*>(rp.drf + size_t(t.aux) * a.V);
+          rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(t.aux & 0xff) * a.V);
+          rows[nrows++] = reinterpret_cast<const char*>(rp.drf + size_t(t.aux & 0xff) * a.V);
         } else {
           const DrawRows dr = draw_rows(K, t.aux);
           rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(dr.j) * a.V);
@@ -1371,7 +1435,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
               finish_fb<E>(a, L, t.b, t.aux);
               break;
           }
-        });
+        },
+        [&](const QTask& t) { return is_piece(t) ? a.R : a.S; });
   } else {
     // ------------------------------------------------ consumers
     const int tid = threadIdx.x;
@@ -1418,15 +1483,29 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
 // ------------------------------------------------------------------ host side
 namespace {
 
+// Refinement pieces per slice: up to 3 (measured best on the bench workload
+// among 1, 2, 3, 4 and 8; at most kMaxSlices per row), no more than the
+// 32-vector units of the smallest slice.
+int pieces_per_slice(int nvec, int S) {
+  int m = kMaxSlices / S;
+  if (m > 3) m = 3;
+  const int min_units = (nvec / S + 31) / 32;
+  if (m > min_units) m = min_units;
+  return m < 1 ? 1 : m;
+}
+
 WsLayout sample_layout(int B, int K, int V, int dtype) {
   const int kvec = (dtype == SPEC_BF16) ? 8 : 4;
   const int nvec = V / kvec;
   const int S = slices_for(nvec, B);
+  const int M = pieces_per_slice(nvec, S);
   const int maxslice = (nvec + S - 1) / S;
   const int ustride = (maxslice + 31) / 32 + 1;
-  const int part = (8 * K > 8) ? 8 * K : 8;
-  // queued stages per row: BS, SW, FA, FB twice (zero residual), AR up to K times
-  return ws_layout(B, S, part, ustride, 5 + K, int(sizeof(RowState)));
+  int part = (8 * K > 8) ? 8 * K : 8;  // P1: 4 floats for each of the 2K rows
+  if (part < 4 * M) part = 4 * M;      // a row's S blocks hold its R = S M piece partials
+  // queued tasks per row: BS, SW (S each); FA, FB twice (zero residual), AR up
+  // to K times (R = S M each)
+  return ws_layout(B, S, part, ustride, (5 + K) * M, int(sizeof(RowState)));
 }
 
 }  // namespace
@@ -1448,6 +1527,8 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.nvec = s.V / kvec;
   const WsLayout wl = sample_layout(s.B, s.K, s.V, s.dtype);
   a.S = wl.S;
+  a.M = pieces_per_slice(a.nvec, a.S);
+  a.R = a.S * a.M;
   a.ws.base = static_cast<uint8_t*>(s.workspace);
   a.ws.L = wl;
   const double C = 1.4426950408889634073599246810018921 / double(s.temperature);  // log2(e)/T
