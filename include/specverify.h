@@ -107,6 +107,14 @@ extern "C" {
  *   err_flag       optional [1] int32, device error bits are OR-ed in (never cleared)
  *   row_info       optional [B] int32, SPEC_ROW_* bits of each row (overwritten)
  *   q_at_d, p_at_d optional [B, K] float, q_i(d_i) and p_i(d_i) (for inspection)
+ *   accept_counters optional [2K + 2] uint64, acceptance statistics ACCUMULATED over
+ *                  calls (the caller zeroes it): [i] += rows in which draft position
+ *                  i was tested (i <= n, i < K), [K + i] += rows in which it was
+ *                  accepted (i < n), [2K] += rows verified, [2K + 1] += tokens
+ *                  emitted (n + 1 per row). Rows with a device error are not
+ *                  counted. Per-position acceptance a_i = [K+i] / [i]; mean
+ *                  acceptance length = [2K+1] / [2K] ([Q] "mean acceptance length";
+ *                  [L] expected accepted tokens).
  *
  * Semantics: for i = 0..K-1, d_i is accepted iff p_i(d_i) <= 0 or
  * u[i] < min(1, q_i(d_i)/p_i(d_i)); at the first rejection j the token is the
@@ -121,7 +129,8 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
                        const int32_t* draft_tokens, const float* uniforms, float temperature,
                        int B, int K, int V, int32_t* out_tokens, int32_t* out_num_accepted,
                        void* stream, int dtype, int32_t* err_flag, int32_t* row_info,
-                       float* q_at_d, float* p_at_d, void* workspace, size_t workspace_bytes);
+                       float* q_at_d, float* p_at_d, void* workspace, size_t workspace_bytes,
+                       uint64_t* accept_counters);
 
 /*
  * spec_verify_greedy - greedy verification ([P] "What it does").
@@ -131,10 +140,12 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
  *   n = number of leading i with d_i == g_i; out_tokens[b] = d_0..d_{n-1}, g_n, -1...;
  *   out_num_accepted[b] = n. Same pointer, alignment and error conventions as
  *   spec_verify_sample; a row with NaN logits is reported as SPEC_DERR_LOGITS.
+ *   accept_counters: optional, as for spec_verify_sample.
  */
 int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int K,
                        int V, int32_t* out_tokens, int32_t* out_num_accepted, void* stream,
-                       int dtype, int32_t* err_flag, void* workspace, size_t workspace_bytes);
+                       int dtype, int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                       uint64_t* accept_counters);
 
 /*
  * spec_verify_greedy_noalloc - spec_verify_greedy without a caller workspace.

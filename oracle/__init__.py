@@ -41,5 +41,6 @@ from .verify import (  # noqa: F401
     verify_sample,
     verify_greedy,
     verify_step,
+    acceptance_counters,
 )
 from .kv import kv_commit, pool_invariant_ok  # noqa: F401

@@ -193,3 +193,28 @@ def verify_step(target, draft, tokens, uniforms, temperature, **kw) -> dict:
     if temperature64(temperature) == 0.0:
         return verify_greedy(target, tokens)
     return verify_sample(target, draft, tokens, uniforms, temperature, **kw)
+
+
+def acceptance_counters(num_accepted, K: int) -> np.ndarray:
+    """Per-position acceptance statistics of a batch of verified rows.
+
+    The quickscale.ai page ("Quand et pourquoi utiliser le speculative
+    decoding") defines the per-position acceptance rate a_i and the mean
+    acceptance length; the lesson's expected-acceptance formula counts the
+    tokens one step emits (accepted drafts plus the correction or bonus).
+    For a row with n accepted drafts (n = -1: a row with an error, not
+    counted): draft position i is tested iff i <= n (and i < K) and accepted
+    iff i < n; the step emits n + 1 tokens.
+
+    Returns int64 [2K + 2]: tested[0..K), accepted[0..K), rows, tokens emitted.
+    """
+    n = np.asarray(num_accepted, np.int64).ravel()
+    n = n[n >= 0]
+    out = np.zeros(2 * K + 2, np.int64)
+    for i in range(K):
+        out[i] = int(np.sum(n >= i))
+        out[K + i] = int(np.sum(n > i))
+    out[2 * K] = n.size
+    out[2 * K + 1] = int(np.sum(n + 1))
+    return out
+

@@ -53,9 +53,9 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         Z = ctypes.c_size_t
-        L.spec_verify_sample.argtypes = [P, P, P, P, F, I, I, I, P, P, P, I, P, P, P, P, P, Z]
+        L.spec_verify_sample.argtypes = [P, P, P, P, F, I, I, I, P, P, P, I, P, P, P, P, P, Z, P]
         L.spec_verify_sample.restype = I
-        L.spec_verify_greedy.argtypes = [P, P, I, I, I, P, P, P, I, P, P, Z]
+        L.spec_verify_greedy.argtypes = [P, P, I, I, I, P, P, P, I, P, P, Z, P]
         L.spec_verify_greedy.restype = I
         L.spec_verify_greedy_noalloc.argtypes = [P, P, I, I, I, P, P, P, I, P]
         L.spec_verify_greedy_noalloc.restype = I
@@ -143,10 +143,24 @@ def _ws_args(ws, B, K, V, code, device):
     return ctypes.c_void_p(ws.data_ptr() + off), ctypes.c_size_t(ws.numel() - off)
 
 
+def _counters(t, K):
+    """Pointer of an optional [2K+2] 64-bit integer device tensor of counters."""
+    if t is None:
+        return None
+    import torch
+    if not t.is_cuda or t.dtype not in (torch.int64, torch.uint64) or t.numel() != 2 * K + 2 \
+            or not t.is_contiguous():
+        raise ValueError(f"accept_counters must be a contiguous 64-bit integer CUDA tensor "
+                         f"of {2 * K + 2} elements")
+    return _ptr(t)
+
+
 def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature: float,
                        out_tokens, out_num_accepted, *, stream=None, err_flag=None,
-                       row_info=None, q_at_d=None, p_at_d=None, workspace=None) -> None:
-    """Sampling-mode verification; shapes [B,K+1,V], [B,K,V], [B,K], [B,K+1] -> [B,K+1], [B]."""
+                       row_info=None, q_at_d=None, p_at_d=None, workspace=None,
+                       accept_counters=None) -> None:
+    """Sampling-mode verification; shapes [B,K+1,V], [B,K,V], [B,K], [B,K+1] -> [B,K+1], [B].
+    accept_counters: optional int64/uint64 [2K+2] device tensor, accumulated (see the header)."""
     import torch
     _check(target_logits, "target_logits", 3)
     B, K1, V = target_logits.shape
@@ -163,13 +177,13 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temp
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(uniforms),
         ctypes.c_float(temperature), B, K, V, _ptr(out_tokens), _ptr(out_num_accepted),
         _stream(stream), code, _ptr(err_flag), _ptr(row_info),
-        _ptr(q_at_d), _ptr(p_at_d), wsp, wsn)
+        _ptr(q_at_d), _ptr(p_at_d), wsp, wsn, _counters(accept_counters, K))
     if st != SPEC_OK:
         raise SpecError("spec_verify_sample", st)
 
 
 def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted, *,
-                       stream=None, err_flag=None, workspace=None) -> None:
+                       stream=None, err_flag=None, workspace=None, accept_counters=None) -> None:
     """Greedy verification; target [B,K+1,V], tokens [B,K] -> [B,K+1], [B]."""
     import torch
     _check(target_logits, "target_logits", 3)
@@ -181,7 +195,8 @@ def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted
     wsp, wsn = _ws_args(workspace, B, K1 - 1, V, code, target_logits.device)
     st = lib().spec_verify_greedy(_ptr(target_logits), _ptr(draft_tokens), B, K1 - 1, V,
                                   _ptr(out_tokens), _ptr(out_num_accepted), _stream(stream),
-                                  code, _ptr(err_flag), wsp, wsn)
+                                  code, _ptr(err_flag), wsp, wsn,
+                                  _counters(accept_counters, K1 - 1))
     if st != SPEC_OK:
         raise SpecError("spec_verify_greedy", st)
 

@@ -51,7 +51,8 @@ static int check_workspace(void* ws, size_t bytes, int B, int K, int V, int dtyp
 
 int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int K,
                        int V, int32_t* out_tokens, int32_t* out_num_accepted, void* stream,
-                       int dtype, int32_t* err_flag, void* workspace, size_t workspace_bytes) {
+                       int dtype, int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                       uint64_t* accept_counters) {
   const int eb = elem_bytes(dtype);
   if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SPEC_EINVAL;
   if (eb == 0 || B < 1 || K < 1 || K > 31 || V < 1) return SPEC_EINVAL;
@@ -60,7 +61,8 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
   if (int64_t(B) * (V / (16 / eb)) > INT32_MAX) return SPEC_EINVAL;
   if (check_workspace(workspace, workspace_bytes, B, K, V, dtype) != SPEC_OK) return SPEC_EINVAL;
   sv::GreedyLaunch g{target_logits, draft_tokens, B, K, V, dtype, out_tokens, out_num_accepted,
-                     err_flag, stream, workspace};
+                     err_flag, stream, workspace,
+                     reinterpret_cast<unsigned long long*>(accept_counters)};
   return sv::launch_verify_greedy(g);
 }
 
@@ -68,12 +70,13 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
                        const int32_t* draft_tokens, const float* uniforms, float temperature,
                        int B, int K, int V, int32_t* out_tokens, int32_t* out_num_accepted,
                        void* stream, int dtype, int32_t* err_flag, int32_t* row_info,
-                       float* q_at_d, float* p_at_d, void* workspace, size_t workspace_bytes) {
+                       float* q_at_d, float* p_at_d, void* workspace, size_t workspace_bytes,
+                       uint64_t* accept_counters) {
   if (std::isnan(temperature) || temperature < 0.0f || std::isinf(temperature)) return SPEC_EINVAL;
   if (temperature == 0.0f) {
     const int st = spec_verify_greedy(target_logits, draft_tokens, B, K, V, out_tokens,
                                       out_num_accepted, stream, dtype, err_flag, workspace,
-                                      workspace_bytes);
+                                      workspace_bytes, accept_counters);
     if (st == SPEC_OK && row_info)
       if (cudaMemsetAsync(row_info, 0, size_t(B) * sizeof(int32_t),
                           static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -92,7 +95,7 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
   if (check_workspace(workspace, workspace_bytes, B, K, V, dtype) != SPEC_OK) return SPEC_EINVAL;
   sv::SampleLaunch s{target_logits, draft_logits, draft_tokens, uniforms, temperature, B, K, V,
                      dtype, out_tokens, out_num_accepted, err_flag, row_info, q_at_d, p_at_d,
-                     stream, workspace};
+                     stream, workspace, reinterpret_cast<unsigned long long*>(accept_counters)};
   return sv::launch_verify_sample(s);
 }
 

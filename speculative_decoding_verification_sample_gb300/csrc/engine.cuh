@@ -246,6 +246,21 @@ __device__ inline bool producer_idle(const Ws& ws, bool exhausted, uint64_t& idl
   return true;
 }
 
+// Acceptance statistics of one verified row with n accepted drafts, one warp:
+// [i] tested (i <= n, i < K), [K + i] accepted (i < n), [2K] rows, [2K + 1]
+// tokens emitted (n + 1).
+__device__ inline void count_acceptance(unsigned long long* c, int K, int n) {
+  const int lane = threadIdx.x & 31;
+  if (lane < K) {
+    if (lane <= n) atomicAdd(&c[lane], 1ull);
+    if (lane < n) atomicAdd(&c[K + lane], 1ull);
+  }
+  if (lane == 0) {
+    atomicAdd(&c[2 * K], 1ull);
+    atomicAdd(&c[2 * K + 1], static_cast<unsigned long long>(n + 1));
+  }
+}
+
 // ------------------------------------------------------------------ ring
 // Per stage: which task (slot of the task table) and which piece of it.
 struct ChunkMeta {

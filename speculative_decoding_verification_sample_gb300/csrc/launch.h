@@ -26,6 +26,7 @@ struct SampleLaunch {
   float* p_at_d;
   void* stream;
   void* workspace;
+  unsigned long long* counters;
 };
 
 struct GreedyLaunch {
@@ -37,6 +38,7 @@ struct GreedyLaunch {
   int32_t* err;
   void* stream;
   void* workspace;
+  unsigned long long* counters;
 };
 
 struct KvLaunch {

@@ -43,7 +43,7 @@ int spec_verify_greedy_noalloc(const void* target_logits, const int32_t* draft_t
   if (need == 0) {
     // arguments spec_verify_greedy rejects: let it report why
     return spec_verify_greedy(target_logits, draft_tokens, B, K, V, out_tokens, out_num_accepted,
-                              stream, dtype, err_flag, nullptr, 0);
+                              stream, dtype, err_flag, nullptr, 0, nullptr);
   }
   if (need > kStaticScratchBytes) return SPEC_ENOTSUP;  // larger than the built-in scratch
   int dev = 0;
@@ -54,7 +54,8 @@ int spec_verify_greedy_noalloc(const void* target_logits, const int32_t* draft_t
     g_scratch_ptr[dev] = p;
   }
   return spec_verify_greedy(target_logits, draft_tokens, B, K, V, out_tokens, out_num_accepted,
-                            stream, dtype, err_flag, g_scratch_ptr[dev], kStaticScratchBytes);
+                            stream, dtype, err_flag, g_scratch_ptr[dev], kStaticScratchBytes,
+                            nullptr);
 }
 
 }  // extern "C"

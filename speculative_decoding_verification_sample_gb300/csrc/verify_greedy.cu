@@ -38,6 +38,7 @@ struct GreedyArgs {
   int32_t* out_tokens;
   int32_t* out_n;
   int32_t* err;
+  unsigned long long* counters;  // optional acceptance statistics [2K + 2]
   Ws ws;
 };
 
@@ -229,6 +230,7 @@ __device__ void write_row(const GreedyArgs& a, int b, int n, int token, bool err
     if (error && a.err) atomicOr(a.err, errbits);
     atomicAdd(&a.ws.hdr()->rows_done, 1u);  // lets the producers stop; no ordering needed
   }
+  if (a.counters && !error) count_acceptance(a.counters, K, n);
   __syncwarp();
 }
 
@@ -396,6 +398,7 @@ int launch_verify_greedy(const GreedyLaunch& g) {
   a.out_tokens = g.out_tokens;
   a.out_n = g.out_n;
   a.err = g.err;
+  a.counters = g.counters;
   cudaStream_t st = static_cast<cudaStream_t>(g.stream);
   if (cudaMemsetAsync(g.workspace, 0, wl.zero_bytes, st) != cudaSuccess) return SPEC_ECUDA;
   const size_t smem = greedy_smem_bytes(g.K);

@@ -79,6 +79,7 @@ struct SampleArgs {
   int32_t* row_info;
   float* q_at_d;
   float* p_at_d;
+  unsigned long long* counters;  // optional acceptance statistics [2K + 2]
   Ws ws;
 };
 
@@ -545,6 +546,7 @@ __device__ void write_outputs(const SampleArgs& a, int b, int n, int token, int 
     if (a.row_info) a.row_info[b] = flags;
     atomicAdd(&a.ws.hdr()->rows_done, 1u);
   }
+  if (a.counters && !error) count_acceptance(a.counters, K, n);
   __syncwarp();
 }
 
@@ -1549,6 +1551,7 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.row_info = s.row_info;
   a.q_at_d = s.q_at_d;
   a.p_at_d = s.p_at_d;
+  a.counters = s.counters;
   cudaStream_t st = static_cast<cudaStream_t>(s.stream);
   if (cudaMemsetAsync(s.workspace, 0, wl.zero_bytes, st) != cudaSuccess) return SPEC_ECUDA;
   const size_t smem = sample_smem_bytes(2 * s.K);

@@ -294,13 +294,13 @@ def test_host_validation(sv):
     ws = m.workspace_for(2, 2, 64, m.SPEC_BF16, "cuda")
     st = m.lib().spec_verify_greedy(mis.data_ptr(), dv["tokens"].data_ptr(), 2, 2, 64,
                                     out.data_ptr(), n.data_ptr(), None, m.SPEC_BF16, None,
-                                    ws.data_ptr(), ws.numel())
+                                    ws.data_ptr(), ws.numel(), None)
     assert st == m.SPEC_EINVAL
     # workspace too small
     import ctypes
     st = m.lib().spec_verify_greedy(dv["target"].data_ptr(), dv["tokens"].data_ptr(), 2, 2, 64,
                                     out.data_ptr(), n.data_ptr(), None, m.SPEC_BF16, None,
-                                    ws.data_ptr(), ctypes.c_size_t(16))
+                                    ws.data_ptr(), ctypes.c_size_t(16), None)
     assert st == m.SPEC_EINVAL
 
 
