@@ -107,6 +107,48 @@ def kv_state(torch, na):
     return c, d, saved, pool
 
 
+def inplace_kv_us(torch, sv, na, reps=200):
+    """Mean device time (us) of kv_commit_inplace on the bench's batch: prefix lengths
+    U[prefix_lo, prefix_hi], the K+1 provisional slots appended in each row's own
+    blocks, the accepted counts of the verify step. State restored between calls."""
+    import numpy as np
+    w = WORKLOAD
+    B, K, bs = w["B"], w["K"], w["block_size"]
+    rng = np.random.default_rng(45)
+    L = rng.integers(w["prefix_lo"], w["prefix_hi"] + 1, size=B)
+    mb = -(-(w["prefix_hi"] + K + 1) // bs)
+    nb = B * mb + 64
+    ids = rng.permutation(nb)
+    bt = -np.ones((B, mb), np.int32)
+    k = 0
+    for b in range(B):
+        for j in range(-(-int(L[b] + K + 1) // bs)):
+            bt[b, j] = ids[k]
+            k += 1
+    fs = -np.ones(nb, np.int32)
+    fs[:nb - k] = ids[k:]
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.int32)).cuda()  # noqa: E731
+    saved = dict(bt=dev(bt), sl=dev(L), fs=dev(fs), ft=dev([nb - k]))
+    cur = {key: v.clone() for key, v in saved.items()}
+    st, n = dev([0]), dev(na)
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for i in range(reps + 3):
+        for key in cur:
+            cur[key].copy_(saved[key], non_blocking=True)
+        if i >= 3:
+            evs[i - 3][0].record(stream)
+        sv.kv_commit_inplace(cur["bt"], cur["sl"], n, cur["fs"], cur["ft"], st, K=K,
+                             block_size=bs, num_blocks=nb)
+        if i >= 3:
+            evs[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"kv_commit_inplace status {int(st.item())}")
+    return 1e3 * statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -398,6 +440,8 @@ def main():
             "gpu_launches": (3 if a.mode == "step" else 1) * a.steps,
             "clocks": clk,
             "extra": {"verify_ms": v_ms, "kv_commit_and_table_restore_ms": ms_per_step - v_ms,
+                      "kv_commit_inplace_us": (inplace_kv_us(torch, sv, na_list[0][0])
+                                               if a.mode == "step" else None),
                       "kv_bytes_per_step": kvb, "refined_row_fraction": refined,
                       "mean_accepted": float(np.mean([x[0].mean() for x in na_list])),
                       "hbm_frac_of_nominal_8TBs": achieved / 8000.0},

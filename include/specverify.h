@@ -223,6 +223,40 @@ int kv_commit_rollback(int32_t* block_table, int32_t* seq_lens, const int32_t* n
                        int32_t* status, void* stream);
 
 /*
+ * kv_commit_inplace - commit for the in-place KV layout ([L] "Rolling back the KV
+ * cache": keep the physical cache and truncate a logical length).
+ *
+ * Layout: before the verify step the caller appended the K+1 provisional slots
+ * at logical positions L_b .. L_b + K of each row's OWN blocks (block_table
+ * entries [0, ceil((L_b + K + 1) / block_size)) valid). The commit sets the
+ * length to L_b + n_b + 1 and frees every block that then holds no position
+ * below it: block indices ceil((L_b + n_b + 1) / bs) .. ceil((L_b + K + 1) / bs) - 1
+ * are pushed onto the free stack (rows ascending, indices ascending) and set to
+ * -1. No KV byte moves, so no pool pointer is needed.
+ *   block_table [B, max_blocks] int32; seq_lens [B] int32 (L_b, becomes L_b + n_b + 1);
+ *   num_accepted [B] int32 in [0, K]; free_stack [num_blocks] int32 with live
+ *   entries [0, *free_top); status REQUIRED [1] int32: 0, or the SPEC_DERR_* bits
+ *   that stopped the call (then nothing changed: all-or-nothing).
+ * Device errors: SPEC_DERR_BAD_ACCEPT (n outside [0, K]), SPEC_DERR_BAD_LENGTH
+ * (L < 0 or L + K + 1 beyond max_blocks * block_size), SPEC_DERR_BAD_BLOCK (a
+ * table entry holding a provisional slot outside [0, num_blocks), or the pushes
+ * would overflow the stack). Host errors: SPEC_EINVAL (null pointer, sizes,
+ * K outside [0, 31]).
+ */
+int kv_commit_inplace(int32_t* block_table, int32_t* seq_lens, const int32_t* num_accepted,
+                      int num_blocks, int block_size, int B, int K, int max_blocks,
+                      int32_t* free_stack, int32_t* free_top, int32_t* status, void* stream);
+
+/*
+ * kv_evict_provisional - preemption of rows in the in-place layout ([S]: a
+ * preempted request's provisional KV is evicted): as kv_commit_inplace with
+ * every row's length reset to L_b (all K+1 provisional slots discarded).
+ */
+int kv_evict_provisional(int32_t* block_table, int32_t* seq_lens, int num_blocks,
+                         int block_size, int B, int K, int max_blocks, int32_t* free_stack,
+                         int32_t* free_top, int32_t* status, void* stream);
+
+/*
  * spec_selftest_ex2 - diagnostic: the maximum relative error of the hardware
  * base-2 exponential over every fp32 argument in [lo, hi] (-126 <= lo <= hi <= 64),
  * measured against fp64 exp2 and written to the device double *out_max_rel.

@@ -43,4 +43,4 @@ from .verify import (  # noqa: F401
     verify_step,
     acceptance_counters,
 )
-from .kv import kv_commit, pool_invariant_ok  # noqa: F401
+from .kv import kv_commit, kv_truncate_inplace, pool_invariant_ok  # noqa: F401

@@ -136,3 +136,57 @@ def pool_invariant_ok(block_table, prov_blocks, free_stack, free_top: int, num_b
     if ids.size != num_blocks:
         return False
     return bool(np.array_equal(np.sort(ids), np.arange(num_blocks)))
+
+
+def kv_truncate_inplace(block_table, seq_lens, num_accepted, free_stack, free_top: int, *,
+                        block_size: int, K: int, num_blocks: int, evict: bool = False) -> dict:
+    """The in-place variant: provisional slots live in the row's own blocks.
+
+    Source: the lesson's "Rolling back the KV cache" gives, besides the scratch
+    buffer, the design that keeps the physical KV cache and truncates a logical
+    length; the sglang_spec_decode README adds eviction of a row's provisional
+    KV on preemption. Reading used here: before the verify step the caller
+    appended the K+1 provisional slots at logical positions L .. L+K of each row
+    (blocks allocated as needed). A commit truncates the row to L + n + 1
+    (`evict`: back to L) and frees every block that then holds no position
+    below the new length: block indices ceil(new/bs) .. ceil((L+K+1)/bs) - 1,
+    pushed onto the free stack rows ascending, indices ascending, and set to -1.
+    No KV byte moves. All-or-nothing, with the same error bits as kv_commit.
+    """
+    bt = np.array(block_table, np.int64, copy=True)
+    sl = np.array(seq_lens, np.int64, copy=True)
+    fs = np.array(free_stack, np.int64, copy=True)
+    top = int(free_top)
+    B, max_blocks = bt.shape
+    na = np.zeros(B, np.int64) if evict else np.asarray(num_accepted, np.int64)
+    err = 0
+    new_len = np.zeros(B, np.int64)
+    frees = []
+    for b in range(B):
+        n, L = int(na[b]), int(sl[b])
+        if not evict and not 0 <= n <= K:
+            err |= ERR_BAD_ACCEPT
+            continue
+        end = _cdiv(L + K + 1, block_size)          # blocks holding prefix + provisional slots
+        if L < 0 or end > max_blocks:
+            err |= ERR_BAD_LENGTH
+            continue
+        for j in range(L // block_size, end):
+            if not 0 <= int(bt[b, j]) < num_blocks:
+                err |= ERR_BAD_BLOCK
+        new_len[b] = L if evict else L + n + 1
+        frees.append((b, _cdiv(int(new_len[b]), block_size), end))
+    n_push = sum(e - s for _, s, e in frees)
+    if err == 0 and (top < 0 or top + n_push > num_blocks):
+        err |= ERR_BAD_BLOCK                        # the pushes would overflow the stack
+    if err:
+        return dict(block_table=np.asarray(block_table, np.int64).copy(),
+                    seq_lens=np.asarray(seq_lens, np.int64).copy(),
+                    free_stack=np.asarray(free_stack, np.int64).copy(), free_top=int(free_top),
+                    err=err)
+    for b, s, e in frees:
+        for j in range(s, e):
+            fs[top] = bt[b, j]
+            top += 1
+            bt[b, j] = -1
+    return dict(block_table=bt, seq_lens=new_len, free_stack=fs, free_top=top, err=0)

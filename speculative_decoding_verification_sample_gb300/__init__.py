@@ -29,7 +29,8 @@ SPEC_ROW_UNCERTIFIED, SPEC_ROW_ZERO_RESIDUAL = 4, 8
 
 EXPORTED = ("spec_verify_sample", "spec_verify_greedy", "spec_verify_workspace_bytes",
             "kv_commit_rollback", "spec_selftest_ex2", "spec_status_string", "spec_version",
-            "spec_verify_greedy_noalloc", "spec_verify_greedy_noalloc_max_bytes")
+            "spec_verify_greedy_noalloc", "spec_verify_greedy_noalloc_max_bytes",
+            "kv_commit_inplace", "kv_evict_provisional")
 
 _lib = None
 
@@ -59,6 +60,10 @@ def lib() -> ctypes.CDLL:
         L.spec_verify_greedy.restype = I
         L.spec_verify_greedy_noalloc.argtypes = [P, P, I, I, I, P, P, P, I, P]
         L.spec_verify_greedy_noalloc.restype = I
+        L.kv_commit_inplace.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P]
+        L.kv_commit_inplace.restype = I
+        L.kv_evict_provisional.argtypes = [P, P, I, I, I, I, I, P, P, P, P]
+        L.kv_evict_provisional.restype = I
         L.spec_verify_greedy_noalloc_max_bytes.argtypes = []
         L.spec_verify_greedy_noalloc_max_bytes.restype = Z
         L.spec_verify_workspace_bytes.argtypes = [I, I, I, I]
@@ -222,6 +227,38 @@ def spec_verify_greedy_noalloc(target_logits, draft_tokens, out_tokens, out_num_
 def spec_verify_greedy_noalloc_max_bytes() -> int:
     """Size of the built-in scratch used by spec_verify_greedy_noalloc."""
     return int(lib().spec_verify_greedy_noalloc_max_bytes())
+
+
+def kv_commit_inplace(block_table, seq_lens, num_accepted, free_stack, free_top, status, *,
+                      K: int, block_size: int, num_blocks: int, stream=None) -> None:
+    """In-place KV commit: truncate each row to L + n + 1 and free the blocks past it."""
+    import torch
+    _check(block_table, "block_table", 2, torch.int32)
+    for t, n in ((seq_lens, "seq_lens"), (num_accepted, "num_accepted"),
+                 (free_stack, "free_stack"), (free_top, "free_top"), (status, "status")):
+        _check(t, n, 1, torch.int32)
+    B, MB = block_table.shape
+    st = lib().kv_commit_inplace(_ptr(block_table), _ptr(seq_lens), _ptr(num_accepted),
+                                 num_blocks, block_size, B, K, MB, _ptr(free_stack),
+                                 _ptr(free_top), _ptr(status), _stream(stream))
+    if st != SPEC_OK:
+        raise SpecError("kv_commit_inplace", st)
+
+
+def kv_evict_provisional(block_table, seq_lens, free_stack, free_top, status, *, K: int,
+                         block_size: int, num_blocks: int, stream=None) -> None:
+    """In-place layout: discard every row's K+1 provisional slots (preemption)."""
+    import torch
+    _check(block_table, "block_table", 2, torch.int32)
+    for t, n in ((seq_lens, "seq_lens"), (free_stack, "free_stack"), (free_top, "free_top"),
+                 (status, "status")):
+        _check(t, n, 1, torch.int32)
+    B, MB = block_table.shape
+    st = lib().kv_evict_provisional(_ptr(block_table), _ptr(seq_lens), num_blocks, block_size, B,
+                                    K, MB, _ptr(free_stack), _ptr(free_top), _ptr(status),
+                                    _stream(stream))
+    if st != SPEC_OK:
+        raise SpecError("kv_evict_provisional", st)
 
 
 def kv_commit_rollback(block_table, seq_lens, num_accepted, prov_blocks, kv_pool, free_stack,

@@ -118,4 +118,30 @@ int kv_commit_rollback(int32_t* block_table, int32_t* seq_lens, const int32_t* n
   return sv::launch_kv_commit(k);
 }
 
+static int kv_truncate(int32_t* block_table, int32_t* seq_lens, const int32_t* num_accepted,
+                       int num_blocks, int block_size, int B, int K, int max_blocks,
+                       int32_t* free_stack, int32_t* free_top, int32_t* status, void* stream) {
+  if (!block_table || !seq_lens || !free_stack || !free_top || !status) return SPEC_EINVAL;
+  if (num_blocks < 1 || block_size < 1 || B < 1 || K < 0 || K > 31 || max_blocks < 1)
+    return SPEC_EINVAL;
+  sv::KvTruncLaunch k{block_table, seq_lens, num_accepted, num_blocks, block_size, B, K,
+                      max_blocks, free_stack, free_top, status, stream};
+  return sv::launch_kv_truncate(k);
+}
+
+int kv_commit_inplace(int32_t* block_table, int32_t* seq_lens, const int32_t* num_accepted,
+                      int num_blocks, int block_size, int B, int K, int max_blocks,
+                      int32_t* free_stack, int32_t* free_top, int32_t* status, void* stream) {
+  if (!num_accepted) return SPEC_EINVAL;
+  return kv_truncate(block_table, seq_lens, num_accepted, num_blocks, block_size, B, K,
+                     max_blocks, free_stack, free_top, status, stream);
+}
+
+int kv_evict_provisional(int32_t* block_table, int32_t* seq_lens, int num_blocks,
+                         int block_size, int B, int K, int max_blocks, int32_t* free_stack,
+                         int32_t* free_top, int32_t* status, void* stream) {
+  return kv_truncate(block_table, seq_lens, nullptr, num_blocks, block_size, B, K, max_blocks,
+                     free_stack, free_top, status, stream);
+}
+
 }  // extern "C"

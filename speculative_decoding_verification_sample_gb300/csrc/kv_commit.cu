@@ -243,6 +243,98 @@ __global__ void __launch_bounds__(kCopyThreads) kv_copy_kernel(const KvArgs a) {
   if (threadIdx.x < a.P) a.pb[size_t(b) * a.P + threadIdx.x] = -1;
 }
 
+// ------------------------------------------------------------------ in place
+// The in-place variant ("Rolling back the KV cache": keep the physical cache
+// and truncate a logical length; the sglang_spec_decode README: evict a row's
+// provisional KV on preemption). The K+1 provisional slots already sit at
+// logical positions L..L+K of the row's own blocks; the new length is
+// L + n + 1 (commit) or L (evict), and every block holding no position below
+// it is pushed onto the free stack (rows ascending, block index ascending)
+// and cleared in the block table. No KV byte moves. One CTA, all-or-nothing.
+struct TruncArgs {
+  int32_t* bt;
+  int32_t* sl;
+  const int32_t* na;  // null: evict
+  int NB, bs, B, K, MB;
+  int32_t* fs;
+  int32_t* ftop;
+  int32_t* status;
+};
+
+// Validation of one row; returns error bits, the new length and the block
+// range [first, end) to free.
+__device__ int validate_trunc_row(const TruncArgs& a, int b, int& new_len, int& first, int& end) {
+  new_len = first = end = 0;
+  const int L = a.sl[b];
+  const int n = a.na ? a.na[b] : 0;
+  if (a.na && (n < 0 || n > a.K)) return SPEC_DERR_BAD_ACCEPT;
+  if (L < 0 || int64_t(L) + a.K + 1 > int64_t(a.MB) * a.bs) return SPEC_DERR_BAD_LENGTH;
+  end = cdiv(L + a.K + 1, a.bs);
+  int e = 0;
+  for (int j = L / a.bs; j < end; ++j) {
+    const int x = a.bt[size_t(b) * a.MB + j];
+    if (x < 0 || x >= a.NB) e |= SPEC_DERR_BAD_BLOCK;
+  }
+  new_len = a.na ? L + n + 1 : L;
+  first = cdiv(new_len, a.bs);
+  return e;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) kv_truncate_kernel(const TruncArgs a) {
+  __shared__ int sh[96];
+  __shared__ int s_err, s_push;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    s_err = 0;
+    s_push = 0;
+  }
+  __syncthreads();
+  int e = 0, push_sum = 0;
+  for (int b = tid; b < a.B; b += kPlanThreads) {
+    int nl, f, en;
+    e |= validate_trunc_row(a, b, nl, f, en);
+    push_sum += en - f;
+  }
+  atomicOr(&s_err, e);
+  atomicAdd(&s_push, push_sum);
+  __syncthreads();
+  const int top = *a.ftop;
+  int err = s_err;
+  if (err == 0 && (top < 0 || top + s_push > a.NB)) err |= SPEC_DERR_BAD_BLOCK;
+  if (err != 0) {
+    if (tid == 0) *a.status = err;
+    return;
+  }
+  int carry = 0;
+  for (int b0 = 0; b0 < a.B; b0 += kPlanThreads) {
+    const int b = b0 + tid;
+    int nl = 0, f = 0, en = 0;
+    if (b < a.B) validate_trunc_row(a, b, nl, f, en);
+    int chunk_total;
+    const int pre = block_excl_scan(en - f, sh, chunk_total) + carry;
+    if (b < a.B) {
+      for (int j = f; j < en; ++j) {
+        int32_t* slot = &a.bt[size_t(b) * a.MB + j];
+        a.fs[top + pre + (j - f)] = *slot;
+        *slot = -1;
+      }
+      a.sl[b] = nl;
+    }
+    carry += chunk_total;
+  }
+  if (tid == 0) {
+    *a.ftop = top + s_push;
+    *a.status = 0;
+  }
+}
+
+int launch_kv_truncate(const KvTruncLaunch& k) {
+  TruncArgs a{k.block_table, k.seq_lens, k.num_accepted, k.num_blocks, k.block_size, k.B, k.K,
+              k.max_blocks, k.free_stack, k.free_top, k.status};
+  kv_truncate_kernel<<<1, kPlanThreads, 0, static_cast<cudaStream_t>(k.stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
 int launch_kv_commit(const KvLaunch& k) {
   KvArgs a;
   a.bt = k.block_table;

@@ -55,11 +55,23 @@ struct KvLaunch {
   void* stream;
 };
 
+struct KvTruncLaunch {
+  int32_t* block_table;
+  int32_t* seq_lens;
+  const int32_t* num_accepted;  // null: evict the provisional slots
+  int num_blocks, block_size, B, K, max_blocks;
+  int32_t* free_stack;
+  int32_t* free_top;
+  int32_t* status;
+  void* stream;
+};
+
 int launch_verify_sample(const SampleLaunch& s);
 size_t sample_workspace_bytes(int B, int K, int V, int dtype);
 size_t greedy_workspace_bytes(int B, int K, int V, int dtype);
 int launch_verify_greedy(const GreedyLaunch& g);
 int launch_kv_commit(const KvLaunch& k);
+int launch_kv_truncate(const KvTruncLaunch& k);
 int verify_cluster_size(int B, int V, int dtype);
 
 }  // namespace sv
