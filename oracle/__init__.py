@@ -40,6 +40,10 @@ from .verify import (  # noqa: F401
     inverse_cdf,
     verify_sample,
     verify_greedy,
+    verify_tree_greedy,
+    tree_survivors,
+    tree_kept_node,
+    tree_path,
     verify_step,
     acceptance_counters,
 )

@@ -14,6 +14,12 @@ cache, new blocks are taken from the top of the free stack (rows in ascending
 order, all pops before any push), then every provisional block is pushed back
 in row order and the row's length becomes seq_len + n + 1.
 
+With a slot map (tree drafts: "Grading every branch in one pass" keeps one
+root-to-node path of the flattened tree, whose nodes need not sit in
+consecutive provisional slots), kept position s = 0..n takes its KV from
+provisional slot slot_map[b, s] instead of slot s; the identity map is the
+linear case.
+
 The whole call is all-or-nothing: if any row is invalid, or the free stack
 cannot cover every row, nothing changes and error bits are returned.
 """
@@ -26,6 +32,7 @@ ERR_BAD_ACCEPT = 1 << 2     # num_accepted outside [0, K]
 ERR_BAD_LENGTH = 1 << 3     # negative seq_len, or the row outgrows its block table
 ERR_NO_SPACE = 1 << 4       # the free stack cannot supply every new block
 ERR_BAD_BLOCK = 1 << 5      # a block id outside [0, num_blocks) where one is needed
+ERR_BAD_SLOT = 1 << 7       # a slot_map entry outside [0, K] for a kept position
 
 
 def _cdiv(a: int, b: int) -> int:
@@ -33,11 +40,12 @@ def _cdiv(a: int, b: int) -> int:
 
 
 def kv_commit(block_table, seq_lens, num_accepted, prov_blocks, free_stack, free_top: int,
-              *, block_size: int, K: int, num_blocks: int) -> dict:
+              *, block_size: int, K: int, num_blocks: int, slot_map=None) -> dict:
     """One commit/rollback of every row. Returns the new state, the copy list and error bits.
 
-    copies: list of (row, slot, src_block, src_offset, dst_block, dst_offset); each
-    entry moves one token's KV (all layers, K and V) from provisional slot `slot`.
+    copies: list of (row, s, src_block, src_offset, dst_block, dst_offset); each
+    entry moves one token's KV (all layers, K and V) into kept position s, from
+    provisional slot slot_map[row, s] (slot s without a map).
     """
     bt = np.array(block_table, np.int64, copy=True)
     sl = np.array(seq_lens, np.int64, copy=True)
@@ -48,6 +56,10 @@ def kv_commit(block_table, seq_lens, num_accepted, prov_blocks, free_stack, free
     B, max_blocks = bt.shape
     P = pb.shape[1]
     err = 0
+    if slot_map is None:
+        sm = np.tile(np.arange(K + 1, dtype=np.int64), (B, 1))
+    else:
+        sm = np.asarray(slot_map, np.int64).reshape(B, K + 1)
 
     def ok_block(x):
         return 0 <= x < num_blocks
@@ -78,8 +90,10 @@ def kv_commit(block_table, seq_lens, num_accepted, prov_blocks, free_stack, free
                     err |= ERR_BAD_BLOCK        # the partly filled tail block
             elif x != -1:
                 err |= ERR_BAD_BLOCK            # a slot the commit must fill is already taken
-        if n // block_size >= P or not all(ok_block(int(pb[b, k]))
-                                           for k in range(n // block_size + 1)):
+        kept = [int(sm[b, s]) for s in range(n + 1)]   # provisional slots kept
+        if any(not 0 <= x <= K for x in kept):
+            err |= ERR_BAD_SLOT
+        elif any(x // block_size >= P or not ok_block(int(pb[b, x // block_size])) for x in kept):
             err |= ERR_BAD_BLOCK
         need[b] = total - have
     need_total = int(need.sum())
@@ -108,7 +122,8 @@ def kv_commit(block_table, seq_lens, num_accepted, prov_blocks, free_stack, free
     for b in range(B):
         L, n = int(sl[b]), int(na[b])
         for s in range(n + 1):
-            src_b, src_o = int(pb[b, s // block_size]), s % block_size
+            x = int(sm[b, s])
+            src_b, src_o = int(pb[b, x // block_size]), x % block_size
             p = L + s
             dst_b, dst_o = int(bt[b, p // block_size]), p % block_size
             copies.append((b, s, src_b, src_o, dst_b, dst_o))

@@ -188,6 +188,97 @@ def verify_greedy(target, tokens) -> dict:
     return dict(out_tokens=out, num_accepted=n, argmax=g)
 
 
+def tree_survivors(g, bad_row, par, tok):
+    """Survival and depth of every node of one tree, parents first.
+
+    Node i is consistent when its token equals g of its parent's row (row
+    p + 1, row 0 for a root child) and that row is usable; it survives when it
+    and every ancestor are consistent. Depth 1 for a root child.
+    """
+    N = len(par)
+    alive = np.zeros(N, bool)
+    depth = np.zeros(N, np.int64)
+    for i in range(N):
+        p = int(par[i])
+        up_ok = p < 0 or alive[p]
+        alive[i] = up_ok and not bad_row[p + 1] and tok[i] == g[p + 1]
+        depth[i] = 1 if p < 0 else depth[p] + 1
+    return alive, depth
+
+
+def tree_kept_node(alive, depth) -> int:
+    """End of the kept path: the deepest survivor, lowest index among equally
+    deep ones; -1 when nothing survives."""
+    best = -1
+    for i in range(len(alive)):
+        if alive[i] and (best < 0 or depth[i] > depth[best]):
+            best = i
+    return best
+
+
+def tree_path(par, node) -> list:
+    """Nodes from the root's child down to `node` (empty for -1)."""
+    path = []
+    while node >= 0:
+        path.append(node)
+        node = int(par[node])
+    return path[::-1]
+
+
+def verify_tree_greedy(target, parents, tokens) -> dict:
+    """Greedy verification of a draft tree, one verifier pass over all nodes.
+
+    Sources: "Grading every branch in one pass" (the page on acceptance rate
+    and serving thresholds): the drafter's branches are flattened into one
+    sequence under an ancestor-only mask, the target grades every node in one
+    forward pass, and the longest surviving path is kept; the lesson's
+    "EAGLE-2" entry and its tree exercise (a [2, 2, 2] tree, one verifier
+    run, the surviving path wins); "devpost.com - phoenix", "What it does"
+    for the greedy acceptance of one token.
+
+    Layout (reading): N nodes in topological order, parents[b, i] in
+    [-1, i) (-1: a child of the last committed token); target row 0 is the
+    distribution after the committed prefix and row 1 + i the one after
+    node i. Node i is consistent when its token equals the argmax of its
+    parent's row (row 0 for the root's children); it survives when it and all
+    its ancestors are consistent. The kept path ends at the deepest survivor,
+    the lowest node index among equally deep ones (depth 0: no survivor), and
+    the step emits the path's tokens and then the argmax of the last kept
+    node's row. slots[p] is the provisional KV slot of kept position p: 0 for
+    the last committed token, 1 + node for the node at depth p.
+
+    An invalid tree or token, or a NaN / all -inf row whose argmax the result
+    uses (row 0 and the rows of survivors), makes the row an error: outputs
+    -1 and num_accepted -1.
+    """
+    target = np.asarray(target, np.float64)
+    parents = np.asarray(parents, np.int64)
+    tokens = np.asarray(tokens, np.int64)
+    B, N1, V = target.shape
+    N = N1 - 1
+    out = np.full((B, N1), -1, np.int64)
+    slots = np.full((B, N1), -1, np.int64)
+    n_out = np.full(B, -1, np.int64)
+    for b in range(B):
+        rows = target[b]
+        bad_row = np.isnan(rows).any(axis=1) | np.all(rows == -np.inf, axis=1)
+        g = np.argmax(np.where(np.isnan(rows), -np.inf, rows), axis=1)
+        par, tok = parents[b], tokens[b]
+        if any(not (0 <= tok[i] < V and -1 <= par[i] < i) for i in range(N)):
+            continue
+        alive, depth = tree_survivors(g, bad_row, par, tok)
+        if bad_row[0] or any(alive[i] and bad_row[i + 1] for i in range(N)):
+            continue
+        path = tree_path(par, tree_kept_node(alive, depth))
+        n = len(path)
+        out[b, :n] = tok[path]
+        out[b, n] = g[0] if n == 0 else g[path[-1] + 1]
+        slots[b, 0] = 0
+        slots[b, 1:n + 1] = np.asarray(path, np.int64) + 1
+        n_out[b] = n
+    return dict(out_tokens=out, num_accepted=n_out, slots=slots)
+
+
 def verify_step(target, draft, tokens, uniforms, temperature, **kw) -> dict:
     """T == 0 selects greedy mode (the pages list temperature 0.0 as greedy)."""
     if temperature64(temperature) == 0.0:

@@ -181,6 +181,108 @@ def greedy_case(B: int, K: int, V: int, *, alpha: float, target_std: float = 3.0
 
 
 # --------------------------------------------------------------------------
+# draft trees
+# --------------------------------------------------------------------------
+@dataclass
+class TreeCase:
+    """One batch of greedy tree-verification inputs.
+
+    target [B, N+1, V] (row 0: after the committed prefix, row 1 + i: after
+    node i), parents [B, N] int32 (topological order, -1 = root child),
+    tokens [B, N] int32.
+    """
+
+    target: np.ndarray
+    parents: np.ndarray
+    tokens: np.ndarray
+    dtype: str
+    recipe: dict = field(default_factory=dict)
+
+    @property
+    def B(self) -> int:
+        return self.target.shape[0]
+
+    @property
+    def N(self) -> int:
+        return self.parents.shape[1]
+
+    @property
+    def V(self) -> int:
+        return self.target.shape[2]
+
+    def target_values(self) -> np.ndarray:
+        return logits_values(self.target, self.dtype)
+
+
+def tree_parents(branching) -> np.ndarray:
+    """Parents of a full tree in breadth-first order: `branching[d]` children
+    per node at depth d (the lesson's exercise uses [2, 2, 2]: 14 nodes)."""
+    par, level = [], [-1]
+    for k in branching:
+        nxt = []
+        for p in level:
+            for _ in range(int(k)):
+                nxt.append(len(par))
+                par.append(p)
+        level = nxt
+    return np.asarray(par, np.int32)
+
+
+def random_parents(rng: np.random.Generator, N: int) -> np.ndarray:
+    """A random tree in topological order: parent of node i uniform in [-1, i)."""
+    return np.asarray([rng.integers(-1, i) for i in range(N)], np.int32)
+
+
+def tree_case(B: int, V: int, *, branching=(2, 2, 2), N: int | None = None, alpha: float = 0.7,
+              target_std: float = 3.0, distinct: bool = True, dtype: str = BF16,
+              seed: int = 0) -> TreeCase:
+    """Greedy tree workload with planted argmaxes.
+
+    Shape: the full tree `branching` (same for every row), or, with N given,
+    a random topological tree per row. Every target row gets one planted
+    maximum g (as in greedy_case). Each sibling group (the children of one
+    row) carries g of that row with probability alpha at a random child;
+    the other children take tokens other than g. distinct=True keeps sibling
+    tokens distinct (a top-k proposal); False draws them independently, so
+    duplicate siblings occur.
+    """
+    rng = _rng(seed)
+    if N is None:
+        par = np.tile(tree_parents(branching), (B, 1))
+    else:
+        par = np.stack([random_parents(rng, N) for _ in range(B)]) if N else np.zeros((B, 0), np.int32)
+    N = par.shape[1]
+    z = np.clip(rng.normal(0.0, target_std, size=(B, N + 1, V)), -CLIP, CLIP).astype(np.float32)
+    g = rng.integers(0, V, size=(B, N + 1))
+    bi, pi = np.meshgrid(np.arange(B), np.arange(N + 1), indexing="ij")
+    z[bi, pi, g] = PLANT_VALUE
+    tok = np.empty((B, N), np.int32)
+    for b in range(B):
+        for r in range(N + 1):                       # sibling group under row r
+            kids = [i for i in range(N) if par[b, i] == r - 1]
+            if not kids:
+                continue
+            if distinct:
+                pool = (g[b, r] + 1 + rng.permutation(V - 1)[:len(kids)]) % V
+            else:
+                pool = (g[b, r] + 1 + rng.integers(0, V - 1, size=len(kids))) % V
+            for j, i in enumerate(kids):
+                tok[b, i] = pool[j]
+            if distinct:
+                if rng.random() < alpha:
+                    tok[b, kids[rng.integers(0, len(kids))]] = g[b, r]
+            else:
+                hit = rng.random(len(kids)) < alpha
+                for j, i in enumerate(kids):
+                    if hit[j]:
+                        tok[b, i] = g[b, r]
+    return TreeCase(_store(z, dtype), par.astype(np.int32), tok, dtype,
+                    dict(kind="tree_greedy", B=B, V=V, N=N, branching=list(branching) if N is None
+                         else None, alpha=alpha, distinct=distinct, target_std=target_std,
+                         dtype=dtype, seed=seed, planted=g.astype(np.int32)))
+
+
+# --------------------------------------------------------------------------
 # paged KV cache state
 # --------------------------------------------------------------------------
 @dataclass

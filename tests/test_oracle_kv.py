@@ -149,3 +149,63 @@ def test_errors_leave_state_unchanged(mutate, bit):
     assert np.array_equal(res["seq_lens"], c.seq_lens)
     assert np.array_equal(res["prov_blocks"], c.prov_blocks)
     assert res["free_top"] == c.free_top
+
+
+# ------------------------------------------------------------- tree slot maps
+def test_identity_slot_map_is_the_linear_commit():
+    c = synth.kv_case(6, 5, block_size=4, seed=9)
+    ident = np.tile(np.arange(6, dtype=np.int32), (6, 1))
+    a = _commit(c)
+    b = oracle.kv_commit(c.block_table, c.seq_lens, c.num_accepted, c.prov_blocks, c.free_stack,
+                         c.free_top, block_size=c.block_size, K=c.K, num_blocks=c.num_blocks,
+                         slot_map=ident)
+    for k in ("block_table", "seq_lens", "prov_blocks", "free_stack"):
+        assert np.array_equal(a[k], b[k])
+    assert a["free_top"] == b["free_top"] and a["copies"] == b["copies"] and b["err"] == 0
+
+
+@pytest.mark.parametrize("bs", [4, 16])
+@pytest.mark.parametrize("branching", [(2, 2, 2), (3, 2)])
+def test_tree_commit_keeps_the_surviving_path(bs, branching):
+    """Greedy tree verification, then the commit with its slot map: each row's
+    sequence becomes prefix + the KV of the last committed token + the KV of
+    the kept nodes, in path order (brute-force slot labels)."""
+    t = synth.tree_case(10, 50, branching=branching, alpha=0.9, seed=bs, dtype=synth.F32)
+    r = oracle.verify_tree_greedy(t.target_values(), t.parents, t.tokens)
+    N = t.N
+    c = synth.kv_case(t.B, N, block_size=bs, prefix_lo=0, prefix_hi=3 * bs,
+                      num_accepted=r["num_accepted"].astype(np.int32), seed=bs + N)
+    slot_map = np.where(r["slots"] < 0, 0, r["slots"]).astype(np.int32)
+    res = oracle.kv_commit(c.block_table, c.seq_lens, c.num_accepted, c.prov_blocks, c.free_stack,
+                           c.free_top, block_size=bs, K=N, num_blocks=c.num_blocks,
+                           slot_map=slot_map)
+    assert res["err"] == 0
+    seqs = _apply_and_read(c, res)
+    assert any(int(n) >= 2 for n in r["num_accepted"])
+    for b in range(c.B):
+        L, n = int(c.seq_lens[b]), int(r["num_accepted"][b])
+        kept = [0] + [1 + int(x) for x in oracle.tree_path(
+            t.parents[b], int(r["slots"][b, n]) - 1 if n else -1)]
+        assert kept == r["slots"][b, :n + 1].tolist()
+        assert seqs[b] == [("prefix", b, p) for p in range(L)] + [("prov", b, s) for s in kept]
+    assert oracle.pool_invariant_ok(res["block_table"], res["prov_blocks"], res["free_stack"],
+                                    res["free_top"], c.num_blocks)
+
+
+@pytest.mark.parametrize("bad", [-1, 5])
+def test_bad_slot_map_entry_leaves_state_unchanged(bad):
+    c = synth.kv_case(3, 4, seq_lens=np.array([5, 9, 16]), num_accepted=np.array([2, 4, 0]),
+                      seed=5)
+    sm = np.tile(np.arange(5, dtype=np.int32), (3, 1))
+    sm[0, 4] = bad                      # beyond row 0's kept positions: ignored
+    ok = oracle.kv_commit(c.block_table, c.seq_lens, c.num_accepted, c.prov_blocks, c.free_stack,
+                          c.free_top, block_size=c.block_size, K=4, num_blocks=c.num_blocks,
+                          slot_map=sm)
+    assert ok["err"] == 0
+    sm[1, 3] = bad                      # a kept position of row 1
+    res = oracle.kv_commit(c.block_table, c.seq_lens, c.num_accepted, c.prov_blocks, c.free_stack,
+                           c.free_top, block_size=c.block_size, K=4, num_blocks=c.num_blocks,
+                           slot_map=sm)
+    assert res["err"] == okv.ERR_BAD_SLOT
+    assert np.array_equal(res["block_table"], c.block_table) and res["copies"] == []
+    assert np.array_equal(res["seq_lens"], c.seq_lens) and res["free_top"] == c.free_top

@@ -134,3 +134,64 @@ def test_kv_push_before_pop_is_caught(monkeypatch):
 
     monkeypatch.setattr(oracle, "kv_commit", wrong)
     assert _fails(tk.test_two_sequences_exercise) or _fails(tk.test_every_rejection_pattern, 4, 16)
+
+
+# ---------------------------------------------------------------- draft trees
+from tests import test_oracle_tree as tt  # noqa: E402
+
+
+def _tree_pins_fail():
+    failed = False
+    for case in tt._fixture()["cases"]:
+        failed |= _fails(tt.test_hand_tree_cases, case)
+    for distinct in (True, False):
+        failed |= _fails(tt.test_brute_force_random_trees, 0, distinct)
+    return failed
+
+
+def test_tree_own_row_instead_of_parent_row_is_caught(monkeypatch):
+    def wrong(g, bad_row, par, tok):
+        N = len(par)
+        alive = np.zeros(N, bool)
+        depth = np.zeros(N, np.int64)
+        for i in range(N):
+            p = int(par[i])
+            alive[i] = (p < 0 or alive[p]) and tok[i] == g[i + 1]   # the node's own row
+            depth[i] = 1 if p < 0 else depth[p] + 1
+        return alive, depth
+    monkeypatch.setattr(ov, "tree_survivors", wrong)
+    assert _tree_pins_fail()
+
+
+def test_tree_first_survivor_instead_of_longest_is_caught(monkeypatch):
+    def wrong(alive, depth):
+        # the lowest-index survivor, not the end of the longest surviving path
+        hits = np.flatnonzero(alive)
+        return int(hits[0]) if hits.size else -1
+    monkeypatch.setattr(ov, "tree_kept_node", wrong)
+    assert _tree_pins_fail()
+
+
+def test_tree_ancestor_not_required_is_caught(monkeypatch):
+    def wrong(g, bad_row, par, tok):
+        N = len(par)
+        alive = np.zeros(N, bool)
+        depth = np.zeros(N, np.int64)
+        for i in range(N):
+            p = int(par[i])
+            alive[i] = tok[i] == g[p + 1]                           # parent's survival dropped
+            depth[i] = 1 if p < 0 else depth[p] + 1
+        return alive, depth
+    monkeypatch.setattr(ov, "tree_survivors", wrong)
+    assert _tree_pins_fail()
+
+
+def test_tree_highest_index_among_equals_is_caught(monkeypatch):
+    def wrong(alive, depth):
+        best = -1
+        for i in range(len(alive)):
+            if alive[i] and (best < 0 or depth[i] >= depth[best]):
+                best = i
+        return best
+    monkeypatch.setattr(ov, "tree_kept_node", wrong)
+    assert _fails(tt.test_hand_tree_cases, tt._fixture()["cases"][2])
