@@ -247,9 +247,10 @@ def verify_tree_greedy(target, parents, tokens) -> dict:
     node's row. slots[p] is the provisional KV slot of kept position p: 0 for
     the last committed token, 1 + node for the node at depth p.
 
-    An invalid tree or token, or a NaN / all -inf row whose argmax the result
+    An invalid tree or token, or a row with a NaN whose argmax the result
     uses (row 0 and the rows of survivors), makes the row an error: outputs
-    -1 and num_accepted -1.
+    -1 and num_accepted -1. As in verify_greedy, a row of equal values (all
+    -inf included) has argmax 0 by the lowest-index rule.
     """
     target = np.asarray(target, np.float64)
     parents = np.asarray(parents, np.int64)
@@ -261,8 +262,8 @@ def verify_tree_greedy(target, parents, tokens) -> dict:
     n_out = np.full(B, -1, np.int64)
     for b in range(B):
         rows = target[b]
-        bad_row = np.isnan(rows).any(axis=1) | np.all(rows == -np.inf, axis=1)
-        g = np.argmax(np.where(np.isnan(rows), -np.inf, rows), axis=1)
+        bad_row = np.isnan(rows).any(axis=1)
+        g = np.argmax(np.where(bad_row[:, None], 0.0, rows), axis=1)
         par, tok = parents[b], tokens[b]
         if any(not (0 <= tok[i] < V and -1 <= par[i] < i) for i in range(N)):
             continue

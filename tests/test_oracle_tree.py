@@ -152,8 +152,9 @@ def test_nan_rows_only_matter_when_used():
         zn[0, row, 7] = np.nan
         assert int(oracle.verify_tree_greedy(zn, [par], [tok])["num_accepted"][0]) == -1
     zi = z.copy()
-    zi[0, 1, :] = -np.inf                 # all -inf row of a survivor
-    assert int(oracle.verify_tree_greedy(zi, [par], [tok])["num_accepted"][0]) == -1
+    zi[0, 1, :] = -np.inf                 # all equal: argmax 0 by the lowest-index rule
+    r = oracle.verify_tree_greedy(zi, [par], [tok])
+    assert int(r["num_accepted"][0]) == 1 and r["out_tokens"][0].tolist() == [3, 0, -1, -1]
 
 
 def test_empty_tree():
