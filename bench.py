@@ -149,6 +149,59 @@ def inplace_kv_us(torch, sv, na, reps=200):
     return 1e3 * statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
 
 
+def tree_greedy_stats(torch, sv, peak, reps=50):
+    """spec_verify_tree_greedy on the lesson's [2, 2, 2] draft tree (14 nodes, 15
+    target rows per batch row) at B=256, V=151936 bf16: mean device time of one
+    launch, its algorithmic HBM bytes (every target row read once) and the
+    fraction of the measured copy peak. Planted argmaxes (target ~ N(0, 3^2)
+    clipped, one logit per row raised to 16); each sibling group carries its
+    row's argmax with probability 0.8. One 1.17 GB input (> L2)."""
+    import numpy as np
+    import synth
+    w = WORKLOAD
+    B, V = w["B"], w["V"]
+    par = synth.tree_parents((2, 2, 2))
+    N = len(par)
+    rng = np.random.default_rng(46)
+    g = rng.integers(0, V, size=(B, N + 1))
+    tok = (g[:, par + 1] + 1 + rng.integers(0, V - 1, size=(B, N))) % V
+    for r in range(N + 1):
+        kids = np.flatnonzero(par == r - 1)
+        if kids.size == 0:
+            continue
+        hit = rng.random(B) < 0.8
+        pick = kids[rng.integers(0, kids.size, size=B)]
+        tok[hit, pick[hit]] = g[hit, r]
+    gen = torch.Generator(device="cuda").manual_seed(46)
+    z = (torch.randn((B, N + 1, V), device="cuda", generator=gen) * w["target_std"]).clamp_(
+        -synth.CLIP, synth.CLIP)
+    gt = torch.from_numpy(g).cuda()
+    z.scatter_(2, gt.unsqueeze(-1), synth.PLANT_VALUE)
+    target = z.to(torch.bfloat16).contiguous()
+    del z
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x, np.int32)).cuda()  # noqa: E731
+    pt, tt = dev(np.tile(par, (B, 1))), dev(tok)
+    out = torch.empty((B, N + 1), dtype=torch.int32, device="cuda")
+    n = torch.empty((B,), dtype=torch.int32, device="cuda")
+    slots = torch.empty((B, N + 1), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for i in range(reps + 3):
+        if i >= 3:
+            evs[i - 3][0].record(stream)
+        sv.spec_verify_tree_greedy(target, pt, tt, out, n, out_slots=slots)
+        if i >= 3:
+            evs[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    us = 1e3 * statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    alg = B * (N + 1) * V * 2 + B * N * 8
+    gbs = alg / (us / 1e6) / 1e9
+    return {"tree": "[2, 2, 2] (14 nodes)", "us": us, "algorithmic_bytes": alg, "gbs": gbs,
+            "frac_of_measured_peak": gbs / peak,
+            "mean_accepted": float(n.float().mean().item())}
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -442,6 +495,8 @@ def main():
             "extra": {"verify_ms": v_ms, "kv_commit_and_table_restore_ms": ms_per_step - v_ms,
                       "kv_commit_inplace_us": (inplace_kv_us(torch, sv, na_list[0][0])
                                                if a.mode == "step" else None),
+                      "tree_greedy": (tree_greedy_stats(torch, sv, peak)
+                                      if a.mode == "step" else None),
                       "kv_bytes_per_step": kvb, "refined_row_fraction": refined,
                       "mean_accepted": float(np.mean([x[0].mean() for x in na_list])),
                       "hbm_frac_of_nominal_8TBs": achieved / 8000.0},

@@ -6,6 +6,7 @@
  *     the accept/reject test of each draft token, the first rejection, and the
  *     correction (residual) or bonus draw;
  *   - spec_verify_greedy: the argmax-match variant;
+ *   - spec_verify_tree_greedy: greedy verification of a draft tree;
  *   - kv_commit_rollback: commit of the accepted provisional KV slots into a
  *     paged cache and release of the provisional blocks.
  *
@@ -24,6 +25,10 @@
  *       there; output identical to the target alone.
  *   [S] "sglang_spec_decode" README, provisional KV layer: provisional blocks
  *       are committed or freed immediately; no block leaked or freed twice.
+ *   [G] the page on acceptance rate and serving thresholds, "Grading every
+ *       branch in one pass": draft branches flattened under an ancestor-only
+ *       mask, graded in one target pass, the longest surviving path kept; [L]
+ *       "EAGLE-2" (dynamic draft tree) and its [2, 2, 2] tree exercise.
  *
  * Notation: q = target (verifier) distribution, p = draft distribution.
  * Positions are 0-based: draft positions 0..K-1, bonus row K.
@@ -77,6 +82,7 @@ extern "C" {
 #define SPEC_DERR_NO_SPACE 16    /* kv: the free stack cannot supply every new block */
 #define SPEC_DERR_BAD_BLOCK 32   /* kv: a block id out of range, or a target slot already taken */
 #define SPEC_DERR_TIMEOUT 64     /* an internal bounded wait gave up (should never happen) */
+#define SPEC_DERR_BAD_SLOT 128   /* kv: a slot_map entry of a kept position outside [0, K] */
 
 /* ---- per-row diagnostic bits written to row_info[b] (optional) ---- */
 #define SPEC_ROW_ACCEPT_REFINED 1 /* an accept test fell inside the fp32 error bound and was
@@ -148,6 +154,41 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
                        uint64_t* accept_counters);
 
 /*
+ * spec_verify_tree_greedy - greedy verification of a draft tree ([G]; [P] for
+ * the greedy acceptance of one token).
+ *
+ *   target_logits [B, N+1, V] dtype: row 0 is the target after the committed
+ *                 prefix, row 1 + i the target after draft node i (the target
+ *                 ran once over the flattened tree with an ancestor-only mask).
+ *   tree_parents  [B, N] int32: parent of node i, in [-1, i) (-1: a child of
+ *                 the last committed token); nodes are in topological order.
+ *   tree_tokens   [B, N] int32 in [0, V): the token of each node.
+ *   1 <= N <= 31.
+ *   g_r = argmax of row r (raw logits, ties to the lowest index). Node i is
+ *   consistent when tree_tokens[i] == g of its parent's row (row parent + 1);
+ *   it survives when it and all its ancestors are consistent. The kept path
+ *   ends at the deepest survivor (the lowest node index among equally deep
+ *   ones; none: empty path). With n = the path's length:
+ *   out_tokens       [B, N+1] int32: the path's tokens, then g of its last
+ *                    node's row (g_0 for an empty path), then -1;
+ *   out_num_accepted [B] int32: n;
+ *   out_slots        optional [B, N+1] int32: provisional KV slot of each kept
+ *                    position, 0 (the last committed token) then 1 + node for
+ *                    the path's nodes, then -1 (the slot_map of
+ *                    kv_commit_rollback with K = N).
+ *   With distinct sibling tokens the output equals target-only greedy decoding.
+ *   An invalid parent or token sets SPEC_DERR_TOKEN; a NaN in row 0 or in the
+ *   row of a surviving node sets SPEC_DERR_LOGITS; such a row's outputs are -1.
+ *   Workspace: spec_verify_workspace_bytes(B, N, V, dtype). Other conventions
+ *   as spec_verify_greedy.
+ */
+int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_parents,
+                            const int32_t* tree_tokens, int B, int N, int V, int32_t* out_tokens,
+                            int32_t* out_num_accepted, int32_t* out_slots, void* stream,
+                            int dtype, int32_t* err_flag, void* workspace,
+                            size_t workspace_bytes);
+
+/*
  * spec_verify_greedy_noalloc - spec_verify_greedy without a caller workspace.
  * The pages have no counterpart: this is a deployment variant for callers
  * that cannot hand the library a device allocation of their own, e.g. code
@@ -176,8 +217,9 @@ size_t spec_verify_greedy_noalloc_max_bytes(void);
 
 /*
  * spec_verify_workspace_bytes - size of the device workspace that
- * spec_verify_sample and spec_verify_greedy need for (B, K, V, dtype); 0 for
- * arguments those calls would reject. One workspace serves both calls.
+ * spec_verify_sample and spec_verify_greedy need for (B, K, V, dtype), and
+ * spec_verify_tree_greedy for K = N; 0 for arguments those calls would reject.
+ * One workspace serves all three calls.
  */
 size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype);
 
@@ -198,6 +240,10 @@ size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype);
  *                live entries free_stack[0 .. *free_top)
  *   status       REQUIRED [1] int32, overwritten on the device with 0 when the call
  *                committed, else with the SPEC_DERR_* bits that stopped it
+ *   slot_map     optional [B, K+1] int32: kept position s takes the provisional
+ *                slot slot_map[b][s] (entries s <= n must lie in [0, K], else
+ *                SPEC_DERR_BAD_SLOT); null means slot s (the linear draft). A tree
+ *                draft ([G]) passes the out_slots of spec_verify_tree_greedy.
  *   K            0 <= K <= 31; P (provisional blocks per row) in [1, 512];
  *                num_kv_heads * head_dim * kv_elem_bytes a multiple of 16, kv_pool
  *                16-byte aligned
@@ -210,7 +256,7 @@ size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype);
  * stack is short, nothing changes and *status receives the error bits. Validation
  * checks, per row: n in [0, K]; L >= 0 and ceil((L+n+1)/bs) <= max_blocks; the
  * partly filled tail block (index L/bs when L % bs != 0) is a valid id; the
- * entries the commit fills are -1; the provisional blocks of slots 0..n are valid
+ * entries the commit fills are -1; the provisional blocks of the kept slots are valid
  * and every provisional id >= 0 is < num_blocks. Globally: 0 <= *free_top <=
  * num_blocks and covers the new blocks, the popped ids are valid, and the pushes fit.
  * Only the accepted bytes move. Blocks freed by the call must not be reused until
@@ -220,7 +266,7 @@ int kv_commit_rollback(int32_t* block_table, int32_t* seq_lens, const int32_t* n
                        int32_t* prov_blocks, void* kv_pool, int num_blocks, int num_layers,
                        int num_kv_heads, int head_dim, int kv_elem_bytes, int block_size, int B,
                        int K, int max_blocks, int P, int32_t* free_stack, int32_t* free_top,
-                       int32_t* status, void* stream);
+                       int32_t* status, void* stream, const int32_t* slot_map);
 
 /*
  * kv_commit_inplace - commit for the in-place KV layout ([L] "Rolling back the KV

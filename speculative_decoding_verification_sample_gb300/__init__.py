@@ -8,6 +8,7 @@ CPU fallback: without the built library (or without a GPU) these calls raise.
 The entry points carry the C names:
   spec_verify_sample(...)   accept/reject with temperature softmax, residual or bonus draw
   spec_verify_greedy(...)   argmax-match verification
+  spec_verify_tree_greedy(...)  argmax-match verification of a draft tree
   kv_commit_rollback(...)   commit accepted provisional KV slots, free provisional blocks
 See include/specverify.h for layouts, ownership and error behaviour.
 """
@@ -24,13 +25,14 @@ SPEC_BF16, SPEC_F32 = 0, 1
 SPEC_DERR_TOKEN, SPEC_DERR_LOGITS = 1, 2
 SPEC_DERR_BAD_ACCEPT, SPEC_DERR_BAD_LENGTH, SPEC_DERR_NO_SPACE, SPEC_DERR_BAD_BLOCK = 4, 8, 16, 32
 SPEC_DERR_TIMEOUT = 64
+SPEC_DERR_BAD_SLOT = 128
 SPEC_ROW_ACCEPT_REFINED, SPEC_ROW_SAMPLE_REFINED = 1, 2
 SPEC_ROW_UNCERTIFIED, SPEC_ROW_ZERO_RESIDUAL = 4, 8
 
 EXPORTED = ("spec_verify_sample", "spec_verify_greedy", "spec_verify_workspace_bytes",
             "kv_commit_rollback", "spec_selftest_ex2", "spec_status_string", "spec_version",
             "spec_verify_greedy_noalloc", "spec_verify_greedy_noalloc_max_bytes",
-            "kv_commit_inplace", "kv_evict_provisional")
+            "kv_commit_inplace", "kv_evict_provisional", "spec_verify_tree_greedy")
 
 _lib = None
 
@@ -58,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.spec_verify_sample.restype = I
         L.spec_verify_greedy.argtypes = [P, P, I, I, I, P, P, P, I, P, P, Z, P]
         L.spec_verify_greedy.restype = I
+        L.spec_verify_tree_greedy.argtypes = [P, P, P, I, I, I, P, P, P, P, I, P, P, Z]
+        L.spec_verify_tree_greedy.restype = I
         L.spec_verify_greedy_noalloc.argtypes = [P, P, I, I, I, P, P, P, I, P]
         L.spec_verify_greedy_noalloc.restype = I
         L.kv_commit_inplace.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P]
@@ -68,7 +72,8 @@ def lib() -> ctypes.CDLL:
         L.spec_verify_greedy_noalloc_max_bytes.restype = Z
         L.spec_verify_workspace_bytes.argtypes = [I, I, I, I]
         L.spec_verify_workspace_bytes.restype = Z
-        L.kv_commit_rollback.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P, P, P, P]
+        L.kv_commit_rollback.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P, P, P, P,
+                                         P]
         L.kv_commit_rollback.restype = I
         L.spec_selftest_ex2.argtypes = [F, F, P, P]
         L.spec_selftest_ex2.restype = I
@@ -206,6 +211,30 @@ def spec_verify_greedy(target_logits, draft_tokens, out_tokens, out_num_accepted
         raise SpecError("spec_verify_greedy", st)
 
 
+def spec_verify_tree_greedy(target_logits, tree_parents, tree_tokens, out_tokens,
+                            out_num_accepted, *, out_slots=None, stream=None, err_flag=None,
+                            workspace=None) -> None:
+    """Greedy verification of a draft tree; target [B,N+1,V], parents and tokens [B,N]
+    -> tokens [B,N+1], accepted [B], optional KV slots [B,N+1]."""
+    import torch
+    _check(target_logits, "target_logits", 3)
+    _check(tree_parents, "tree_parents", 2, torch.int32)
+    _check(tree_tokens, "tree_tokens", 2, torch.int32)
+    _check(out_tokens, "out_tokens", 2, torch.int32)
+    _check(out_num_accepted, "out_num_accepted", 1, torch.int32)
+    if out_slots is not None:
+        _check(out_slots, "out_slots", 2, torch.int32)
+    B, N1, V = target_logits.shape
+    code = _dtype_code(target_logits)
+    wsp, wsn = _ws_args(workspace, B, N1 - 1, V, code, target_logits.device)
+    st = lib().spec_verify_tree_greedy(_ptr(target_logits), _ptr(tree_parents),
+                                       _ptr(tree_tokens), B, N1 - 1, V, _ptr(out_tokens),
+                                       _ptr(out_num_accepted), _ptr(out_slots), _stream(stream),
+                                       code, _ptr(err_flag), wsp, wsn)
+    if st != SPEC_OK:
+        raise SpecError("spec_verify_tree_greedy", st)
+
+
 def spec_verify_greedy_noalloc(target_logits, draft_tokens, out_tokens, out_num_accepted, *,
                                stream=None, err_flag=None) -> None:
     """Greedy verification on the library's built-in device scratch (no workspace
@@ -262,10 +291,14 @@ def kv_evict_provisional(block_table, seq_lens, free_stack, free_top, status, *,
 
 
 def kv_commit_rollback(block_table, seq_lens, num_accepted, prov_blocks, kv_pool, free_stack,
-                       free_top, status, *, K: int, block_size: int, stream=None) -> None:
+                       free_top, status, *, K: int, block_size: int, stream=None,
+                       slot_map=None) -> None:
     """Commit the accepted provisional slots. kv_pool: [num_blocks, layers, 2, block_size,
-    heads, head_dim] (any element type); tables int32 as in include/specverify.h."""
+    heads, head_dim] (any element type); tables int32 as in include/specverify.h.
+    slot_map: optional [B, K+1] int32 (a tree draft's kept slots)."""
     import torch
+    if slot_map is not None:
+        _check(slot_map, "slot_map", 2, torch.int32)
     for t, n in ((block_table, "block_table"), (prov_blocks, "prov_blocks")):
         _check(t, n, 2, torch.int32)
     for t, n in ((seq_lens, "seq_lens"), (num_accepted, "num_accepted"),
@@ -280,7 +313,7 @@ def kv_commit_rollback(block_table, seq_lens, num_accepted, prov_blocks, kv_pool
     st = lib().kv_commit_rollback(
         _ptr(block_table), _ptr(seq_lens), _ptr(num_accepted), _ptr(prov_blocks), _ptr(kv_pool),
         NB, NL, H, D, kv_pool.element_size(), block_size, B, K, MB, P, _ptr(free_stack),
-        _ptr(free_top), _ptr(status), _stream(stream))
+        _ptr(free_top), _ptr(status), _stream(stream), _ptr(slot_map))
     if st != SPEC_OK:
         raise SpecError("kv_commit_rollback", st)
 

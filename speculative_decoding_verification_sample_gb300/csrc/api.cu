@@ -62,7 +62,25 @@ int spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens, i
   if (check_workspace(workspace, workspace_bytes, B, K, V, dtype) != SPEC_OK) return SPEC_EINVAL;
   sv::GreedyLaunch g{target_logits, draft_tokens, B, K, V, dtype, out_tokens, out_num_accepted,
                      err_flag, stream, workspace,
-                     reinterpret_cast<unsigned long long*>(accept_counters)};
+                     reinterpret_cast<unsigned long long*>(accept_counters), nullptr, nullptr};
+  return sv::launch_verify_greedy(g);
+}
+
+int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_parents,
+                            const int32_t* tree_tokens, int B, int N, int V, int32_t* out_tokens,
+                            int32_t* out_num_accepted, int32_t* out_slots, void* stream,
+                            int dtype, int32_t* err_flag, void* workspace,
+                            size_t workspace_bytes) {
+  const int eb = elem_bytes(dtype);
+  if (!target_logits || !tree_parents || !tree_tokens || !out_tokens || !out_num_accepted)
+    return SPEC_EINVAL;
+  if (eb == 0 || B < 1 || N < 1 || N > 31 || V < 1) return SPEC_EINVAL;
+  if (!aligned16(target_logits)) return SPEC_EINVAL;
+  if ((int64_t(V) * eb) % 16 != 0) return SPEC_ENOTSUP;
+  if (int64_t(B) * (V / (16 / eb)) > INT32_MAX) return SPEC_EINVAL;
+  if (check_workspace(workspace, workspace_bytes, B, N, V, dtype) != SPEC_OK) return SPEC_EINVAL;
+  sv::GreedyLaunch g{target_logits, tree_tokens, B, N, V, dtype, out_tokens, out_num_accepted,
+                     err_flag, stream, workspace, nullptr, tree_parents, out_slots};
   return sv::launch_verify_greedy(g);
 }
 
@@ -103,7 +121,7 @@ int kv_commit_rollback(int32_t* block_table, int32_t* seq_lens, const int32_t* n
                        int32_t* prov_blocks, void* kv_pool, int num_blocks, int num_layers,
                        int num_kv_heads, int head_dim, int kv_elem_bytes, int block_size, int B,
                        int K, int max_blocks, int P, int32_t* free_stack, int32_t* free_top,
-                       int32_t* status, void* stream) {
+                       int32_t* status, void* stream, const int32_t* slot_map) {
   if (!block_table || !seq_lens || !num_accepted || !prov_blocks || !kv_pool || !free_stack ||
       !free_top || !status)
     return SPEC_EINVAL;
@@ -114,7 +132,7 @@ int kv_commit_rollback(int32_t* block_table, int32_t* seq_lens, const int32_t* n
   if (slot % 16 != 0 || !aligned16(kv_pool)) return SPEC_ENOTSUP;
   sv::KvLaunch k{block_table, seq_lens, num_accepted, prov_blocks, kv_pool, num_blocks,
                  num_layers,  num_kv_heads, head_dim, kv_elem_bytes, block_size, B, K,
-                 max_blocks,  P, free_stack, free_top, status, stream};
+                 max_blocks,  P, free_stack, free_top, status, stream, slot_map};
   return sv::launch_kv_commit(k);
 }
 

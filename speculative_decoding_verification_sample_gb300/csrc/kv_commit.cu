@@ -12,10 +12,13 @@
 //                    new tail blocks from the free stack (rows ascending),
 //                    then pushes every provisional block (rows ascending) and
 //                    writes the call's status word;
-//   kv_copy_kernel   one CTA per row: if the status is 0, copies slots 0..n of
-//                    the row's provisional blocks, for every layer and both K
-//                    and V planes, to logical positions L..L+n, then sets the
-//                    new length and clears the provisional entries.
+//   kv_copy_kernel   one CTA per row: if the status is 0, copies the n + 1
+//                    kept slots of the row's provisional blocks (slots 0..n,
+//                    or slot_map[b][0..n] for a tree draft, whose kept path
+//                    need not be contiguous: "Grading every branch in one
+//                    pass"), for every layer and both K and V planes, to
+//                    logical positions L..L+n, then sets the new length and
+//                    clears the provisional entries.
 // Only the accepted bytes move: 2 * (n + 1) * layers * heads * head_dim * elem
 // bytes read and written per row.
 #include <cuda_runtime.h>
@@ -42,8 +45,14 @@ struct KvArgs {
   int32_t* fs;
   int32_t* ftop;
   int32_t* status;
-  int64_t slot_bytes;  // H * D * eb
+  const int32_t* smap;  // [B, K + 1] or null (identity)
+  int64_t slot_bytes;   // H * D * eb
 };
+
+// Provisional slot that kept position s of row b is copied from.
+__device__ __forceinline__ int kept_slot(const KvArgs& a, int b, int s) {
+  return a.smap ? a.smap[size_t(b) * (a.K + 1) + s] : s;
+}
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
 
@@ -101,14 +110,20 @@ __device__ int validate_row(const KvArgs& a, int b, int& need, int& npush) {
       e |= SPEC_DERR_BAD_BLOCK;  // a slot the commit must fill is already taken
     }
   }
-  if (n / a.bs >= a.P) {
-    e |= SPEC_DERR_BAD_BLOCK;
-  } else {
-    for (int k = 0; k <= n / a.bs; ++k) {
-      const int x = a.pb[size_t(b) * a.P + k];
-      if (x < 0 || x >= a.NB) e |= SPEC_DERR_BAD_BLOCK;
+  int slot_err = 0, blk_err = 0;
+  for (int s = 0; s <= n; ++s) {  // the provisional blocks of the kept slots
+    const int x = kept_slot(a, b, s);
+    if (x < 0 || x > a.K) {
+      slot_err = 1;
+    } else if (x / a.bs >= a.P) {
+      blk_err = 1;
+    } else {
+      const int y = a.pb[size_t(b) * a.P + x / a.bs];
+      if (y < 0 || y >= a.NB) blk_err = 1;
     }
   }
+  if (slot_err) e |= SPEC_DERR_BAD_SLOT;
+  else if (blk_err) e |= SPEC_DERR_BAD_BLOCK;
   need = tot - have;
   return e;
 }
@@ -204,11 +219,11 @@ __global__ void __launch_bounds__(kCopyThreads) kv_copy_kernel(const KvArgs a) {
   const int64_t layer_stride = int64_t(2) * a.bs * a.slot_bytes;  // one layer: K and V planes
   const int64_t block_stride = int64_t(a.NL) * layer_stride;
   if (threadIdx.x <= n) {
-    const int s = threadIdx.x;
-    const int sb = a.pb[size_t(b) * a.P + s / a.bs];
+    const int s = threadIdx.x, x = kept_slot(a, b, s);
+    const int sb = a.pb[size_t(b) * a.P + x / a.bs];
     const int pos = L + s;
     const int db = a.bt[size_t(b) * a.MB + pos / a.bs];
-    s_src[s] = int64_t(sb) * block_stride + int64_t(s % a.bs) * a.slot_bytes;
+    s_src[s] = int64_t(sb) * block_stride + int64_t(x % a.bs) * a.slot_bytes;
     s_dst[s] = int64_t(db) * block_stride + int64_t(pos % a.bs) * a.slot_bytes;
   }
   __syncthreads();
@@ -355,6 +370,7 @@ int launch_kv_commit(const KvLaunch& k) {
   a.fs = k.free_stack;
   a.ftop = k.free_top;
   a.status = k.status;
+  a.smap = k.slot_map;
   a.slot_bytes = int64_t(k.num_kv_heads) * k.head_dim * k.elem_bytes;
   cudaStream_t st = static_cast<cudaStream_t>(k.stream);
   kv_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);

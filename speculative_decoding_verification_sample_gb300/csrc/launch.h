@@ -39,6 +39,8 @@ struct GreedyLaunch {
   void* stream;
   void* workspace;
   unsigned long long* counters;
+  const int32_t* parents;  // tree mode: [B, K] node parents; null for a chain
+  int32_t* out_slots;      // tree mode: [B, K + 1]
 };
 
 struct KvLaunch {
@@ -53,6 +55,7 @@ struct KvLaunch {
   int32_t* free_top;
   int32_t* status;
   void* stream;
+  const int32_t* slot_map;  // [B, K + 1] provisional slot of each kept position; null: identity
 };
 
 struct KvTruncLaunch {

@@ -13,6 +13,15 @@
 // either writes the row or (all K accepted) enqueues the slices of target row
 // K, whose completing finisher writes the bonus token. Raw logits are compared
 // exactly (no temperature).
+//
+// Tree mode (spec_verify_tree_greedy; "Grading every branch in one pass": the
+// flattened draft tree is graded in one target pass and the longest surviving
+// path is kept): N nodes in topological order, target row 0 after the
+// committed prefix and row 1 + i after node i. The single stage streams all
+// N + 1 rows; the finisher that completes a row keeps the deepest node whose
+// whole root path matches the target's argmaxes and emits the path, then the
+// argmax of its last node's row. With distinct sibling tokens this equals
+// target-only greedy decoding, as in the linear case.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -34,16 +43,18 @@ constexpr int kFinWarp = kCW + 1;  // warp index of the finisher
 struct GreedyArgs {
   const void* target;
   const int32_t* tokens;
-  int B, K, V, S, nvec;
+  int B, K, V, S, nvec;  // tree mode: K = N nodes
   int32_t* out_tokens;
   int32_t* out_n;
   int32_t* err;
+  const int32_t* parents;  // tree mode: [B, N] parent of each node (-1: root); else null
+  int32_t* out_slots;      // tree mode, optional: [B, N + 1] KV slot of each kept position
   unsigned long long* counters;  // optional acceptance statistics [2K + 2]
   Ws ws;
 };
 
 // Hand-off slot: the task (16 bytes), then float wM[R][kCW], int wI[R][kCW]
-// (index -2: a NaN was seen).
+// (index -2: a NaN was seen); R = rows a first-stage task reads.
 __host__ __device__ inline int slot_bytes(int R) { return (16 + R * kCW * 8 + 15) / 16 * 16; }
 
 struct Smem {
@@ -83,6 +94,11 @@ __device__ inline Smem make_smem(uint8_t* base, int R) {
   L.ho.data = base + o;
   L.ho.slot_bytes = slot_bytes(R);
   return L;
+}
+
+// Target rows a first-stage task reads: 0..K-1, or 0..N in tree mode.
+__device__ __host__ __forceinline__ int rows_of(const GreedyArgs& a) {
+  return a.parents ? a.K + 1 : a.K;
 }
 
 // (value, index) order: larger value first, then smaller index.
@@ -157,7 +173,7 @@ struct ArgmaxOp {
 // Finisher: slice partial (value, index) of the task's rows into out[2r], out[2r+1].
 __device__ void combine_task(const GreedyArgs& a, const QTask& t, const uint8_t* slot) {
   const int lane = threadIdx.x & 31;
-  const int R = a.K, nrows = (t.type == kG1) ? a.K : 1;
+  const int R = rows_of(a), nrows = (t.type == kG1) ? rows_of(a) : 1;
   const float* wM = reinterpret_cast<const float*>(slot + 16);
   const int* wI = reinterpret_cast<const int*>(wM + R * kCW);
   float* out = a.ws.part(t.b, t.s);
@@ -266,12 +282,78 @@ __device__ void finish_gb(const GreedyArgs& a, const Smem& L, int b) {
   write_row(a, b, a.K, tok, tok < 0, SPEC_DERR_LOGITS);
 }
 
+// Tree mode. Lane i holds node i (parent, token) and the argmax of row i.
+// Node i is consistent when its token is the argmax of its parent's row; it
+// survives when every node on its root path is consistent. Pointer jumping
+// (five rounds cover depth 31) gives each node its survival and depth at
+// once; the kept path ends at the deepest survivor, the lowest index among
+// equally deep ones, and is read back by walking its parents.
+__device__ void finish_tree(const GreedyArgs& a, const Smem& L, int b) {
+  const int lane = threadIdx.x & 31, N = a.K;
+  int par = -1, tok = -1, bad = 0;
+  if (lane < N) {
+    par = a.parents[size_t(b) * N + lane];
+    tok = a.tokens[size_t(b) * N + lane];
+    bad = tok < 0 || tok >= a.V || par < -1 || par >= lane;
+  }
+  const int g = argmax_rows(a, L, b, N + 1);  // lane r: argmax of row r, -1 if unusable
+  bad = __any_sync(0xffffffffu, bad);
+  if (bad) par = -1;  // keeps the shuffles below in range
+  const int g_par = __shfl_sync(0xffffffffu, g, par + 1);
+  int alive = lane < N && g_par >= 0 && tok == g_par;
+  int depth = 1, anc = par;
+#pragma unroll
+  for (int round = 0; round < 5; ++round) {
+    const int src = anc >= 0 ? anc : lane;
+    const int a_alive = __shfl_sync(0xffffffffu, alive, src);
+    const int a_depth = __shfl_sync(0xffffffffu, depth, src);
+    const int a_anc = __shfl_sync(0xffffffffu, anc, src);
+    if (anc >= 0) {
+      alive &= a_alive;
+      depth += a_depth;
+      anc = a_anc;
+    }
+  }
+  alive = alive && lane < N;
+  const int g_own = __shfl_sync(0xffffffffu, g, min(lane + 1, 31));
+  const bool error = bad || __shfl_sync(0xffffffffu, g, 0) < 0 ||
+                     __any_sync(0xffffffffu, alive && g_own < 0);
+  const int key = __reduce_max_sync(0xffffffffu, alive ? (depth << 8) | (255 - lane) : -1);
+  const int best = key < 0 ? -1 : 255 - (key & 255);
+  const int n = key < 0 ? 0 : key >> 8;
+  int my_node = -1;  // lane p: the node at depth p + 1 of the kept path
+  for (int cur = best; cur >= 0;) {
+    if (lane == __shfl_sync(0xffffffffu, depth, cur) - 1) my_node = cur;
+    cur = __shfl_sync(0xffffffffu, par, cur);
+  }
+  const int node_tok = __shfl_sync(0xffffffffu, tok, my_node < 0 ? 0 : my_node);
+  const int prev_node = __shfl_up_sync(0xffffffffu, my_node, 1);
+  const int last = __shfl_sync(0xffffffffu, g, best + 1);
+  if (lane <= N) {
+    int32_t v = -1, sl = -1;
+    if (!error) {
+      if (lane < n) v = node_tok;
+      if (lane == n) v = last;
+      // kept position p: slot 0 (last committed token) or 1 + the node at depth p
+      if (lane <= n) sl = lane == 0 ? 0 : 1 + prev_node;
+    }
+    a.out_tokens[size_t(b) * (N + 1) + lane] = v;
+    if (a.out_slots) a.out_slots[size_t(b) * (N + 1) + lane] = sl;
+  }
+  if (lane == 0) {
+    a.out_n[b] = error ? -1 : n;
+    if (error && a.err) atomicOr(a.err, bad ? SPEC_DERR_TOKEN : SPEC_DERR_LOGITS);
+    atomicAdd(&a.ws.hdr()->rows_done, 1u);
+  }
+  __syncwarp();
+}
+
 template <class E>
 __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const GreedyArgs a) {
   using T = typename E::T;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  const int K = a.K;
-  const Smem L = make_smem(smem_raw, K);
+  const int K = a.K, R = rows_of(a);
+  const Smem L = make_smem(smem_raw, R);
   ring_init(L.ring);
   handoff_init(L.ho);
   __syncthreads();
@@ -294,10 +376,11 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
         const T* tgt = static_cast<const T*>(a.target) + size_t(t.b) * (K + 1) * a.V;
         int v0, v1;
         slice_range(a.nvec, a.S, t.s, v0, v1);
-        const char* rows[kMaxK + 1];
+        const char* rows[kMaxK + 2];
         int nrows = 0;
         if (t.type == kG1) {
-          for (int i = 0; i < K; ++i) rows[nrows++] = reinterpret_cast<const char*>(tgt + size_t(i) * a.V);
+          for (int i = 0; i < R; ++i)
+            rows[nrows++] = reinterpret_cast<const char*>(tgt + size_t(i) * a.V);
         } else {
           rows[nrows++] = reinterpret_cast<const char*>(tgt + size_t(K) * a.V);
         }
@@ -312,7 +395,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
         a.ws, L.ho, L.ring.abort,
         [&](const QTask& t, const uint8_t* slot) { combine_task(a, t, slot); },
         [&](const QTask& t) {
-          if (t.type == kG1) finish_g1(a, L, t.b);
+          if (a.parents) finish_tree(a, L, t.b);
+          else if (t.type == kG1) finish_g1(a, L, t.b);
           else finish_gb(a, L, t.b);
         },
         [&](const QTask&) { return a.S; });
@@ -340,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
         release_stage(L.ring, it);
         ++it;
         if (m.last_k) {
-          op.end_row(slot, K, m.r);
+          op.end_row(slot, R, m.r);
           op.begin();
         }
         if (m.last) break;
@@ -398,10 +482,12 @@ int launch_verify_greedy(const GreedyLaunch& g) {
   a.out_tokens = g.out_tokens;
   a.out_n = g.out_n;
   a.err = g.err;
-  a.counters = g.counters;
+  a.counters = g.parents ? nullptr : g.counters;
+  a.parents = g.parents;
+  a.out_slots = g.out_slots;
   cudaStream_t st = static_cast<cudaStream_t>(g.stream);
   if (cudaMemsetAsync(g.workspace, 0, wl.zero_bytes, st) != cudaSuccess) return SPEC_ECUDA;
-  const size_t smem = greedy_smem_bytes(g.K);
+  const size_t smem = greedy_smem_bytes(rows_of(a));
   if (g.dtype == SPEC_BF16) return launch_dataflow(verify_greedy_kernel<EBf16>, a, smem, st);
   return launch_dataflow(verify_greedy_kernel<EF32>, a, smem, st);
 }
