@@ -25,8 +25,8 @@
  *       there; output identical to the target alone.
  *   [S] "sglang_spec_decode" README, provisional KV layer: provisional blocks
  *       are committed or freed immediately; no block leaked or freed twice.
- *   [G] the page on acceptance rate and serving thresholds, "Grading every
- *       branch in one pass": draft branches flattened under an ancestor-only
+ *   [G] thakicloud.com, "Speculative decoding: when it loses", section "Grading
+ *       every branch in one pass": draft branches flattened under an ancestor-only
  *       mask, graded in one target pass, the longest surviving path kept; [L]
  *       "EAGLE-2" (dynamic draft tree) and its [2, 2, 2] tree exercise.
  *

@@ -14,7 +14,8 @@ cache, new blocks are taken from the top of the free stack (rows in ascending
 order, all pops before any push), then every provisional block is pushed back
 in row order and the row's length becomes seq_len + n + 1.
 
-With a slot map (tree drafts: "Grading every branch in one pass" keeps one
+With a slot map (tree drafts: thakicloud.com's "Speculative decoding: when it
+loses", section "Grading every branch in one pass", keeps one
 root-to-node path of the flattened tree, whose nodes need not sit in
 consecutive provisional slots), kept position s = 0..n takes its KV from
 provisional slot slot_map[b, s] instead of slot s; the identity map is the

@@ -228,8 +228,8 @@ def tree_path(par, node) -> list:
 def verify_tree_greedy(target, parents, tokens) -> dict:
     """Greedy verification of a draft tree, one verifier pass over all nodes.
 
-    Sources: "Grading every branch in one pass" (the page on acceptance rate
-    and serving thresholds): the drafter's branches are flattened into one
+    Sources: "thakicloud.com - Speculative decoding: when it loses", section
+    "Grading every branch in one pass": the drafter's branches are flattened into one
     sequence under an ancestor-only mask, the target grades every node in one
     forward pass, and the longest surviving path is kept; the lesson's
     "EAGLE-2" entry and its tree exercise (a [2, 2, 2] tree, one verifier

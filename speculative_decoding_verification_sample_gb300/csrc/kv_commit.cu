@@ -15,7 +15,8 @@
 //   kv_copy_kernel   one CTA per row: if the status is 0, copies the n + 1
 //                    kept slots of the row's provisional blocks (slots 0..n,
 //                    or slot_map[b][0..n] for a tree draft, whose kept path
-//                    need not be contiguous: "Grading every branch in one
+//                    need not be contiguous: thakicloud.com, "Speculative
+//                    decoding: when it loses", "Grading every branch in one
 //                    pass"), for every layer and both K and V planes, to
 //                    logical positions L..L+n, then sets the new length and
 //                    clears the provisional entries.

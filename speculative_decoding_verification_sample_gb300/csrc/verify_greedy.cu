@@ -14,7 +14,8 @@
 // K, whose completing finisher writes the bonus token. Raw logits are compared
 // exactly (no temperature).
 //
-// Tree mode (spec_verify_tree_greedy; "Grading every branch in one pass": the
+// Tree mode (spec_verify_tree_greedy; thakicloud.com, "Speculative decoding:
+// when it loses", section "Grading every branch in one pass": the
 // flattened draft tree is graded in one target pass and the longest surviving
 // path is kept): N nodes in topological order, target row 0 after the
 // committed prefix and row 1 + i after node i. The single stage streams all
