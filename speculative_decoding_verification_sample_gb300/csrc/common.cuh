@@ -81,6 +81,31 @@ __device__ __forceinline__ float warp_sum_f(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+// Warp sums of N values per lane at once (N a power of two <= 32), by
+// recursive halving: at each of the first log2(N) butterfly steps a lane
+// keeps half of its values and trades the other half with its partner, so
+// the warp issues N - 1 + 5 - log2(N) shuffles instead of 5 N. The sum of
+// slot k ends on the lanes l with l >> (5 - log2 N) == k; the additions pair
+// the same lanes as warp_sum_f, so each slot's sum equals warp_sum_f of it.
+template <int N>
+__device__ __forceinline__ float warp_sum_slots(float (&v)[N]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int t = 0; (N >> (t + 1)) >= 1; ++t) {
+    const int h = N >> (t + 1), o = 16 >> t;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? v[i] : v[i + h];
+      const float keep = up ? v[i + h] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+#pragma unroll
+  for (int o = 16 / N; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+  return v[0];
+}
+
 __device__ __forceinline__ float warp_max_f(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -301,8 +301,7 @@ __device__ __forceinline__ void slice_range(int nvec, int S, int s, int& v0, int
 
 // Chunking of a row slice of nv vectors: chunks of cv vectors, cv a multiple of
 // 32 (units of 32 vectors never straddle chunks) and cv * 16 <= kChunk.
-__device__ __forceinline__ void chunking(int nv, int& nchunk, int& cv) {
-  constexpr int kMaxCv = kChunk / 16;
+__device__ __forceinline__ void chunking(int nv, int& nchunk, int& cv, int kMaxCv = kChunk / 16) {
   nchunk = nv > 0 ? (nv + kMaxCv - 1) / kMaxCv : 0;
   cv = nchunk > 0 ? ((nv + nchunk - 1) / nchunk + 31) / 32 * 32 : 0;
   if (cv > kMaxCv) cv = kMaxCv;
@@ -319,8 +318,10 @@ __device__ __forceinline__ bool claim_stage(const Ring& ring, uint32_t it) {
   return true;
 }
 
-// Producer: streams the rows of one task (rows[] are row base pointers,
-// `paired` interleaves chunk k of every row: r0k0, r1k0, r0k1, r1k1, ...).
+// Producer: streams the rows of one task (rows[] are row base pointers).
+// `paired` (two rows read element by element together) puts chunk k of both
+// rows in one stage, row 0 in the first half and row 1 in the second, so a
+// stage is self-contained and the ring keeps kStages pairs in flight.
 // `after_first` runs once the first stage is issued: the producer fetches its
 // next task there, so the fetch's memory round trips overlap the streaming
 // instead of leaving the ring to drain between tasks.
@@ -335,11 +336,11 @@ __device__ inline bool produce_task(const Ring& ring, uint32_t& it, uint32_t& nt
   const int slot = int(nt % kStages);
   ++nt;
   int nchunk, cv;
-  chunking(v1 - v0, nchunk, cv);
-  const int total = nrows * nchunk;
+  chunking(v1 - v0, nchunk, cv, paired ? kChunk / 32 : kChunk / 16);
+  const int total = paired ? nchunk : nrows * nchunk;
   for (int q = 0; q < total; ++q, ++it) {
-    const int r = paired ? (q % nrows) : (q / nchunk);
-    const int k = paired ? (q / nrows) : (q % nchunk);
+    const int r = paired ? 0 : (q / nchunk);
+    const int k = paired ? q : (q % nchunk);
     if (!claim_stage(ring, it)) return false;
     if (q == 0) ring.ttab[slot] = t;
     const int stage = it % kStages;
@@ -356,9 +357,15 @@ __device__ inline bool produce_task(const Ring& ring, uint32_t& it, uint32_t& nt
     m.pad = 0;
     ring.meta[stage] = m;
     const uint32_t bytes = uint32_t(c1 - c0) * 16u;
-    mbar_arrive_expect_tx(&ring.full[stage], bytes);
-    bulk_g2s(ring.buf + size_t(stage) * kChunk, rows[r] + size_t(c0) * 16, bytes,
-             &ring.full[stage]);
+    uint8_t* dst = ring.buf + size_t(stage) * kChunk;
+    if (paired) {
+      mbar_arrive_expect_tx(&ring.full[stage], 2u * bytes);
+      bulk_g2s(dst, rows[0] + size_t(c0) * 16, bytes, &ring.full[stage]);
+      bulk_g2s(dst + kChunk / 2, rows[1] + size_t(c0) * 16, bytes, &ring.full[stage]);
+    } else {
+      mbar_arrive_expect_tx(&ring.full[stage], bytes);
+      bulk_g2s(dst, rows[r] + size_t(c0) * 16, bytes, &ring.full[stage]);
+    }
     if (q == 0) after_first();
   }
   return true;

@@ -19,10 +19,17 @@
 //   SW  fp32 residual (q_j - p_j)+ (or q_K) over the slice of row j, re-read
 //       while hot in L2; per 32-vector unit sums kept in the workspace;
 //       finish: locate u_K * total mass slice -> unit -> entry, certify
-//   FA  (rare) double-float row sums of the draw's rows
-//   FB  (rare) double-float residual and unit sums; finish: certified search
+//   FR  (rare) one double-float pass over the draw's rows: their row sums
+//       S_q, S_p and, per unit, the sums of e_q and e_p over the tokens whose
+//       residual is positive. The sign of q - p = e_q/S_q - e_p/S_p is
+//       decided from the fp32 normalisers with a proven margin; the few
+//       tokens inside the margin are listed and decided exactly by the
+//       finisher, which forms each unit's residual e_q-sum/S_q - e_p-sum/S_p
+//       and runs the certified search
+//   FA, FB (fallback when the list overflows) double-float row sums, then
+//       the double-float residual and unit sums
 // Only row j of the draft/target pair is ever re-read for the draw. The rare
-// stages AR, FA and FB are cut finer (each slice into M pieces) so that a
+// stages AR, FR, FA and FB are cut finer (each slice into M pieces) so that a
 // refined row's compute-heavy passes spread over more CTAs.
 //
 // Arithmetic. No fp64 arithmetic (GB300 runs fp64 at a small fraction of its
@@ -51,7 +58,7 @@
 namespace sv {
 namespace {
 
-enum TaskType { kP1 = 1, kBS = 2, kSW = 3, kFA = 4, kFB = 5, kAR = 6 };
+enum TaskType { kP1 = 1, kBS = 2, kSW = 3, kFA = 4, kFB = 5, kAR = 6, kFR = 7 };
 enum { kAccept = 0, kReject = 1, kAmbiguous = 2, kInvalid = 3 };
 constexpr int kModeResidual = 0, kModeQ = 1;  // draw modes (task aux bits 8+)
 constexpr int kFinWarp = kCW + 1;             // warp index of the finisher
@@ -86,6 +93,14 @@ struct SampleArgs {
 // Per-row state kept in the workspace between a row's stages. Written by the
 // finisher of one stage, read (through L2) by the tasks and finisher of the
 // next.
+// A token whose residual sign the FR pass could not decide from the fp32
+// normalisers: element index, e_q and e_p (double-float).
+struct AmbEntry {
+  int v, pad;
+  float qh, ql, ph, pl;
+};
+constexpr int kAmbCap = 32;
+
 struct RowState {
   int flags, pad0, pad1, pad2;       // SPEC_ROW_* bits so far
   float Kq, Kp, Rq, Rp;              // offsets and fp32 1/S of the draw's rows
@@ -93,6 +108,10 @@ struct RowState {
   int8_t acc[32];                    // accept-test states of positions 0..K-1
   float rK[2 * kMaxK];  // offsets of rows 0..2K-1 (target i: 2i, draft i: 2i+1)
   float rR[2 * kMaxK];  // fp32 1/S of those rows
+  float amb_delta;      // FR: relative margin of the fp32 sign test
+  int namb;             // FR: tokens inside the margin (may exceed kAmbCap)
+  int pad3, pad4;
+  AmbEntry amb[kAmbCap];
 };
 
 __device__ __forceinline__ RowState* row_state(const SampleArgs& a, int b) {
@@ -105,8 +124,9 @@ __device__ __forceinline__ RowState* row_state(const SampleArgs& a, int b) {
 //   SW:      float wAcc[kCW], wAq[kCW], wAp[kCW]
 //   FA / AR: df wA[kCW], wB[kCW]
 //   FB:      df wR[kCW], float wQ[kCW], wP[kCW]
+//   FR:      df wTq[kCW], wTp[kCW], wAq[kCW], wAp[kCW]
 __host__ __device__ inline int slot_bytes(int R) {
-  const int body = R * kCW * 12 > 2 * kCW * 8 ? R * kCW * 12 : 2 * kCW * 8;
+  const int body = R * kCW * 12 > 4 * kCW * 8 ? R * kCW * 12 : 4 * kCW * 8;
   return (16 + body + 15) / 16 * 16;
 }
 
@@ -405,7 +425,8 @@ __device__ __forceinline__ DrawRows draw_rows(int K, int aux) {
 constexpr int kPieceBit = 1 << 9;
 
 __device__ __forceinline__ bool is_piece(const QTask& t) {
-  return (t.type == kAR || t.type == kFA || t.type == kFB) && (t.aux & kPieceBit);
+  return (t.type == kAR || t.type == kFA || t.type == kFB || t.type == kFR) &&
+         (t.aux & kPieceBit);
 }
 
 // kPieceBit if the next rare stage of a row should run on pieces.
@@ -440,9 +461,9 @@ __device__ __forceinline__ void task_range(const SampleArgs& a, bool pieces, int
   pv0 = s0;
 }
 
-// Partials of piece p of row b (4 floats) inside the row's partial block.
+// Partials of piece p of row b (8 floats) inside the row's partial block.
 __device__ __forceinline__ float* piece_part(const SampleArgs& a, int b, int p) {
-  return a.ws.part(b, 0) + 4 * p;
+  return a.ws.part(b, 0) + 8 * p;
 }
 
 // Partials of a task's slice or piece.
@@ -800,13 +821,25 @@ __device__ DrawSlices draw_slices(const SampleArgs& a, int b, bool pieces) {
   return r;
 }
 
+// Unit sums as stored by SW and FB: one pair per unit.
+struct PlainUnits {
+  const SampleArgs* a;
+  int b;
+  // unit `u` of slice `ps` (index from the slice start); all lanes call it
+  __device__ __forceinline__ df get(int ps, int u, bool valid) const {
+    if (!valid) return df{0.f, 0.f};
+    const float2 w = __ldcg(a->ws.units(b, ps) + u);
+    return df{w.x, w.y};
+  }
+};
+
 // Locates t in the row's draw entries: the slice (from the lanes' slice
 // sums), then the 32-vector unit, then the entry (the warp walks the unit).
 // Returns the token (-1 if none) and whether it is certified: both
 // boundaries of the drawn entry farther than 2.02 E from t.
-template <class E, class Entries>
+template <class E, class Entries, class Units>
 __device__ int search_draw(const SampleArgs& a, int b, const Entries& ent, const DrawSlices& sl,
-                           df t, float Eb, bool& cert) {
+                           df t, float Eb, bool& cert, const Units& units_src) {
   const int lane = threadIdx.x & 31;
   // slice: lanes scan 32 slices at a time; the first slice with mass whose
   // end passes t, else the last slice with mass (rounding fallback)
@@ -846,16 +879,12 @@ __device__ int search_draw(const SampleArgs& a, int b, const Entries& ent, const
     task_range(a, sl.pieces, ss, v0, v1, ps, pv0);
     const int nu = (v1 - v0 + 31) / 32;
     // unit: lanes scan 32 units at a time
-    const float2* up = a.ws.units(b, ps) + (v0 - pv0) / 32;
+    const int ub = (v0 - pv0) / 32;
     int us = -1;
     df ubase = pre_s, ubase_s = pre_s;
     for (int u0 = 0; u0 < nu && us < 0; u0 += 32) {
       const int u = u0 + lane;
-      df x{0.f, 0.f};
-      if (u < nu) {
-        const float2 w = __ldcg(&up[u]);
-        x = df{w.x, w.y};
-      }
+      const df x = units_src.get(ps, ub + u, u < nu);
       df inc = x;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -951,8 +980,11 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
   // each), 1/S and the product (3u), and the row sum behind 1/S (ex2 + ln2 u
   // sum q|x| + gamma1); summed with weights q (resp. p), whose sum is at most
   // kQmax. sum q|x| <= kQmax/2 - sum q x, since x <= 1/4 (the offset is the
-  // ceiling of the rounded max * c, below 2^22 in magnitude). Rounding of the
-  // unit, slice and row sums adds 16 u Sr.
+  // ceiling of the rounded max * c, below 2^22 in magnitude). Summation: each
+  // term reaches a unit sum through the 8-term vector tree and the 32-lane
+  // warp tree (gamma_8), and every unit, slice and row sum above that is pair
+  // arithmetic, so t and each computed boundary are within about 8.1 u Sr of
+  // their exact sums over the computed terms; 16 u Sr covers that.
   auto side = [&](float A) {
     const float absx = 1.01f * fmaxf(0.0f, -A) + 0.5f * kQmax;
     return 1.05f * (kQmax * (2.0f * a.bd.ex2 + 3.0f * kU + a.bd.gamma1 + 4.0f * kLn2f * kU) +
@@ -973,19 +1005,73 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
     fe.Rq = Rq;
     fe.Kp = Kp;
     fe.Rp = Rp;
-    token = search_draw<E>(a, b, fe, sl, t, Eb, cert);
+    token = search_draw<E>(a, b, fe, sl, t, Eb, cert, PlainUnits{&a, b});
   }
   if (token >= 0 && cert) {
     write_outputs(a, b, dr.j, token, flags, false, d);
     return;
   }
   if (lane == 0) {
+    // FR's sign test compares fp32 approximations x = e_q.hi * Rq and
+    // y = e_p.hi * Rp of q and p. Relative error of each: the fp32 row sum
+    // behind R (ex2 + gamma1 + 2 ln2 u sum q|x|), the reciprocal, the hi
+    // part and the product (about 3u), and the double-float exponential.
+    auto eps = [&](float A) {
+      const float absx = 1.01f * fmaxf(0.0f, -A) + 0.5f * kQmax;
+      return a.bd.ex2 + a.bd.gamma1 + 2.0f * kLn2f * kU * absx + 4.0f * kU + 1e-10f;
+    };
+    st->amb_delta = 1.05f * (eps(sl.f2) + eps(sl.f3)) + 4.0f * kU;
+    st->namb = 0;
     st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
     const int pb = piece_choice(a);
-    enqueue_row_stage(a.ws, kFA, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
+    enqueue_row_stage(a.ws, kFR, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
   }
   __syncwarp();
 }
+
+// Element index (token) of an ambiguous FR entry -> its slice or piece.
+__device__ __forceinline__ int part_of_token(const SampleArgs& a, bool pieces, int v) {
+  const int vv = v / (a.V / a.nvec);
+  int s = int(int64_t(vv) * a.S / a.nvec);
+  int s0, s1;
+  slice_range(a.nvec, a.S, s, s0, s1);
+  while (s > 0 && vv < s0) slice_range(a.nvec, a.S, --s, s0, s1);
+  while (s < a.S - 1 && vv >= s1) slice_range(a.nvec, a.S, ++s, s0, s1);
+  if (!pieces) return s;
+  const int units = (s1 - s0 + 31) / 32, uu = (vv - s0) / 32;
+  int i = 0;
+  while (i < a.M - 1 && uu >= units * (i + 1) / a.M) ++i;
+  return s * a.M + i;
+}
+
+// FR unit values: residual of unit u = Aq_u / S_q - Ap_u / S_p plus the
+// positive ambiguous tokens inside it (held one per lane: token av, value ad).
+struct FrUnits {
+  const SampleArgs* a;
+  int b, namb, av;
+  bool pair;
+  df Iq, Ip, ad;
+  __device__ __forceinline__ df get(int ps, int u, bool valid) const {
+    df x{0.f, 0.f};
+    if (valid) {
+      const float4 w = __ldcg(reinterpret_cast<const float4*>(a->ws.units(b, ps)) + u);
+      x = df_mul(df{w.x, w.y}, Iq);
+      if (pair) x = df_sub(x, df_mul(df{w.z, w.w}, Ip));
+    }
+    if (namb > 0) {
+      int s0, s1;
+      slice_range(a->nvec, a->S, ps, s0, s1);
+      const int kv = a->V / a->nvec;
+      const int e0 = (s0 + 32 * u) * kv, e1 = e0 + 32 * kv;
+      for (int e = 0; e < namb; ++e) {
+        const int ve = __shfl_sync(0xffffffffu, av, e);
+        const df de = df_shfl(ad, e);
+        if (valid && ve >= e0 && ve < e1) x = df_add(x, de);
+      }
+    }
+    return x;
+  }
+};
 
 // FA complete: accurate normalisers of the draw's rows, then FB.
 __device__ void finish_fa(const SampleArgs& a, int b, int aux) {
@@ -1049,7 +1135,7 @@ __device__ void finish_fb(const SampleArgs& a, const Smem& L, int b, int aux) {
     ae.Ip = Ip;
     ae.th = L.tab_hi;
     ae.tl = L.tab_lo;
-    token = search_draw<E>(a, b, ae, sl, df_mul_f(Sr, uK), Eb, cert);
+    token = search_draw<E>(a, b, ae, sl, df_mul_f(Sr, uK), Eb, cert, PlainUnits{&a, b});
   }
   const int fl = flags | (cert ? 0 : SPEC_ROW_UNCERTIFIED);
   if (token < 0 && lane == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
@@ -1088,13 +1174,14 @@ __device__ void combine_task(const SampleArgs& a, const QTask& t, const uint8_t*
     }
   } else if (lane == 0) {
     if (t.type == kSW) {
-      const float* w = reinterpret_cast<const float*>(slot + 16);
+      const df* wd = reinterpret_cast<const df*>(slot + 16);
+      const float* w = reinterpret_cast<const float*>(wd + kCW);
       df acc{0.f, 0.f};
       float aq = 0.f, ap = 0.f;
       for (int q = 0; q < kCW; ++q) {
-        acc = df_add_f(acc, w[q]);
-        aq += w[kCW + q];
-        ap += w[2 * kCW + q];
+        acc = df_add(acc, wd[q]);
+        aq += w[q];
+        ap += w[kCW + q];
       }
       o[0] = acc.hi;
       o[1] = acc.lo;
@@ -1111,6 +1198,17 @@ __device__ void combine_task(const SampleArgs& a, const QTask& t, const uint8_t*
       o[1] = s0.lo;
       o[2] = s1.hi;
       o[3] = s1.lo;
+    } else if (t.type == kFR) {
+      const df* w = reinterpret_cast<const df*>(slot + 16);
+      df x[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+      for (int q = 0; q < kCW; ++q)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) x[c] = df_add(x[c], w[c * kCW + q]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        o[2 * c] = x[c].hi;
+        o[2 * c + 1] = x[c].lo;
+      }
     } else {  // kFB
       const df* w = reinterpret_cast<const df*>(slot + 16);
       const float* f = reinterpret_cast<const float*>(w + kCW);
@@ -1153,6 +1251,22 @@ __device__ bool consume_stats(const SampleArgs& a, const Smem& L, uint32_t& it, 
   }
 }
 
+// Unit sums of one stage: vs[k] is this lane's vector (pair) sum of unit
+// warp + kCons / 32 * k of the stage; the transposed warp reduction leaves
+// unit k's sum on lanes (32 / N) k .. (32 / N) (k + 1) - 1.
+// Returns the unit sum on the first lane of each unit's group, 0 elsewhere,
+// so that the warp's sum of the returned values counts every unit once.
+template <int N>
+__device__ __forceinline__ float store_units(float (&vs)[N], float2* units, int u0, int cnt) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = lane / (32 / N);
+  const float us = warp_sum_slots<N>(vs);
+  const int i0 = warp * 32 + k * kCons;
+  const bool mine = lane % (32 / N) == 0 && i0 < cnt;
+  if (mine) units[u0 + i0 / 32] = make_float2(us, 0.f);
+  return mine ? us : 0.0f;
+}
+
 template <class E>
 __device__ bool consume_sw(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot,
                            const QTask& t) {
@@ -1170,63 +1284,63 @@ __device__ bool consume_sw(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   fe.Rp = dr.pair ? __ldcg(&st->Rp) : 0.f;
   int v0, v1;
   slice_range(a.nvec, a.S, t.s, v0, v1);
-  constexpr int kPer = kChunk / 16 / kCons;
-  float accf = 0.f, Aq = 0.f, Ap = 0.f;
+  // the slice total is the pair-arithmetic sum of its unit sums, so slice and
+  // unit prefixes come from one summation tree (depth 3 + 5 per term)
+  df acc{0.f, 0.f};
+  float Aq = 0.f, Ap = 0.f;
   float2* units = a.ws.units(t.b, t.s);
   bool ok = true;
   for (;;) {
     const ChunkMeta m = L.ring.meta[it % kStages];
     const uint4* bq = stage_data(L.ring, it);
-    const uint4* bp = bq;
-    uint32_t it2 = it;
-    if (dr.pair) {
-      if (!wait_stage(L.ring, it + 1)) {
-        ok = false;
-        break;
-      }
-      bp = stage_data(L.ring, it + 1);
-      it2 = it + 1;
-    }
     const int cnt = m.c1 - m.c0;
-    // unit u of this stage = vectors [32u, 32u + 32): warp w takes units
-    // w, w + 8, ...; every lane one vector (pair) of each
-    float vs[kPer];
+    const int u0 = (m.c0 - v0) / 32;
+    if (dr.pair) {
+      // a stage holds the same vectors of both rows, q first, then p
+      constexpr int kPer = kChunk / 32 / kCons;
+      const uint4* bp = bq + kChunk / 32;
+      float vs[kPer];
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int i = warp * 32 + k * kCons + lane;
-      vs[k] = 0.f;
-      if (i < cnt) {
-        float r[E::kVec];
-        vs[k] = fe.run(bq[i], bp[i], r, Aq, Ap);
+      for (int k = 0; k < kPer; ++k) {
+        const int i = warp * 32 + k * kCons + lane;
+        vs[k] = 0.f;
+        if (i < cnt) {
+          float r[E::kVec];
+          vs[k] = fe.run(bq[i], bp[i], r, Aq, Ap);
+        }
       }
-    }
+      acc = df_add_f(acc, store_units<kPer>(vs, units, u0, cnt));
+    } else {
+      constexpr int kPer = kChunk / 16 / kCons;
+      float vs[kPer];
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      const int i0 = warp * 32 + k * kCons;
-      if (i0 < cnt) {
-        const float us = warp_sum_f(vs[k]);
-        if (lane == 0) units[(m.c0 - v0 + i0) / 32] = make_float2(us, 0.f);
+      for (int k = 0; k < kPer; ++k) {
+        const int i = warp * 32 + k * kCons + lane;
+        vs[k] = 0.f;
+        if (i < cnt) {
+          float r[E::kVec];
+          vs[k] = fe.run(bq[i], bq[i], r, Aq, Ap);
+        }
       }
-      accf = __fadd_rn(accf, vs[k]);
+      acc = df_add_f(acc, store_units<kPer>(vs, units, u0, cnt));
     }
-    const bool lastc = L.ring.meta[it2 % kStages].last != 0;
     release_stage(L.ring, it);
-    if (dr.pair) release_stage(L.ring, it2);
-    it = it2 + 1;
-    if (lastc) break;
+    ++it;
+    if (m.last) break;
     if (!wait_stage(L.ring, it)) {
       ok = false;
       break;
     }
   }
-  accf = warp_sum_f(accf);
+  acc = df_warp_sum(acc);
   Aq = warp_sum_f(Aq);
   Ap = warp_sum_f(Ap);
   if (lane == 0) {
-    float* w = reinterpret_cast<float*>(slot + 16);
-    w[warp] = accf;
-    w[kCW + warp] = Aq;
-    w[2 * kCW + warp] = Ap;
+    df* wd = reinterpret_cast<df*>(slot + 16);
+    float* w = reinterpret_cast<float*>(wd + kCW);
+    wd[warp] = acc;
+    w[warp] = Aq;
+    w[kCW + warp] = Ap;
   }
   return ok;
 }
@@ -1308,16 +1422,7 @@ __device__ bool consume_fb(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   for (;;) {
     const ChunkMeta m = L.ring.meta[it % kStages];
     const uint4* bq = stage_data(L.ring, it);
-    const uint4* bp = bq;
-    uint32_t it2 = it;
-    if (dr.pair) {
-      if (!wait_stage(L.ring, it + 1)) {
-        ok = false;
-        break;
-      }
-      bp = stage_data(L.ring, it + 1);
-      it2 = it + 1;
-    }
+    const uint4* bp = dr.pair ? bq + kChunk / 32 : bq;
     const int cnt = m.c1 - m.c0;
     for (int i0 = warp * 32; i0 < cnt; i0 += kCons) {
       const int i = i0 + lane;
@@ -1325,16 +1430,16 @@ __device__ bool consume_fb(const SampleArgs& a, const Smem& L, uint32_t& it, uin
       if (i < cnt) {
         df r[E::kVec];
         vs = ae.run(bq[i], bp[i], r, Q, P);
-        acc = df_add(acc, vs);
       }
       const df us = df_warp_sum(vs);
-      if (lane == 0) units[(m.c0 - pv0 + i0) / 32] = make_float2(us.hi, us.lo);
+      if (lane == 0) {
+        units[(m.c0 - pv0 + i0) / 32] = make_float2(us.hi, us.lo);
+        acc = df_add(acc, us);
+      }
     }
-    const bool lastc = L.ring.meta[it2 % kStages].last != 0;
     release_stage(L.ring, it);
-    if (dr.pair) release_stage(L.ring, it2);
-    it = it2 + 1;
-    if (lastc) break;
+    ++it;
+    if (m.last) break;
     if (!wait_stage(L.ring, it)) {
       ok = false;
       break;
@@ -1351,6 +1456,206 @@ __device__ bool consume_fb(const SampleArgs& a, const Smem& L, uint32_t& it, uin
     f[kCW + warp] = P;
   }
   return ok;
+}
+
+// FR: one double-float pass over the draw's rows (see the header). Per unit
+// the pair sums of e_q and e_p over the tokens with a certainly positive
+// residual; per task the row sums and the unit sums' totals; tokens inside
+// the sign test's margin go to the row's list.
+template <class E>
+__device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot,
+                           const QTask& t) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const DrawRows dr = draw_rows(a.K, t.aux);
+  RowState* st = row_state(a, t.b);
+  const float Kq = __ldcg(&st->Kq), Kp = dr.pair ? __ldcg(&st->Kp) : 0.f;
+  const float Rq = __ldcg(&st->Rq), Rp = dr.pair ? __ldcg(&st->Rp) : 0.f;
+  const float up1 = 1.0f + (dr.pair ? __ldcg(&st->amb_delta) : 0.f);
+  int v0, v1, ps, pv0;
+  task_range(a, is_piece(t), t.s, v0, v1, ps, pv0);
+  float4* units = reinterpret_cast<float4*>(a.ws.units(t.b, ps));
+  df Tq{0.f, 0.f}, Tp{0.f, 0.f}, Aq{0.f, 0.f}, Ap{0.f, 0.f};
+  bool ok = true;
+  for (;;) {
+    const ChunkMeta m = L.ring.meta[it % kStages];
+    const uint4* bq = stage_data(L.ring, it);
+    const uint4* bp = dr.pair ? bq + kChunk / 32 : bq;
+    const int cnt = m.c1 - m.c0;
+    for (int i0 = warp * 32; i0 < cnt; i0 += kCons) {
+      const int i = i0 + lane;
+      df vq{0.f, 0.f}, vp{0.f, 0.f};
+      if (i < cnt) {
+        float zq[E::kVec], zp[E::kVec];
+        E::unpack(bq[i], zq);
+        if (dr.pair) E::unpack(bp[i], zp);
+#pragma unroll
+        for (int k = 0; k < E::kVec; ++k) {
+          const df eq = acc_elem(zq[k], a.Chi, a.Clo, Kq, L.tab_hi, L.tab_lo);
+          Tq = df_add(Tq, eq);
+          if (!dr.pair) {
+            vq = df_add(vq, eq);
+            continue;
+          }
+          const df ep = acc_elem(zp[k], a.Chi, a.Clo, Kp, L.tab_hi, L.tab_lo);
+          Tp = df_add(Tp, ep);
+          const float x = __fmul_rn(eq.hi, Rq), y = __fmul_rn(ep.hi, Rp);
+          if (x > __fmul_rn(y, up1)) {
+            vq = df_add(vq, eq);
+            vp = df_add(vp, ep);
+          } else if (!(__fmul_rn(x, up1) <= y)) {
+            const int slot_i = atomicAdd(&st->namb, 1);
+            if (slot_i < kAmbCap) {
+              AmbEntry e;
+              e.v = (m.c0 + i) * E::kVec + k;
+              e.pad = 0;
+              e.qh = eq.hi;
+              e.ql = eq.lo;
+              e.ph = ep.hi;
+              e.pl = ep.lo;
+              st->amb[slot_i] = e;
+            }
+          }
+        }
+      }
+      const df uq = df_warp_sum(vq);
+      const df uv = dr.pair ? df_warp_sum(vp) : df{0.f, 0.f};
+      if (lane == 0) {
+        units[(m.c0 - pv0 + i0) / 32] = make_float4(uq.hi, uq.lo, uv.hi, uv.lo);
+        Aq = df_add(Aq, uq);
+        Ap = df_add(Ap, uv);
+      }
+    }
+    release_stage(L.ring, it);
+    ++it;
+    if (m.last) break;
+    if (!wait_stage(L.ring, it)) {
+      ok = false;
+      break;
+    }
+  }
+  Tq = df_warp_sum(Tq);
+  Tp = df_warp_sum(Tp);
+  if (lane == 0) {
+    df* w = reinterpret_cast<df*>(slot + 16);
+    w[warp] = Tq;
+    w[kCW + warp] = Tp;
+    w[2 * kCW + warp] = Aq;
+    w[3 * kCW + warp] = Ap;
+  }
+  return ok;
+}
+
+// FR complete: accurate normalisers, the ambiguous tokens decided exactly,
+// residual unit sums and the certified search (or the FA / FB fallback).
+template <class E>
+__device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
+  const int lane = threadIdx.x & 31;
+  RowState* st = row_state(a, b);
+  const DrawRows dr = draw_rows(a.K, aux);
+  const bool pieces = aux & kPieceBit;
+  const int np = pieces ? a.R : a.S;
+  const int d = load_tokens(a, b);
+  const int flags = __ldcg(&st->flags);
+  const float Kq = __ldcg(&st->Kq), Kp = dr.pair ? __ldcg(&st->Kp) : 0.f;
+  const float uK = a.uniforms[size_t(b) * (a.K + 1) + a.K];
+  // lanes hold parts lane and lane + 32: (Tq, Tp, Aq, Ap)
+  df tq[2], tp[2], aq[2], ap[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    tq[h] = tp[h] = aq[h] = ap[h] = df{0.f, 0.f};
+    const int sidx = lane + 32 * h;
+    if (sidx < np) {
+      const float4* w = reinterpret_cast<const float4*>(task_part(a, pieces, b, sidx));
+      const float4 v0 = __ldcg(w), v1 = __ldcg(w + 1);
+      tq[h] = df{v0.x, v0.y};
+      tp[h] = df{v0.z, v0.w};
+      aq[h] = df{v1.x, v1.y};
+      ap[h] = df{v1.z, v1.w};
+    }
+  }
+  const df Sq = df_warp_sum(df_add(tq[0], tq[1]));
+  const df Sp = dr.pair ? df_warp_sum(df_add(tp[0], tp[1])) : df{0.f, 0.f};
+  const int namb = dr.pair ? __ldcg(&st->namb) : 0;
+  if (!(Sq.hi > 0.0f) || (dr.pair && !(Sp.hi > 0.0f)) || namb > kAmbCap) {
+    // list overflow (or a degenerate row): the two-pass FA / FB path
+    if (lane == 0) {
+      const int pb = piece_choice(a);
+      enqueue_row_stage(a.ws, kFA, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
+    }
+    __syncwarp();
+    return;
+  }
+  const df Iq = df_recip(Sq), Ip = dr.pair ? df_recip(Sp) : df{0.f, 0.f};
+  // ambiguous tokens: residual e_q/S_q - e_p/S_p in pair arithmetic, kept if positive
+  int av = -1;
+  df ad{0.f, 0.f};
+  if (lane < namb) {
+    const AmbEntry e = st->amb[lane];
+    av = e.v;
+    ad = df_sub(df_mul(df{e.qh, e.ql}, Iq), df_mul(df{e.ph, e.pl}, Ip));
+    if (!(ad.hi > 0.0f)) ad = df{0.f, 0.f};
+  }
+  const int apart = lane < namb ? part_of_token(a, pieces, av) : -1;
+  // residual of each part
+  DrawSlices sl;
+  sl.pieces = pieces;
+  sl.n = np;
+  df xr[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    xr[h] = df_mul(aq[h], Iq);
+    if (dr.pair) xr[h] = df_sub(xr[h], df_mul(ap[h], Ip));
+    for (int e = 0; e < namb; ++e) {
+      const int pe = __shfl_sync(0xffffffffu, apart, e);
+      const df de = df_shfl(ad, e);
+      if (pe == lane + 32 * h) xr[h] = df_add(xr[h], de);
+    }
+  }
+  sl.xa = xr[0];
+  sl.xb = xr[1];
+  sl.total = df_warp_sum(df_add(xr[0], xr[1]));
+  sl.f2 = sl.f3 = 0.f;
+  const df Sr = sl.total;
+  if (!(Sr.hi > 0.0f) && dr.pair) {
+    // zero residual mass: the draw uses q_j itself
+    if (lane == 0) {
+      st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;
+      st->namb = 0;
+      const int pb = piece_choice(a);
+      enqueue_row_stage(a.ws, kFR, b, stage_tasks(a, pb), dr.j | (kModeQ << 8) | pb);
+    }
+    __syncwarp();
+    return;
+  }
+  // Error bound: per token, relative error below acc_rho for e_q / S_q and
+  // e_p / S_p (exponential, argument, normaliser and reciprocal), whatever
+  // the order of the pair-arithmetic sums and products; summed with weights
+  // q and p (total 1 each, margin 10%). A token whose sign is undecidable
+  // within that error moves by at most its own error.
+  const float Eb = 1.1f * fmaxf(acc_rho(Kq), acc_rho(Kp)) * (dr.pair ? 2.0f : 1.0f) +
+                   1e-14f * Sr.hi + 1e-36f;
+  int token = -1;
+  bool cert = false;
+  {
+    const RowPtrs<E> rp = row_ptrs<E>(a, b);
+    AccEntries<E> ae;
+    ae.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
+    ae.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
+    ae.pair = dr.pair;
+    ae.Chi = a.Chi;
+    ae.Clo = a.Clo;
+    ae.Kq = Kq;
+    ae.Kp = Kp;
+    ae.Iq = Iq;
+    ae.Ip = Ip;
+    ae.th = L.tab_hi;
+    ae.tl = L.tab_lo;
+    FrUnits fu{&a, b, namb, av, dr.pair, Iq, Ip, ad};
+    token = search_draw<E>(a, b, ae, sl, df_mul_f(Sr, uK), Eb, cert, fu);
+  }
+  const int fl = flags | (cert ? 0 : SPEC_ROW_UNCERTIFIED);
+  if (token < 0 && lane == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
+  write_outputs(a, b, dr.j, token, fl, token < 0, d);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1433,6 +1738,9 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
             case kFA:
               finish_fa(a, t.b, t.aux);
               break;
+            case kFR:
+              finish_fr<E>(a, L, t.b, t.aux);
+              break;
             default:
               finish_fb<E>(a, L, t.b, t.aux);
               break;
@@ -1458,6 +1766,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
       if (t.type == kP1 || t.type == kBS) ok = consume_stats<E>(a, L, it, slot);
       else if (t.type == kSW) ok = consume_sw<E>(a, L, it, slot, t);
       else if (t.type == kFA || t.type == kAR) ok = consume_rowsums<E>(a, L, it, slot, t);
+      else if (t.type == kFR) ok = consume_fr<E>(a, L, it, slot, t);
       else ok = consume_fb<E>(a, L, it, slot, t);
       handoff_post(L.ho, n);
       if (!ok) {
@@ -1502,12 +1811,13 @@ WsLayout sample_layout(int B, int K, int V, int dtype) {
   const int S = slices_for(nvec, B);
   const int M = pieces_per_slice(nvec, S);
   const int maxslice = (nvec + S - 1) / S;
-  const int ustride = (maxslice + 31) / 32 + 1;
-  int part = (8 * K > 8) ? 8 * K : 8;  // P1: 4 floats for each of the 2K rows
-  if (part < 4 * M) part = 4 * M;      // a row's S blocks hold its R = S M piece partials
-  // queued tasks per row: BS, SW (S each); FA, FB twice (zero residual), AR up
-  // to K times (R = S M each)
-  return ws_layout(B, S, part, ustride, (5 + K) * M, int(sizeof(RowState)));
+  // unit slots (float2) per slice: FR keeps two pairs per unit (float4)
+  const int ustride = 2 * ((maxslice + 31) / 32) + 2;
+  int part = (8 * K > 8) ? 8 * K : 8;  // P1: 4 floats for each of the 2K rows; FR: 8
+  if (part < 8 * M) part = 8 * M;      // a row's S blocks hold its R = S M piece partials
+  // queued tasks per row: BS, SW (S each); FR twice (zero residual), FA, FB
+  // twice, AR up to K times (R = S M each)
+  return ws_layout(B, S, part, ustride, (6 + K) * M, int(sizeof(RowState)));
 }
 
 }  // namespace
