@@ -386,7 +386,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
           rows[nrows++] = reinterpret_cast<const char*>(tgt + size_t(K) * a.V);
         }
         auto prefetch = [&]() { fx.prepare(a.ws); };
-        if (!produce_task(L.ring, it, nt, t, rows, nrows, false, v0, v1, prefetch)) break;
+        auto peek = [&]() { fx.peek(a.ws); };
+        if (!produce_task(L.ring, it, nt, t, rows, nrows, false, v0, v1, prefetch, peek)) break;
       }
       produce_end(L.ring, it);
     }

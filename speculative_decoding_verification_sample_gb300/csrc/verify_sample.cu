@@ -1712,7 +1712,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
           }
         }
         auto prefetch = [&]() { fx.prepare(a.ws); };
-        if (!produce_task(L.ring, it, nt, t, rows, nrows, paired, v0, v1, prefetch)) break;
+        auto peek = [&]() { fx.peek(a.ws); };
+        if (!produce_task(L.ring, it, nt, t, rows, nrows, paired, v0, v1, prefetch, peek)) break;
       }
       produce_end(L.ring, it);
     }
