@@ -48,3 +48,4 @@ from .verify import (  # noqa: F401
     acceptance_counters,
 )
 from .kv import kv_commit, kv_truncate_inplace, pool_invariant_ok  # noqa: F401
+from .filters import filter_threshold, filter_thresholds, apply_threshold  # noqa: F401

@@ -195,3 +195,29 @@ def test_tree_highest_index_among_equals_is_caught(monkeypatch):
         return best
     monkeypatch.setattr(ov, "tree_kept_node", wrong)
     assert _fails(tt.test_hand_tree_cases, tt._fixture()["cases"][2])
+
+
+# ---------------------------------------------------------------- top-k / top-p
+from oracle import filters as ofl  # noqa: E402
+from tests import test_oracle_filters as tf  # noqa: E402
+
+
+def test_top_p_ignoring_top_k_is_caught(monkeypatch):
+    real = ofl.filter_threshold
+
+    def wrong(z, temperature, top_k=0, top_p=1.0):
+        # top-p over the whole row instead of the renormalised top-k set
+        return max(real(z, temperature, top_k, 1.0), real(z, temperature, 0, top_p))
+    monkeypatch.setattr(ofl, "filter_threshold", wrong)
+    monkeypatch.setattr(oracle, "filter_threshold", wrong)
+    assert _fails(tf.test_top_p_hand_rows) or _fails(tf.test_brute_force, 0)
+
+
+def test_top_p_without_temperature_is_caught(monkeypatch):
+    real = ofl.filter_threshold
+
+    def wrong(z, temperature, top_k=0, top_p=1.0):
+        return real(z, 1.0, top_k, top_p)
+    monkeypatch.setattr(ofl, "filter_threshold", wrong)
+    monkeypatch.setattr(oracle, "filter_threshold", wrong)
+    assert _fails(tf.test_brute_force, 1) or _fails(tf.test_parameter_limits)
