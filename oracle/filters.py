@@ -40,18 +40,15 @@ def filter_threshold(z, temperature: float, top_k: int = 0, top_p: float = 1.0) 
     # top-p on the renormalised top-k distribution
     if top_p < 1.0:
         T = float(np.float32(temperature))
-        keep = z >= tau
-        m = float(np.max(z[keep]))
+        kept = z[z >= tau]
+        m = float(np.max(kept))
         if np.isfinite(m):
-            w = np.where(keep, np.exp((z - m) / T), 0.0)
-            Z = w.sum()
-            values = np.unique(z[keep])[::-1]          # distinct kept values, descending
-            cum = 0.0
-            for t in values:
-                cum += w[z == t].sum()
-                if cum >= top_p * Z:
-                    tau = max(tau, float(t))
-                    break
+            zs = np.sort(kept)[::-1]                    # descending
+            cs = np.cumsum(np.exp((zs - m) / T))
+            # the first sorted position whose cumulative mass reaches p; every
+            # earlier tie group ends before it, so its value is t*
+            i = int(np.argmax(cs >= float(np.float32(top_p)) * cs[-1]))
+            tau = max(tau, float(zs[i]))
     return tau
 
 
