@@ -25,6 +25,9 @@
  *       there; output identical to the target alone.
  *   [S] "sglang_spec_decode" README, provisional KV layer: provisional blocks
  *       are committed or freed immediately; no block leaked or freed twice.
+ *   [Q] quickscale.ai, "Quand et pourquoi utiliser le speculative decoding":
+ *       "Influence du sampling" (temperature, top-p, top-k shape the verified
+ *       distributions); per-position acceptance, mean acceptance length.
  *   [G] thakicloud.com, "Speculative decoding: when it loses", section "Grading
  *       every branch in one pass": draft branches flattened under an ancestor-only
  *       mask, graded in one target pass, the longest surviving path kept; [L]
@@ -121,6 +124,12 @@ extern "C" {
  *                  counted. Per-position acceptance a_i = [K+i] / [i]; mean
  *                  acceptance length = [2K+1] / [2K] ([Q] "mean acceptance length";
  *                  [L] expected accepted tokens).
+ *   target_threshold optional [B, K+1] float, draft_threshold optional [B, K] float:
+ *                  per-row logit thresholds from spec_filter_thresholds (top-k /
+ *                  top-p); every token of a row whose logit is below the row's
+ *                  threshold counts as logit -inf (probability 0) in the softmax,
+ *                  the accept tests and the draw. Null: no filtering of that tensor.
+ *                  Ignored in greedy mode (the argmax is never filtered).
  *
  * Semantics: for i = 0..K-1, d_i is accepted iff p_i(d_i) <= 0 or
  * u[i] < min(1, q_i(d_i)/p_i(d_i)); at the first rejection j the token is the
@@ -136,7 +145,8 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
                        int B, int K, int V, int32_t* out_tokens, int32_t* out_num_accepted,
                        void* stream, int dtype, int32_t* err_flag, int32_t* row_info,
                        float* q_at_d, float* p_at_d, void* workspace, size_t workspace_bytes,
-                       uint64_t* accept_counters);
+                       uint64_t* accept_counters, const float* target_threshold,
+                       const float* draft_threshold);
 
 /*
  * spec_verify_greedy - greedy verification ([P] "What it does").
@@ -187,6 +197,34 @@ int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_paren
                             int32_t* out_num_accepted, int32_t* out_slots, void* stream,
                             int dtype, int32_t* err_flag, void* workspace,
                             size_t workspace_bytes);
+
+/*
+ * spec_filter_thresholds - top-k / top-p logit threshold of every row
+ * ([Q] "Influence du sampling" names temperature, top-k and top-p as the
+ * parameters shaping the verified distributions; the pages define neither).
+ *
+ *   logits        [R, V] dtype (SPEC_BF16 or SPEC_F32), 16-byte aligned rows
+ *                 (V * sizeof(dtype) a multiple of 16)
+ *   temperature   > 0 (top-p is taken on softmax(z / T); top-k ignores T)
+ *   top_k         0 (off) or k: keep the tokens whose logit is >= the k-th
+ *                 largest logit of the row (ties all kept; k >= V is off)
+ *   top_p         in (0, 1] (1 is off): on the renormalised top-k distribution,
+ *                 keep the tokens whose logit is >= t*, the largest logit value
+ *                 t at which the tokens with logit >= t reach probability p
+ *                 (ties all kept)
+ *   out_threshold [R] float: the row's threshold (keep z >= threshold); -inf when
+ *                 nothing is filtered; +inf for a row with a NaN logit (its
+ *                 verification then reports SPEC_DERR_LOGITS; the bit is also set here)
+ *   err_flag      optional [1] int32, device error bits OR-ed in
+ * Top-k is an exact integer selection. Top-p compares exactly summed fixed-point
+ * masses whose per-token error is bounded; a row whose comparison falls inside
+ * the fp32 bound is recomputed with double-float exponentials (error < 1e-11).
+ * The thresholds feed spec_verify_sample's target_threshold / draft_threshold
+ * (the same k and p for both tensors). Two kernels are enqueued on `stream`.
+ */
+int spec_filter_thresholds(const void* logits, int R, int V, int dtype, float temperature,
+                           int top_k, float top_p, float* out_threshold, void* stream,
+                           int32_t* err_flag);
 
 /*
  * spec_verify_greedy_noalloc - spec_verify_greedy without a caller workspace.

@@ -32,7 +32,8 @@ SPEC_ROW_UNCERTIFIED, SPEC_ROW_ZERO_RESIDUAL = 4, 8
 EXPORTED = ("spec_verify_sample", "spec_verify_greedy", "spec_verify_workspace_bytes",
             "kv_commit_rollback", "spec_selftest_ex2", "spec_status_string", "spec_version",
             "spec_verify_greedy_noalloc", "spec_verify_greedy_noalloc_max_bytes",
-            "kv_commit_inplace", "kv_evict_provisional", "spec_verify_tree_greedy")
+            "kv_commit_inplace", "kv_evict_provisional", "spec_verify_tree_greedy",
+            "spec_filter_thresholds")
 
 _lib = None
 
@@ -56,12 +57,15 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         Z = ctypes.c_size_t
-        L.spec_verify_sample.argtypes = [P, P, P, P, F, I, I, I, P, P, P, I, P, P, P, P, P, Z, P]
+        L.spec_verify_sample.argtypes = [P, P, P, P, F, I, I, I, P, P, P, I, P, P, P, P, P, Z, P,
+                                         P, P]
         L.spec_verify_sample.restype = I
         L.spec_verify_greedy.argtypes = [P, P, I, I, I, P, P, P, I, P, P, Z, P]
         L.spec_verify_greedy.restype = I
         L.spec_verify_tree_greedy.argtypes = [P, P, P, I, I, I, P, P, P, P, I, P, P, Z]
         L.spec_verify_tree_greedy.restype = I
+        L.spec_filter_thresholds.argtypes = [P, I, I, I, F, I, F, P, P, P]
+        L.spec_filter_thresholds.restype = I
         L.spec_verify_greedy_noalloc.argtypes = [P, P, I, I, I, P, P, P, I, P]
         L.spec_verify_greedy_noalloc.restype = I
         L.kv_commit_inplace.argtypes = [P, P, P, I, I, I, I, I, P, P, P, P]
@@ -165,12 +169,25 @@ def _counters(t, K):
     return _ptr(t)
 
 
+def _thr(t, B, n):
+    """Pointer of an optional [B, n] float32 CUDA tensor of row thresholds."""
+    if t is None:
+        return None
+    import torch
+    if not t.is_cuda or t.dtype != torch.float32 or t.numel() != B * n or not t.is_contiguous():
+        raise ValueError(f"thresholds must be a contiguous float32 CUDA tensor of {B * n} values")
+    return _ptr(t)
+
+
 def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature: float,
                        out_tokens, out_num_accepted, *, stream=None, err_flag=None,
                        row_info=None, q_at_d=None, p_at_d=None, workspace=None,
-                       accept_counters=None) -> None:
+                       accept_counters=None, target_threshold=None,
+                       draft_threshold=None) -> None:
     """Sampling-mode verification; shapes [B,K+1,V], [B,K,V], [B,K], [B,K+1] -> [B,K+1], [B].
-    accept_counters: optional int64/uint64 [2K+2] device tensor, accumulated (see the header)."""
+    accept_counters: optional int64/uint64 [2K+2] device tensor, accumulated (see the header).
+    target_threshold [B,K+1] / draft_threshold [B,K]: optional float32 logit thresholds
+    (spec_filter_thresholds) for top-k / top-p filtering."""
     import torch
     _check(target_logits, "target_logits", 3)
     B, K1, V = target_logits.shape
@@ -187,7 +204,8 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temp
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), _ptr(uniforms),
         ctypes.c_float(temperature), B, K, V, _ptr(out_tokens), _ptr(out_num_accepted),
         _stream(stream), code, _ptr(err_flag), _ptr(row_info),
-        _ptr(q_at_d), _ptr(p_at_d), wsp, wsn, _counters(accept_counters, K))
+        _ptr(q_at_d), _ptr(p_at_d), wsp, wsn, _counters(accept_counters, K),
+        _thr(target_threshold, B, K + 1), _thr(draft_threshold, B, K))
     if st != SPEC_OK:
         raise SpecError("spec_verify_sample", st)
 
@@ -233,6 +251,25 @@ def spec_verify_tree_greedy(target_logits, tree_parents, tree_tokens, out_tokens
                                        code, _ptr(err_flag), wsp, wsn)
     if st != SPEC_OK:
         raise SpecError("spec_verify_tree_greedy", st)
+
+
+def spec_filter_thresholds(logits, temperature: float, top_k: int, top_p: float, out_threshold,
+                           *, stream=None, err_flag=None) -> None:
+    """Top-k / top-p logit threshold of every row of logits [..., V] -> out_threshold [...]
+    (float32; keep tokens with logit >= threshold)."""
+    import torch
+    _check(logits, "logits")
+    _check(out_threshold, "out_threshold", None, torch.float32)
+    V = logits.shape[-1]
+    R = logits.numel() // V
+    if out_threshold.numel() != R:
+        raise ValueError(f"out_threshold must hold {R} values")
+    st = lib().spec_filter_thresholds(_ptr(logits), R, V, _dtype_code(logits),
+                                      ctypes.c_float(temperature), int(top_k),
+                                      ctypes.c_float(top_p), _ptr(out_threshold),
+                                      _stream(stream), _ptr(err_flag))
+    if st != SPEC_OK:
+        raise SpecError("spec_filter_thresholds", st)
 
 
 def spec_verify_greedy_noalloc(target_logits, draft_tokens, out_tokens, out_num_accepted, *,

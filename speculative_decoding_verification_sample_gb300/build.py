@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
 SOURCES = ["api.cu", "verify_sample.cu", "verify_greedy.cu", "kv_commit.cu", "selftest.cu",
-           "static_scratch.cu"]
+           "static_scratch.cu", "filter.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
                 "-I", INCLUDE]

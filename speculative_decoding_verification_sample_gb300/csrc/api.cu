@@ -89,7 +89,8 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
                        int B, int K, int V, int32_t* out_tokens, int32_t* out_num_accepted,
                        void* stream, int dtype, int32_t* err_flag, int32_t* row_info,
                        float* q_at_d, float* p_at_d, void* workspace, size_t workspace_bytes,
-                       uint64_t* accept_counters) {
+                       uint64_t* accept_counters, const float* target_threshold,
+                       const float* draft_threshold) {
   if (std::isnan(temperature) || temperature < 0.0f || std::isinf(temperature)) return SPEC_EINVAL;
   if (temperature == 0.0f) {
     const int st = spec_verify_greedy(target_logits, draft_tokens, B, K, V, out_tokens,
@@ -113,8 +114,25 @@ int spec_verify_sample(const void* target_logits, const void* draft_logits,
   if (check_workspace(workspace, workspace_bytes, B, K, V, dtype) != SPEC_OK) return SPEC_EINVAL;
   sv::SampleLaunch s{target_logits, draft_logits, draft_tokens, uniforms, temperature, B, K, V,
                      dtype, out_tokens, out_num_accepted, err_flag, row_info, q_at_d, p_at_d,
-                     stream, workspace, reinterpret_cast<unsigned long long*>(accept_counters)};
+                     stream, workspace, reinterpret_cast<unsigned long long*>(accept_counters),
+                     target_threshold, draft_threshold};
   return sv::launch_verify_sample(s);
+}
+
+int spec_filter_thresholds(const void* logits, int R, int V, int dtype, float temperature,
+                           int top_k, float top_p, float* out_threshold, void* stream,
+                           int32_t* err_flag) {
+  const int eb = elem_bytes(dtype);
+  if (!logits || !out_threshold) return SPEC_EINVAL;
+  if (eb == 0 || R < 1 || V < 1 || top_k < 0) return SPEC_EINVAL;
+  if (!(top_p > 0.0f) || top_p > 1.0f) return SPEC_EINVAL;
+  if (std::isnan(temperature) || !(temperature > 0.0f) || std::isinf(temperature)) return SPEC_EINVAL;
+  if (!aligned16(logits)) return SPEC_EINVAL;
+  if ((int64_t(V) * eb) % 16 != 0) return SPEC_ENOTSUP;
+  if (V > (1 << 24)) return SPEC_ENOTSUP;
+  sv::FilterLaunch f{logits, R, V, dtype, top_k, temperature, top_p, out_threshold, err_flag,
+                     stream};
+  return sv::launch_filter(f);
 }
 
 int kv_commit_rollback(int32_t* block_table, int32_t* seq_lens, const int32_t* num_accepted,

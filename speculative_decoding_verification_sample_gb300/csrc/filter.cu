@@ -1,0 +1,357 @@
+// Top-k / top-p logit thresholds (spec_filter_thresholds).
+//
+// Method: "quickscale.ai - Quand et pourquoi utiliser le speculative
+// decoding", section "Influence du sampling", names temperature, top-k and
+// top-p as the sampling parameters that shape the verified distributions.
+// Reading used (the pages give no definition): temperature, then top-k
+// (every token whose logit is at least the k-th largest), then top-p on the
+// renormalised top-k distribution (every token whose logit is at least the
+// largest value t at which the tokens with logit >= t reach probability p).
+// The result is one logit threshold per row; verification treats the tokens
+// below it as logit -inf.
+//
+// GB300 mapping: one CTA per row, a radix selection on order-preserving
+// integer keys of the logits (16 bits for bf16, 32 for fp32), 8 bits per
+// level. Top-k needs only counts, so it is exact. Top-p needs probability
+// mass: each token's mass 2^(z c - Kc) (c = log2(e)/T, Kc the row's integer
+// offset) is rounded to a 64-bit fixed-point integer and summed with
+// shared-memory integer atomics, which is exact and independent of the
+// order. The fast pass takes the mass from the MUFU exp2 and certifies the
+// final comparison against p with a proven bound on that mass's error; a row
+// it cannot certify gets NaN, and the second launch recomputes exactly those
+// rows with double-float exponentials (relative error < 1e-11).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/specverify.h"
+#include "common.cuh"
+#include "df.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kFT = 256;  // threads per CTA, one row per CTA
+
+// Order-preserving keys: larger key <=> larger value (NaN excluded).
+template <class E>
+struct KeyOf;
+template <>
+struct KeyOf<EBf16> {
+  static constexpr int kBits = 16;
+  __device__ static __forceinline__ uint32_t key(float z) {
+    const uint32_t b = __float_as_uint(z) >> 16;
+    return (b & 0x8000u) ? (~b & 0xffffu) : (b | 0x8000u);
+  }
+  __device__ static __forceinline__ float value(uint32_t k) {
+    const uint32_t b = (k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu);
+    return __uint_as_float(b << 16);
+  }
+};
+template <>
+struct KeyOf<EF32> {
+  static constexpr int kBits = 32;
+  __device__ static __forceinline__ uint32_t key(float z) {
+    const uint32_t b = __float_as_uint(z);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  __device__ static __forceinline__ float value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+  }
+};
+
+struct FilterArgs {
+  const void* logits;
+  int R, V, nvec, top_k;
+  float top_p, c, Chi, Clo, ex2, fixscale;
+  float* out;
+  int32_t* err;
+};
+
+// Certification slack of one histogram bin's mass (fixed-point units): the
+// relative error of each token's mass there is at most ex2 + ln2 u (2|x| + 2)
+// with |x| <= xmax (argument and temperature-constant rounding; the part of
+// the latter common to all tokens cancels in the ratio to the row total).
+__device__ __forceinline__ double bin_err(unsigned long long m, float eps, float xmax) {
+  if (m == 0) return 0.0;
+  const float x = fminf(xmax, 200.0f);
+  return double(m) * double(eps + kLn2f * kU * (2.0f * x + 2.0f)) * 1.02;
+}
+
+template <class E, bool kAcc>
+__global__ void __launch_bounds__(kFT) filter_kernel(const FilterArgs a) {
+  using KO = KeyOf<E>;
+  constexpr int KB = KO::kBits, ND = KB / 8;
+  __shared__ uint32_t hcnt[256];
+  __shared__ unsigned long long hmass[256];
+  __shared__ unsigned long long hbuck[256];
+  __shared__ uint32_t s_u[kFT / 32];
+  __shared__ int s_i[kFT / 32];
+  __shared__ uint32_t s_need, s_digit;
+  __shared__ unsigned long long s_A, s_mb, s_Z;
+  __shared__ double s_EA, s_EZ;
+  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (kAcc && !isnan(a.out[row])) return;  // second launch: uncertain rows only
+  const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const char*>(a.logits) +
+                                                   size_t(row) * size_t(a.V) * sizeof(typename E::T));
+  const bool topk = a.top_k > 0 && a.top_k < a.V;
+  const bool topp = a.top_p < 1.0f;
+  auto sweep = [&](auto&& f) {
+    for (int i = tid; i < a.nvec; i += kFT) {
+      float z[E::kVec];
+      E::unpack(ldg_nc_v4(rp + i), z);
+#pragma unroll
+      for (int k = 0; k < E::kVec; ++k) f(z[k]);
+    }
+  };
+  auto clear = [&]() {
+    for (int i = tid; i < 256; i += kFT) {
+      hcnt[i] = 0;
+      hmass[i] = 0;
+      hbuck[i] = 0;
+    }
+  };
+  // ---- pass 0: maximum key, NaN, top-k level-0 counts
+  clear();
+  __syncthreads();
+  uint32_t mk = 0;
+  int nan = 0;
+  sweep([&](float z) {
+    if (z != z) {
+      nan = 1;
+      return;
+    }
+    const uint32_t k = KO::key(z);
+    mk = max(mk, k);
+    if (topk) atomicAdd(&hcnt[k >> (KB - 8)], 1u);
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+    nan |= __shfl_xor_sync(0xffffffffu, nan, o);
+  }
+  if (lane == 0) {
+    s_u[warp] = mk;
+    s_i[warp] = nan;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t m = 0;
+    int n = 0;
+    for (int w = 0; w < kFT / 32; ++w) {
+      m = max(m, s_u[w]);
+      n |= s_i[w];
+    }
+    s_u[0] = m;
+    s_i[0] = n;
+  }
+  __syncthreads();
+  mk = s_u[0];
+  if (s_i[0]) {  // NaN logits: every token filtered; the verification reports the row
+    if (tid == 0) {
+      a.out[row] = INFINITY;
+      if (a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
+    }
+    return;
+  }
+  const float maxv = KO::value(mk);
+  if (!(maxv > -INFINITY) || (!topk && !topp)) {
+    if (tid == 0) a.out[row] = -INFINITY;
+    return;
+  }
+  const float Kc = offset_of(maxv, a.c);
+  // fixed-point mass of one token (0 for -inf)
+  auto mass = [&](float z) -> unsigned long long {
+    if (kAcc) {
+      const df p = two_prod(z, a.Chi);
+      const float pl = __fmaf_rn(z, a.Clo, p.lo);
+      const df s = two_sum(p.hi, -Kc);
+      // the double-float exponential reads its 2^(j/256) table from constant
+      // memory (this kernel keeps no shared copy)
+      const df w = df_exp2(s.hi, __fadd_rn(s.lo, pl), kExp2Tab.hi, kExp2Tab.lo);
+      const long long lo = __float2ll_rn(__fmul_rn(w.lo, a.fixscale));
+      return static_cast<unsigned long long>(
+          static_cast<long long>(__float2ull_rn(__fmul_rn(w.hi, a.fixscale))) + lo);
+    }
+    return __float2ull_rn(__fmul_rn(ex2_approx(__fmaf_rn(z, a.c, -Kc)), a.fixscale));
+  };
+  const float eps = kAcc ? 2e-12f + 2.2e-14f * (fabsf(Kc) + 256.0f) : a.ex2;
+  // |x| bound of the tokens in the key range starting at key k0
+  auto xmax_from = [&](uint32_t k0) { return Kc - __fmul_rn(KO::value(k0), a.c) + 1.0f; };
+
+  // ---- top-k: radix selection on counts
+  uint32_t KA = 0;  // keep keys >= KA
+  if (topk) {
+    uint32_t pre = 0, need = uint32_t(a.top_k);
+    for (int lvl = 0; lvl < ND; ++lvl) {
+      const int sh = KB - 8 * (lvl + 1);  // shift of this level's digit
+      if (lvl > 0) {
+        __syncthreads();
+        clear();
+        __syncthreads();
+        const bool last = lvl == ND - 1;
+        sweep([&](float z) {
+          const uint32_t k = KO::key(z);
+          const uint32_t up = k >> (sh + 8);
+          if (up == pre) atomicAdd(&hcnt[(k >> sh) & 255u], 1u);
+          if (topp && last) {  // top-p level-0 masses, merged into this pass
+            if (up > pre) {
+              const unsigned long long q = mass(z);
+              if (q) atomicAdd(&hmass[k >> (KB - 8)], q);
+            } else if (up == pre) {
+              const unsigned long long q = mass(z);
+              if (q) atomicAdd(&hbuck[k & 255u], q);
+            }
+          }
+        });
+        __syncthreads();
+      }
+      if (tid == 0) {
+        uint32_t cum = 0, d = 0;
+        for (int b = 255; b >= 0; --b) {
+          if (cum + hcnt[b] >= need) {
+            d = uint32_t(b);
+            break;
+          }
+          cum += hcnt[b];
+        }
+        s_digit = d;
+        s_need = need - cum;
+      }
+      __syncthreads();
+      pre = (pre << 8) | s_digit;
+      need = s_need;
+    }
+    KA = pre;
+  }
+  float tau = topk ? KO::value(KA) : -INFINITY;
+
+  // ---- top-p: radix selection on fixed-point masses of the keys >= KA
+  if (topp) {
+    __syncthreads();
+    if (topk) {
+      // the merged pass left the masses of keys above KA's last-level bucket
+      // by top digit (hmass) and the bucket's masses by last digit (hbuck)
+      if (tid == 0) {
+        unsigned long long add = 0;
+        for (int d = int(KA & 255u); d < 256; ++d) add += hbuck[d];
+        hmass[KA >> (KB - 8)] += add;
+        for (int d = 0; d < int(KA & 255u); ++d) hbuck[d] = 0;  // below KA: not kept
+      }
+    } else {
+      clear();
+      __syncthreads();
+      sweep([&](float z) {
+        const unsigned long long q = mass(z);
+        if (q) atomicAdd(&hmass[KO::key(z) >> (KB - 8)], q);
+      });
+    }
+    __syncthreads();
+    if (tid == 0) {
+      unsigned long long Z = 0;
+      double EZ = 0.0;
+      for (int b = 0; b < 256; ++b) {
+        Z += hmass[b];
+        EZ += bin_err(hmass[b], eps, xmax_from(uint32_t(b) << (KB - 8)));
+      }
+      s_Z = Z;
+      s_EZ = EZ;
+      s_A = 0;
+      s_EA = 0.0;
+    }
+    __syncthreads();
+    const double target = double(a.top_p) * double(s_Z);
+    uint32_t pre = 0;
+    for (int lvl = 0; lvl < ND; ++lvl) {
+      const int sh = KB - 8 * (lvl + 1);
+      if (lvl > 0) {
+        const bool reuse = topk && lvl == ND - 1 && pre == (KA >> 8);
+        __syncthreads();
+        if (reuse) {
+          for (int i = tid; i < 256; i += kFT) hmass[i] = hbuck[i];
+        } else {
+          for (int i = tid; i < 256; i += kFT) hmass[i] = 0;
+          __syncthreads();
+          sweep([&](float z) {
+            const uint32_t k = KO::key(z);
+            if (k >= KA && (k >> (sh + 8)) == pre) {
+              const unsigned long long q = mass(z);
+              if (q) atomicAdd(&hmass[(k >> sh) & 255u], q);
+            }
+          });
+        }
+        __syncthreads();
+      }
+      if (tid == 0) {
+        unsigned long long A = s_A;
+        double EA = s_EA;
+        uint32_t d = 0;
+        for (int b = 255; b >= 0; --b) {
+          if (double(A + hmass[b]) >= target) {
+            d = uint32_t(b);
+            break;
+          }
+          A += hmass[b];
+          EA += bin_err(hmass[b], eps, xmax_from(((pre << 8) | uint32_t(b)) << sh));
+        }
+        s_digit = d;
+        s_A = A;
+        s_EA = EA;
+        s_mb = hmass[d];
+      }
+      __syncthreads();
+      pre = (pre << 8) | s_digit;
+    }
+    if (tid == 0) {
+      // certify: mass(keys >= K) >= p Z and mass(keys > K) < p Z hold exactly
+      const double C = double(s_A + s_mb), Cm = double(s_A);
+      const double q = 0.5 * double(a.V) + 2.0;  // rounding to fixed point
+      const double EC = s_EA + bin_err(s_mb, eps, xmax_from(pre)) + q;
+      const double ECm = s_EA + q;
+      const double Zlo = double(s_Z) - s_EZ - q, Zhi = double(s_Z) + s_EZ + q;
+      const bool ok = (C - EC >= double(a.top_p) * Zhi) && (Cm + ECm < double(a.top_p) * Zlo);
+      const float tp = KO::value(pre);
+      a.out[row] = (ok || kAcc) ? fmaxf(tau, tp) : NAN;
+    }
+    return;
+  }
+  if (tid == 0) a.out[row] = tau;
+}
+
+}  // namespace
+
+int launch_filter(const FilterLaunch& f) {
+  FilterArgs a;
+  a.logits = f.logits;
+  a.R = f.R;
+  a.V = f.V;
+  const int kvec = (f.dtype == SPEC_BF16) ? 8 : 4;
+  a.nvec = f.V / kvec;
+  a.top_k = f.top_k;
+  a.top_p = f.top_p;
+  const double C = 1.4426950408889634073599246810018921 / double(f.temperature);
+  a.c = float(C);
+  a.Chi = float(C);
+  a.Clo = float(C - double(a.Chi));
+  a.ex2 = float(kEx2RelErrBound);
+  // fixed-point scale 2^s with 2 V 2^s < 2^63 (each mass is at most 2)
+  int lg = 0;
+  while ((1 << lg) < f.V) ++lg;
+  a.fixscale = std::ldexp(1.0f, 61 - lg);
+  a.out = f.out;
+  a.err = f.err;
+  cudaStream_t st = static_cast<cudaStream_t>(f.stream);
+  if (f.dtype == SPEC_BF16) {
+    filter_kernel<EBf16, false><<<f.R, kFT, 0, st>>>(a);
+    if (f.top_p < 1.0f) filter_kernel<EBf16, true><<<f.R, kFT, 0, st>>>(a);
+  } else {
+    filter_kernel<EF32, false><<<f.R, kFT, 0, st>>>(a);
+    if (f.top_p < 1.0f) filter_kernel<EF32, true><<<f.R, kFT, 0, st>>>(a);
+  }
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+}  // namespace sv

@@ -27,6 +27,8 @@ struct SampleLaunch {
   void* stream;
   void* workspace;
   unsigned long long* counters;
+  const float* thr_t;  // optional [B, K + 1] target-row logit thresholds
+  const float* thr_d;  // optional [B, K] draft-row logit thresholds
 };
 
 struct GreedyLaunch {
@@ -69,7 +71,17 @@ struct KvTruncLaunch {
   void* stream;
 };
 
+struct FilterLaunch {
+  const void* logits;
+  int R, V, dtype, top_k;
+  float temperature, top_p;
+  float* out;
+  int32_t* err;
+  void* stream;
+};
+
 int launch_verify_sample(const SampleLaunch& s);
+int launch_filter(const FilterLaunch& f);
 size_t sample_workspace_bytes(int B, int K, int V, int dtype);
 size_t greedy_workspace_bytes(int B, int K, int V, int dtype);
 int launch_verify_greedy(const GreedyLaunch& g);

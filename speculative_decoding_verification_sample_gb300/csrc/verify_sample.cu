@@ -87,8 +87,24 @@ struct SampleArgs {
   float* q_at_d;
   float* p_at_d;
   unsigned long long* counters;  // optional acceptance statistics [2K + 2]
+  const float* thr_t;            // optional [B, K + 1] target-row logit thresholds
+  const float* thr_d;            // optional [B, K] draft-row logit thresholds
+  int masked;                    // either is given
   Ws ws;
 };
+
+// Top-k / top-p filtering (spec_filter_thresholds): tokens whose logit is
+// below their row's threshold count as logit -inf in every stage.
+__device__ __forceinline__ float thr_of(const SampleArgs& a, int b, bool target, int i) {
+  const float* t = target ? a.thr_t : a.thr_d;
+  if (!t) return -INFINITY;
+  return __ldg(t + size_t(b) * (target ? a.K + 1 : a.K) + i);
+}
+template <int N>
+__device__ __forceinline__ void mask_vals(float (&z)[N], float tau) {
+#pragma unroll
+  for (int k = 0; k < N; ++k) z[k] = (z[k] >= tau) ? z[k] : -INFINITY;
+}
 
 // Per-row state kept in the workspace between a row's stages. Written by the
 // finisher of one stage, read (through L2) by the tasks and finisher of the
@@ -213,8 +229,8 @@ __device__ inline Smem make_smem(uint8_t* base, int R) {
 // Per-thread running max M, integer offset Kc = ceil(M c) and S = sum exp2(z c - Kc).
 template <class E>
 struct StatOp {
-  float c, M, Kc, S;
-  int bad;
+  float c, M, Kc, S, tau;
+  int bad, masked;
   __device__ __forceinline__ void begin() {
     M = -INFINITY;
     Kc = -INFINITY;
@@ -251,6 +267,7 @@ struct StatOp {
       if (tid + k * kCons < cnt) {
         float z[E::kVec];
         E::unpack(v[k], z);
+        if (masked) mask_vals(z, tau);
         float e[E::kVec];
 #pragma unroll
         for (int j = 0; j < E::kVec; ++j) e[j] = ex2_approx(__fmaf_rn(z[j], c, -Kc));
@@ -313,11 +330,17 @@ struct FastEntries {
   const uint4* tp;
   bool pair;        // residual q - p (else q alone)
   float c, Kq, Rq, Kp, Rp;
+  bool masked = false;
+  float tauq = -INFINITY, taup = -INFINITY;
   __device__ __forceinline__ float run(const uint4& vq, const uint4& vp, float (&r)[E::kVec],
                                        float& aq, float& ap) const {
     float zq[E::kVec], zp[E::kVec];
     E::unpack(vq, zq);
     if (pair) E::unpack(vp, zp);
+    if (masked) {
+      mask_vals(zq, tauq);
+      if (pair) mask_vals(zp, taup);
+    }
 #pragma unroll
     for (int k = 0; k < E::kVec; ++k) {
       const float xa = __fmaf_rn(zq[k], c, -Kq);
@@ -363,11 +386,17 @@ struct AccEntries {
   df Iq, Ip;
   const float* th;
   const float* tl;
+  bool masked = false;
+  float tauq = -INFINITY, taup = -INFINITY;
   __device__ __forceinline__ df run(const uint4& vq, const uint4& vp, df (&r)[E::kVec], float& qs,
                                     float& ps) const {
     float zq[E::kVec], zp[E::kVec];
     E::unpack(vq, zq);
     if (pair) E::unpack(vp, zp);
+    if (masked) {
+      mask_vals(zq, tauq);
+      if (pair) mask_vals(zp, taup);
+    }
     df vs{0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < E::kVec; ++k) {
@@ -650,6 +679,10 @@ __device__ void finish_p1(const SampleArgs& a, const Smem& L, int b) {
   if (lane < K && !badtok_lane) {
     zt = E::load(rp.tgt + size_t(lane) * V, d);
     zd = E::load(rp.drf + size_t(lane) * V, d);
+    if (a.masked) {
+      if (!(zt >= thr_of(a, b, true, lane))) zt = -INFINITY;
+      if (!(zd >= thr_of(a, b, false, lane))) zd = -INFINITY;
+    }
   }
   for (int r = lane; r < 2 * K; r += 32) {
     st->rK[r] = F.rowKc[r];
@@ -733,8 +766,12 @@ __device__ void finish_ar(const SampleArgs& a, const Smem& L, int b, int aux) {
   const df S0 = ss.p0, S1 = ss.p1;
   const RowPtrs<E> rp = row_ptrs<E>(a, b);
   const int di = __shfl_sync(0xffffffffu, d, i);
-  const float zt = E::load(rp.tgt + size_t(i) * a.V, di);
-  const float zd = E::load(rp.drf + size_t(i) * a.V, di);
+  float zt = E::load(rp.tgt + size_t(i) * a.V, di);
+  float zd = E::load(rp.drf + size_t(i) * a.V, di);
+  if (a.masked) {
+    if (!(zt >= thr_of(a, b, true, i))) zt = -INFINITY;
+    if (!(zd >= thr_of(a, b, false, i))) zd = -INFINITY;
+  }
   // ratio = 2^((zt C - Kt) - (zd C - Kd)) * S_d / S_t in pair arithmetic
   const df xt = df_add_f(df_add(two_prod(zt, a.Chi), df{__fmul_rn(zt, a.Clo), 0.f}),
                          -__shfl_sync(0xffffffffu, rk_t, i));
@@ -1001,6 +1038,9 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
     fe.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
     fe.pair = dr.pair;
     fe.c = a.c;
+    fe.masked = a.masked;
+    fe.tauq = thr_of(a, b, true, dr.j);
+    fe.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
     fe.Kq = Kq;
     fe.Rq = Rq;
     fe.Kp = Kp;
@@ -1127,6 +1167,9 @@ __device__ void finish_fb(const SampleArgs& a, const Smem& L, int b, int aux) {
     ae.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
     ae.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
     ae.pair = dr.pair;
+    ae.masked = a.masked;
+    ae.tauq = thr_of(a, b, true, dr.j);
+    ae.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
     ae.Chi = a.Chi;
     ae.Clo = a.Clo;
     ae.Kq = Kq;
@@ -1232,13 +1275,19 @@ __device__ void combine_task(const SampleArgs& a, const QTask& t, const uint8_t*
 // Each returns false on a timeout; `it` advances past the task's stages.
 
 template <class E>
-__device__ bool consume_stats(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot) {
+__device__ bool consume_stats(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot,
+                              const QTask& t) {
   const int tid = threadIdx.x;
   StatOp<E> op;
   op.c = a.c;
+  op.masked = a.masked;
+  op.tau = -INFINITY;
   op.begin();
   for (;;) {
     const ChunkMeta m = L.ring.meta[it % kStages];
+    // P1 rows: target i = 2i, draft i = 2i + 1; BS: target row K
+    if (a.masked)
+      op.tau = (t.type == kBS) ? thr_of(a, t.b, true, a.K) : thr_of(a, t.b, (m.r & 1) == 0, m.r >> 1);
     op.chunk(stage_data(L.ring, it), m.c1 - m.c0, tid);
     release_stage(L.ring, it);
     ++it;
@@ -1278,6 +1327,9 @@ __device__ bool consume_sw(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   fe.tp = nullptr;
   fe.pair = dr.pair;
   fe.c = a.c;
+  fe.masked = a.masked;
+  fe.tauq = thr_of(a, t.b, true, dr.j);
+  fe.taup = dr.pair ? thr_of(a, t.b, false, dr.j) : -INFINITY;
   fe.Kq = __ldcg(&st->Kq);
   fe.Rq = __ldcg(&st->Rq);
   fe.Kp = dr.pair ? __ldcg(&st->Kp) : 0.f;
@@ -1360,16 +1412,23 @@ __device__ bool consume_rowsums(const SampleArgs& a, const Smem& L, uint32_t& it
     K0 = __ldcg(&st->Kq);
     K1 = draw_rows(a.K, t.aux).pair ? __ldcg(&st->Kp) : 0.f;
   }
+  // rows: AR target / draft i, FA target / draft j
+  const int ri = (t.type == kAR) ? (t.aux & 0xff) : draw_rows(a.K, t.aux).j;
+  const bool two = (t.type == kAR) || draw_rows(a.K, t.aux).pair;  // draft row ri < K exists
+  const float tau0 = thr_of(a, t.b, true, ri);
+  const float tau1 = two ? thr_of(a, t.b, false, ri) : -INFINITY;
   df s0{0.f, 0.f}, s1{0.f, 0.f};
   bool ok = true;
   for (;;) {
     const ChunkMeta m = L.ring.meta[it % kStages];
     const uint4* buf = stage_data(L.ring, it);
     const float Kr = (m.r == 0) ? K0 : K1;
+    const float tau = (m.r == 0) ? tau0 : tau1;
     df acc{0.f, 0.f};
     for (int i = tid; i < m.c1 - m.c0; i += kCons) {
       float z[E::kVec];
       E::unpack(buf[i], z);
+      if (a.masked) mask_vals(z, tau);
 #pragma unroll
       for (int k = 0; k < E::kVec; ++k)
         acc = df_add(acc, acc_elem(z[k], a.Chi, a.Clo, Kr, L.tab_hi, L.tab_lo));
@@ -1405,6 +1464,9 @@ __device__ bool consume_fb(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   ae.tq = nullptr;  // the sweep reads the ring stages
   ae.tp = nullptr;
   ae.pair = dr.pair;
+  ae.masked = a.masked;
+  ae.tauq = thr_of(a, t.b, true, dr.j);
+  ae.taup = dr.pair ? thr_of(a, t.b, false, dr.j) : -INFINITY;
   ae.Chi = a.Chi;
   ae.Clo = a.Clo;
   ae.Kq = __ldcg(&st->Kq);
@@ -1471,6 +1533,8 @@ __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   const float Kq = __ldcg(&st->Kq), Kp = dr.pair ? __ldcg(&st->Kp) : 0.f;
   const float Rq = __ldcg(&st->Rq), Rp = dr.pair ? __ldcg(&st->Rp) : 0.f;
   const float up1 = 1.0f + (dr.pair ? __ldcg(&st->amb_delta) : 0.f);
+  const float tauq = thr_of(a, t.b, true, dr.j);
+  const float taup = dr.pair ? thr_of(a, t.b, false, dr.j) : -INFINITY;
   int v0, v1, ps, pv0;
   task_range(a, is_piece(t), t.s, v0, v1, ps, pv0);
   float4* units = reinterpret_cast<float4*>(a.ws.units(t.b, ps));
@@ -1488,6 +1552,10 @@ __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uin
         float zq[E::kVec], zp[E::kVec];
         E::unpack(bq[i], zq);
         if (dr.pair) E::unpack(bp[i], zp);
+        if (a.masked) {
+          mask_vals(zq, tauq);
+          if (dr.pair) mask_vals(zp, taup);
+        }
 #pragma unroll
         for (int k = 0; k < E::kVec; ++k) {
           const df eq = acc_elem(zq[k], a.Chi, a.Clo, Kq, L.tab_hi, L.tab_lo);
@@ -1642,6 +1710,9 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
     ae.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
     ae.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
     ae.pair = dr.pair;
+    ae.masked = a.masked;
+    ae.tauq = thr_of(a, b, true, dr.j);
+    ae.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
     ae.Chi = a.Chi;
     ae.Clo = a.Clo;
     ae.Kq = Kq;
@@ -1764,7 +1835,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
       uint8_t* slot = L.ho.slot(n);
       if (tid == 0) *reinterpret_cast<QTask*>(slot) = t;
       bool ok;
-      if (t.type == kP1 || t.type == kBS) ok = consume_stats<E>(a, L, it, slot);
+      if (t.type == kP1 || t.type == kBS) ok = consume_stats<E>(a, L, it, slot, t);
       else if (t.type == kSW) ok = consume_sw<E>(a, L, it, slot, t);
       else if (t.type == kFA || t.type == kAR) ok = consume_rowsums<E>(a, L, it, slot, t);
       else if (t.type == kFR) ok = consume_fr<E>(a, L, it, slot, t);
@@ -1863,6 +1934,9 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.q_at_d = s.q_at_d;
   a.p_at_d = s.p_at_d;
   a.counters = s.counters;
+  a.thr_t = s.thr_t;
+  a.thr_d = s.thr_d;
+  a.masked = (s.thr_t || s.thr_d) ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(s.stream);
   if (cudaMemsetAsync(s.workspace, 0, wl.zero_bytes, st) != cudaSuccess) return SPEC_ECUDA;
   const size_t smem = sample_smem_bytes(2 * s.K);

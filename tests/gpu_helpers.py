@@ -47,7 +47,8 @@ def dev_case(case: synth.VerifyCase) -> dict:
     return d
 
 
-def run_sample(sv, case: synth.VerifyCase, dev: dict | None = None, temperature=None) -> dict:
+def run_sample(sv, case: synth.VerifyCase, dev: dict | None = None, temperature=None,
+               **kw) -> dict:
     import torch
     dev = dev or dev_case(case)
     B, K = case.B, case.K
@@ -59,7 +60,7 @@ def run_sample(sv, case: synth.VerifyCase, dev: dict | None = None, temperature=
     qd = torch.zeros((B, K), dtype=torch.float32, device="cuda")
     pd = torch.zeros((B, K), dtype=torch.float32, device="cuda")
     sv.spec_verify_sample(dev["target"], dev["draft"], dev["tokens"], dev["uniforms"], T, out, n,
-                          err_flag=err, row_info=info, q_at_d=qd, p_at_d=pd)
+                          err_flag=err, row_info=info, q_at_d=qd, p_at_d=pd, **kw)
     torch.cuda.synchronize()
     return dict(out_tokens=out.cpu().numpy(), num_accepted=n.cpu().numpy(),
                 row_info=info.cpu().numpy(), err=int(err.item()), q_at_d=qd.cpu().numpy(),
