@@ -55,9 +55,9 @@ __host__ __device__ inline int slices_for(int nvec, int B) {
 // ------------------------------------------------------------------ workspace
 struct WsHeader {           // zeroed by the host before every launch
   uint32_t p1_next;         // next first-stage task
+  uint32_t dq_tail;         // queue reservations
+  uint32_t dq_head;         // queue tickets handed out
   uint32_t rows_done;       // rows whose outputs are written
-  uint32_t dq_tail;         // queue reservations (8-byte aligned: read together
-  uint32_t dq_head;         // queue tickets handed out   with dq_head)
   uint32_t abort;           // set on any timeout or overflow
   uint32_t pad[3];
 };
@@ -168,78 +168,44 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
-// The producer's task source. Queued tasks are claimed by ticket: a
-// producer takes one ticket (dq_head, one atomicAdd, no compare-and-swap
+// The producer's task source. Queued tasks are claimed by ticket: every
+// producer holds one ticket (dq_head, one atomicAdd, no compare-and-swap
 // retries, which serialise hundreds of producers on one word) and runs the
-// queue entry of that number once it is written. A ticket pins a future
-// entry to its holder, so while first-stage tasks remain a producer takes a
-// ticket only at a task boundary and only if the queue held unclaimed
-// entries when it last looked (peek(), one relaxed 8-byte load of dq_tail
-// and dq_head per issued stage, read one stage later); a queued task thus
-// waits for the next producer to reach a boundary, not for a chosen one to
-// finish a long first-stage task. Once the first-stage tasks are all
-// reserved, an idle producer holds a ticket and polls its entry. A ticket
-// whose entry never comes is dropped when every row is done. First-stage
-// tasks are reserved one at a time (p1_next), one task ahead (prepare(),
-// called once the first stage of a task is issued, without waiting).
-// Entries are read with relaxed loads and acquired with a fence once seen.
+// queue entry of that number once it is written. Tickets run ahead of the
+// queue; a ticket whose entry never comes is dropped when every row is done.
+// First-stage tasks are reserved one at a time (p1_next).
+//
+// The round trips are pipelined behind the streaming: prepare(), called once
+// the first stage of a task is issued, takes the next ticket, loads the held
+// ticket's entry and reserves the next first-stage task, all without waiting;
+// next(), called at the task boundary, uses what prepare() found. Only when
+// nothing was prepared does next() wait on memory itself. Entries are read
+// with relaxed loads and acquired with a fence once seen.
 struct Fetcher {
   static constexpr uint32_t kNone = 0xffffffffu;
-  int64_t ticket = -1;    // held queue ticket
-  uint64_t word = 0;      // its entry as last loaded (0: not written yet)
-  uint32_t kres = kNone;  // reserved first-stage index
+  int64_t ticket = -1;   // held queue ticket
+  uint64_t word = 0;     // its entry as last loaded (0: not written yet)
+  uint32_t kres = kNone; // reserved first-stage index
   bool first_left = true;
-  uint64_t pend = 0;      // dq_tail | dq_head << 32, load in flight
-  uint64_t seen = 0;      // the previous stage's load (complete)
 
   __device__ __forceinline__ void prepare(const Ws& ws) {
     WsHeader* h = ws.hdr();
-    if (ticket < 0 && !first_left) ticket = int64_t(atomicAdd(&h->dq_head, 1u));
-    else if (ticket >= 0 && word == 0 && ticket < int64_t(ws.L.qcap))
-      word = ld_relaxed_u64(&ws.entries()[ticket]);
+    if (ticket < 0) ticket = int64_t(atomicAdd(&h->dq_head, 1u));
+    else if (word == 0 && ticket < int64_t(ws.L.qcap)) word = ld_relaxed_u64(&ws.entries()[ticket]);
     if (kres == kNone && first_left) kres = atomicAdd(&h->p1_next, 1u);
-  }
-
-  // Called after each issued stage: keeps the queue counters one stage fresh.
-  __device__ __forceinline__ void peek(const Ws& ws) {
-    seen = pend;
-    pend = ld_relaxed_u64(reinterpret_cast<const uint64_t*>(&ws.hdr()->dq_tail));
   }
 
   // 1: task in t; 0: nothing runnable now; the caller backs off and retries.
   __device__ __forceinline__ int next(const Ws& ws, int first_type, QTask& t) {
     WsHeader* h = ws.hdr();
     const uint32_t total = uint32_t(ws.L.B) * uint32_t(ws.L.S);
-    const int64_t qcap = int64_t(ws.L.qcap);
     for (int pass = 0; pass < 2; ++pass) {
-      if (ticket >= 0 && word == 0 && pass == 1 && ticket < qcap)
-        word = ld_relaxed_u64(&ws.entries()[ticket]);
       if (ticket >= 0 && word != 0) {
         fence_acq_rel_gpu();
         t = unpack_task(word);
         ticket = -1;
         word = 0;
         return 1;
-      }
-      const uint32_t tail = uint32_t(seen), head = uint32_t(seen >> 32);
-      if (ticket < 0 && (tail > head || !first_left)) {
-        ticket = int64_t(atomicAdd(&h->dq_head, 1u));
-        seen = 0;
-        if (ticket < qcap) {
-          word = ld_relaxed_u64(&ws.entries()[ticket]);
-          // an entry below the seen tail is written within microseconds
-          if (word == 0 && ticket < int64_t(tail)) {
-            const uint64_t t0 = global_ns();
-            while (word == 0 && global_ns() - t0 < 4000) word = ld_relaxed_u64(&ws.entries()[ticket]);
-          }
-        }
-        if (word != 0) {
-          fence_acq_rel_gpu();
-          t = unpack_task(word);
-          ticket = -1;
-          word = 0;
-          return 1;
-        }
       }
       if (kres != kNone) {
         const uint32_t k = kres;
@@ -251,7 +217,10 @@ struct Fetcher {
         first_left = false;
       }
       if (pass == 1) break;
-      if (first_left) kres = atomicAdd(&h->p1_next, 1u);
+      // nothing prepared: fetch now
+      if (ticket < 0) ticket = int64_t(atomicAdd(&h->dq_head, 1u));
+      if (ticket < int64_t(ws.L.qcap)) word = ld_relaxed_u64(&ws.entries()[ticket]);
+      if (word == 0 && first_left) kres = atomicAdd(&h->p1_next, 1u);
     }
     return 0;
   }
@@ -356,10 +325,10 @@ __device__ __forceinline__ bool claim_stage(const Ring& ring, uint32_t it) {
 // `after_first` runs once the first stage is issued: the producer fetches its
 // next task there, so the fetch's memory round trips overlap the streaming
 // instead of leaving the ring to drain between tasks.
-template <class AfterFirst, class EachStage>
+template <class AfterFirst>
 __device__ inline bool produce_task(const Ring& ring, uint32_t& it, uint32_t& nt, const QTask& t,
                                     const char* const* rows, int nrows, bool paired, int v0,
-                                    int v1, AfterFirst&& after_first, EachStage&& each_stage) {
+                                    int v1, AfterFirst&& after_first) {
   // The table entry of task nt is reused by task nt + kStages; it is written
   // only once the task's first stage is claimed, i.e. after every consumer
   // warp released the stage kStages earlier and so has read the entry of every
@@ -398,7 +367,6 @@ __device__ inline bool produce_task(const Ring& ring, uint32_t& it, uint32_t& nt
       bulk_g2s(dst, rows[r] + size_t(c0) * 16, bytes, &ring.full[stage]);
     }
     if (q == 0) after_first();
-    each_stage();
   }
   return true;
 }

@@ -386,8 +386,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
           rows[nrows++] = reinterpret_cast<const char*>(tgt + size_t(K) * a.V);
         }
         auto prefetch = [&]() { fx.prepare(a.ws); };
-        auto peek = [&]() { fx.peek(a.ws); };
-        if (!produce_task(L.ring, it, nt, t, rows, nrows, false, v0, v1, prefetch, peek)) break;
+        if (!produce_task(L.ring, it, nt, t, rows, nrows, false, v0, v1, prefetch)) break;
       }
       produce_end(L.ring, it);
     }

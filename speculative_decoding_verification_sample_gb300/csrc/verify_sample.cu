@@ -100,6 +100,13 @@ __device__ __forceinline__ float thr_of(const SampleArgs& a, int b, bool target,
   if (!t) return -INFINITY;
   return __ldg(t + size_t(b) * (target ? a.K + 1 : a.K) + i);
 }
+// Element traits plus whether the launch filters (a separate instantiation,
+// so an unfiltered launch carries no compare).
+template <class E0, bool M>
+struct EM : E0 {
+  static constexpr bool kMask = M;
+};
+
 template <int N>
 __device__ __forceinline__ void mask_vals(float (&z)[N], float tau) {
 #pragma unroll
@@ -230,7 +237,7 @@ __device__ inline Smem make_smem(uint8_t* base, int R) {
 template <class E>
 struct StatOp {
   float c, M, Kc, S, tau;
-  int bad, masked;
+  int bad;
   __device__ __forceinline__ void begin() {
     M = -INFINITY;
     Kc = -INFINITY;
@@ -267,7 +274,7 @@ struct StatOp {
       if (tid + k * kCons < cnt) {
         float z[E::kVec];
         E::unpack(v[k], z);
-        if (masked) mask_vals(z, tau);
+        if (E::kMask) mask_vals(z, tau);
         float e[E::kVec];
 #pragma unroll
         for (int j = 0; j < E::kVec; ++j) e[j] = ex2_approx(__fmaf_rn(z[j], c, -Kc));
@@ -330,14 +337,13 @@ struct FastEntries {
   const uint4* tp;
   bool pair;        // residual q - p (else q alone)
   float c, Kq, Rq, Kp, Rp;
-  bool masked = false;
   float tauq = -INFINITY, taup = -INFINITY;
   __device__ __forceinline__ float run(const uint4& vq, const uint4& vp, float (&r)[E::kVec],
                                        float& aq, float& ap) const {
     float zq[E::kVec], zp[E::kVec];
     E::unpack(vq, zq);
     if (pair) E::unpack(vp, zp);
-    if (masked) {
+    if (E::kMask) {
       mask_vals(zq, tauq);
       if (pair) mask_vals(zp, taup);
     }
@@ -386,14 +392,13 @@ struct AccEntries {
   df Iq, Ip;
   const float* th;
   const float* tl;
-  bool masked = false;
   float tauq = -INFINITY, taup = -INFINITY;
   __device__ __forceinline__ df run(const uint4& vq, const uint4& vp, df (&r)[E::kVec], float& qs,
                                     float& ps) const {
     float zq[E::kVec], zp[E::kVec];
     E::unpack(vq, zq);
     if (pair) E::unpack(vp, zp);
-    if (masked) {
+    if (E::kMask) {
       mask_vals(zq, tauq);
       if (pair) mask_vals(zp, taup);
     }
@@ -679,7 +684,7 @@ __device__ void finish_p1(const SampleArgs& a, const Smem& L, int b) {
   if (lane < K && !badtok_lane) {
     zt = E::load(rp.tgt + size_t(lane) * V, d);
     zd = E::load(rp.drf + size_t(lane) * V, d);
-    if (a.masked) {
+    if (E::kMask) {
       if (!(zt >= thr_of(a, b, true, lane))) zt = -INFINITY;
       if (!(zd >= thr_of(a, b, false, lane))) zd = -INFINITY;
     }
@@ -768,7 +773,7 @@ __device__ void finish_ar(const SampleArgs& a, const Smem& L, int b, int aux) {
   const int di = __shfl_sync(0xffffffffu, d, i);
   float zt = E::load(rp.tgt + size_t(i) * a.V, di);
   float zd = E::load(rp.drf + size_t(i) * a.V, di);
-  if (a.masked) {
+  if (E::kMask) {
     if (!(zt >= thr_of(a, b, true, i))) zt = -INFINITY;
     if (!(zd >= thr_of(a, b, false, i))) zd = -INFINITY;
   }
@@ -1038,7 +1043,6 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
     fe.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
     fe.pair = dr.pair;
     fe.c = a.c;
-    fe.masked = a.masked;
     fe.tauq = thr_of(a, b, true, dr.j);
     fe.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
     fe.Kq = Kq;
@@ -1167,7 +1171,6 @@ __device__ void finish_fb(const SampleArgs& a, const Smem& L, int b, int aux) {
     ae.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
     ae.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
     ae.pair = dr.pair;
-    ae.masked = a.masked;
     ae.tauq = thr_of(a, b, true, dr.j);
     ae.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
     ae.Chi = a.Chi;
@@ -1280,13 +1283,12 @@ __device__ bool consume_stats(const SampleArgs& a, const Smem& L, uint32_t& it, 
   const int tid = threadIdx.x;
   StatOp<E> op;
   op.c = a.c;
-  op.masked = a.masked;
   op.tau = -INFINITY;
   op.begin();
   for (;;) {
     const ChunkMeta m = L.ring.meta[it % kStages];
     // P1 rows: target i = 2i, draft i = 2i + 1; BS: target row K
-    if (a.masked)
+    if (E::kMask)
       op.tau = (t.type == kBS) ? thr_of(a, t.b, true, a.K) : thr_of(a, t.b, (m.r & 1) == 0, m.r >> 1);
     op.chunk(stage_data(L.ring, it), m.c1 - m.c0, tid);
     release_stage(L.ring, it);
@@ -1327,7 +1329,6 @@ __device__ bool consume_sw(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   fe.tp = nullptr;
   fe.pair = dr.pair;
   fe.c = a.c;
-  fe.masked = a.masked;
   fe.tauq = thr_of(a, t.b, true, dr.j);
   fe.taup = dr.pair ? thr_of(a, t.b, false, dr.j) : -INFINITY;
   fe.Kq = __ldcg(&st->Kq);
@@ -1428,7 +1429,7 @@ __device__ bool consume_rowsums(const SampleArgs& a, const Smem& L, uint32_t& it
     for (int i = tid; i < m.c1 - m.c0; i += kCons) {
       float z[E::kVec];
       E::unpack(buf[i], z);
-      if (a.masked) mask_vals(z, tau);
+      if (E::kMask) mask_vals(z, tau);
 #pragma unroll
       for (int k = 0; k < E::kVec; ++k)
         acc = df_add(acc, acc_elem(z[k], a.Chi, a.Clo, Kr, L.tab_hi, L.tab_lo));
@@ -1464,7 +1465,6 @@ __device__ bool consume_fb(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   ae.tq = nullptr;  // the sweep reads the ring stages
   ae.tp = nullptr;
   ae.pair = dr.pair;
-  ae.masked = a.masked;
   ae.tauq = thr_of(a, t.b, true, dr.j);
   ae.taup = dr.pair ? thr_of(a, t.b, false, dr.j) : -INFINITY;
   ae.Chi = a.Chi;
@@ -1552,7 +1552,7 @@ __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uin
         float zq[E::kVec], zp[E::kVec];
         E::unpack(bq[i], zq);
         if (dr.pair) E::unpack(bp[i], zp);
-        if (a.masked) {
+        if (E::kMask) {
           mask_vals(zq, tauq);
           if (dr.pair) mask_vals(zp, taup);
         }
@@ -1710,7 +1710,6 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
     ae.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
     ae.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
     ae.pair = dr.pair;
-    ae.masked = a.masked;
     ae.tauq = thr_of(a, b, true, dr.j);
     ae.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
     ae.Chi = a.Chi;
@@ -1783,8 +1782,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
           }
         }
         auto prefetch = [&]() { fx.prepare(a.ws); };
-        auto peek = [&]() { fx.peek(a.ws); };
-        if (!produce_task(L.ring, it, nt, t, rows, nrows, paired, v0, v1, prefetch, peek)) break;
+        if (!produce_task(L.ring, it, nt, t, rows, nrows, paired, v0, v1, prefetch)) break;
       }
       produce_end(L.ring, it);
     }
@@ -1940,8 +1938,13 @@ int launch_verify_sample(const SampleLaunch& s) {
   cudaStream_t st = static_cast<cudaStream_t>(s.stream);
   if (cudaMemsetAsync(s.workspace, 0, wl.zero_bytes, st) != cudaSuccess) return SPEC_ECUDA;
   const size_t smem = sample_smem_bytes(2 * s.K);
-  if (s.dtype == SPEC_BF16) return launch_dataflow(verify_sample_kernel<EBf16>, a, smem, st);
-  return launch_dataflow(verify_sample_kernel<EF32>, a, smem, st);
+  if (a.masked) {
+    if (s.dtype == SPEC_BF16)
+      return launch_dataflow(verify_sample_kernel<EM<EBf16, true>>, a, smem, st);
+    return launch_dataflow(verify_sample_kernel<EM<EF32, true>>, a, smem, st);
+  }
+  if (s.dtype == SPEC_BF16) return launch_dataflow(verify_sample_kernel<EM<EBf16, false>>, a, smem, st);
+  return launch_dataflow(verify_sample_kernel<EM<EF32, false>>, a, smem, st);
 }
 
 }  // namespace sv
