@@ -202,6 +202,47 @@ def tree_greedy_stats(torch, sv, peak, reps=50):
             "mean_accepted": float(n.float().mean().item())}
 
 
+def filter_stats(torch, sv, bt, T, peak, reps=10, top_k=50, top_p=0.95):
+    """spec_filter_thresholds (top-k 50, top-p 0.95) on one bench batch: the
+    target [B, K+1, V] and draft [B, K, V] bf16 tensors (700 MB of logits per
+    read), then spec_verify_sample with those thresholds. Mean device
+    times; algorithmic bytes of the filter = every logit read once."""
+    w = WORKLOAD
+    B, K, V = w["B"], w["K"], w["V"]
+    tt = torch.empty((B, K + 1), dtype=torch.float32, device="cuda")
+    td = torch.empty((B, K), dtype=torch.float32, device="cuda")
+    out = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
+    n = torch.empty((B,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def filt():
+        sv.spec_filter_thresholds(bt["target"], T, top_k, top_p, tt)
+        sv.spec_filter_thresholds(bt["draft"], T, top_k, top_p, td)
+
+    def ver():
+        sv.spec_verify_sample(bt["target"], bt["draft"], bt["tokens"], bt["uniforms"], T, out, n,
+                              target_threshold=tt, draft_threshold=td)
+
+    res = {}
+    for name, fn in (("filter", filt), ("verify_filtered", ver)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res[name + "_us"] = 1e3 * e0.elapsed_time(e1) / reps
+    alg = B * (2 * K + 1) * V * 2
+    res["filter_algorithmic_bytes"] = alg
+    res["filter_gbs"] = alg / (res["filter_us"] / 1e6) / 1e9
+    res["filter_frac_of_measured_peak"] = res["filter_gbs"] / peak
+    res["top_k"], res["top_p"] = top_k, top_p
+    return res
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -496,6 +537,8 @@ def main():
                       "kv_commit_inplace_us": (inplace_kv_us(torch, sv, na_list[0][0])
                                                if a.mode == "step" else None),
                       "tree_greedy": (tree_greedy_stats(torch, sv, peak)
+                                      if a.mode == "step" else None),
+                      "top_k_top_p": (filter_stats(torch, sv, batches[0], T, peak)
                                       if a.mode == "step" else None),
                       "kv_bytes_per_step": kvb, "refined_row_fraction": refined,
                       "mean_accepted": float(np.mean([x[0].mean() for x in na_list])),

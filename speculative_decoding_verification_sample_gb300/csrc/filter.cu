@@ -34,7 +34,9 @@
 namespace sv {
 namespace {
 
-constexpr int kFT = 256;  // threads per CTA, one row per CTA
+constexpr int kFT = 256;      // threads per CTA, one row per CTA
+constexpr int kFTAcc = 1024;  // the double-float rerun of the few uncertain rows
+constexpr int kCand = 8;      // top-digit bins a one-pass top-p search may span
 
 // Order-preserving keys: larger key <=> larger value (NaN excluded).
 template <class E>
@@ -71,6 +73,17 @@ struct FilterArgs {
   int32_t* err;
 };
 
+// Nonnegative float (below 2^62) to a fixed-point integer, within 1 of its
+// value: the significand shifted by the exponent (plain integer operations,
+// no conversion instruction).
+__device__ __forceinline__ unsigned long long to_fixed(float f) {
+  const uint32_t b = __float_as_uint(f);
+  const int e = int(b >> 23) - 127;
+  if (e < 0) return f >= 0.5f ? 1ull : 0ull;
+  const unsigned long long m = (b & 0x7fffffu) | 0x800000u;
+  return e >= 23 ? (m << (e - 23)) : (m >> (23 - e));
+}
+
 // Certification slack of one histogram bin's mass (fixed-point units): the
 // relative error of each token's mass there is at most ex2 + ln2 u (2|x| + 2)
 // with |x| <= xmax (argument and temperature-constant rounding; the part of
@@ -82,25 +95,37 @@ __device__ __forceinline__ double bin_err(unsigned long long m, float eps, float
 }
 
 template <class E, bool kAcc>
-__global__ void __launch_bounds__(kFT) filter_kernel(const FilterArgs a) {
+__global__ void __launch_bounds__(kAcc ? kFTAcc : kFT) filter_kernel(const FilterArgs a) {
   using KO = KeyOf<E>;
+  constexpr int NT = kAcc ? kFTAcc : kFT;
   constexpr int KB = KO::kBits, ND = KB / 8;
   __shared__ uint32_t hcnt[256];
   __shared__ unsigned long long hmass[256];
   __shared__ unsigned long long hbuck[256];
-  __shared__ uint32_t s_u[kFT / 32];
-  __shared__ int s_i[kFT / 32];
+  __shared__ uint32_t s_u[NT / 32];
+  __shared__ int s_i[NT / 32];
   __shared__ uint32_t s_need, s_digit;
   __shared__ unsigned long long s_A, s_mb, s_Z;
   __shared__ double s_EA, s_EZ;
+  __shared__ unsigned long long s_red[NT / 32], s_ztot;
+  __shared__ uint32_t s_floor, s_bl, s_bh, s_pre16;
+  __shared__ int s_cand;
+  __shared__ unsigned long long hwarp[NT / 32][256];  // per-warp level-0 masses
+  __shared__ float s_th[kAcc ? 256 : 1], s_tl[kAcc ? 256 : 1];
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (kAcc && !isnan(a.out[row])) return;  // second launch: uncertain rows only
+  if (kAcc) {
+    for (int i = tid; i < 256; i += NT) {
+      s_th[i] = kExp2Tab.hi[i];
+      s_tl[i] = kExp2Tab.lo[i];
+    }
+  }
   const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const char*>(a.logits) +
                                                    size_t(row) * size_t(a.V) * sizeof(typename E::T));
   const bool topk = a.top_k > 0 && a.top_k < a.V;
   const bool topp = a.top_p < 1.0f;
   auto sweep = [&](auto&& f) {
-    for (int i = tid; i < a.nvec; i += kFT) {
+    for (int i = tid; i < a.nvec; i += NT) {
       float z[E::kVec];
       E::unpack(ldg_nc_v4(rp + i), z);
 #pragma unroll
@@ -108,7 +133,7 @@ __global__ void __launch_bounds__(kFT) filter_kernel(const FilterArgs a) {
     }
   };
   auto clear = [&]() {
-    for (int i = tid; i < 256; i += kFT) {
+    for (int i = tid; i < 256; i += NT) {
       hcnt[i] = 0;
       hmass[i] = 0;
       hbuck[i] = 0;
@@ -126,7 +151,7 @@ __global__ void __launch_bounds__(kFT) filter_kernel(const FilterArgs a) {
     }
     const uint32_t k = KO::key(z);
     mk = max(mk, k);
-    if (topk) atomicAdd(&hcnt[k >> (KB - 8)], 1u);
+    if (topk || topp) atomicAdd(&hcnt[k >> (KB - 8)], 1u);
   });
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -141,7 +166,7 @@ __global__ void __launch_bounds__(kFT) filter_kernel(const FilterArgs a) {
   if (tid == 0) {
     uint32_t m = 0;
     int n = 0;
-    for (int w = 0; w < kFT / 32; ++w) {
+    for (int w = 0; w < NT / 32; ++w) {
       m = max(m, s_u[w]);
       n |= s_i[w];
     }
@@ -169,14 +194,13 @@ __global__ void __launch_bounds__(kFT) filter_kernel(const FilterArgs a) {
       const df p = two_prod(z, a.Chi);
       const float pl = __fmaf_rn(z, a.Clo, p.lo);
       const df s = two_sum(p.hi, -Kc);
-      // the double-float exponential reads its 2^(j/256) table from constant
-      // memory (this kernel keeps no shared copy)
-      const df w = df_exp2(s.hi, __fadd_rn(s.lo, pl), kExp2Tab.hi, kExp2Tab.lo);
-      const long long lo = __float2ll_rn(__fmul_rn(w.lo, a.fixscale));
-      return static_cast<unsigned long long>(
-          static_cast<long long>(__float2ull_rn(__fmul_rn(w.hi, a.fixscale))) + lo);
+      const df w = df_exp2(s.hi, __fadd_rn(s.lo, pl), s_th, s_tl);
+      const float l = __fmul_rn(w.lo, a.fixscale);
+      const unsigned long long h = to_fixed(__fmul_rn(w.hi, a.fixscale));
+      const unsigned long long lm = to_fixed(fabsf(l));
+      return l >= 0.0f ? h + lm : h - lm;
     }
-    return __float2ull_rn(__fmul_rn(ex2_approx(__fmaf_rn(z, a.c, -Kc)), a.fixscale));
+    return to_fixed(__fmul_rn(ex2_approx(__fmaf_rn(z, a.c, -Kc)), a.fixscale));
   };
   const float eps = kAcc ? 2e-12f + 2.2e-14f * (fabsf(Kc) + 256.0f) : a.ex2;
   // |x| bound of the tokens in the key range starting at key k0
@@ -242,20 +266,150 @@ __global__ void __launch_bounds__(kFT) filter_kernel(const FilterArgs a) {
         for (int d = 0; d < int(KA & 255u); ++d) hbuck[d] = 0;  // below KA: not kept
       }
     } else {
-      clear();
+      // the row total Z, summed per thread (no atomics)
+      unsigned long long zt = 0;
+      sweep([&](float z) { zt += mass(z); });
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) zt += __shfl_xor_sync(0xffffffffu, zt, o);
+      if (lane == 0) s_red[warp] = zt;
       __syncthreads();
-      sweep([&](float z) {
-        const unsigned long long q = mass(z);
-        if (q) atomicAdd(&hmass[KO::key(z) >> (KB - 8)], q);
-      });
+      if (tid == 0) {
+        unsigned long long Z = 0;
+        for (int w = 0; w < NT / 32; ++w) Z += s_red[w];
+        s_ztot = Z;
+        // Candidate top-digit bins of t*: per bin, count x (mass of its
+        // highest key) bounds the bin's mass from above and count x (mass of
+        // its lowest key) from below; t*'s bin b* has mass(bins > b*) < p Z <=
+        // mass(bins >= b*), so it lies in [bl, bh]: bh the highest bin whose
+        // upper-bounded mass from the top reaches p Z, bl the lowest whose
+        // lower-bounded mass strictly above stays below p Z.
+        const double pZ = double(a.top_p) * double(Z);
+        double ub = 0.0, lbab = 0.0, ez = 0.0, ea = 0.0;
+        int bh = -1, bl = -1;
+        for (int b = 255; b >= 0; --b) {
+          const uint32_t k0 = uint32_t(b) << (KB - 8), k1 = k0 | ((1u << (KB - 8)) - 1u);
+          const float zh = KO::value(k1), zl = KO::value(k0);
+          const float wh = (zh == zh) ? ex2_approx(fminf(__fmaf_rn(zh, a.c, -Kc), 1.0f)) : 0.0f;
+          const float wl = (zl == zl) ? ex2_approx(fminf(__fmaf_rn(zl, a.c, -Kc), 1.0f)) : 0.0f;
+          const double n = double(hcnt[b]);
+          const double mhi = n * (double(wh) * 1.01 * double(a.fixscale) + 1.0);
+          const double mlo = n * fmax(0.0, double(wl) * 0.99 * double(a.fixscale) - 1.0);
+          const double e = bin_err(1, eps, xmax_from(k0)) * mhi;
+          ez += e;
+          if (lbab < pZ) bl = b;      // mass strictly above b may still be short of p Z
+          ub += mhi;
+          if (bh < 0) {
+            if (ub >= pZ) bh = b;
+            else ea += e;              // bins above bh: summed in registers
+          }
+          lbab += mlo;
+        }
+        const bool ok = bh >= 0 && bl >= 0 && bl <= bh && bh - bl < kCand;
+        s_cand = ok ? 1 : 0;
+        s_bl = uint32_t(bl);
+        s_bh = uint32_t(bh);
+        s_EZ = ez;
+        s_EA = ea;
+        // floor bin for the fallback: the bins below it hold at most
+        // count x (mass of the bin's highest key) < (1 - p) Z / 2 in total
+        const double budget = 0.5 * (1.0 - double(a.top_p)) * double(Z);
+        double below = 0.0;
+        uint32_t fb = 0;
+        for (uint32_t b = 0; b < 256; ++b) {
+          const uint32_t khi = (b << (KB - 8)) | ((1u << (KB - 8)) - 1u);
+          const float zhi = KO::value(khi);
+          const float w = (zhi == zhi) ? ex2_approx(fminf(__fmaf_rn(zhi, a.c, -Kc), 1.0f)) : 0.0f;
+          below += double(hcnt[b]) * (double(w) * 1.01 * double(a.fixscale) + 1.0);
+          if (below >= budget) break;
+          fb = b + 1;
+        }
+        s_floor = fb;
+      }
+      __syncthreads();
+      if (s_cand) {
+        // one pass: tokens above bh summed per thread, tokens in [bl, bh]
+        // into a histogram of (top digit, second digit)
+        const uint32_t bl = s_bl, bh = s_bh;
+        unsigned long long* hsub = &hwarp[0][0];
+        for (int i = tid; i < kCand * 256; i += NT) hsub[i] = 0;
+        __syncthreads();
+        unsigned long long ra = 0;
+        sweep([&](float z) {
+          const uint32_t k = KO::key(z), tb = k >> (KB - 8);
+          if (tb > bh) {
+            ra += mass(z);
+          } else if (tb >= bl) {
+            const unsigned long long q = mass(z);
+            if (q) atomicAdd(&hsub[(tb - bl) * 256u + ((k >> (KB - 16)) & 255u)], q);
+          }
+        });
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ra += __shfl_xor_sync(0xffffffffu, ra, o);
+        if (lane == 0) s_red[warp] = ra;
+        __syncthreads();
+        if (tid == 0) {
+          unsigned long long A = 0;
+          for (int w = 0; w < NT / 32; ++w) A += s_red[w];
+          const double target = double(a.top_p) * double(s_ztot);
+          double EA = s_EA;
+          uint32_t key16 = 0;
+          unsigned long long mb = 0;
+          bool found = false;
+          for (int tb = int(bh); tb >= int(bl) && !found; --tb) {
+            for (int d = 255; d >= 0; --d) {
+              const unsigned long long m = hsub[(tb - int(bl)) * 256 + d];
+              const uint32_t k16 = (uint32_t(tb) << 8) | uint32_t(d);
+              if (double(A + m) >= target) {
+                key16 = k16;
+                mb = m;
+                found = true;
+                break;
+              }
+              A += m;
+              EA += bin_err(m, eps, xmax_from(k16 << (KB - 16)));
+            }
+          }
+          s_pre16 = key16;
+          s_A = A;
+          s_EA = EA;
+          s_mb = mb;
+          s_Z = s_ztot;
+        }
+        __syncthreads();
+      } else {
+        const uint32_t fb = s_floor;
+        clear();
+        for (int i = tid; i < (NT / 32) * 256; i += NT) (&hwarp[0][0])[i] = 0;
+        __syncthreads();
+        // a private histogram per warp: the few hot bins are not shared by
+        // all warps' atomics
+        sweep([&](float z) {
+          const uint32_t k = KO::key(z);
+          if ((k >> (KB - 8)) >= fb) {
+            const unsigned long long q = mass(z);
+            if (q) atomicAdd(&hwarp[warp][k >> (KB - 8)], q);
+          }
+        });
+        __syncthreads();
+        for (int b = tid; b < 256; b += NT) {
+          unsigned long long m = 0;
+          for (int w = 0; w < NT / 32; ++w) m += hwarp[w][b];
+          hmass[b] = m;
+        }
+      }
     }
     __syncthreads();
-    if (tid == 0) {
+    const bool cand = !topk && s_cand;
+    if (tid == 0 && !cand) {
       unsigned long long Z = 0;
       double EZ = 0.0;
       for (int b = 0; b < 256; ++b) {
         Z += hmass[b];
         EZ += bin_err(hmass[b], eps, xmax_from(uint32_t(b) << (KB - 8)));
+      }
+      if (!topk) {  // the bins below the floor: in the total, not in the histogram
+        EZ += bin_err(s_ztot - Z, eps, 200.0f);
+        Z = s_ztot;
       }
       s_Z = Z;
       s_EZ = EZ;
@@ -264,24 +418,30 @@ __global__ void __launch_bounds__(kFT) filter_kernel(const FilterArgs a) {
     }
     __syncthreads();
     const double target = double(a.top_p) * double(s_Z);
-    uint32_t pre = 0;
-    for (int lvl = 0; lvl < ND; ++lvl) {
+    uint32_t pre = cand ? s_pre16 : 0;
+    for (int lvl = cand ? 2 : 0; lvl < ND; ++lvl) {
       const int sh = KB - 8 * (lvl + 1);
       if (lvl > 0) {
         const bool reuse = topk && lvl == ND - 1 && pre == (KA >> 8);
         __syncthreads();
         if (reuse) {
-          for (int i = tid; i < 256; i += kFT) hmass[i] = hbuck[i];
+          for (int i = tid; i < 256; i += NT) hmass[i] = hbuck[i];
         } else {
-          for (int i = tid; i < 256; i += kFT) hmass[i] = 0;
+          for (int i = tid; i < (NT / 32) * 256; i += NT) (&hwarp[0][0])[i] = 0;
           __syncthreads();
           sweep([&](float z) {
             const uint32_t k = KO::key(z);
             if (k >= KA && (k >> (sh + 8)) == pre) {
               const unsigned long long q = mass(z);
-              if (q) atomicAdd(&hmass[(k >> sh) & 255u], q);
+              if (q) atomicAdd(&hwarp[warp][(k >> sh) & 255u], q);
             }
           });
+          __syncthreads();
+          for (int b = tid; b < 256; b += NT) {
+            unsigned long long m = 0;
+            for (int w = 0; w < NT / 32; ++w) m += hwarp[w][b];
+            hmass[b] = m;
+          }
         }
         __syncthreads();
       }
@@ -308,7 +468,7 @@ __global__ void __launch_bounds__(kFT) filter_kernel(const FilterArgs a) {
     if (tid == 0) {
       // certify: mass(keys >= K) >= p Z and mass(keys > K) < p Z hold exactly
       const double C = double(s_A + s_mb), Cm = double(s_A);
-      const double q = 0.5 * double(a.V) + 2.0;  // rounding to fixed point
+      const double q = 2.0 * double(a.V) + 2.0;  // rounding to fixed point
       const double EC = s_EA + bin_err(s_mb, eps, xmax_from(pre)) + q;
       const double ECm = s_EA + q;
       const double Zlo = double(s_Z) - s_EZ - q, Zhi = double(s_Z) + s_EZ + q;
@@ -346,10 +506,10 @@ int launch_filter(const FilterLaunch& f) {
   cudaStream_t st = static_cast<cudaStream_t>(f.stream);
   if (f.dtype == SPEC_BF16) {
     filter_kernel<EBf16, false><<<f.R, kFT, 0, st>>>(a);
-    if (f.top_p < 1.0f) filter_kernel<EBf16, true><<<f.R, kFT, 0, st>>>(a);
+    if (f.top_p < 1.0f) filter_kernel<EBf16, true><<<f.R, kFTAcc, 0, st>>>(a);
   } else {
     filter_kernel<EF32, false><<<f.R, kFT, 0, st>>>(a);
-    if (f.top_p < 1.0f) filter_kernel<EF32, true><<<f.R, kFT, 0, st>>>(a);
+    if (f.top_p < 1.0f) filter_kernel<EF32, true><<<f.R, kFTAcc, 0, st>>>(a);
   }
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
 }
