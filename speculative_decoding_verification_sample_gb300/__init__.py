@@ -398,3 +398,63 @@ def verify_host(target_logits, draft_logits, draft_tokens, uniforms, temperature
         out_h = out.to("cpu", non_blocking=False)
         n_h = n.to("cpu", non_blocking=False)
     return out_h, n_h
+
+
+class HostVerifier:
+    """End-to-end sampling verification of batches held in HOST memory (pinned).
+
+    The batch rows are copied to preallocated device buffers in `chunks` row
+    chunks on a copy stream; chunk c is verified (spec_verify_sample on its
+    rows) as soon as its copy lands, while the next chunk is still in flight,
+    so the verification hides behind the transfer. Outputs stay on the device
+    (`out_tokens`, `num_accepted`); `to_host` copies them into pinned host
+    tensors on the same stream.
+    """
+
+    def __init__(self, B: int, K: int, V: int, *, dtype=None, chunks: int = 8, device="cuda"):
+        import torch
+        dtype = dtype or torch.bfloat16
+        self.B, self.K, self.V = B, K, V
+        self.chunks = max(1, min(chunks, B))
+        d = torch.device(device)
+        self.target = torch.empty((B, K + 1, V), dtype=dtype, device=d)
+        self.draft = torch.empty((B, K, V), dtype=dtype, device=d)
+        self.tokens = torch.empty((B, K), dtype=torch.int32, device=d)
+        self.uniforms = torch.empty((B, K + 1), dtype=torch.float32, device=d)
+        self.out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=d)
+        self.num_accepted = torch.empty((B,), dtype=torch.int32, device=d)
+        self.copy_stream = torch.cuda.Stream(device=d)
+        self.events = [torch.cuda.Event() for _ in range(self.chunks)]
+        step = -(-B // self.chunks)
+        self.bounds = [(r0, min(B, r0 + step)) for r0 in range(0, B, step)]
+
+    def __call__(self, target_h, draft_h, tokens_h, uniforms_h, temperature: float, *,
+                 stream=None):
+        import torch
+        main = stream or torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(main)                      # earlier work on the buffers is ordered first
+        cs = self.copy_stream
+        cs.wait_event(start)
+        with torch.cuda.stream(cs):
+            for (r0, r1), ev in zip(self.bounds, self.events):
+                self.target[r0:r1].copy_(target_h[r0:r1], non_blocking=True)
+                self.draft[r0:r1].copy_(draft_h[r0:r1], non_blocking=True)
+                self.tokens[r0:r1].copy_(tokens_h[r0:r1], non_blocking=True)
+                self.uniforms[r0:r1].copy_(uniforms_h[r0:r1], non_blocking=True)
+                ev.record(cs)
+        for (r0, r1), ev in zip(self.bounds, self.events):
+            main.wait_event(ev)
+            spec_verify_sample(self.target[r0:r1], self.draft[r0:r1], self.tokens[r0:r1],
+                               self.uniforms[r0:r1], temperature, self.out_tokens[r0:r1],
+                               self.num_accepted[r0:r1], stream=main)
+        return self.out_tokens, self.num_accepted
+
+    def to_host(self, out_h, n_h, *, stream=None):
+        """Copies the outputs into host tensors (pinned for an asynchronous copy)."""
+        import torch
+        main = stream or torch.cuda.current_stream()
+        with torch.cuda.stream(main):
+            out_h.copy_(self.out_tokens, non_blocking=True)
+            n_h.copy_(self.num_accepted, non_blocking=True)
+
