@@ -201,9 +201,9 @@ def test_sample_full_size_sampled_rows(sv, T):
 @pytest.mark.parametrize("B,K,V,dtype", [
     (3, 1, 64, synth.BF16),          # K = 1
     (2, 31, 256, synth.F32),         # K = 31 (maximum), tiny V
-    (5, 3, 8, synth.BF16),           # V = one 16-byte vector: clusters shrink to 1 CTA
+    (5, 3, 8, synth.BF16),           # V = one 16-byte vector: one slice per row
     (4, 5, 32008, synth.BF16),       # ragged V: slices of unequal length
-    (3, 4, 1000, synth.F32),         # fp32, V not a multiple of the cluster split
+    (3, 4, 1000, synth.F32),         # fp32, V not a multiple of the slice split
     (7, 2, 4, synth.F32),            # V = 4
 ])
 def test_sample_shapes(sv, B, K, V, dtype):
@@ -216,13 +216,16 @@ def test_sample_shapes(sv, B, K, V, dtype):
     assert np.array_equal(gg["out_tokens"], og["out_tokens"])
 
 
-@pytest.mark.parametrize("csize", ["1", "2", "4", "8", "16"])
-def test_cluster_sizes_agree(sv, monkeypatch, csize):
-    monkeypatch.setenv("SPECVERIFY_CLUSTER", csize)
+@pytest.mark.parametrize("grid", ["1", "3", "37", "151"])
+def test_grid_sizes_agree(sv, monkeypatch, grid):
+    """The persistent grid capped at fewer CTAs (one CTA runs every task of
+    the launch) gives the same rows: no task depends on which or how many
+    CTAs run it."""
+    monkeypatch.setenv("SPECVERIFY_GRID", grid)
     c = synth.sampling_case(6, 3, 20000, temperature=0.7, target_std=3.0, draft_noise_std=0.5,
                             seed=5)
     g = gh.run_sample(sv, c)
-    gh.assert_sample_parity(g, oracle_sample(c), label=csize)
+    gh.assert_sample_parity(g, oracle_sample(c), label=grid)
     gg = gh.run_greedy(sv, c)
     assert np.array_equal(gg["out_tokens"], oracle_greedy(c)["out_tokens"])
 
