@@ -16,7 +16,6 @@ constexpr int kThreads = kCons + 64;   // + producer warp (bulk-copy issue) + fi
 constexpr int kStages = 3;             // ring depth (3 x 32 KB: two CTAs per SM)
 constexpr int kChunk = 32768;          // bytes per ring stage
 constexpr int kMaxK = 31;              // draft positions (fits a warp ballot)
-constexpr int kMaxRows = 2 * kMaxK + 1;
 
 constexpr float kU = 5.9604644775390625e-8f;  // fp32 unit roundoff 2^-24
 constexpr float kLn2f = 0.693147180559945309417232121458176568f;

@@ -133,8 +133,6 @@ struct Ws {
 };
 
 // ------------------------------------------------------------------ memory helpers
-__device__ __forceinline__ float ld_cg_f(const float* p) { return __ldcg(p); }
-__device__ __forceinline__ int ld_cg_i(const int* p) { return __ldcg(p); }
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }

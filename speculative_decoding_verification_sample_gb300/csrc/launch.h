@@ -87,6 +87,5 @@ size_t greedy_workspace_bytes(int B, int K, int V, int dtype);
 int launch_verify_greedy(const GreedyLaunch& g);
 int launch_kv_commit(const KvLaunch& k);
 int launch_kv_truncate(const KvTruncLaunch& k);
-int verify_cluster_size(int B, int V, int dtype);
 
 }  // namespace sv

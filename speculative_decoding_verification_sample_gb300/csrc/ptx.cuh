@@ -1,6 +1,6 @@
 // Thin inline-PTX helpers for sm_103a: mbarrier, 1-D bulk async copies
-// (global -> shared, completion counted on an mbarrier), named barriers, the
-// global timer and the MUFU exponential. Each wrapper is one PTX instruction
+// (global -> shared, completion counted on an mbarrier), the global timer,
+// the MUFU exponential and a streaming load. Each wrapper is one PTX instruction
 // (or a bounded loop around one) with its documented semantics.
 #pragma once
 #include <cstdint>
@@ -99,11 +99,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
           "r"(smem_u32(dst_smem)),
       "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
-}
-
-// Named barrier for a subset of the CTA's warps.
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ----------------------------------------------------------------- math
