@@ -79,7 +79,9 @@ extern "C" {
 
 /* ---- device error bits OR-ed into *err_flag ---- */
 #define SPEC_DERR_TOKEN 1        /* a draft token outside [0, V); that row's outputs are -1 */
-#define SPEC_DERR_LOGITS 2       /* a row needed by the step has NaN/+inf logits or only -inf */
+#define SPEC_DERR_LOGITS 2       /* a row needed by the step has NaN/+inf logits, only -inf, or
+                                    (sampling, top-p) a maximum logit m with
+                                    |m log2(e) / T| >= 2^18, beyond the exponent range */
 #define SPEC_DERR_BAD_ACCEPT 4   /* kv: num_accepted outside [0, K] */
 #define SPEC_DERR_BAD_LENGTH 8   /* kv: negative seq_len, or the row outgrows max_blocks */
 #define SPEC_DERR_NO_SPACE 16    /* kv: the free stack cannot supply every new block */
@@ -213,7 +215,8 @@ int spec_verify_tree_greedy(const void* target_logits, const int32_t* tree_paren
  *                 t at which the tokens with logit >= t reach probability p
  *                 (ties all kept)
  *   out_threshold [R] float: the row's threshold (keep z >= threshold); -inf when
- *                 nothing is filtered; +inf for a row with a NaN logit (its
+ *                 nothing is filtered; +inf for a row with a NaN logit, or with
+ *                 top-p a maximum logit out of range (see SPEC_DERR_LOGITS; its
  *                 verification then reports SPEC_DERR_LOGITS; the bit is also set here)
  *   err_flag      optional [1] int32, device error bits OR-ed in
  * Top-k is an exact integer selection. Top-p compares exactly summed fixed-point

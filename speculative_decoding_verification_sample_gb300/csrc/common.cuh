@@ -18,6 +18,10 @@ constexpr int kChunk = 32768;          // bytes per ring stage
 constexpr int kMaxK = 31;              // draft positions (fits a warp ballot)
 
 constexpr float kU = 5.9604644775390625e-8f;  // fp32 unit roundoff 2^-24
+// Largest row offset |ceil(max z * log2(e)/T)| (exclusive) that the sampling
+// and top-p paths accept: within it the double-float terms keep their error
+// bound; a row beyond it is reported as invalid logits.
+constexpr float kMaxOffset = 262144.0f;  // 2^18
 constexpr float kLn2f = 0.693147180559945309417232121458176568f;
 
 // max that returns NaN when either input is NaN (PTX max.NaN).

@@ -138,10 +138,13 @@ constexpr float kLn2Lo = static_cast<float>(kLn2d - 0.693147182464599609375);
 //   m + j/256 = round(256 xh) / 256, g = xh - (m + j/256) is exact because
 //   xh is a multiple of ulp(xh) <= 2^-16 (|xh| < 2^8), so is g, and |g| <= 2^-9;
 //   t = (g + xl) ln2 is formed as a float pair (error < 2^-46 |t|);
-//   exp(t) = 1 + t + t^2/2 + t^3/6 + t^4/24 with |t| < 1.36e-3: truncation
-//   < 3e-17, the t^2.. part (< 9.3e-7) evaluated in fp32 (error < 2.2e-13);
+//   exp(t) = 1 + t + t^2/2 + t^3/6 + t^4/24 with |t| < 1.37e-3 when |xl| <=
+//   2^-16 (a normalised pair, or a term below 2^7 in magnitude): truncation
+//   < 4e-17, the t^2.. part (< 9.4e-7) evaluated in fp32 (error < 2.3e-13);
 //   the product with the table pair adds < 2^-46.
-// Total relative error < kDfExpRelErr = 4e-13.
+// Total relative error < kDfExpRelErr = 4e-13 when |xl| <= 2^-16. A larger xl
+// (|t| <= ln2 (2^-9 + |xl|)) adds the truncation |t|^5/120 and an fp32 error
+// below 1.5 u t^2: the caller's budget takes them (see acc_rho).
 constexpr double kDfExpRelErr = 4e-13;
 
 __device__ __forceinline__ df df_exp2(float xh, float xl, const float* tab_hi,

@@ -188,6 +188,13 @@ __global__ void __launch_bounds__(kAcc ? kFTAcc : kFT) filter_kernel(const Filte
     return;
   }
   const float Kc = offset_of(maxv, a.c);
+  if (topp && !(fabsf(Kc) < kMaxOffset)) {  // max * log2(e)/T out of range (or +inf)
+    if (tid == 0) {
+      a.out[row] = INFINITY;
+      if (a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
+    }
+    return;
+  }
   // fixed-point mass of one token (0 for -inf)
   auto mass = [&](float z) -> unsigned long long {
     if (kAcc) {

@@ -315,10 +315,13 @@ __device__ __forceinline__ df acc_elem(float z, float Chi, float Clo, float Kc, 
 }
 
 // Relative error bound of one normalised double-float term, for a row whose
-// offset is Kc: the exponential (< 4e-13, or two table entries and their
-// product, < 1e-12), its argument (< 2^-46 (|z C| + |Kc|) with |z C| below
-// |Kc| + 127 for every term that is not flushed), the normaliser sum and
-// reciprocal; kept above their total.
+// offset is Kc: the exponential (< 4e-13 while |z C| <= 2^7; beyond, the low
+// part of its argument, below 2^-23 |z C| + 2^-18, adds |t|^5/120 + 1.5 u t^2
+// with |t| <= ln2 (2^-9 + 2^-23 (|Kc| + 128) + 2^-18)), its argument (< 2^-46
+// (|z C| + |Kc|) with |z C| below |Kc| + 127 for every term that is not
+// flushed), the normaliser sum and reciprocal (< 1e-12); kept above their
+// total for every offset |Kc| < kMaxOffset = 2^18 (at 2^18 the total is 0.92
+// of the bound; past about 2^18.8 the truncation would exceed it).
 __device__ __forceinline__ float acc_rho(float Kc) {
   return 2e-12f + 2.2e-14f * (fabsf(Kc) + 256.0f);
 }
@@ -540,7 +543,7 @@ __device__ void stats_rows(const SampleArgs& a, Fin& F, int b, int nrows) {
           Ssum = df_add(Ssum, df{__fmul_rn(it[sl].y, sc), __fmul_rn(it[sl].z, sc)});
         }
       }
-      const bool ok = !bad && isfinite(M) && fabsf(Kc) < 4194304.0f && Ssum.hi > 0.0f &&
+      const bool ok = !bad && isfinite(M) && fabsf(Kc) < kMaxOffset && Ssum.hi > 0.0f &&
                       isfinite(Ssum.hi);
       const int r = r0 + rr;
       F.rowKc[r] = Kc;
@@ -1022,7 +1025,7 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
   // each), 1/S and the product (3u), and the row sum behind 1/S (ex2 + ln2 u
   // sum q|x| + gamma1); summed with weights q (resp. p), whose sum is at most
   // kQmax. sum q|x| <= kQmax/2 - sum q x, since x <= 1/4 (the offset is the
-  // ceiling of the rounded max * c, below 2^22 in magnitude). Summation: each
+  // ceiling of the rounded max * c, below 2^18 in magnitude). Summation: each
   // term reaches a unit sum through the 8-term vector tree and the 32-lane
   // warp tree (gamma_8), and every unit, slice and row sum above that is pair
   // arithmetic, so t and each computed boundary are within about 8.1 u Sr of

@@ -102,6 +102,42 @@ def test_boundary_p_uses_the_accurate_pass(sv):
             assert g[0] == oracle.filter_threshold(z, T, 0, p), (r, i, p)
 
 
+@pytest.mark.parametrize("shift,T", [(20000.0, 0.5), (1.5e5, 1.0)])
+def test_large_offsets(sv, shift, T):
+    """fp32 rows shifted by a constant (the distributions do not change), row
+    offsets up to 2^17.7 (the range ends at 2^18): p on cumulative-mass
+    boundaries forces the double-float pass, which keeps its bound."""
+    stored, vals = _rows(4, 3000, synth.F32, seed=31)
+    stored = (stored + np.float32(shift)).astype(np.float32)
+    vals = stored.astype(np.float64)
+    for r in range(4):
+        z = vals[r]
+        zs = np.sort(z)[::-1]
+        cs = np.cumsum(np.exp((zs - zs[0]) / float(np.float32(T))))
+        for i in (5, 200):
+            j = i
+            while j + 1 < zs.size and zs[j + 1] == zs[i]:
+                j += 1
+            p = float(np.float32(cs[j] / cs[-1]))
+            g, err = _run(sv, stored[r:r + 1], synth.F32, T, 0, p)
+            assert err == 0
+            assert g[0] == oracle.filter_threshold(z, T, 0, p), (r, i, p)
+    g, _ = _run(sv, stored, synth.F32, T, 40, 0.9)
+    assert np.array_equal(g, _oracle(vals, T, 40, float(np.float32(0.9))))
+
+
+def test_top_p_offset_beyond_range(sv):
+    """With top-p, a maximum logit whose offset reaches 2^18 is out of range:
+    +inf and SPEC_DERR_LOGITS. Top-k alone needs no exponentials."""
+    stored, vals = _rows(2, 256, synth.F32, seed=2)
+    stored = (stored + np.float32(2.0e5)).astype(np.float32)
+    g, err = _run(sv, stored, synth.F32, 1.0, 0, 0.9)
+    assert (g == np.inf).all() and err == sv.SPEC_DERR_LOGITS
+    g, err = _run(sv, stored, synth.F32, 1.0, 10, 1.0)
+    assert err == 0
+    assert np.array_equal(g, _oracle(stored.astype(np.float64), 1.0, 10, 1.0))
+
+
 def test_input_validation(sv):
     import torch
     x = torch.zeros((2, 64), dtype=torch.bfloat16, device="cuda")

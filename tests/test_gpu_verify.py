@@ -230,6 +230,35 @@ def test_grid_sizes_agree(sv, monkeypatch, grid):
     assert np.array_equal(gg["out_tokens"], oracle_greedy(c)["out_tokens"])
 
 
+@pytest.mark.parametrize("shift,T", [(0.0, 0.05), (20000.0, 0.5), (1.5e5, 1.0), (-1.5e5, 1.0)])
+def test_large_exponent_offsets(sv, shift, T):
+    """Rows whose offset max * log2(e)/T is large in magnitude (a low
+    temperature, or fp32 logits shifted by a constant, which leaves every
+    distribution unchanged; up to 2^17.7 here, the range ends at 2^18): the
+    double-float refinements keep their bound, parity with the oracle."""
+    c = synth.sampling_case(32, 4, 20000, temperature=T, target_std=3.0, draft_noise_std=0.5,
+                            dtype=synth.F32, seed=int(abs(shift)) % 997 + 11)
+    c.target = (c.target + np.float32(shift)).astype(np.float32)
+    c.draft = (c.draft + np.float32(shift)).astype(np.float32)
+    g = gh.run_sample(sv, c)
+    o = oracle_sample(c)
+    gh.assert_sample_parity(g, o, label=f"shift={shift} T={T}")
+    assert g["err"] == 0
+    print(f"shift={shift} T={T}: refined rows", int(np.sum(g["row_info"] != 0)))
+
+
+def test_offset_beyond_range_is_a_logits_error(sv):
+    """max * log2(e)/T at or beyond 2^18 in magnitude: the exponent offset is
+    out of range, every row reports SPEC_DERR_LOGITS with outputs -1."""
+    c = synth.sampling_case(4, 3, 512, temperature=1.0, target_std=2.0, draft_noise_std=0.5,
+                            dtype=synth.F32, seed=4)
+    c.target = (c.target + np.float32(2.0e5)).astype(np.float32)
+    c.draft = (c.draft + np.float32(2.0e5)).astype(np.float32)
+    g = gh.run_sample(sv, c)
+    assert g["err"] & sv.SPEC_DERR_LOGITS
+    assert (g["num_accepted"] == -1).all() and (g["out_tokens"] == -1).all()
+
+
 def test_identical_draft_accepts_everything(sv):
     c = synth.sampling_case(8, 4, 4096, temperature=1.0, target_std=3.0, draft_noise_std=0.0,
                             seed=3)
