@@ -20,6 +20,10 @@
 // final comparison against p with a proven bound on that mass's error; a row
 // it cannot certify gets NaN, and the second launch recomputes exactly those
 // rows with double-float exponentials (relative error < 1e-11).
+// bf16 rows with top-k on first take a two-pass kernel (filter_topk_bf16_
+// kernel): the exact counts of the 256 keys below the row maximum give the
+// k-th largest logit, and top-p on the kept tokens follows from those bins'
+// masses in fp64; the rows it cannot settle go to the kernels above.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -68,7 +72,8 @@ struct KeyOf<EF32> {
 struct FilterArgs {
   const void* logits;
   int R, V, nvec, top_k;
-  float top_p, c, Chi, Clo, ex2, fixscale;
+  float top_p, T, c, Chi, Clo, ex2, fixscale;
+  int skip_done;  // general kernel after the bf16 top-k kernel: rows not NaN are done
   float* out;
   int32_t* err;
 };
@@ -113,7 +118,9 @@ __global__ void __launch_bounds__(kAcc ? kFTAcc : kFT) filter_kernel(const Filte
   __shared__ unsigned long long hwarp[NT / 32][256];  // per-warp level-0 masses
   __shared__ float s_th[kAcc ? 256 : 1], s_tl[kAcc ? 256 : 1];
   const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (kAcc && !isnan(a.out[row])) return;  // second launch: uncertain rows only
+  // the accurate launch takes the uncertain rows only; so does the fast
+  // launch after the bf16 top-k kernel (the rows it left)
+  if ((kAcc || a.skip_done) && !isnan(a.out[row])) return;
   if (kAcc) {
     for (int i = tid; i < 256; i += NT) {
       s_th[i] = kExp2Tab.hi[i];
@@ -488,6 +495,158 @@ __global__ void __launch_bounds__(kAcc ? kFTAcc : kFT) filter_kernel(const Filte
   if (tid == 0) a.out[row] = tau;
 }
 
+// ---------------------------------------------------------------- bf16 top-k
+// bf16 rows with top-k on (0 < k < V), two passes per row. Pass A takes the
+// row maximum (NaN propagates). Pass B counts the logits within 255 keys of
+// the maximum's key, one shared-memory bin per key, so that a bin holds one
+// logit value exactly and the logits outside the window cost one compare. The
+// k-th largest logit is the bin where the count from the top reaches k; top-p
+// on the kept tokens needs only their masses, count x exp((v - max) / T) per
+// bin, taken in fp64 with suffix sums formed by additions from the top. A row
+// whose window holds fewer than k logits gets NaN and the general kernel
+// takes it. Persistent CTAs, two per SM, walk the rows: a row read by pass A
+// is still in L2 for pass B.
+constexpr int kFTK = 512;
+
+__global__ void __launch_bounds__(kFTK, 2) filter_topk_bf16_kernel(const FilterArgs a) {
+  using KO = KeyOf<EBf16>;
+  __shared__ uint32_t hist[256];
+  __shared__ float s_m[kFTK / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned full = 0xffffffffu;
+  const bool topp = a.top_p < 1.0f;
+  for (int row = blockIdx.x; row < a.R; row += gridDim.x) {
+    const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const char*>(a.logits) +
+                                                     size_t(row) * size_t(a.V) * 2);
+    // pass A: row maximum
+    float vm = -INFINITY;
+    int i = tid;
+    for (; i + 3 * kFTK < a.nvec; i += 4 * kFTK) {  // four loads in flight per thread
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = ldg_nc_v4(rp + i + u * kFTK);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) vm = max_nan(vm, EBf16::vmax(v[u]));
+    }
+    for (; i < a.nvec; i += kFTK) vm = max_nan(vm, EBf16::vmax(ldg_nc_v4(rp + i)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) vm = max_nan(vm, __shfl_xor_sync(full, vm, o));
+    if (lane == 0) s_m[warp] = vm;
+    for (int i = tid; i < 256; i += kFTK) hist[i] = 0;
+    __syncthreads();
+    float mx = s_m[0];
+    for (int w = 1; w < kFTK / 32; ++w) mx = max_nan(mx, s_m[w]);
+    const bool nan_row = mx != mx;
+    const bool range_bad = topp && !(fabsf(offset_of(mx, a.c)) < kMaxOffset);
+    if (nan_row || range_bad || !(mx > -INFINITY)) {
+      if (tid == 0) {
+        a.out[row] = (nan_row || range_bad) ? INFINITY : -INFINITY;
+        if ((nan_row || range_bad) && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
+      }
+      __syncthreads();  // s_m is written again for the next row
+      continue;
+    }
+    // the maximum's key (+0 when the maximum is a zero: -0 and +0 are both in)
+    const uint32_t mk = (mx == 0.0f) ? 0x8000u : KO::key(mx);
+    const uint32_t lo = mk >= 255u ? mk - 255u : 0u;
+    // pass B: exact counts of the keys in [lo, mk]
+    auto count = [&](const uint4& v) {
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const uint32_t b = (w4[h >> 1] >> (16 * (h & 1))) & 0xffffu;
+        const uint32_t k = (b & 0x8000u) ? (~b & 0xffffu) : (b | 0x8000u);
+        if (k >= lo) atomicAdd(&hist[k - lo], 1u);
+      }
+    };
+    i = tid;
+    for (; i + 3 * kFTK < a.nvec; i += 4 * kFTK) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = ldg_nc_v4(rp + i + u * kFTK);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) count(v[u]);
+    }
+    for (; i < a.nvec; i += kFTK) count(ldg_nc_v4(rp + i));
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds bins 8l .. 8l + 7 (ascending keys)
+      uint32_t c[8], s = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[lane * 8 + j];
+        s += c[j];
+      }
+      uint32_t S = s;  // count in the bins of lanes >= lane
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_down_sync(full, S, o);
+        if (lane + o < 32) S += t;
+      }
+      const uint32_t need = uint32_t(a.top_k);
+      const unsigned bal = __ballot_sync(full, S >= need);
+      float out = NAN;  // fewer than k logits in the window: the general kernel
+      if (bal != 0) {
+        const int L = 31 - __clz(int(bal));
+        int tb = -1;  // highest bin whose count from the top reaches k
+        if (lane == L) {
+          uint32_t suf = S;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (suf >= need) tb = 8 * L + j;
+            suf -= c[j];
+          }
+        }
+        tb = __shfl_sync(full, tb, L);
+        int pb = tb;
+        if (topp) {
+          // kept bins tb .. 255, bin 255 - lane - 32 m in lane `lane` (one
+          // fp64 exponential per lane for up to 32 kept bins)
+          double e[8], zs = 0.0;
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            const int b = 255 - lane - 32 * m;
+            e[m] = 0.0;
+            if (b >= tb) {
+              const uint32_t cb = hist[b];
+              if (cb != 0u)
+                e[m] = double(cb) *
+                       exp((double(KO::value(lo + uint32_t(b))) - double(mx)) / double(a.T));
+            }
+            zs += e[m];
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(full, zs, o);
+          const double target = double(a.top_p) * zs;
+          // mass from the top, bin by bin: the highest bin where it reaches p Z
+          double carry = 0.0;
+          pb = tb;
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            if (255 - 32 * m < tb) break;
+            double inc = e[m];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const double t = __shfl_up_sync(full, inc, o);
+              if (lane >= o) inc += t;
+            }
+            const int b = 255 - lane - 32 * m;
+            const unsigned hit = __ballot_sync(full, b >= tb && carry + inc >= target);
+            if (hit) {
+              pb = 255 - (__ffs(int(hit)) - 1) - 32 * m;
+              break;
+            }
+            carry += __shfl_sync(full, inc, 31);
+          }
+        }
+        out = KO::value(lo + uint32_t(pb));
+      }
+      if (lane == 0) a.out[row] = out;
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 int launch_filter(const FilterLaunch& f) {
@@ -499,6 +658,8 @@ int launch_filter(const FilterLaunch& f) {
   a.nvec = f.V / kvec;
   a.top_k = f.top_k;
   a.top_p = f.top_p;
+  a.T = f.temperature;
+  a.skip_done = 0;
   const double C = 1.4426950408889634073599246810018921 / double(f.temperature);
   a.c = float(C);
   a.Chi = float(C);
@@ -512,6 +673,17 @@ int launch_filter(const FilterLaunch& f) {
   a.err = f.err;
   cudaStream_t st = static_cast<cudaStream_t>(f.stream);
   if (f.dtype == SPEC_BF16) {
+    if (f.top_k > 0 && f.top_k < f.V) {
+      static int sms = 0;
+      if (sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (sms < 1) sms = 1;
+      }
+      filter_topk_bf16_kernel<<<f.R < 2 * sms ? f.R : 2 * sms, kFTK, 0, st>>>(a);
+      a.skip_done = 1;
+    }
     filter_kernel<EBf16, false><<<f.R, kFT, 0, st>>>(a);
     if (f.top_p < 1.0f) filter_kernel<EBf16, true><<<f.R, kFTAcc, 0, st>>>(a);
   } else {
