@@ -20,10 +20,11 @@
 // final comparison against p with a proven bound on that mass's error; a row
 // it cannot certify gets NaN, and the second launch recomputes exactly those
 // rows with double-float exponentials (relative error < 1e-11).
-// bf16 rows with top-k on first take a two-pass kernel (filter_topk_bf16_
-// kernel): the exact counts of the 256 keys below the row maximum give the
-// k-th largest logit, and top-p on the kept tokens follows from those bins'
-// masses in fp64; the rows it cannot settle go to the kernels above.
+// bf16 rows first take a two-pass kernel (filter_topk_bf16_kernel): the
+// exact counts of the 256 keys below the row maximum give the k-th largest
+// logit, top-p on the kept tokens follows from those bins' masses in fp64,
+// and top-p alone from them plus the fp32 mass below the window, certified;
+// the rows it cannot settle go to the kernels above.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -495,26 +496,47 @@ __global__ void __launch_bounds__(kAcc ? kFTAcc : kFT) filter_kernel(const Filte
   if (tid == 0) a.out[row] = tau;
 }
 
-// ---------------------------------------------------------------- bf16 top-k
-// bf16 rows with top-k on (0 < k < V), two passes per row. Pass A takes the
-// row maximum (NaN propagates). Pass B counts the logits within 255 keys of
-// the maximum's key, one shared-memory bin per key, so that a bin holds one
-// logit value exactly and the logits outside the window cost one compare. The
-// k-th largest logit is the bin where the count from the top reaches k; top-p
-// on the kept tokens needs only their masses, count x exp((v - max) / T) per
-// bin, taken in fp64 with suffix sums formed by additions from the top. A row
-// whose window holds fewer than k logits gets NaN and the general kernel
-// takes it. Persistent CTAs, two per SM, walk the rows: a row read by pass A
-// is still in L2 for pass B.
+// ---------------------------------------------------------------- bf16 rows
+// bf16 rows with top-k or top-p on, two passes per row. Pass A takes the row
+// maximum (NaN propagates). Pass B counts the logits within 255 keys of the
+// maximum's key, one shared-memory bin per key, so that a bin holds one logit
+// value exactly and the logits outside the window cost one compare. Top-k:
+// the k-th largest logit is the bin where the count from the top reaches k;
+// top-p on the kept tokens needs only their masses, count x exp((v - max) /
+// T) per bin, in fp64 with sums formed by additions from the top. Top-p
+// alone: pass B also sums the fp32 masses below the window, and the bin where
+// the window's mass from the top reaches p Z is taken when the comparison
+// holds within the error bounds of both parts. A row the kernel cannot settle
+// (fewer than k logits in the window, the top-p boundary below it, or an
+// uncertified comparison) gets NaN and the general kernel takes it.
+// Persistent CTAs, two per SM, walk the rows: a row read by pass A is still
+// in L2 for pass B.
 constexpr int kFTK = 512;
 
+// Relative error bound of one fp32 mass 2^x outside the window (pass B, top-p
+// alone): ex2.approx, the two roundings of x = (z Chi - Kc) + z Clo (ln2 u |x|
+// with |x| <= 127 for every term not flushed) and the truncation of C to
+// Chi + Clo (below 1e-9 for offsets under 2^18); the vector tree (3u) and the
+// compensated running sum (below 2u) on top.
+constexpr double kOutRelErr = 1.6e-7 * 1.1 + 0.6931471805599453 * 5.9604644775390625e-8 * 128.0 +
+                              1e-9 + 5.0 * 5.9604644775390625e-8;
+
+template <bool kPAlone>
 __global__ void __launch_bounds__(kFTK, 2) filter_topk_bf16_kernel(const FilterArgs a) {
   using KO = KeyOf<EBf16>;
   __shared__ uint32_t hist[256];
   __shared__ float s_m[kFTK / 32];
+  __shared__ double s_zo[kFTK / 32];
+  __shared__ float s_th[kPAlone ? 256 : 1], s_tl[kPAlone ? 256 : 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned full = 0xffffffffu;
   const bool topp = a.top_p < 1.0f;
+  if (kPAlone) {
+    for (int j = tid; j < 256; j += kFTK) {
+      s_th[j] = kExp2Tab.hi[j];
+      s_tl[j] = kExp2Tab.lo[j];
+    }
+  }
   for (int row = blockIdx.x; row < a.R; row += gridDim.x) {
     const uint4* rp = reinterpret_cast<const uint4*>(static_cast<const char*>(a.logits) +
                                                      size_t(row) * size_t(a.V) * 2);
@@ -532,12 +554,13 @@ __global__ void __launch_bounds__(kFTK, 2) filter_topk_bf16_kernel(const FilterA
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) vm = max_nan(vm, __shfl_xor_sync(full, vm, o));
     if (lane == 0) s_m[warp] = vm;
-    for (int i = tid; i < 256; i += kFTK) hist[i] = 0;
+    for (int j = tid; j < 256; j += kFTK) hist[j] = 0;
     __syncthreads();
     float mx = s_m[0];
     for (int w = 1; w < kFTK / 32; ++w) mx = max_nan(mx, s_m[w]);
+    const float Kc = offset_of(mx, a.c);
     const bool nan_row = mx != mx;
-    const bool range_bad = topp && !(fabsf(offset_of(mx, a.c)) < kMaxOffset);
+    const bool range_bad = topp && mx > -INFINITY && !(fabsf(Kc) < kMaxOffset);
     if (nan_row || range_bad || !(mx > -INFINITY)) {
       if (tid == 0) {
         a.out[row] = (nan_row || range_bad) ? INFINITY : -INFINITY;
@@ -549,14 +572,31 @@ __global__ void __launch_bounds__(kFTK, 2) filter_topk_bf16_kernel(const FilterA
     // the maximum's key (+0 when the maximum is a zero: -0 and +0 are both in)
     const uint32_t mk = (mx == 0.0f) ? 0x8000u : KO::key(mx);
     const uint32_t lo = mk >= 255u ? mk - 255u : 0u;
-    // pass B: exact counts of the keys in [lo, mk]
+    // pass B: exact counts of the keys in [lo, mk]; with top-p alone also the
+    // mass of the logits below the window, 2^(z C - Kc) in fp32 (compensated)
+    float zo = 0.0f, zol = 0.0f;
     auto count = [&](const uint4& v) {
       const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      float m[8];
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
         const uint32_t b = (w4[h >> 1] >> (16 * (h & 1))) & 0xffffu;
         const uint32_t k = (b & 0x8000u) ? (~b & 0xffffu) : (b | 0x8000u);
         if (k >= lo) atomicAdd(&hist[k - lo], 1u);
+        if (kPAlone) {
+          const float z = __uint_as_float(b << 16);
+          const float x = __fmaf_rn(z, a.Clo, __fmaf_rn(z, a.Chi, -Kc));
+          m[h] = (k >= lo) ? 0.0f : ex2_approx(x);
+        }
+      }
+      if (kPAlone) {
+#pragma unroll
+        for (int w = 1; w < 8; w <<= 1)
+#pragma unroll
+          for (int h = 0; h < 8; h += 2 * w) m[h] = __fadd_rn(m[h], m[h + w]);
+        const df t = two_sum(zo, m[0]);
+        zo = t.hi;
+        zol = __fadd_rn(zol, t.lo);
       }
     };
     i = tid;
@@ -568,78 +608,138 @@ __global__ void __launch_bounds__(kFTK, 2) filter_topk_bf16_kernel(const FilterA
       for (int u = 0; u < 4; ++u) count(v[u]);
     }
     for (; i < a.nvec; i += kFTK) count(ldg_nc_v4(rp + i));
+    if (kPAlone) {
+      double d = double(zo) + double(zol);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(full, d, o);
+      if (lane == 0) s_zo[warp] = d;
+    }
     __syncthreads();
     if (warp == 0) {
-      // lane l holds bins 8l .. 8l + 7 (ascending keys)
-      uint32_t c[8], s = 0;
+      float out = NAN;  // the general kernel takes the rows left NaN
+      if (!kPAlone) {
+        // top-k (then top-p on the kept tokens): lane l holds bins 8l .. 8l + 7
+        uint32_t c[8], s = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = hist[lane * 8 + j];
-        s += c[j];
-      }
-      uint32_t S = s;  // count in the bins of lanes >= lane
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_down_sync(full, S, o);
-        if (lane + o < 32) S += t;
-      }
-      const uint32_t need = uint32_t(a.top_k);
-      const unsigned bal = __ballot_sync(full, S >= need);
-      float out = NAN;  // fewer than k logits in the window: the general kernel
-      if (bal != 0) {
-        const int L = 31 - __clz(int(bal));
-        int tb = -1;  // highest bin whose count from the top reaches k
-        if (lane == L) {
-          uint32_t suf = S;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (suf >= need) tb = 8 * L + j;
-            suf -= c[j];
-          }
+        for (int j = 0; j < 8; ++j) {
+          c[j] = hist[lane * 8 + j];
+          s += c[j];
         }
-        tb = __shfl_sync(full, tb, L);
-        int pb = tb;
-        if (topp) {
-          // kept bins tb .. 255, bin 255 - lane - 32 m in lane `lane` (one
-          // fp64 exponential per lane for up to 32 kept bins)
-          double e[8], zs = 0.0;
+        uint32_t S = s;  // count in the bins of lanes >= lane
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const int b = 255 - lane - 32 * m;
-            e[m] = 0.0;
-            if (b >= tb) {
-              const uint32_t cb = hist[b];
-              if (cb != 0u)
-                e[m] = double(cb) *
-                       exp((double(KO::value(lo + uint32_t(b))) - double(mx)) / double(a.T));
-            }
-            zs += e[m];
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(full, zs, o);
-          const double target = double(a.top_p) * zs;
-          // mass from the top, bin by bin: the highest bin where it reaches p Z
-          double carry = 0.0;
-          pb = tb;
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            if (255 - 32 * m < tb) break;
-            double inc = e[m];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const double t = __shfl_up_sync(full, inc, o);
-              if (lane >= o) inc += t;
-            }
-            const int b = 255 - lane - 32 * m;
-            const unsigned hit = __ballot_sync(full, b >= tb && carry + inc >= target);
-            if (hit) {
-              pb = 255 - (__ffs(int(hit)) - 1) - 32 * m;
-              break;
-            }
-            carry += __shfl_sync(full, inc, 31);
-          }
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_down_sync(full, S, o);
+          if (lane + o < 32) S += t;
         }
-        out = KO::value(lo + uint32_t(pb));
+        const uint32_t need = uint32_t(a.top_k);
+        const unsigned bal = __ballot_sync(full, S >= need);
+        if (bal != 0) {  // else fewer than k logits in the window
+          const int L = 31 - __clz(int(bal));
+          int tb = -1;  // highest bin whose count from the top reaches k
+          if (lane == L) {
+            uint32_t suf = S;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              if (suf >= need) tb = 8 * L + j;
+              suf -= c[j];
+            }
+          }
+          tb = __shfl_sync(full, tb, L);
+          int pb = tb;
+          if (topp) {
+            // kept bins tb .. 255, bin 255 - lane - 32 m in lane `lane`: masses
+            // count x exp((v - max) / T) in fp64, one exponential per lane for
+            // up to 32 kept bins
+            double e[8], zs = 0.0;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              const int b = 255 - lane - 32 * m;
+              e[m] = 0.0;
+              if (b >= tb) {
+                const uint32_t cb = hist[b];
+                if (cb != 0u)
+                  e[m] = double(cb) *
+                         exp((double(KO::value(lo + uint32_t(b))) - double(mx)) / double(a.T));
+              }
+              zs += e[m];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(full, zs, o);
+            const double target = double(a.top_p) * zs;
+            // mass from the top, bin by bin: the highest bin where it reaches p Z
+            double carry = 0.0;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+              if (255 - 32 * m < tb) break;
+              double inc = e[m];
+#pragma unroll
+              for (int o = 1; o < 32; o <<= 1) {
+                const double t = __shfl_up_sync(full, inc, o);
+                if (lane >= o) inc += t;
+              }
+              const int b = 255 - lane - 32 * m;
+              const unsigned hit = __ballot_sync(full, b >= tb && carry + inc >= target);
+              if (hit) {
+                pb = 255 - (__ffs(int(hit)) - 1) - 32 * m;
+                break;
+              }
+              carry += __shfl_sync(full, inc, 31);
+            }
+          }
+          out = KO::value(lo + uint32_t(pb));
+        }
+      } else {
+        // top-p alone: window masses count x 2^(v C - Kc) in pair arithmetic
+        // (relative error below acc_rho), the mass below the window from pass
+        // B (relative error below kOutRelErr); the bin is taken when the
+        // comparisons with p Z hold for every value within those bounds
+        double e[8], zs = 0.0;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const int b = 255 - lane - 32 * m;
+          const uint32_t cb = hist[b];
+          e[m] = 0.0;
+          if (cb != 0u) {
+            const float v = KO::value(lo + uint32_t(b));
+            const df p = two_prod(v, a.Chi);
+            const float pl = __fmaf_rn(v, a.Clo, p.lo);
+            const df sx = two_sum(p.hi, -Kc);
+            const df r = df_exp2(sx.hi, __fadd_rn(sx.lo, pl), s_th, s_tl);
+            e[m] = double(cb) * (double(r.hi) + double(r.lo));
+          }
+          zs += e[m];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(full, zs, o);
+        double zo = lane < kFTK / 32 ? s_zo[lane] : 0.0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) zo += __shfl_xor_sync(full, zo, o);
+        const double Z = zs + zo;
+        const double ew = 2e-12 + 2.2e-14 * (fabs(double(Kc)) + 256.0);
+        const double err = zs * ew + zo * kOutRelErr * 1.05 + Z * 1e-15;
+        const double target = double(a.top_p) * Z;
+        double carry = 0.0;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          double inc = e[m];
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const double t = __shfl_up_sync(full, inc, o);
+            if (lane >= o) inc += t;
+          }
+          const unsigned hit = __ballot_sync(full, carry + inc >= target);
+          if (hit) {
+            const int f = __ffs(int(hit)) - 1;
+            const double incl = carry + __shfl_sync(full, inc, f);
+            const double excl = incl - __shfl_sync(full, e[m], f);
+            const double slack = zs * ew + 1e-15 * Z;
+            const bool ok = incl - slack >= double(a.top_p) * (Z + err) &&
+                            excl + slack < double(a.top_p) * (Z - err);
+            if (ok) out = KO::value(lo + uint32_t(255 - f - 32 * m));
+            break;
+          }
+          carry += __shfl_sync(full, inc, 31);
+        }
       }
       if (lane == 0) a.out[row] = out;
     }
@@ -673,7 +773,8 @@ int launch_filter(const FilterLaunch& f) {
   a.err = f.err;
   cudaStream_t st = static_cast<cudaStream_t>(f.stream);
   if (f.dtype == SPEC_BF16) {
-    if (f.top_k > 0 && f.top_k < f.V) {
+    const bool topk = f.top_k > 0 && f.top_k < f.V;
+    if (topk || f.top_p < 1.0f) {
       static int sms = 0;
       if (sms == 0) {
         int dev = 0;
@@ -681,7 +782,9 @@ int launch_filter(const FilterLaunch& f) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms < 1) sms = 1;
       }
-      filter_topk_bf16_kernel<<<f.R < 2 * sms ? f.R : 2 * sms, kFTK, 0, st>>>(a);
+      const int grid = f.R < 2 * sms ? f.R : 2 * sms;
+      if (topk) filter_topk_bf16_kernel<false><<<grid, kFTK, 0, st>>>(a);
+      else filter_topk_bf16_kernel<true><<<grid, kFTK, 0, st>>>(a);
       a.skip_done = 1;
     }
     filter_kernel<EBf16, false><<<f.R, kFT, 0, st>>>(a);

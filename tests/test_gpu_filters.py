@@ -81,6 +81,33 @@ def test_edges(sv):
             assert g[r] == oracle.filter_threshold(vals[r], 1.0, k, float(np.float32(p))), (r, k, p)
 
 
+def test_bf16_edges(sv):
+    """bf16 rows through the two-pass top-k kernel and its fallback: a NaN
+    row, an all -inf row, a mostly -inf row, a maximum of zero with both
+    signed zeros present, a +inf maximum (top-k only), and k beyond the 256
+    keys below the maximum (the general kernel takes the row)."""
+    rng = np.random.default_rng(13)
+    V = 1024
+    z = rng.normal(0, 2, (6, V)).astype(np.float32)
+    z[1, :] = -np.inf
+    z[2, :1000] = -np.inf
+    z[3] = -np.abs(z[3])
+    z[3, 5] = 0.0
+    z[3, 9] = -0.0
+    z[4, 17] = np.inf
+    stored = synth.f32_to_bf16_bits(z)
+    stored[0, 33] = 0x7FC0                     # NaN
+    vals = synth.logits_values(stored, synth.BF16).astype(np.float64)
+    for k, p in ((1, 1.0), (7, 1.0), (30, 0.6), (900, 1.0), (1000, 0.9)):
+        g, err = _run(sv, stored, synth.BF16, 1.0, k, p)
+        assert g[0] == np.inf and err & sv.SPEC_DERR_LOGITS
+        rows = (1, 2, 3, 5) if p < 1.0 else (1, 2, 3, 4, 5)
+        for r in rows:
+            assert g[r] == oracle.filter_threshold(vals[r], 1.0, k, float(np.float32(p))), (r, k, p)
+    g, _ = _run(sv, stored[3:4], synth.BF16, 1.0, 2, 1.0)
+    assert g[0] == 0.0                         # both zeros kept
+
+
 def test_boundary_p_uses_the_accurate_pass(sv):
     """p set to the cumulative mass of a prefix (rounded to float32): the
     comparison with p lies within the fp32 pass's error bound, so the
