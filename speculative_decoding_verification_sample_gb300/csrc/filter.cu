@@ -509,8 +509,9 @@ __global__ void __launch_bounds__(kAcc ? kFTAcc : kFT) filter_kernel(const Filte
 // holds within the error bounds of both parts. A row the kernel cannot settle
 // (fewer than k logits in the window, the top-p boundary below it, or an
 // uncertified comparison) gets NaN and the general kernel takes it.
-// Persistent CTAs, two per SM, walk the rows: a row read by pass A is still
-// in L2 for pass B.
+// Persistent CTAs, three per SM (measured faster than one, two, or more
+// smaller ones), walk the rows; a row read by pass A is still in L2 for
+// pass B.
 constexpr int kFTK = 512;
 
 // Relative error bound of one fp32 mass 2^x outside the window (pass B, top-p
@@ -522,7 +523,7 @@ constexpr double kOutRelErr = 1.6e-7 * 1.1 + 0.6931471805599453 * 5.960464477539
                               1e-9 + 5.0 * 5.9604644775390625e-8;
 
 template <bool kPAlone>
-__global__ void __launch_bounds__(kFTK, 2) filter_topk_bf16_kernel(const FilterArgs a) {
+__global__ void __launch_bounds__(kFTK, 3) filter_topk_bf16_kernel(const FilterArgs a) {
   using KO = KeyOf<EBf16>;
   __shared__ uint32_t hist[256];
   __shared__ float s_m[kFTK / 32];
@@ -782,7 +783,7 @@ int launch_filter(const FilterLaunch& f) {
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (sms < 1) sms = 1;
       }
-      const int grid = f.R < 2 * sms ? f.R : 2 * sms;
+      const int grid = f.R < 3 * sms ? f.R : 3 * sms;
       if (topk) filter_topk_bf16_kernel<false><<<grid, kFTK, 0, st>>>(a);
       else filter_topk_bf16_kernel<true><<<grid, kFTK, 0, st>>>(a);
       a.skip_done = 1;
