@@ -7,19 +7,20 @@
 // "sglang_spec_decode" README, provisional layer (provisional blocks are freed
 // at once; no block leaked or freed twice).
 //
-// Two launches on the caller's stream:
+// Three launches on the caller's stream:
 //   kv_plan_kernel   one CTA: validates every row (all-or-nothing), pops the
 //                    new tail blocks from the free stack (rows ascending),
 //                    then pushes every provisional block (rows ascending) and
 //                    writes the call's status word;
-//   kv_copy_kernel   one CTA per row: if the status is 0, copies the n + 1
-//                    kept slots of the row's provisional blocks (slots 0..n,
+//   kv_copy_kernel   one CTA per (row, position <= K): if the status is 0,
+//                    copies kept slot s <= n of the row's provisional blocks (slots 0..n,
 //                    or slot_map[b][0..n] for a tree draft, whose kept path
 //                    need not be contiguous: thakicloud.com, "Speculative
 //                    decoding: when it loses", "Grading every branch in one
 //                    pass"), for every layer and both K and V planes, to
-//                    logical positions L..L+n, then sets the new length and
-//                    clears the provisional entries.
+//                    logical positions L..L+n;
+//   kv_finish_kernel one thread per row: sets the new length and clears the
+//                    provisional entries.
 // Only the accepted bytes move: 2 * (n + 1) * layers * heads * head_dim * elem
 // bytes read and written per row.
 #include <cuda_runtime.h>
@@ -33,7 +34,7 @@
 namespace sv {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kCopyThreads = 512;
+constexpr int kCopyThreads = 256;
 
 struct KvArgs {
   int32_t* bt;
@@ -213,50 +214,51 @@ __global__ void __launch_bounds__(kPlanThreads) kv_plan_kernel(const KvArgs a) {
 }
 
 __global__ void __launch_bounds__(kCopyThreads) kv_copy_kernel(const KvArgs a) {
-  __shared__ int64_t s_src[32 + 1], s_dst[32 + 1];
-  const int b = blockIdx.x;
+  // one CTA per (row, kept position): every SM takes a share of the slots,
+  // whatever the rows' accepted lengths
+  const int b = blockIdx.x / (a.K + 1), s = blockIdx.x % (a.K + 1);
   if (*a.status != 0) return;
-  const int n = a.na[b], L = a.sl[b];
+  const int n = a.na[b];
+  if (s > n) return;
+  const int L = a.sl[b];
   const int64_t layer_stride = int64_t(2) * a.bs * a.slot_bytes;  // one layer: K and V planes
   const int64_t block_stride = int64_t(a.NL) * layer_stride;
-  if (threadIdx.x <= n) {
-    const int s = threadIdx.x, x = kept_slot(a, b, s);
-    const int sb = a.pb[size_t(b) * a.P + x / a.bs];
-    const int pos = L + s;
-    const int db = a.bt[size_t(b) * a.MB + pos / a.bs];
-    s_src[s] = int64_t(sb) * block_stride + int64_t(x % a.bs) * a.slot_bytes;
-    s_dst[s] = int64_t(db) * block_stride + int64_t(pos % a.bs) * a.slot_bytes;
-  }
-  __syncthreads();
-  const int vpu = int(a.slot_bytes / 16);          // 16-byte vectors per (slot, layer, plane)
-  const int64_t units = int64_t(n + 1) * a.NL * 2;  // (slot, layer, plane) units
-  const int64_t total = units * vpu;
-  const int64_t step = kCopyThreads;
-  constexpr int kUnroll = 4;
-  for (int64_t g0 = threadIdx.x; g0 < total; g0 += step * kUnroll) {
+  const int x = kept_slot(a, b, s);
+  const int sb = a.pb[size_t(b) * a.P + x / a.bs];
+  const int pos = L + s;
+  const int db = a.bt[size_t(b) * a.MB + pos / a.bs];
+  const uint8_t* src = a.pool + int64_t(sb) * block_stride + int64_t(x % a.bs) * a.slot_bytes;
+  uint8_t* dst = a.pool + int64_t(db) * block_stride + int64_t(pos % a.bs) * a.slot_bytes;
+  const int vpu = int(a.slot_bytes / 16);  // 16-byte vectors per (layer, plane)
+  const int total = 2 * a.NL * vpu;
+  const int64_t plane_stride = int64_t(a.bs) * a.slot_bytes;
+  constexpr int kUnroll = 8;
+  for (int g0 = threadIdx.x; g0 < total; g0 += kCopyThreads * kUnroll) {
     uint4 v[kUnroll];
-    int64_t dsto[kUnroll];
+    int64_t off[kUnroll];
 #pragma unroll
     for (int i = 0; i < kUnroll; ++i) {
-      const int64_t g = g0 + i * step;
-      dsto[i] = -1;
+      const int g = g0 + i * kCopyThreads;
+      off[i] = -1;
       if (g < total) {
-        const int64_t u = g / vpu;
-        const int w = int(g - u * vpu);
-        const int s = int(u / (2 * a.NL));
-        const int rem = int(u - int64_t(s) * 2 * a.NL);  // layer * 2 + plane
-        const int64_t within = int64_t(rem) * a.bs * a.slot_bytes + int64_t(w) * 16;
-        v[i] = ldg_nc_v4(a.pool + s_src[s] + within);
-        dsto[i] = s_dst[s] + within;
+        const int u = g / vpu;  // layer * 2 + plane
+        off[i] = int64_t(u) * plane_stride + int64_t(g - u * vpu) * 16;
+        v[i] = ldg_nc_v4(src + off[i]);
       }
     }
 #pragma unroll
     for (int i = 0; i < kUnroll; ++i)
-      if (dsto[i] >= 0) *reinterpret_cast<uint4*>(a.pool + dsto[i]) = v[i];
+      if (off[i] >= 0) *reinterpret_cast<uint4*>(dst + off[i]) = v[i];
   }
-  __syncthreads();
-  if (threadIdx.x == 0) a.sl[b] = L + n + 1;
-  if (threadIdx.x < a.P) a.pb[size_t(b) * a.P + threadIdx.x] = -1;
+}
+
+// After every copy: the new lengths and the cleared provisional entries (the
+// copy CTAs read both, so they change only once all have run).
+__global__ void __launch_bounds__(256) kv_finish_kernel(const KvArgs a) {
+  const int b = blockIdx.x * 256 + threadIdx.x;
+  if (b >= a.B || *a.status != 0) return;
+  a.sl[b] = a.sl[b] + a.na[b] + 1;
+  for (int i = 0; i < a.P; ++i) a.pb[size_t(b) * a.P + i] = -1;
 }
 
 // ------------------------------------------------------------------ in place
@@ -376,7 +378,9 @@ int launch_kv_commit(const KvLaunch& k) {
   cudaStream_t st = static_cast<cudaStream_t>(k.stream);
   kv_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ECUDA;
-  kv_copy_kernel<<<k.B, kCopyThreads, 0, st>>>(a);
+  kv_copy_kernel<<<k.B * (k.K + 1), kCopyThreads, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return SPEC_ECUDA;
+  kv_finish_kernel<<<(k.B + 255) / 256, 256, 0, st>>>(a);
   if (cudaGetLastError() != cudaSuccess) return SPEC_ECUDA;
   return SPEC_OK;
 }
