@@ -98,10 +98,17 @@ def kv_state(torch, na):
     w = WORKLOAD
     c = synth.kv_case(w["B"], w["K"], block_size=w["block_size"], prefix_lo=w["prefix_lo"],
                       prefix_hi=w["prefix_hi"], num_accepted=na, seed=44)
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()  # noqa: E731
-    d = dict(bt=t(c.block_table), sl=t(c.seq_lens), pb=t(c.prov_blocks), fs=t(c.free_stack),
-             ft=t([c.free_top]), st=t([0]))
-    saved = {k: v.clone() for k, v in d.items()}
+    # the tables a commit changes live in one buffer, restored by one copy per step
+    host = dict(bt=c.block_table, sl=c.seq_lens, pb=c.prov_blocks, fs=c.free_stack,
+                ft=[c.free_top])
+    host = {k: np.ascontiguousarray(v, np.int32) for k, v in host.items()}
+    buf = torch.from_numpy(np.concatenate([v.ravel() for v in host.values()])).cuda()
+    d, o = {}, 0
+    for k, v in host.items():
+        d[k] = buf[o:o + v.size].view(v.shape)
+        o += v.size
+    d["st"] = torch.zeros(1, dtype=torch.int32, device="cuda")
+    saved = (buf, buf.clone())
     pool = torch.empty((c.num_blocks, w["kv_layers"], 2, w["block_size"], w["kv_heads"],
                         w["head_dim"]), dtype=torch.bfloat16, device="cuda")
     return c, d, saved, pool
@@ -409,8 +416,7 @@ def main():
     def step(i, ev=None):
         bt = batches[i % nb]
         if a.mode == "step":
-            for k in ("bt", "sl", "pb", "fs", "ft"):
-                kd[k].copy_(saved[k], non_blocking=True)
+            saved[0].copy_(saved[1], non_blocking=True)
         if ev is not None:
             ev[0].record(stream)
         if a.mode == "greedy":
@@ -481,8 +487,7 @@ def main():
             db = batches[(i + 1) % nb]   # device buffers that receive the copy
             for k in ("target", "draft", "tokens", "uniforms"):
                 db[k].copy_(hb[k], non_blocking=True)
-            for k in ("bt", "sl", "pb", "fs", "ft"):
-                kd[k].copy_(saved[k], non_blocking=True)
+            saved[0].copy_(saved[1], non_blocking=True)
             sv.spec_verify_sample(db["target"], db["draft"], db["tokens"], db["uniforms"], T, out, n)
             sv.kv_commit_rollback(kd["bt"], kd["sl"], n, kd["pb"], pool, kd["fs"], kd["ft"],
                                   kd["st"], K=K, block_size=w["block_size"])
