@@ -482,17 +482,19 @@ def main():
         out_h = torch.empty_like(out, device="cpu").pin_memory()
         n_h = torch.empty_like(n, device="cpu").pin_memory()
 
+        # HostVerifier: the rows are copied in chunks on a copy stream and each
+        # chunk is verified as soon as it lands, hiding the verification
+        # behind the host-to-device transfer
+        hv = sv.HostVerifier(B, K, batches[0]["target"].shape[-1], dtype=batches[0]["target"].dtype,
+                             chunks=8)
+
         def e2e_step(i):
             hb = host[i % nb]
-            db = batches[(i + 1) % nb]   # device buffers that receive the copy
-            for k in ("target", "draft", "tokens", "uniforms"):
-                db[k].copy_(hb[k], non_blocking=True)
             saved[0].copy_(saved[1], non_blocking=True)
-            sv.spec_verify_sample(db["target"], db["draft"], db["tokens"], db["uniforms"], T, out, n)
-            sv.kv_commit_rollback(kd["bt"], kd["sl"], n, kd["pb"], pool, kd["fs"], kd["ft"],
+            _, nd = hv(hb["target"], hb["draft"], hb["tokens"], hb["uniforms"], T)
+            sv.kv_commit_rollback(kd["bt"], kd["sl"], nd, kd["pb"], pool, kd["fs"], kd["ft"],
                                   kd["st"], K=K, block_size=w["block_size"])
-            out_h.copy_(out, non_blocking=True)
-            n_h.copy_(n, non_blocking=True)
+            hv.to_host(out_h, n_h)
 
         for i in range(3):
             e2e_step(i)
