@@ -455,11 +455,9 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     verify_ms = [e0.elapsed_time(e1) for e0, e1 in evs]
     if world > 1:
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        total_ms = max_over_ranks(total_ms, "cuda")
     ms_per_step = total_ms / a.steps
-    value = world * B * K / (ms_per_step / 1e3)
+    value = job_rate(world, B, K, ms_per_step)
 
     # roofline of the dominant kernel (spec_verify_sample), live CUDA-event durations
     if a.mode == "greedy":
@@ -507,10 +505,8 @@ def main():
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / a.e2e_steps
         if world > 1:
-            tt = torch.tensor([e2e_ms], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
-        e2e = {"value": world * B * K / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            e2e_ms = max_over_ranks(e2e_ms, "cuda")
+        e2e = {"value": job_rate(world, B, K, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     cpu = None
@@ -554,6 +550,25 @@ def main():
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def max_over_ranks(x, device=None):
+    """The maximum of a per-rank float over the process group (x itself when
+    no group is initialised). Tensors live on `device` (CUDA under NCCL, CPU
+    under gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, B, K, ms_per_step):
+    """Whole-job verified positions per second: every rank verifies B rows of
+    K draft positions per step (weak scaling, replicas)."""
+    return world * B * K / (ms_per_step / 1e3)
 
 
 def run_reference(a, rank, world, T):
