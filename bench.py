@@ -534,7 +534,7 @@ def main():
                          "algorithmic_bytes_per_launch": alg, "avg_launch_ms": v_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (3 if a.mode == "step" else 1) * a.steps,
+            "gpu_launches": (4 if a.mode == "step" else 1) * a.steps,  # verify (+ kv plan, copy, finish)
             "clocks": clk,
             "extra": {"verify_ms": v_ms, "kv_commit_and_table_restore_ms": ms_per_step - v_ms,
                       "kv_commit_inplace_us": (inplace_kv_us(torch, sv, na_list[0][0])
