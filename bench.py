@@ -54,6 +54,8 @@ def parse():
                    help="step: verify + KV commit (the benchmark); verify / greedy: that kernel "
                         "alone on the same logits, no KV pool (small footprint, for profiling)")
     p.add_argument("--batches", type=int, default=3, help="input batches to rotate over")
+    p.add_argument("--sweep", action="store_true",
+                   help="time the verify launch over the B x K x V x T grid (one JSON line per cell)")
     return p.parse_args()
 
 
@@ -73,13 +75,14 @@ def workload_name(T):
 
 
 # ------------------------------------------------------------------ inputs
-def gen_batch(torch, seed, T):
+def gen_batch(torch, seed, T, B=None, K=None, V=None):
     """Synthetic verifier inputs on the GPU (the draft token is the draft model's
-    own Gumbel-max sample; the verifier never sees how it was drawn)."""
+    own Gumbel-max sample; the verifier never sees how it was drawn). Shape
+    defaults to the bench workload."""
     import numpy as np
     import synth
     w = WORKLOAD
-    B, K, V = w["B"], w["K"], w["V"]
+    B, K, V = B or w["B"], K or w["K"], V or w["V"]
     g = torch.Generator(device="cuda").manual_seed(seed)
     zt = (torch.randn((B, K + 1, V), device="cuda", generator=g) * w["target_std"]).to(torch.bfloat16)
     zd = (zt[:, :K].float() + torch.randn((B, K, V), device="cuda", generator=g) * w["sigma"]
@@ -345,6 +348,26 @@ def algorithmic_verify_bytes(na, K, V, e=2):
     return B * 2 * K * V * e + full * V * e + meta
 
 
+def sequential_verify_bytes(na, K, V, e=2):
+    """Secondary figure: the bytes a verifier that reads only the positions it
+    needs would move (target and draft rows 0..n of a row rejected at n, all 2K
+    rows plus the bonus row of a fully accepted one), plus the per-row I/O."""
+    import numpy as np
+    na = np.asarray(na)
+    rows = np.where(na < K, 2 * (na + 1), 2 * K + 1)
+    meta = len(na) * (4 * K + 4 * (K + 1) + 4 * (K + 1) + 4)
+    return int(np.sum(rows)) * V * e + meta
+
+
+def greedy_verify_bytes(na, K, V, e=2):
+    """Bytes the greedy launch must move: target rows 0..K-1 of every row, row K of
+    the rows that accept everything, and the per-row I/O."""
+    import numpy as np
+    B = len(na)
+    full = int(np.sum(np.asarray(na) == K))
+    return B * K * V * e + full * V * e + B * (4 * K + 4 * (K + 1) + 4)
+
+
 def kv_bytes(na, w):
     import numpy as np
     slot = w["kv_layers"] * 2 * w["kv_heads"] * w["head_dim"] * 2  # bytes of one token's KV
@@ -379,8 +402,76 @@ def oracle_sample_rate(rows: int, T: float, budget_s: float):
 
 
 # ------------------------------------------------------------------ main
+SWEEP = dict(B=(1, 8, 64, 256, 1024), K=(2, 4, 8), V=(32000, 128256, 151936), T=(0.0, 0.6, 1.0))
+
+
+def run_sweep(a):
+    """Verify-launch times over the grid of batch sizes, draft lengths, vocabularies
+    and temperatures (T = 0: greedy), bf16 logits generated like the bench
+    workload (target N(0, 3^2), draft = target + N(0, 0.5^2)). Each cell: 3
+    warm-up launches, then `--steps` (at most 20) timed launches with CUDA events
+    around each one and a 256 MB write between them (L2 flush); the median is
+    reported with its algorithmic bytes against the measured HBM peak."""
+    import numpy as np
+    import torch
+    import speculative_decoding_verification_sample_gb300 as sv
+    from speculative_decoding_verification_sample_gb300 import build
+    build.build()
+    sv.lib()
+    peak, peak_kind = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    reps = max(5, min(20, a.steps))
+    for V in SWEEP["V"]:
+        for K in SWEEP["K"]:
+            for B in SWEEP["B"]:
+                bt = None
+                for T in SWEEP["T"]:
+                    bt = gen_batch(torch, 7 + B + K, T if T > 0 else 1.0, B=B, K=K, V=V)
+                    out = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
+                    n = torch.empty((B,), dtype=torch.int32, device="cuda")
+                    if T > 0:
+                        def call():
+                            sv.spec_verify_sample(bt["target"], bt["draft"], bt["tokens"],
+                                                  bt["uniforms"], T, out, n)
+                    else:
+                        def call():
+                            sv.spec_verify_greedy(bt["target"], bt["tokens"], out, n)
+                    for _ in range(3):
+                        call()
+                    torch.cuda.synchronize()
+                    na = n.cpu().numpy()
+                    ts = []
+                    for _ in range(reps):
+                        flush.zero_()
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record()
+                        call()
+                        e1.record()
+                        torch.cuda.synchronize()
+                        ts.append(e0.elapsed_time(e1))
+                    ms = float(np.median(ts))
+                    alg = (algorithmic_verify_bytes(na, K, V) if T > 0
+                           else greedy_verify_bytes(na, K, V))
+                    gbs = alg / (ms / 1e3) / 1e9
+                    cell = {"sweep": {"B": B, "K": K, "V": V, "T": T,
+                                      "mode": "sample" if T > 0 else "greedy"},
+                            "us": ms * 1e3, "positions_per_s": B * K / (ms / 1e3),
+                            "algorithmic_bytes": alg, "gbs": gbs, "frac": gbs / peak,
+                            "peak_kind": peak_kind, "mean_accepted": float(na.mean())}
+                    if T > 0:
+                        cell["sequential_frac"] = (sequential_verify_bytes(na, K, V)
+                                                   / (ms / 1e3) / 1e9 / peak)
+                    print(json.dumps(cell), flush=True)
+                    del bt
+                    bt = None
+                torch.cuda.empty_cache()
+
+
 def main():
     a = parse()
+    if a.sweep:
+        return run_sweep(a)
     rank, world, local = dist_env()
     T = a.temperature
     if a.impl == "reference":
@@ -469,6 +560,7 @@ def main():
     peak, peak_kind = peaks()
     achieved = alg / (v_ms / 1e3) / 1e9
     refined = float(np.mean([np.mean(x[1] != 0) for x in na_list]))
+    seqb = statistics.mean(sequential_verify_bytes(x[0], K, V) for x in na_list)
     kvb = statistics.mean(kv_bytes(x[0], w) for x in na_list)
 
     # end-to-end through the public API with host buffers
@@ -545,7 +637,10 @@ def main():
                                       if a.mode == "step" else None),
                       "kv_bytes_per_step": kvb, "refined_row_fraction": refined,
                       "mean_accepted": float(np.mean([x[0].mean() for x in na_list])),
-                      "hbm_frac_of_nominal_8TBs": achieved / 8000.0},
+                      "hbm_frac_of_nominal_8TBs": achieved / 8000.0,
+                      "sequential_bytes_per_launch": (seqb if a.mode != "greedy" else None),
+                      "sequential_frac_of_measured_peak": (
+                          seqb / (v_ms / 1e3) / 1e9 / peak if a.mode != "greedy" else None)},
         }
         print(json.dumps(line))
     if world > 1:
