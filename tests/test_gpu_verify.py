@@ -197,6 +197,28 @@ def test_sample_full_size_sampled_rows(sv, T):
     print(f"full size T={T}:", r, "refined rows:", int(np.sum(g["row_info"] != 0)))
 
 
+@pytest.mark.parametrize("B,K,T", [(1024, 8, 1.0), (1, 8, 0.6), (8, 2, 1.0)])
+def test_sweep_extremes(sv, B, K, T):
+    """Corners of the B x K grid of the sweep at V = 151936 bf16: the largest
+    batch (5.3 GB of logits; 24 rows re-derived by the oracle) and single or
+    few rows (all rows), greedy on the same inputs."""
+    c = synth.sampling_case(B, K, 151936, temperature=T, target_std=3.0, draft_noise_std=0.5,
+                            seed=B + 10 * K, uniform_seed=3)
+    dev = gh.dev_case(c)
+    g = gh.run_sample(sv, c, dev)
+    gg = gh.run_greedy(sv, c, dev)
+    del dev
+    rows = np.sort(np.random.default_rng(1).choice(B, size=min(B, 24), replace=False))
+    t = synth.logits_values(c.target[rows], c.dtype).astype(np.float64)
+    d = synth.logits_values(c.draft[rows], c.dtype).astype(np.float64)
+    o = oracle.verify_sample(t, d, c.tokens[rows], c.uniforms[rows], c.temperature)
+    r = gh.assert_sample_parity(g, o, rows=rows, label=f"B={B} K={K}")
+    assert (g["num_accepted"] >= 0).all() and g["err"] == 0
+    og = oracle.verify_greedy(t, c.tokens[rows])
+    assert np.array_equal(gg["out_tokens"][rows], og["out_tokens"])
+    print(f"B={B} K={K} T={T}:", r)
+
+
 # ------------------------------------------------------------------ edge cases
 @pytest.mark.parametrize("B,K,V,dtype", [
     (3, 1, 64, synth.BF16),          # K = 1
