@@ -15,10 +15,13 @@
 //       finish: combine -> K accept tests -> first rejection j
 //   AR  (rare) double-float sums of target and draft row i when accept test i
 //       falls inside the fp32 error bound; finish: decide test i, go on
-//   BS  (only when all K are accepted) statistics of target row K
-//   SW  fp32 residual (q_j - p_j)+ (or q_K) over the slice of row j, re-read
-//       while hot in L2; per 32-vector unit sums kept in the workspace;
-//       finish: locate u_K * total mass slice -> unit -> entry, certify
+//   BS  (fallback of the bonus draw) statistics of target row K
+//   SW  fp32 residual (q_j - p_j)+ over the slice of row j, re-read
+//       while hot in L2, or for the bonus draw (all K accepted) the raw
+//       masses 2^(z c - Kg) of target row K with an offset Kg guessed from
+//       rows 0..K-1, which needs no statistics stage; per 32-vector unit
+//       sums kept in the workspace; finish: locate u_K * total mass
+//       slice -> unit -> entry, certify
 //   FR  (rare) one double-float pass over the draw's rows: their row sums
 //       S_q, S_p and, per unit, the sums of e_q and e_p over the tokens whose
 //       residual is positive. The sign of q - p = e_q/S_q - e_p/S_p is
@@ -341,6 +344,7 @@ struct FastEntries {
   bool pair;        // residual q - p (else q alone)
   float c, Kq, Rq, Kp, Rp;
   float tauq = -INFINITY, taup = -INFINITY;
+  bool absx = false;  // aq sums q |x| (raw bonus draw) instead of q x
   __device__ __forceinline__ float run(const uint4& vq, const uint4& vp, float (&r)[E::kVec],
                                        float& aq, float& ap) const {
     float zq[E::kVec], zp[E::kVec];
@@ -354,7 +358,8 @@ struct FastEntries {
     for (int k = 0; k < E::kVec; ++k) {
       const float xa = __fmaf_rn(zq[k], c, -Kq);
       const float q = __fmul_rn(ex2_approx(xa), Rq);
-      aq = __fmaf_rn(q, fmaxf(xa, -1.0e4f), aq);
+      const float xc = fmaxf(xa, -1.0e4f);
+      aq = __fmaf_rn(q, absx ? fabsf(xc) : xc, aq);
       if (pair) {
         const float xb = __fmaf_rn(zp[k], c, -Kp);
         const float p = __fmul_rn(ex2_approx(xb), Rp);
@@ -460,6 +465,12 @@ __device__ __forceinline__ DrawRows draw_rows(int K, int aux) {
 // first-stage task is claimed, when the launch's tail has idle CTAs and few
 // runnable tasks; before that whole slices keep the task count low.
 constexpr int kPieceBit = 1 << 9;
+// The bonus draw from q_K without a statistics stage (task aux bit kRawBit):
+// the sweep sums e = 2^(z c - Kg) with a guessed offset Kg (the largest of
+// target rows 0..K-1's) and the draw compares u_K times their total with
+// their prefix sums, so no normaliser enters; a total that is not finite or
+// below 2^-60 (the guess far off) sends the row to the statistics stage BS.
+constexpr int kRawBit = 1 << 10;
 
 __device__ __forceinline__ bool is_piece(const QTask& t) {
   return (t.type == kAR || t.type == kFA || t.type == kFB || t.type == kFR) &&
@@ -616,12 +627,18 @@ __device__ __forceinline__ int load_tokens(const SampleArgs& a, int b) {
 
 // Starts the draw at position j: the residual of target / draft row j with
 // the fp32 statistics given (lane 0's values), or (j == K) the bonus
-// distribution q_K, whose statistics the BS stage supplies first.
+// distribution q_K, drawn without its statistics (kRawBit) with the offset
+// guessed from target rows 0..K-1.
 __device__ void start_draw(const SampleArgs& a, int b, int j, int flags, float Kq, float Rq,
                            float Kp, float Rp) {
   const int lane = threadIdx.x & 31;
+  RowState* st = row_state(a, b);
+  float Kg = 0.f;
+  if (j == a.K) {
+    __syncwarp();  // orders finish_p1's stores of the row offsets
+    Kg = warp_max_f(lane < a.K ? __ldcg(&st->rK[2 * lane]) : -INFINITY);
+  }
   if (lane == 0) {
-    RowState* st = row_state(a, b);
     st->flags = flags;
     if (j < a.K) {
       st->Kq = Kq;
@@ -630,7 +647,9 @@ __device__ void start_draw(const SampleArgs& a, int b, int j, int flags, float K
       st->Rp = Rp;
       enqueue_row_stage(a.ws, kSW, b, a.S, j | (kModeResidual << 8));
     } else {
-      enqueue_row_stage(a.ws, kBS, b, a.S, a.K | (kModeQ << 8));
+      st->Kq = Kg;
+      st->Rq = 1.0f;  // the raw sweep sums e, not q
+      enqueue_row_stage(a.ws, kSW, b, a.S, a.K | (kModeQ << 8) | kRawBit);
     }
   }
   __syncwarp();
@@ -1020,6 +1039,14 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
   const float uK = a.uniforms[size_t(b) * (a.K + 1) + a.K];
   const DrawSlices sl = draw_slices(a, b, false);
   const df Sr = sl.total;
+  const bool raw = (aux & kRawBit) != 0;
+  if (raw && !(Sr.hi > 8.6736174e-19f && Sr.hi < 1e37f)) {
+    // the guessed offset is far off (total below 2^-60, or not finite): the
+    // statistics stage, then the normalised draw
+    if (lane == 0) enqueue_row_stage(a.ws, kBS, b, a.S, a.K | (kModeQ << 8));
+    __syncwarp();
+    return;
+  }
   // Error bound (probability units) of the fp32 sweep. Per term, relative:
   // exp2 (ex2), argument rounding and the fp32 temperature constant (ln2 u |x|
   // each), 1/S and the product (3u), and the row sum behind 1/S (ex2 + ln2 u
@@ -1035,7 +1062,19 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
     return 1.05f * (kQmax * (2.0f * a.bd.ex2 + 3.0f * kU + a.bd.gamma1 + 4.0f * kLn2f * kU) +
                     4.0f * kLn2f * kU * absx);
   };
-  const float Eb = side(sl.f2) + (dr.pair ? side(sl.f3) : 0.f) + 16.0f * kU * Sr.hi + 1e-30f;
+  // Raw bonus draw (units of e, total Sr): t = u_K Sr and every boundary are
+  // sums of the same computed terms, so a factor common to all terms cancels
+  // and no normaliser enters. Per term, relative: exp2 (ex2) and the argument
+  // and temperature-constant roundings (ln2 u |x| each; the constant's part
+  // common to all terms cancels); weights q = e / Sr, sum q|x| from the sweep
+  // (x may be positive here: the offset is a guess).
+  auto side_raw = [&](float A) {
+    const float absx = 1.01f * A / Sr.hi + 1e-6f;
+    return Sr.hi * 1.05f * (kQmax * (a.bd.ex2 + 3.0f * kU + 4.0f * kLn2f * kU) +
+                            2.0f * kLn2f * kU * absx);
+  };
+  const float Eb = (raw ? side_raw(sl.f2) : side(sl.f2) + (dr.pair ? side(sl.f3) : 0.f)) +
+                   16.0f * kU * Sr.hi + 1e-30f;
   const df t = df_mul_f(Sr, uK);
   int token = -1;
   bool cert = false;
@@ -1338,6 +1377,7 @@ __device__ bool consume_sw(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   fe.Rq = __ldcg(&st->Rq);
   fe.Kp = dr.pair ? __ldcg(&st->Kp) : 0.f;
   fe.Rp = dr.pair ? __ldcg(&st->Rp) : 0.f;
+  fe.absx = (t.aux & kRawBit) != 0;
   int v0, v1;
   slice_range(a.nvec, a.S, t.s, v0, v1);
   // the slice total is the pair-arithmetic sum of its unit sums, so slice and
