@@ -281,6 +281,44 @@ def test_offset_beyond_range_is_a_logits_error(sv):
     assert (g["num_accepted"] == -1).all() and (g["out_tokens"] == -1).all()
 
 
+@pytest.mark.parametrize("shift", [-1000.0, -30.0, 40.0, 300.0])
+def test_bonus_row_offset_guess(sv, shift):
+    """Every draft accepted (draft rows = target rows), target row K shifted
+    against rows 0..K-1: the bonus draw's offset, guessed from rows 0..K-1, is
+    then far too high (-1000: every term flushed, the statistics stage takes
+    the row), somewhat high (-30), low (+40: terms up to 2^58, still drawn
+    raw) or far too low (+300: the sums overflow, the statistics stage takes
+    the row). The draws match the oracle in every case."""
+    c = synth.sampling_case(16, 4, 4096, temperature=1.0, target_std=3.0, draft_noise_std=0.0,
+                            dtype=synth.F32, seed=17)
+    t = c.target.copy()
+    t[:, 4, :] += np.float32(shift)
+    c.target = t
+    c.draft = t[:, :4].copy()
+    g = gh.run_sample(sv, c)
+    o = oracle_sample(c)
+    assert (o["num_accepted"] == 4).all()
+    gh.assert_sample_parity(g, o, label=f"shift={shift}")
+    assert g["err"] == 0
+
+
+def test_bonus_row_nan(sv):
+    """A NaN in target row K of a row that accepts every draft: the raw bonus
+    draw's total is NaN, the statistics stage takes the row and reports it."""
+    import speculative_decoding_verification_sample_gb300 as m
+    c = synth.sampling_case(6, 4, 4096, temperature=1.0, target_std=3.0, draft_noise_std=0.0,
+                            dtype=synth.F32, seed=23)
+    t = c.target.copy()
+    t[2, 4, 100] = np.nan
+    c.target = t
+    c.draft = t[:, :4].copy()
+    g = gh.run_sample(sv, c)
+    assert g["num_accepted"][2] == -1 and (g["out_tokens"][2] == -1).all()
+    assert g["err"] & m.SPEC_DERR_LOGITS
+    good = np.array([0, 1, 3, 4, 5])
+    gh.assert_sample_parity(g, oracle_sample(c, good), rows=good)
+
+
 def test_identical_draft_accepts_everything(sv):
     c = synth.sampling_case(8, 4, 4096, temperature=1.0, target_std=3.0, draft_noise_std=0.0,
                             seed=3)
