@@ -141,17 +141,28 @@ def kv_commit(block_table, seq_lens, num_accepted, prov_blocks, free_stack, free
                 copies=copies, err=0)
 
 
-def pool_invariant_ok(block_table, prov_blocks, free_stack, free_top: int, num_blocks: int,
-                      seq_lens=None, block_size: int | None = None) -> bool:
-    """No leak, no double free: the live free-stack entries, the block-table entries
-    and the provisional blocks together hold every block id exactly once."""
-    bt = np.asarray(block_table).ravel()
-    pb = np.asarray(prov_blocks).ravel()
-    fs = np.asarray(free_stack)[: int(free_top)]
-    ids = np.concatenate([bt[bt >= 0], pb[pb >= 0], fs])
-    if ids.size != num_blocks:
+def pool_invariant_ok(block_table, prov_blocks, free_stack, free_top: int, num_blocks: int) -> bool:
+    """No leak, no double free (sglang_spec_decode README, provisional layer:
+    no block may be leaked or freed twice across all rejection patterns).
+
+    The live holders of a block are the block-table entries, the provisional
+    entries and the free-stack entries below free_top; -1 marks an unused
+    table or provisional entry, and stack entries at or above free_top are
+    dead. The pool is sound when every id 0..num_blocks-1 has exactly one
+    live holder and no live entry holds anything else (an id out of range,
+    or a negative value other than -1).
+    """
+    bt = np.asarray(block_table, np.int64).ravel()
+    pb = np.asarray(prov_blocks, np.int64).ravel()
+    stack = np.asarray(free_stack, np.int64).ravel()
+    top = int(free_top)
+    if top < 0 or top > stack.size:
         return False
-    return bool(np.array_equal(np.sort(ids), np.arange(num_blocks)))
+    live = np.concatenate([bt[bt != -1], pb[pb != -1], stack[:top]])
+    if np.any((live < 0) | (live >= num_blocks)):
+        return False
+    holders = np.bincount(live, minlength=num_blocks)
+    return bool(np.all(holders == 1))
 
 
 def kv_truncate_inplace(block_table, seq_lens, num_accepted, free_stack, free_top: int, *,

@@ -175,16 +175,28 @@ def verify_greedy(target, tokens) -> dict:
     g_i = argmax of target row i over raw logits, ties to the lowest index
     (temperature does not change an argmax). n = number of leading positions
     with d_i == g_i; the emitted tokens are d_0..d_{n-1}, g_n, then -1.
+
+    Unusable input (the pages are silent; same reading as verify_tree_greedy):
+    a row with a NaN has no argmax and never matches a draft token; if the
+    step uses it (row n, the first position not accepted, or row K after K
+    acceptances) the batch row is an error. A draft token outside [0, V) is an
+    error too. An error row has out_tokens all -1 and num_accepted -1. A row of
+    equal values (all -inf included) has argmax 0 by the lowest-index rule.
     """
     target = np.asarray(target)
     tokens = np.asarray(tokens, np.int64)
     B, K1, V = target.shape
     K = K1 - 1
+    rows = np.arange(B)
+    bad_row = np.isnan(target).any(axis=-1)
     g = np.argmax(target.astype(np.float64), axis=-1)
-    n = _leading_true(tokens == g[:, :K])
+    n = _leading_true((tokens == g[:, :K]) & ~bad_row[:, :K])
+    error = bad_row[rows, n] | ((tokens < 0) | (tokens >= V)).any(axis=1)
     out = np.full((B, K1), -1, np.int64)
     out[:, :K] = np.where(np.arange(K)[None, :] < n[:, None], tokens, -1)
-    out[np.arange(B), n] = g[np.arange(B), n]
+    out[rows, n] = g[rows, n]
+    out[error] = -1
+    n = np.where(error, -1, n)
     return dict(out_tokens=out, num_accepted=n, argmax=g)
 
 

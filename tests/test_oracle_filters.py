@@ -1,7 +1,8 @@
 """Pins of the top-k / top-p filter oracle (CPU only).
 
-The oracle scans the distinct kept values in descending order. The pins check
-it against hand-worked rows, a brute force that tries every logit of the row
+The oracle takes the k-th largest logit for top-k and, for top-p, the first
+position of the descending sort whose cumulative mass reaches p. The pins
+check it against hand-worked rows, a brute force that tries every logit of the row
 as a candidate threshold, the defining properties of the kept set, the
 limits of the parameters, and the losslessness of verification on the
 filtered distributions (the emitted token follows the filtered target).

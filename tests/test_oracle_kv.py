@@ -209,3 +209,91 @@ def test_bad_slot_map_entry_leaves_state_unchanged(bad):
     assert res["err"] == okv.ERR_BAD_SLOT
     assert np.array_equal(res["block_table"], c.block_table) and res["copies"] == []
     assert np.array_equal(res["seq_lens"], c.seq_lens) and res["free_top"] == c.free_top
+
+
+# ------------------------------------------------------- the pool checker itself
+def _pool(case):
+    return dict(block_table=case.block_table.copy(), prov_blocks=case.prov_blocks.copy(),
+                free_stack=case.free_stack.copy(), free_top=int(case.free_top),
+                num_blocks=case.num_blocks)
+
+
+def _sound_pool():
+    c = synth.kv_case(3, 4, seq_lens=np.array([20, 33, 16]), num_accepted=np.array([1, 4, 0]),
+                      spare_blocks=5, seed=11)
+    st = _pool(c)
+    assert oracle.pool_invariant_ok(**st)
+    return st
+
+
+def test_pool_checker_rejects_a_leaked_block():
+    """A block that no table, provisional entry or live stack entry holds."""
+    st = _sound_pool()
+    st["block_table"][1, 0] = -1
+    assert not oracle.pool_invariant_ok(**st)
+    st = _sound_pool()
+    st["free_top"] -= 1                     # the top stack entry becomes dead
+    assert not oracle.pool_invariant_ok(**st)
+
+
+def test_pool_checker_rejects_a_block_in_two_tables():
+    st = _sound_pool()
+    leaked = int(st["block_table"][1, 0])
+    st["block_table"][1, 0] = st["block_table"][0, 0]      # double allocation
+    assert not oracle.pool_invariant_ok(**st)
+    # even when the count of live entries is restored by freeing the lost id
+    st["free_stack"][st["free_top"]] = leaked
+    st["free_top"] += 1
+    st["block_table"][2, 0] = -1
+    assert not oracle.pool_invariant_ok(**st)
+
+
+def test_pool_checker_rejects_a_block_in_a_table_and_on_the_stack():
+    st = _sound_pool()
+    top = st["free_top"]
+    st["free_stack"][top - 1] = st["block_table"][0, 1]    # double free
+    assert not oracle.pool_invariant_ok(**st)
+
+
+def test_pool_checker_rejects_a_provisional_block_also_free():
+    st = _sound_pool()
+    st["free_stack"][st["free_top"]] = st["prov_blocks"][2, 0]
+    st["free_top"] += 1
+    assert not oracle.pool_invariant_ok(**st)
+
+
+@pytest.mark.parametrize("where", ["table", "prov", "stack"])
+@pytest.mark.parametrize("bad", ["num_blocks", "minus_two"])
+def test_pool_checker_rejects_an_out_of_range_id(where, bad):
+    st = _sound_pool()
+    v = st["num_blocks"] if bad == "num_blocks" else -2
+    if where == "table":
+        st["block_table"][0, 0] = v
+    elif where == "prov":
+        st["prov_blocks"][1, 0] = v
+    else:
+        st["free_stack"][0] = v
+    assert not oracle.pool_invariant_ok(**st)
+
+
+def test_pool_checker_ignores_dead_stack_entries_only():
+    """Entries at or above free_top are dead: a stale copy there of a block in a
+    table is fine, but a block whose only copy is there is leaked."""
+    st = _sound_pool()
+    top = st["free_top"]
+    st["free_stack"][top] = st["block_table"][2, 0]        # stale, dead entry
+    assert oracle.pool_invariant_ok(**st)
+    st = _sound_pool()
+    top = st["free_top"]
+    st["free_stack"][top], st["free_stack"][top - 1] = st["free_stack"][top - 1], -1
+    st["free_top"] = top - 1                               # the only copy is now dead
+    assert not oracle.pool_invariant_ok(**st)
+
+
+def test_pool_checker_rejects_a_top_outside_the_stack():
+    st = _sound_pool()
+    st["free_top"] = -1
+    assert not oracle.pool_invariant_ok(**st)
+    st = _sound_pool()
+    st["free_top"] = st["free_stack"].size + 1
+    assert not oracle.pool_invariant_ok(**st)

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
+from oracle import kv as okv
 from oracle import verify as ov
 from tests import test_oracle_verify as tv
 
@@ -221,3 +222,25 @@ def test_top_p_without_temperature_is_caught(monkeypatch):
     monkeypatch.setattr(ofl, "filter_threshold", wrong)
     monkeypatch.setattr(oracle, "filter_threshold", wrong)
     assert _fails(tf.test_brute_force, 1) or _fails(tf.test_parameter_limits)
+
+
+def test_always_true_pool_checker_is_caught(monkeypatch):
+    """A pool checker that accepts everything fails the checker's own pins."""
+    from tests import test_oracle_kv as tk
+    monkeypatch.setattr(okv, "pool_invariant_ok", lambda *a, **k: True)
+    monkeypatch.setattr(oracle, "pool_invariant_ok", lambda *a, **k: True)
+    assert _fails(tk.test_pool_checker_rejects_a_leaked_block)
+    assert _fails(tk.test_pool_checker_rejects_a_block_in_a_table_and_on_the_stack)
+
+
+def test_stack_counted_past_top_is_caught(monkeypatch):
+    """A checker that counts every stack entry, live or dead."""
+    from tests import test_oracle_kv as tk
+
+    def wrong(block_table, prov_blocks, free_stack, free_top, num_blocks):
+        fs = np.asarray(free_stack)
+        return okv.__dict__["_real_pool_ok"](block_table, prov_blocks, fs, fs.size, num_blocks)
+
+    okv.__dict__["_real_pool_ok"] = okv.pool_invariant_ok
+    monkeypatch.setattr(oracle, "pool_invariant_ok", wrong)
+    assert _fails(tk.test_pool_checker_ignores_dead_stack_entries_only)

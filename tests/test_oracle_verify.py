@@ -219,3 +219,31 @@ def test_sampling_prefix_is_accepted_drafts():
         assert r["out_tokens"][b, :n].tolist() == c.tokens[b, :n].tolist()
         assert 0 <= r["out_tokens"][b, n] < c.V
         assert (r["out_tokens"][b, n + 1:] == -1).all()
+
+
+def test_greedy_unusable_rows_by_hand():
+    """Greedy with a NaN row or a bad draft token, worked by hand: a NaN row
+    has no argmax; it makes the batch row an error only when the step uses it
+    (the first position not accepted, or row K after K acceptances); a draft
+    token outside [0, V) is always an error. Rows of equal values (-inf
+    included) have argmax 0."""
+    nan, inf = np.nan, np.inf
+    V = 4
+    good = [0.0, 3.0, 1.0, 2.0]                  # argmax 1
+    cases = [
+        # (rows 0..K, draft tokens, expected out, expected n)
+        ([[0, nan, 1, 2], good, good], [1, 1], [-1, -1, -1], -1),   # row 0 used, NaN
+        ([good, [0, 1, nan, 2], good], [1, 1], [-1, -1, -1], -1),   # row 1 is the first mismatch
+        ([good, good, [nan] * 4], [1, 1], [-1, -1, -1], -1),        # all accepted, bonus row NaN
+        ([good, good, [nan] * 4], [1, 3], [1, 1, -1], 1),           # row 2 never used
+        ([good, [2, 9, 9, 0], [nan] * 4], [2, 1], [1, -1, -1], 0),  # mismatch at 0
+        ([good, good, good], [1, 4], [-1, -1, -1], -1),             # token out of range
+        ([good, good, good], [-1, 1], [-1, -1, -1], -1),            # negative token
+        ([[-inf] * 4, good, good], [0, 1], [0, 1, 1], 2),           # all -inf: argmax 0
+        ([[5, 5, 5, 5], good, good], [1, 1], [0, -1, -1], 0),       # tie: lowest index
+    ]
+    for rows, tok, exp_out, exp_n in cases:
+        z = np.array([rows], np.float64)
+        r = oracle.verify_greedy(z, np.array([tok]))
+        assert r["out_tokens"][0].tolist() == exp_out, (rows, tok)
+        assert int(r["num_accepted"][0]) == exp_n, (rows, tok)
