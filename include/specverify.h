@@ -39,8 +39,10 @@
  * Conventions for every entry point:
  *   - All array arguments are DEVICE pointers owned by the caller. The library
  *     allocates no device or host memory and keeps no state between calls
- *     (its only static data is a read-only constant table and a per-process
- *     cache of occupancy queries). The verify calls take a caller-allocated
+ *     (its only static data is a read-only constant table, a per-process cache
+ *     of occupancy queries and, as the one exception, the 4 MiB writable
+ *     device scratch of spec_verify_greedy_noalloc, which all of that entry
+ *     point's calls on a device share). The verify calls take a caller-allocated
  *     device workspace of spec_verify_workspace_bytes(B, K, V, dtype) bytes
  *     (256-byte aligned) that holds per-slice partial sums and the work queue;
  *     its contents need no initialisation, and calls that share one workspace
@@ -236,14 +238,17 @@ int spec_filter_thresholds(const void* logits, int R, int V, int dtype, float te
  * whose device memory is owned by another framework's pool, or plain C
  * callers with no device allocator at hand. The call itself allocates
  * nothing either: it uses one built-in device array of
- * spec_verify_greedy_noalloc_max_bytes() bytes (4 MiB), located on the
- * first call on each device with cudaGetSymbolAddress (that first call does
- * this setup and may load the module; issue it before any stream capture).
+ * spec_verify_greedy_noalloc_max_bytes() bytes (4 MiB), which every GPU that
+ * loads the library holds until the process exits. Each call looks up the
+ * array's address on the current device with cudaGetSymbolAddress; the first
+ * call on a device may load the library's module there, so issue it before
+ * any stream capture.
  *
  *   Arguments, outputs and errors: as spec_verify_greedy, without workspace.
  *   Returns SPEC_ENOTSUP when the step needs more scratch than the built-in
  *   array holds (spec_verify_workspace_bytes(B, K, V, dtype) > 4 MiB; e.g.
- *   B = 256, K = 4, V = 151936 bf16 needs about 1.6 MiB), SPEC_ECUDA when the
+ *   B = 256, K = 4, V = 151936 bf16 needs about 3.1 MiB; B = 1024 steps with
+ *   V >= 128256 need 9.8 to 12.4 MiB and are refused), SPEC_ECUDA when the
  *   array's address cannot be obtained.
  *   The scratch's counters and queue are cleared on `stream` at every call.
  *   All calls on one device share the array: calls that can overlap on the
@@ -345,10 +350,10 @@ int kv_evict_provisional(int32_t* block_table, int32_t* seq_lens, int num_blocks
 
 /*
  * spec_selftest_ex2 - diagnostic: the maximum relative error of the hardware
- * base-2 exponential over every fp32 argument in [lo, hi] (-126 <= lo <= hi <= 64),
+ * base-2 exponential over every fp32 argument in [lo, hi] (-126 <= lo <= hi <= 127),
  * measured against fp64 exp2 and written to the device double *out_max_rel.
  * The sampler's certification assumes this maximum stays below its built-in
- * bound on [-126, 1]; tests re-measure it on the GPU in use.
+ * bound on [-126, 127]; tests re-measure it on the GPU in use.
  */
 int spec_selftest_ex2(float lo, float hi, double* out_max_rel, void* stream);
 

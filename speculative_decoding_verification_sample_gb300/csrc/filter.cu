@@ -776,13 +776,10 @@ int launch_filter(const FilterLaunch& f) {
   if (f.dtype == SPEC_BF16) {
     const bool topk = f.top_k > 0 && f.top_k < f.V;
     if (topk || f.top_p < 1.0f) {
-      static int sms = 0;
-      if (sms == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (sms < 1) sms = 1;
-      }
+      int dev = 0, sms = 0;  // a cheap attribute query on every call: no shared host state
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (sms < 1) sms = 1;
       const int grid = f.R < 3 * sms ? f.R : 3 * sms;
       if (topk) filter_topk_bf16_kernel<false><<<grid, kFTK, 0, st>>>(a);
       else filter_topk_bf16_kernel<true><<<grid, kFTK, 0, st>>>(a);

@@ -33,7 +33,7 @@ __global__ void ex2_error_kernel(uint32_t lo_bits, uint64_t count, int negative,
 }  // namespace sv
 
 extern "C" int spec_selftest_ex2(float lo, float hi, double* out_max_rel, void* stream) {
-  if (!out_max_rel || !(lo <= hi) || lo < -126.0f || hi > 64.0f) return SPEC_EINVAL;
+  if (!out_max_rel || !(lo <= hi) || lo < -126.0f || hi > 127.0f) return SPEC_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   auto* out = reinterpret_cast<unsigned long long*>(out_max_rel);
   if (cudaMemsetAsync(out, 0, sizeof(double), st) != cudaSuccess) return SPEC_ECUDA;

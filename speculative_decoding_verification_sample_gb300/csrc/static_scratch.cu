@@ -1,15 +1,19 @@
 // spec_verify_greedy_noalloc: spec_verify_greedy with the library's own
 // built-in device scratch instead of a caller-provided workspace.
 //
-// The scratch is one file-scope device array of kStaticScratchBytes. Its
-// device address is looked up once per device with cudaGetSymbolAddress (the
-// first call on a device does that setup, which may load the module) and
-// cached; every call then hands that address to spec_verify_greedy as its
-// workspace. Nothing is allocated: no cudaMalloc, no cudaFree, no library
-// routine that allocates. Of the scratch, the header, row counters and work
-// queue must start at zero for every launch; spec_verify_greedy clears them
-// itself with cudaMemsetAsync on the caller's stream, so no state carries
-// over between calls.
+// The scratch is one file-scope device array of kStaticScratchBytes; every
+// GPU that loads the library holds it until the process exits. Host code
+// cannot use the array's name as a device address, so every call looks the
+// address up with cudaGetSymbolAddress on the current device and checks the
+// result. The first call on a device may load the library's module there,
+// so that first call should come before any stream capture. Looking the
+// address up on every call (instead of caching it) keeps it right after a
+// context is torn down and re-created, and leaves no shared host state for
+// concurrent callers to race on. Nothing is allocated: no cudaMalloc, no
+// cudaFree, no library routine that allocates. Of the scratch, the header,
+// row counters and work queue must start at zero for every launch;
+// spec_verify_greedy clears them itself with cudaMemsetAsync on the caller's
+// stream, so no state carries over between calls.
 //
 // All calls on one device share the one scratch: two calls whose launches
 // can overlap on the device (different streams without ordering, several
@@ -24,11 +28,8 @@
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) uint8_t g_scratch[kStaticScratchBytes];
-
-void* g_scratch_ptr[kMaxDevices];  // per-device address, set on first use
 
 }  // namespace
 
@@ -46,16 +47,11 @@ int spec_verify_greedy_noalloc(const void* target_logits, const int32_t* draft_t
                               stream, dtype, err_flag, nullptr, 0, nullptr);
   }
   if (need > kStaticScratchBytes) return SPEC_ENOTSUP;  // larger than the built-in scratch
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPEC_ECUDA;
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return SPEC_ECUDA;
-    g_scratch_ptr[dev] = p;
-  }
+  void* scratch = nullptr;  // the array's device address on the current device
+  if (cudaGetSymbolAddress(&scratch, g_scratch) != cudaSuccess || scratch == nullptr)
+    return SPEC_ECUDA;
   return spec_verify_greedy(target_logits, draft_tokens, B, K, V, out_tokens, out_num_accepted,
-                            stream, dtype, err_flag, g_scratch_ptr[dev], kStaticScratchBytes,
-                            nullptr);
+                            stream, dtype, err_flag, scratch, kStaticScratchBytes, nullptr);
 }
 
 }  // extern "C"

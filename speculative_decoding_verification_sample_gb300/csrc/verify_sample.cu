@@ -1040,9 +1040,11 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
   const DrawSlices sl = draw_slices(a, b, false);
   const df Sr = sl.total;
   const bool raw = (aux & kRawBit) != 0;
-  if (raw && !(Sr.hi > 8.6736174e-19f && Sr.hi < 1e37f)) {
-    // the guessed offset is far off (total below 2^-60, or not finite): the
-    // statistics stage, then the normalised draw
+  if (raw && !(Sr.hi > 8.6736174e-19f && Sr.hi < 1.2676506e30f)) {
+    // the guessed offset is far off (total below 2^-60 or above 2^100, or not
+    // finite): the statistics stage, then the normalised draw. Below 2^100
+    // every exponent argument is below 100, inside the range over which the
+    // ex2 bound is measured, and the sweep's sum of q|x| stays finite.
     if (lane == 0) enqueue_row_stage(a.ws, kBS, b, a.S, a.K | (kModeQ << 8));
     __syncwarp();
     return;
