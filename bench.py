@@ -375,18 +375,18 @@ def kv_bytes(na, w):
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
-def oracle_sample_rate(rows: int, T: float, budget_s: float):
-    """Times the fp64 oracle (verify + KV bookkeeping) on `rows` rows of the workload
-    until `budget_s` seconds; returns positions/s and a description."""
-    import numpy as np
+def _oracle_worker(job):
+    """One host process: the fp64 oracle (verify + KV bookkeeping) on `rows` rows
+    of the workload, repeated until `budget_s` seconds; returns (positions, s)."""
+    rows, T, budget_s, seed = job
     import oracle
     import synth
     w = WORKLOAD
     c = synth.sampling_case(rows, w["K"], w["V"], temperature=T, target_std=w["target_std"],
-                            draft_noise_std=w["sigma"], seed=99, uniform_seed=99)
+                            draft_noise_std=w["sigma"], seed=seed, uniform_seed=seed)
     t_vals, d_vals = c.target_values(), c.draft_values()
     kc = synth.kv_case(rows, w["K"], block_size=w["block_size"], prefix_lo=w["prefix_lo"],
-                       prefix_hi=w["prefix_hi"], seed=45)
+                       prefix_hi=w["prefix_hi"], seed=seed)
     done, t0 = 0, time.perf_counter()
     while True:
         r = oracle.verify_sample(t_vals, d_vals, c.tokens, c.uniforms, T)
@@ -397,22 +397,84 @@ def oracle_sample_rate(rows: int, T: float, budget_s: float):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    rate = done * rows * w["K"] / el
-    return rate, el, done
+    return done * rows * w["K"], el
+
+
+def oracle_rate(T: float, budget_s: float, procs: int | None = None):
+    """The fp64 oracle on the host cores, rows split over `procs` processes (all
+    cores by default; started with `spawn`, so no process inherits a CUDA
+    context), one batch row each, each repeating its row for `budget_s`
+    seconds. Returns (positions/s over all processes, processes, description)."""
+    import multiprocessing as mp
+    procs = procs or os.cpu_count() or 1
+    jobs = [(1, T, budget_s, 99 + i) for i in range(procs)]
+    if procs == 1:
+        res = [_oracle_worker(jobs[0])]
+    else:
+        with mp.get_context("spawn").Pool(procs) as pool:
+            res = pool.map(_oracle_worker, jobs)
+    positions = sum(r[0] for r in res)
+    el = max(r[1] for r in res)
+    rate = positions / el
+    desc = (f"{procs} host processes (os.cpu_count() = {os.cpu_count()}), one batch row of the "
+            f"workload each (K={WORKLOAD['K']}, V={WORKLOAD['V']}, T={T}), verify + KV "
+            f"bookkeeping repeated for {el:.1f} s; rate = positions of all processes / the "
+            f"longest process time; NumPy fp64")
+    return rate, procs, desc
 
 
 # ------------------------------------------------------------------ main
 SWEEP = dict(B=(1, 8, 64, 256, 1024), K=(2, 4, 8), V=(32000, 128256, 151936), T=(0.0, 0.6, 1.0))
 
 
+def sweep_cell(torch, sv, B, K, V, T, reps, flush, peak, peak_kind):
+    """One cell of the sweep: 3 warm-up launches, then `reps` launches timed with
+    CUDA events around each one and a write of `flush` (larger than L2) between
+    them; the median launch with its algorithmic bytes against the peak."""
+    import numpy as np
+    bt = gen_batch(torch, 7 + B + K, T if T > 0 else 1.0, B=B, K=K, V=V)
+    out = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
+    n = torch.empty((B,), dtype=torch.int32, device="cuda")
+    if T > 0:
+        def call():
+            sv.spec_verify_sample(bt["target"], bt["draft"], bt["tokens"], bt["uniforms"], T,
+                                  out, n)
+    else:
+        def call():
+            sv.spec_verify_greedy(bt["target"], bt["tokens"], out, n)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    na = n.cpu().numpy()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = float(np.median(ts))
+    alg = algorithmic_verify_bytes(na, K, V) if T > 0 else greedy_verify_bytes(na, K, V)
+    gbs = alg / (ms / 1e3) / 1e9
+    cell = {"sweep": {"B": B, "K": K, "V": V, "T": T, "mode": "sample" if T > 0 else "greedy"},
+            "us": ms * 1e3, "positions_per_s": B * K / (ms / 1e3), "algorithmic_bytes": alg,
+            "gbs": gbs, "frac": gbs / peak, "peak_kind": peak_kind,
+            "mean_accepted": float(na.mean())}
+    if T > 0:
+        cell["sequential_frac"] = sequential_verify_bytes(na, K, V) / (ms / 1e3) / 1e9 / peak
+    del bt
+    torch.cuda.empty_cache()
+    return cell
+
+
 def run_sweep(a):
     """Verify-launch times over the grid of batch sizes, draft lengths, vocabularies
     and temperatures (T = 0: greedy), bf16 logits generated like the bench
-    workload (target N(0, 3^2), draft = target + N(0, 0.5^2)). Each cell: 3
-    warm-up launches, then `--steps` (at most 20) timed launches with CUDA events
-    around each one and a 256 MB write between them (L2 flush); the median is
-    reported with its algorithmic bytes against the measured HBM peak."""
-    import numpy as np
+    workload (target N(0, 3^2), draft = target + N(0, 0.5^2)); one JSON line
+    per cell (sweep_cell, at most 20 timed launches)."""
     import torch
     import speculative_decoding_verification_sample_gb300 as sv
     from speculative_decoding_verification_sample_gb300 import build
@@ -424,48 +486,64 @@ def run_sweep(a):
     for V in SWEEP["V"]:
         for K in SWEEP["K"]:
             for B in SWEEP["B"]:
-                bt = None
                 for T in SWEEP["T"]:
-                    bt = gen_batch(torch, 7 + B + K, T if T > 0 else 1.0, B=B, K=K, V=V)
-                    out = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
-                    n = torch.empty((B,), dtype=torch.int32, device="cuda")
-                    if T > 0:
-                        def call():
-                            sv.spec_verify_sample(bt["target"], bt["draft"], bt["tokens"],
-                                                  bt["uniforms"], T, out, n)
-                    else:
-                        def call():
-                            sv.spec_verify_greedy(bt["target"], bt["tokens"], out, n)
-                    for _ in range(3):
-                        call()
-                    torch.cuda.synchronize()
-                    na = n.cpu().numpy()
-                    ts = []
-                    for _ in range(reps):
-                        flush.zero_()
-                        e0 = torch.cuda.Event(enable_timing=True)
-                        e1 = torch.cuda.Event(enable_timing=True)
-                        e0.record()
-                        call()
-                        e1.record()
-                        torch.cuda.synchronize()
-                        ts.append(e0.elapsed_time(e1))
-                    ms = float(np.median(ts))
-                    alg = (algorithmic_verify_bytes(na, K, V) if T > 0
-                           else greedy_verify_bytes(na, K, V))
-                    gbs = alg / (ms / 1e3) / 1e9
-                    cell = {"sweep": {"B": B, "K": K, "V": V, "T": T,
-                                      "mode": "sample" if T > 0 else "greedy"},
-                            "us": ms * 1e3, "positions_per_s": B * K / (ms / 1e3),
-                            "algorithmic_bytes": alg, "gbs": gbs, "frac": gbs / peak,
-                            "peak_kind": peak_kind, "mean_accepted": float(na.mean())}
-                    if T > 0:
-                        cell["sequential_frac"] = (sequential_verify_bytes(na, K, V)
-                                                   / (ms / 1e3) / 1e9 / peak)
+                    cell = sweep_cell(torch, sv, B, K, V, T, reps, flush, peak, peak_kind)
                     print(json.dumps(cell), flush=True)
-                    del bt
-                    bt = None
-                torch.cuda.empty_cache()
+
+
+SWEEP_SMALL = dict(B=(1, 8, 1024), K=4, V=151936, T=(0.0, 1.0))
+
+
+def sweep_small(torch, sv, peak, peak_kind, reps=20):
+    """The sweep cells B in {1, 8, 1024} x T in {0 (greedy), 1} at K=4, V=151936."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    cells = []
+    for B in SWEEP_SMALL["B"]:
+        for T in SWEEP_SMALL["T"]:
+            c = sweep_cell(torch, sv, B, SWEEP_SMALL["K"], SWEEP_SMALL["V"], T, reps, flush,
+                           peak, peak_kind)
+            cells.append({k: c[k] for k in ("sweep", "us", "positions_per_s", "gbs", "frac",
+                                            "mean_accepted")})
+    del flush
+    torch.cuda.empty_cache()
+    return cells
+
+
+def greedy_stats(torch, sv, batches, peak, reps=100):
+    """verify_greedy_kernel on the bench's rotating batches (B=256, K=4,
+    V=151936 bf16): mean device time per launch (CUDA events around each
+    launch), algorithmic bytes = target rows 0..K-1 of every row + row K of
+    the rows the greedy rule accepts in full + per-row I/O, and the fraction
+    of the measured HBM peak."""
+    import numpy as np
+    w = WORKLOAD
+    B, K, V = w["B"], w["K"], w["V"]
+    out = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
+    n = torch.empty((B,), dtype=torch.int32, device="cuda")
+    nas = []
+    for bt in batches:
+        sv.spec_verify_greedy(bt["target"], bt["tokens"], out, n)
+        torch.cuda.synchronize()
+        nas.append(n.cpu().numpy().copy())
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    nb = len(batches)
+    for i in range(reps + 3):
+        bt = batches[i % nb]
+        if i >= 3:
+            evs[i - 3][0].record(stream)
+        sv.spec_verify_greedy(bt["target"], bt["tokens"], out, n)
+        if i >= 3:
+            evs[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    us = 1e3 * statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    alg = statistics.mean(greedy_verify_bytes(x, K, V) for x in nas)
+    gbs = alg / (us / 1e6) / 1e9
+    return {"kernel": "verify_greedy_kernel<bf16>", "us": us, "algorithmic_bytes": alg,
+            "gbs": gbs, "frac_of_measured_peak": gbs / peak,
+            "mean_accepted": float(np.mean([x.mean() for x in nas])),
+            "positions_per_s": B * K / (us / 1e6)}
 
 
 def main():
@@ -553,7 +631,12 @@ def main():
     # roofline of the dominant kernel (spec_verify_sample), live CUDA-event durations
     if a.mode == "greedy":
         # greedy reads target rows 0..K-1, plus row K for rows that accept everything
-        alg = statistics.mean(B * K * V * 2 + B * 8 * K for _ in range(nb))
+        gna = []
+        for bt in batches:
+            sv.spec_verify_greedy(bt["target"], bt["tokens"], out, n)
+            torch.cuda.synchronize()
+            gna.append(n.cpu().numpy().copy())
+        alg = statistics.mean(greedy_verify_bytes(x, K, V) for x in gna)
     else:
         alg = statistics.mean(algorithmic_verify_bytes(x[0], K, V) for x in na_list)
     v_ms = statistics.mean(verify_ms)
@@ -603,10 +686,9 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline and a.mode == "step":
-        rate, el, reps = oracle_sample_rate(4, T, 12.0)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"4 rows of the workload (B=4, K=4, V=151936, T={T}) verify + KV "
-                         f"bookkeeping, {reps} repetitions in {el:.1f} s, single-threaded NumPy fp64"}
+        rate, procs, desc = oracle_rate(T, 10.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": procs, "nproc": os.cpu_count(),
+               "kind": "oracle", "rows_split_over_processes": procs > 1, "sample": desc}
 
     if rank == 0:
         line = {
@@ -634,6 +716,10 @@ def main():
                       "tree_greedy": (tree_greedy_stats(torch, sv, peak)
                                       if a.mode == "step" else None),
                       "top_k_top_p": (filter_stats(torch, sv, batches[0], T, peak)
+                                      if a.mode == "step" else None),
+                      "greedy": (greedy_stats(torch, sv, batches, peak)
+                                 if a.mode == "step" else None),
+                      "sweep_small": (sweep_small(torch, sv, peak, peak_kind)
                                       if a.mode == "step" else None),
                       "kv_bytes_per_step": kvb, "refined_row_fraction": refined,
                       "mean_accepted": float(np.mean([x[0].mean() for x in na_list])),
@@ -666,44 +752,69 @@ def job_rate(world, B, K, ms_per_step):
     return world * B * K / (ms_per_step / 1e3)
 
 
-def run_reference(a, rank, world, T):
-    """Reference arm: the fp64 CPU oracle on a bounded sample of the same workload."""
-    if rank != 0:
-        return
-    import numpy as np
-    import oracle
+_REF_CASES = {}
+
+
+def _reference_init(rows, T):
+    """Pool initializer: every process generates all `rows` batch rows once, so
+    whichever row a step hands it is ready."""
     import synth
     w = WORKLOAD
-    rows = 1
-    c = synth.sampling_case(rows, w["K"], w["V"], temperature=T, target_std=w["target_std"],
-                            draft_noise_std=w["sigma"], seed=99, uniform_seed=99)
-    tv, dv = c.target_values(), c.draft_values()
-    kc = synth.kv_case(rows, w["K"], block_size=w["block_size"], prefix_lo=w["prefix_lo"],
-                       prefix_hi=w["prefix_hi"], seed=45)
+    for i in range(rows):
+        c = synth.sampling_case(1, w["K"], w["V"], temperature=T, target_std=w["target_std"],
+                                draft_noise_std=w["sigma"], seed=99 + i, uniform_seed=99 + i)
+        kc = synth.kv_case(1, w["K"], block_size=w["block_size"], prefix_lo=w["prefix_lo"],
+                           prefix_hi=w["prefix_hi"], seed=99 + i)
+        _REF_CASES[i] = (c, c.target_values(), c.draft_values(), kc)
 
-    def step():
-        r = oracle.verify_sample(tv, dv, c.tokens, c.uniforms, T)
-        oracle.kv_commit(kc.block_table, kc.seq_lens, r["num_accepted"], kc.prov_blocks,
-                         kc.free_stack, kc.free_top, block_size=w["block_size"], K=w["K"],
-                         num_blocks=kc.num_blocks)
 
-    for _ in range(max(3, a.warmup)):
-        step()
+def _reference_row(job):
+    """One row of the reference arm in a host process: the fp64 oracle's verify +
+    KV bookkeeping on batch row `i` of the workload."""
+    i, T = job
+    import oracle
+    w = WORKLOAD
+    c, tv, dv, kc = _REF_CASES[i]
     t0 = time.perf_counter()
-    for _ in range(a.steps):
-        step()
-    el = time.perf_counter() - t0
+    r = oracle.verify_sample(tv, dv, c.tokens, c.uniforms, T)
+    oracle.kv_commit(kc.block_table, kc.seq_lens, r["num_accepted"], kc.prov_blocks,
+                     kc.free_stack, kc.free_top, block_size=w["block_size"], K=w["K"],
+                     num_blocks=kc.num_blocks)
+    return time.perf_counter() - t0
+
+
+def run_reference(a, rank, world, T):
+    """Reference arm: the fp64 CPU oracle on a bounded sample of the same workload.
+    Each step verifies one batch row per host core, the rows split over a pool of
+    `spawn`ed processes (one row per process, generated once); the step time is
+    the wall time of that parallel map."""
+    if rank != 0:
+        return
+    import multiprocessing as mp
+    w = WORKLOAD
+    procs = os.cpu_count() or 1
+    jobs = [(i, T) for i in range(procs)]
+    with mp.get_context("spawn").Pool(procs, initializer=_reference_init,
+                                      initargs=(procs, T)) as pool:
+        for _ in range(max(3, a.warmup)):
+            pool.map(_reference_row, jobs)
+        t0 = time.perf_counter()
+        for _ in range(a.steps):
+            pool.map(_reference_row, jobs)
+        el = time.perf_counter() - t0
     ms = el * 1e3 / a.steps
-    value = rows * w["K"] / (el / a.steps)
+    value = procs * w["K"] / (el / a.steps)
+    sample = (f"{procs} batch rows per step (one per host process, os.cpu_count() = "
+              f"{os.cpu_count()}), verify + KV bookkeeping, NumPy fp64")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": a.steps, "warmup": max(3, a.warmup), "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": workload_name(T) + " (oracle: 1 row per step)",
-                       "global_batch": rows, "K": w["K"], "V": w["V"]},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": "1 batch row per step (verify + KV bookkeeping), "
-                                       "single-threaded NumPy fp64"},
+            "config": {"workload": workload_name(T) + f" (oracle: {procs} rows per step)",
+                       "global_batch": procs, "K": w["K"], "V": w["V"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": procs,
+                             "nproc": os.cpu_count(), "kind": "oracle",
+                             "rows_split_over_processes": procs > 1, "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))

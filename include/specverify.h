@@ -88,7 +88,13 @@ extern "C" {
 #define SPEC_DERR_BAD_LENGTH 8   /* kv: negative seq_len, or the row outgrows max_blocks */
 #define SPEC_DERR_NO_SPACE 16    /* kv: the free stack cannot supply every new block */
 #define SPEC_DERR_BAD_BLOCK 32   /* kv: a block id out of range, or a target slot already taken */
-#define SPEC_DERR_TIMEOUT 64     /* an internal bounded wait gave up (should never happen) */
+#define SPEC_DERR_TIMEOUT 64     /* an internal bounded wait gave up (should never happen);
+                                    the launch drains and unfinished rows' outputs are not
+                                    written. Failure-detection tests provoke it with the
+                                    environment knobs SPECVERIFY_STALL_ROW=b (every stage
+                                    arrival of batch row b is withheld) and
+                                    SPECVERIFY_IDLE_NS (the producers' idle limit, default
+                                    2 s), read at every verify launch */
 #define SPEC_DERR_BAD_SLOT 128   /* kv: a slot_map entry of a kept position outside [0, K] */
 
 /* ---- per-row diagnostic bits written to row_info[b] (optional) ---- */

@@ -19,10 +19,11 @@
 // Task sources, in priority order: the work queue (later stages of rows
 // already started, which keeps their data hot in L2), then the static list of
 // first-stage tasks (b, s) in row order. Every wait is bounded; a timeout sets
-// the workspace abort word, the kernel drains, and unfinished rows keep the -1
-// outputs the host pre-filled.
+// the workspace abort word, the kernel drains, and the outputs of unfinished
+// rows are not written (they keep what the caller's arrays held).
 #pragma once
 #include <cstdint>
+#include <cstdlib>
 
 #include "../../include/specverify.h"
 #include "common.cuh"
@@ -118,6 +119,10 @@ __host__ __device__ inline WsLayout ws_layout(int B, int S, int part_floats, int
 struct Ws {
   uint8_t* base;
   WsLayout L;
+  // Failure-detection test knobs (set_test_knobs): a batch row whose stage
+  // arrivals are withheld (-1: none), and the producers' idle limit.
+  int stall_row = -1;
+  uint64_t idle_ns = kWaitNs;
   __device__ WsHeader* hdr() const { return reinterpret_cast<WsHeader*>(base + L.header); }
   __device__ uint32_t* row_cnt() const { return reinterpret_cast<uint32_t*>(base + L.row_cnt); }
   __device__ uint64_t* entries() const { return reinterpret_cast<uint64_t*>(base + L.entries); }
@@ -131,6 +136,24 @@ struct Ws {
     return base + L.rowstate + size_t(b) * L.rowstate_bytes;
   }
 };
+
+// Failure-detection test knobs, read from the environment at every launch.
+// SPECVERIFY_STALL_ROW=b withholds every stage arrival of batch row b, so
+// that row never completes: once nothing else is runnable the producers'
+// bounded idle wait runs out, the launch aborts and reports
+// SPEC_DERR_TIMEOUT, and row b's outputs are left unwritten.
+// SPECVERIFY_IDLE_NS sets that idle limit in nanoseconds (default kWaitNs;
+// at most kWaitNs). Without them a launch runs normally.
+__host__ inline void set_test_knobs(Ws& ws) {
+  if (const char* e = std::getenv("SPECVERIFY_STALL_ROW")) {
+    const long v = std::strtol(e, nullptr, 10);
+    if (v >= 0 && v < ws.L.B) ws.stall_row = int(v);
+  }
+  if (const char* e = std::getenv("SPECVERIFY_IDLE_NS")) {
+    const long long v = std::strtoll(e, nullptr, 10);
+    if (v > 0 && uint64_t(v) < kWaitNs) ws.idle_ns = uint64_t(v);
+  }
+}
 
 // ------------------------------------------------------------------ memory helpers
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
@@ -236,7 +259,7 @@ __device__ inline bool producer_idle(const Ws& ws, bool exhausted, uint64_t& idl
   const uint64_t now = global_ns();
   if (idle_t0 == 0) {
     idle_t0 = now;
-  } else if (now - idle_t0 > kWaitNs) {
+  } else if (now - idle_t0 > ws.idle_ns) {
     atomicExch(&h->abort, 1u);
     return false;
   }
@@ -471,7 +494,7 @@ __device__ inline void finisher_loop(const Ws& ws, const Handoff& ho, volatile i
     if (lane == 0)
       for (int k = 0; k < cnt; ++k) mbar_arrive(&ho.freed[(n + k) % kSlots]);
     int last = 0;
-    if (lane < cnt) {
+    if (lane < cnt && mine.b != ws.stall_row) {
       const uint32_t old = atomicAdd(&ws.row_cnt()[mine.b], 1u);
       last = (old == uint32_t(expect(mine)) - 1);  // tasks in the row's stage
       if (last) ws.row_cnt()[mine.b] = 0;  // the row's next stage counts from zero

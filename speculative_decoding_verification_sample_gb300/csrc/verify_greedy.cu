@@ -480,6 +480,7 @@ int launch_verify_greedy(const GreedyLaunch& g) {
   a.S = wl.S;
   a.ws.base = static_cast<uint8_t*>(g.workspace);
   a.ws.L = wl;
+  set_test_knobs(a.ws);
   a.out_tokens = g.out_tokens;
   a.out_n = g.out_n;
   a.err = g.err;

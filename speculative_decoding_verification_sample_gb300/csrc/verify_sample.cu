@@ -1958,6 +1958,7 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.R = a.S * a.M;
   a.ws.base = static_cast<uint8_t*>(s.workspace);
   a.ws.L = wl;
+  set_test_knobs(a.ws);
   const double C = 1.4426950408889634073599246810018921 / double(s.temperature);  // log2(e)/T
   a.c = float(C);
   a.Chi = float(C);

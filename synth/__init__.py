@@ -152,6 +152,15 @@ def sampling_case(B: int, K: int, V: int, *, temperature: float, target_std: flo
                            uniform_seed=uniform_seed))
 
 
+def normal_target(B: int, K: int, V: int, *, target_std: float = 3.0, dtype: str = BF16,
+                  seed: int = 0) -> np.ndarray:
+    """Target logits [B, K+1, V] ~ N(0, target_std^2) iid, stored in `dtype`,
+    unaltered (no clipping, nothing planted): in bf16 the largest values of a
+    long row often round to the same value, so argmax ties occur naturally."""
+    rng = _rng(seed)
+    return _store(rng.normal(0.0, target_std, size=(B, K + 1, V)).astype(np.float32), dtype)
+
+
 PLANT_VALUE = 16.0      # exactly representable in bf16
 CLIP = 14.5             # every other logit is clipped below PLANT_VALUE
 

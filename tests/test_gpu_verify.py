@@ -105,6 +105,47 @@ def test_greedy_parity_config(sv, B, K):
         assert g["err"] == 0
 
 
+@pytest.mark.parametrize("B", [1, 8])
+@pytest.mark.parametrize("K", [2, 4, 6, 8])
+def test_greedy_parity_unaltered_rows(sv, B, K):
+    """Greedy mode on unaltered N(0, 3^2) bf16 rows of V = 151936 (nothing
+    clipped or planted), where the largest values of a row often round to the
+    same bf16 value. Draft token i is the oracle's own argmax of row i with
+    probability alpha (input generation), else a uniform other id. On top of
+    the natural ties, every other target row gets a copy of its maximum half a
+    row away, below or above the first maximum, so that a tie between two
+    vocabulary slices occurs in every batch (any slicing into two or more
+    slices separates positions V/2 apart); the lowest index must win."""
+    V = 151936
+    for alpha in (0.5, 0.8, 0.95):
+        seed = 500 + 100 * K + B + int(alpha * 100)
+        tgt = synth.normal_target(B, K, V, seed=seed)
+        z = synth.logits_values(tgt, synth.BF16)
+        rng = np.random.default_rng(seed)
+        g0 = oracle.verify_greedy(z, np.zeros((B, K), np.int64))["argmax"]
+        planted = 0
+        for b in range(B):
+            for i in range(K + 1):
+                if (b * (K + 1) + i) % 2 == 0:
+                    at = (int(g0[b, i]) + V // 2) % V
+                    tgt[b, i, at] = tgt[b, i, g0[b, i]]
+                    planted += 1
+        z = synth.logits_values(tgt, synth.BF16)
+        g = oracle.verify_greedy(z, np.zeros((B, K), np.int64))["argmax"]
+        other = (g[:, :K] + 1 + rng.integers(0, V - 1, size=(B, K))) % V
+        tok = np.where(rng.random((B, K)) < alpha, g[:, :K], other).astype(np.int32)
+        c = synth.VerifyCase(tgt, None, tok, np.zeros((B, K + 1), np.float32), 0.0, synth.BF16)
+        gg = gh.run_greedy(sv, c)
+        o = oracle.verify_greedy(z, tok)
+        assert np.array_equal(gg["num_accepted"], o["num_accepted"]), alpha
+        assert np.array_equal(gg["out_tokens"], o["out_tokens"]), alpha
+        assert gg["err"] == 0
+        # the ties are there: rows whose maximum occurs at least twice
+        ties = sum(int(np.count_nonzero(z[b, i] == z[b, i].max()) >= 2)
+                   for b in range(B) for i in range(K + 1))
+        assert ties >= planted >= 1
+
+
 @pytest.mark.parametrize("alpha", [0.5, 0.8, 0.95])
 @pytest.mark.parametrize("K", [2, 4, 6, 8])
 def test_greedy_planted_alpha_mean(sv, alpha, K):
