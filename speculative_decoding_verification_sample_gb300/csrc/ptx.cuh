@@ -111,6 +111,50 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// ----------------------------------------------------------------- packed fp32 pairs
+// Two floats in one 64-bit register, operated on by the f32x2 instructions of
+// sm_100-class GPUs: one instruction does the same IEEE round-to-nearest
+// operation on both halves, so results equal those of the scalar
+// __fadd_rn / __fmul_rn / __fmaf_rn on each half, bit for bit.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float f2_lo(uint64_t r) {
+  float lo, hi;
+  f2_unpack(r, lo, hi);
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(uint64_t r) {
+  float lo, hi;
+  f2_unpack(r, lo, hi);
+  return hi;
+}
+
 // Streaming 16-byte global load that does not allocate in L1.
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   uint4 v;

@@ -168,8 +168,7 @@ struct Smem {
   Ring ring;
   Handoff ho;
   Fin* fin;
-  float* tab_hi;
-  float* tab_lo;
+  float2* tab2;  // 2^(j/256) as (hi, lo) pairs
 };
 
 __host__ __device__ inline size_t al(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -224,8 +223,7 @@ __device__ inline Smem make_smem(uint8_t* base, int R) {
         L.fin = reinterpret_cast<Fin*>(p);
         break;
       case 6:
-        L.tab_hi = reinterpret_cast<float*>(p);
-        L.tab_lo = L.tab_hi + 256;
+        L.tab2 = reinterpret_cast<float2*>(p);
         break;
       case 7:
         L.ho.data = p;
@@ -239,17 +237,24 @@ __device__ inline Smem make_smem(uint8_t* base, int R) {
 // Per-thread running max M, integer offset Kc = ceil(M c) and S = sum exp2(z c - Kc).
 template <class E>
 struct StatOp {
-  float c, M, Kc, S, tau;
+  float c, M, Kc, S, tau;  // S: 1 once a term was added, else 0
+  uint64_t S2;             // packed partial sums (even terms, odd terms)
   int bad;
   __device__ __forceinline__ void begin() {
     M = -INFINITY;
     Kc = -INFINITY;
     S = 0.0f;
+    S2 = f2_pack(0.0f, 0.0f);
     bad = 0;
   }
   // The vectors i = tid, tid + kCons, ... < cnt of one ring stage (at most
   // kPer per thread): loaded together, one running-maximum update per stage,
-  // then the exponentials, so the loads and MUFU operations overlap.
+  // then the exponentials, so the loads and MUFU operations overlap. The
+  // exponent arguments and the sums run on packed float pairs (f32x2): the
+  // running sum is a pair S2 whose halves add up the even and the odd terms
+  // of each vector through a depth-2 tree, and end_row adds the halves, so
+  // every term still reaches the row sum through at most 3 + run + 5 fp32
+  // additions (the bound gamma1 counts).
   __device__ __forceinline__ void chunk(const uint4* buf, int cnt, int tid) {
     constexpr int kPer = kChunk / 16 / kCons;
     uint4 v[kPer];
@@ -267,25 +272,35 @@ struct StatOp {
     }
     if (vm > M) {
       const float Kn = offset_of(vm, c);
-      if (S != 0.0f) S = __fmul_rn(S, pow2i(__fsub_rn(Kc, Kn)));
+      if (S != 0.0f) {
+        const float sc = pow2i(__fsub_rn(Kc, Kn));
+        S2 = f2_mul(S2, f2_pack(sc, sc));
+        S = sc != 0.0f ? 1.0f : 0.0f;  // S only records whether any term was added
+      }
       M = vm;
       Kc = Kn;
     }
     if (Kc == -INFINITY) return;  // only -inf logits so far
+    const uint64_t c2 = f2_pack(c, c), nk2 = f2_pack(-Kc, -Kc);
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       if (tid + k * kCons < cnt) {
         float z[E::kVec];
         E::unpack(v[k], z);
         if (E::kMask) mask_vals(z, tau);
-        float e[E::kVec];
+        uint64_t e2[E::kVec / 2];
 #pragma unroll
-        for (int j = 0; j < E::kVec; ++j) e[j] = ex2_approx(__fmaf_rn(z[j], c, -Kc));
+        for (int j = 0; j < E::kVec / 2; ++j) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(z[2 * j], z[2 * j + 1]), c2, nk2), x0, x1);
+          e2[j] = f2_pack(ex2_approx(x0), ex2_approx(x1));
+        }
 #pragma unroll
-        for (int w = 1; w < E::kVec; w <<= 1)
+        for (int w = 1; w < E::kVec / 2; w <<= 1)
 #pragma unroll
-          for (int j = 0; j < E::kVec; j += 2 * w) e[j] = __fadd_rn(e[j], e[j + w]);
-        S = __fadd_rn(S, e[0]);
+          for (int j = 0; j < E::kVec / 2; j += 2 * w) e2[j] = f2_add(e2[j], e2[j + w]);
+        S2 = f2_add(S2, e2[0]);
+        S = 1.0f;
       }
     }
   }
@@ -295,7 +310,11 @@ struct StatOp {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const float Mw = warp_max_f(M);
     float s = 0.0f;
-    if (S != 0.0f) s = __fmul_rn(S, pow2i(__fsub_rn(Kc, offset_of(Mw, c))));
+    if (S != 0.0f) {
+      float s0, s1;
+      f2_unpack(S2, s0, s1);
+      s = __fmul_rn(__fadd_rn(s0, s1), pow2i(__fsub_rn(Kc, offset_of(Mw, c))));
+    }
     s = warp_sum_f(s);
     const int anybad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
@@ -309,12 +328,12 @@ struct StatOp {
 
 // ------------------------------------------------------------------ accurate path
 // 2^(z C - Kc) in pair arithmetic (C = log2(e)/T as Chi + Clo, Kc an integer).
-__device__ __forceinline__ df acc_elem(float z, float Chi, float Clo, float Kc, const float* th,
-                                       const float* tl) {
+__device__ __forceinline__ df acc_elem(float z, float Chi, float Clo, float Kc,
+                                       const float2* tab) {
   const df p = two_prod(z, Chi);
   const float pl = __fmaf_rn(z, Clo, p.lo);
   const df s = two_sum(p.hi, -Kc);
-  return df_exp2(s.hi, __fadd_rn(s.lo, pl), th, tl);
+  return df_exp2(s.hi, __fadd_rn(s.lo, pl), tab);
 }
 
 // Relative error bound of one normalised double-float term, for a row whose
@@ -328,6 +347,11 @@ __device__ __forceinline__ df acc_elem(float z, float Chi, float Clo, float Kc, 
 __device__ __forceinline__ float acc_rho(float Kc) {
   return 2e-12f + 2.2e-14f * (fabsf(Kc) + 256.0f);
 }
+
+// Relative error bound of one normalised FR term e / S: the exponential in
+// the term and in each term of the normaliser (kLiteExpRelErr each), their
+// pair sums (2 n^2 u^2 with n below 2^10 per thread) and the reciprocal.
+constexpr float kFrRho = float(2.0 * kLiteExpRelErr + 1e-10);
 
 // Upper bound on the sum of the computed fp32 probabilities of a row.
 constexpr float kQmax = 1.001f;
@@ -345,6 +369,10 @@ struct FastEntries {
   float c, Kq, Rq, Kp, Rp;
   float tauq = -INFINITY, taup = -INFINITY;
   bool absx = false;  // aq sums q |x| (raw bonus draw) instead of q x
+  // The arithmetic runs on packed float pairs (f32x2): for a residual, the
+  // pair (q term, p term) of each token; for q alone, two neighbouring tokens.
+  // Each half rounds exactly like the scalar operation, and the vector's sum
+  // goes through a depth-3 tree as before.
   __device__ __forceinline__ float run(const uint4& vq, const uint4& vp, float (&r)[E::kVec],
                                        float& aq, float& ap) const {
     float zq[E::kVec], zp[E::kVec];
@@ -354,29 +382,52 @@ struct FastEntries {
       mask_vals(zq, tauq);
       if (pair) mask_vals(zp, taup);
     }
+    const uint64_t c2 = f2_pack(c, c);
+    if (pair) {
+      const uint64_t nk2 = f2_pack(-Kq, -Kp), r2 = f2_pack(Rq, Rp);
+      uint64_t a2 = f2_pack(aq, ap);
 #pragma unroll
-    for (int k = 0; k < E::kVec; ++k) {
-      const float xa = __fmaf_rn(zq[k], c, -Kq);
-      const float q = __fmul_rn(ex2_approx(xa), Rq);
-      const float xc = fmaxf(xa, -1.0e4f);
-      aq = __fmaf_rn(q, absx ? fabsf(xc) : xc, aq);
-      if (pair) {
-        const float xb = __fmaf_rn(zp[k], c, -Kp);
-        const float p = __fmul_rn(ex2_approx(xb), Rp);
-        ap = __fmaf_rn(p, fmaxf(xb, -1.0e4f), ap);
+      for (int k = 0; k < E::kVec; ++k) {
+        float xa, xb;
+        f2_unpack(f2_fma(f2_pack(zq[k], zp[k]), c2, nk2), xa, xb);
+        float q, p;
+        f2_unpack(f2_mul(f2_pack(ex2_approx(xa), ex2_approx(xb)), r2), q, p);
+        a2 = f2_fma(f2_pack(q, p), f2_pack(fmaxf(xa, -1.0e4f), fmaxf(xb, -1.0e4f)), a2);
         r[k] = fmaxf(__fsub_rn(q, p), 0.0f);
-      } else {
-        r[k] = q;
       }
+      f2_unpack(a2, aq, ap);
+    } else {
+      const uint64_t nk2 = f2_pack(-Kq, -Kq), r2 = f2_pack(Rq, Rq);
+      uint64_t a2 = f2_pack(0.0f, 0.0f);
+#pragma unroll
+      for (int k = 0; k < E::kVec; k += 2) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(zq[k], zq[k + 1]), c2, nk2), x0, x1);
+        float q0, q1;
+        f2_unpack(f2_mul(f2_pack(ex2_approx(x0), ex2_approx(x1)), r2), q0, q1);
+        const float w0 = fmaxf(x0, -1.0e4f), w1 = fmaxf(x1, -1.0e4f);
+        a2 = f2_fma(f2_pack(q0, q1), absx ? f2_pack(fabsf(w0), fabsf(w1)) : f2_pack(w0, w1), a2);
+        r[k] = q0;
+        r[k + 1] = q1;
+      }
+      float a0, a1;
+      f2_unpack(a2, a0, a1);
+      aq = __fadd_rn(aq, __fadd_rn(a0, a1));
     }
-    float t[E::kVec];
+    // depth-3 tree over the vector: (r0 + r1, r2 + r3) + (r4 + r5, r6 + r7), then the halves
+    uint64_t t2[E::kVec / 2];
 #pragma unroll
-    for (int k = 0; k < E::kVec; ++k) t[k] = r[k];
+    for (int j = 0; j < E::kVec / 2; ++j) t2[j] = f2_pack(r[(j & ~1) * 2 + (j & 1)], r[(j & ~1) * 2 + (j & 1) + 2]);
+    // t2[0] = (r0, r2), t2[1] = (r1, r3), t2[2] = (r4, r6), t2[3] = (r5, r7) for 8 terms
 #pragma unroll
-    for (int w = 1; w < E::kVec; w <<= 1)
+    for (int j = 0; j < E::kVec / 2; j += 2) t2[j] = f2_add(t2[j], t2[j + 1]);
 #pragma unroll
-      for (int k = 0; k < E::kVec; k += 2 * w) t[k] = __fadd_rn(t[k], t[k + w]);
-    return t[0];
+    for (int w = 2; w < E::kVec / 2; w <<= 1)
+#pragma unroll
+      for (int j = 0; j < E::kVec / 2; j += 2 * w) t2[j] = f2_add(t2[j], t2[j + w]);
+    float h0, h1;
+    f2_unpack(t2[0], h0, h1);
+    return __fadd_rn(h0, h1);
   }
   __device__ __forceinline__ df entries(int vi, df (&rd)[E::kVec]) const {
     float r[E::kVec];
@@ -398,8 +449,7 @@ struct AccEntries {
   bool pair;        // residual q - p (else q alone)
   float Chi, Clo, Kq, Kp;
   df Iq, Ip;
-  const float* th;
-  const float* tl;
+  const float2* tab;
   float tauq = -INFINITY, taup = -INFINITY;
   __device__ __forceinline__ df run(const uint4& vq, const uint4& vp, df (&r)[E::kVec], float& qs,
                                     float& ps) const {
@@ -413,11 +463,11 @@ struct AccEntries {
     df vs{0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < E::kVec; ++k) {
-      const df q = df_mul(acc_elem(zq[k], Chi, Clo, Kq, th, tl), Iq);
+      const df q = df_mul(acc_elem(zq[k], Chi, Clo, Kq, tab), Iq);
       qs = __fadd_rn(qs, q.hi);
       df rk = q;
       if (pair) {
-        const df p = df_mul(acc_elem(zp[k], Chi, Clo, Kp, th, tl), Ip);
+        const df p = df_mul(acc_elem(zp[k], Chi, Clo, Kp, tab), Ip);
         ps = __fadd_rn(ps, p.hi);
         rk = df_sub(q, p);
         if (!(rk.hi > 0.0f)) rk = {0.f, 0.f};
@@ -811,7 +861,7 @@ __device__ void finish_ar(const SampleArgs& a, const Smem& L, int b, int aux) {
   } else if (ar.hi < -126.0f) {
     acc = false;  // ratio < 2^-100 < u (u > 0 here)
   } else {
-    const df ratio = df_mul(df_mul(df_exp2(ar.hi, ar.lo, L.tab_hi, L.tab_lo), S1), df_recip(S0));
+    const df ratio = df_mul(df_mul(df_exp2(ar.hi, ar.lo, L.tab2), S1), df_recip(S0));
     acc = (ratio.hi >= 1.0f) || df_gt(ratio, df{u, 0.f});
     if (fabsf(__fsub_rn(u, fminf(1.0f, ratio.hi))) <= 1e-10f * ratio.hi)
       flags |= SPEC_ROW_UNCERTIFIED;
@@ -1103,16 +1153,20 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
     // FR's sign test compares fp32 approximations x = e_q.hi * Rq and
     // y = e_p.hi * Rp of q and p. Relative error of each: the fp32 row sum
     // behind R (ex2 + gamma1 + 2 ln2 u sum q|x|), the reciprocal, the hi
-    // part and the product (about 3u), and the double-float exponential.
+    // part and the product (about 3u), and FR's exponential (kLiteExpRelErr).
     auto eps = [&](float A) {
       const float absx = 1.01f * fmaxf(0.0f, -A) + 0.5f * kQmax;
-      return a.bd.ex2 + a.bd.gamma1 + 2.0f * kLn2f * kU * absx + 4.0f * kU + 1e-10f;
+      return a.bd.ex2 + a.bd.gamma1 + 2.0f * kLn2f * kU * absx + 4.0f * kU +
+             float(kLiteExpRelErr);
     };
     st->amb_delta = 1.05f * (eps(sl.f2) + eps(sl.f3)) + 4.0f * kU;
     st->namb = 0;
     st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
     const int pb = piece_choice(a);
-    enqueue_row_stage(a.ws, kFR, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
+    // FR's exponential needs offsets within kLiteMaxOffset; beyond, the
+    // double-float stages FA and FB refine the draw
+    const bool lite = fabsf(Kq) <= kLiteMaxOffset && (!dr.pair || fabsf(Kp) <= kLiteMaxOffset);
+    enqueue_row_stage(a.ws, lite ? kFR : kFA, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
   }
   __syncwarp();
 }
@@ -1223,8 +1277,7 @@ __device__ void finish_fb(const SampleArgs& a, const Smem& L, int b, int aux) {
     ae.Kp = Kp;
     ae.Iq = Iq;
     ae.Ip = Ip;
-    ae.th = L.tab_hi;
-    ae.tl = L.tab_lo;
+    ae.tab = L.tab2;
     token = search_draw<E>(a, b, ae, sl, df_mul_f(Sr, uK), Eb, cert, PlainUnits{&a, b});
   }
   const int fl = flags | (cert ? 0 : SPEC_ROW_UNCERTIFIED);
@@ -1477,7 +1530,7 @@ __device__ bool consume_rowsums(const SampleArgs& a, const Smem& L, uint32_t& it
       if (E::kMask) mask_vals(z, tau);
 #pragma unroll
       for (int k = 0; k < E::kVec; ++k)
-        acc = df_add(acc, acc_elem(z[k], a.Chi, a.Clo, Kr, L.tab_hi, L.tab_lo));
+        acc = df_add(acc, acc_elem(z[k], a.Chi, a.Clo, Kr, L.tab2));
     }
     if (m.r == 0) s0 = df_add(s0, acc);
     else s1 = df_add(s1, acc);
@@ -1518,8 +1571,7 @@ __device__ bool consume_fb(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   ae.Kp = dr.pair ? __ldcg(&st->Kp) : 0.f;
   ae.Iq = df{__ldcg(&st->Iq_hi), __ldcg(&st->Iq_lo)};
   ae.Ip = dr.pair ? df{__ldcg(&st->Ip_hi), __ldcg(&st->Ip_lo)} : df{0.f, 0.f};
-  ae.th = L.tab_hi;
-  ae.tl = L.tab_lo;
+  ae.tab = L.tab2;
   int v0, v1, ps, pv0;
   task_range(a, is_piece(t), t.s, v0, v1, ps, pv0);
   df acc{0.f, 0.f};
@@ -1565,10 +1617,46 @@ __device__ bool consume_fb(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   return ok;
 }
 
-// FR: one double-float pass over the draw's rows (see the header). Per unit
-// the pair sums of e_q and e_p over the tokens with a certainly positive
-// residual; per task the row sums and the unit sums' totals; tokens inside
-// the sign test's margin go to the row's list.
+// Packed pair accumulation: (H, Lo) += (s, e) for two independent sums at
+// once (halves of the f32x2 registers), TwoSum on the high parts, the errors
+// and the low parts summed in Lo. With n additions the result is within
+// 2 n^2 u^2 of the exact sum (relative), far below the exponentials' error.
+__device__ __forceinline__ void acc2(uint64_t& H, uint64_t& Lo, uint64_t sh, uint64_t sl) {
+  const uint64_t S = f2_add(H, sh);
+  const uint64_t bb = f2_sub(S, H);
+  const uint64_t err = f2_add(f2_sub(H, f2_sub(S, bb)), f2_sub(sh, bb));
+  Lo = f2_add(Lo, f2_add(err, sl));
+  H = S;
+}
+
+// Pair sum (as df_add) of two packed pairs, half by half.
+__device__ __forceinline__ void df_add2(uint64_t& H, uint64_t& Lo, uint64_t yh, uint64_t yl) {
+  const uint64_t s = f2_add(H, yh);
+  const uint64_t bb = f2_sub(s, H);
+  const uint64_t err = f2_add(f2_sub(H, f2_sub(s, bb)), f2_sub(yh, bb));
+  const uint64_t e = f2_add(err, f2_add(Lo, yl));
+  H = f2_add(s, e);
+  Lo = f2_sub(e, f2_sub(H, s));
+}
+
+// Warp sum of two pairs at once (df_warp_sum of each half); every lane ends
+// with the totals.
+__device__ __forceinline__ void df_warp_sum2(uint64_t& H, uint64_t& Lo) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const uint64_t yh = __shfl_xor_sync(0xffffffffu, H, o);
+    const uint64_t yl = __shfl_xor_sync(0xffffffffu, Lo, o);
+    df_add2(H, Lo, yh, yl);
+  }
+}
+
+// FR: one pass over the draw's rows (see the header) with the lighter
+// exponential (lite_exp2x2, relative error < kLiteExpRelErr) on packed pairs.
+// Per unit the pair sums of e_q and e_p over the tokens with a certainly
+// positive residual; per task the row sums and the unit sums' totals;
+// tokens inside the sign test's margin go to the row's list. Each term is
+// first normalised to a pair (s, e) with |e| <= u |s| (FastTwoSum), so the
+// accumulations keep the error bound of acc2.
 template <class E>
 __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot,
                            const QTask& t) {
@@ -1580,10 +1668,16 @@ __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   const float up1 = 1.0f + (dr.pair ? __ldcg(&st->amb_delta) : 0.f);
   const float tauq = thr_of(a, t.b, true, dr.j);
   const float taup = dr.pair ? thr_of(a, t.b, false, dr.j) : -INFINITY;
+  const LiteConsts LC = lite_consts(a.Chi, a.Clo);
+  const LiteRow Lq = lite_row(Kq, a.Chi);
+  const LiteRow Lp = dr.pair ? lite_row(Kp, a.Chi) : Lq;
+  const uint64_t r2 = f2_pack(Rq, Rp);
   int v0, v1, ps, pv0;
   task_range(a, is_piece(t), t.s, v0, v1, ps, pv0);
   float4* units = reinterpret_cast<float4*>(a.ws.units(t.b, ps));
-  df Tq{0.f, 0.f}, Tp{0.f, 0.f}, Aq{0.f, 0.f}, Ap{0.f, 0.f};
+  const uint64_t zero2 = f2_pack(0.f, 0.f);
+  uint64_t Th = zero2, Tl = zero2;  // (Tq, Tp) partial row sums of this thread
+  df Aq{0.f, 0.f}, Ap{0.f, 0.f};
   bool ok = true;
   for (;;) {
     const ChunkMeta m = L.ring.meta[it % kStages];
@@ -1592,7 +1686,7 @@ __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uin
     const int cnt = m.c1 - m.c0;
     for (int i0 = warp * 32; i0 < cnt; i0 += kCons) {
       const int i = i0 + lane;
-      df vq{0.f, 0.f}, vp{0.f, 0.f};
+      uint64_t Vh = zero2, Vl = zero2;  // this lane's (q, p) unit partials
       if (i < cnt) {
         float zq[E::kVec], zp[E::kVec];
         E::unpack(bq[i], zq);
@@ -1601,41 +1695,67 @@ __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uin
           mask_vals(zq, tauq);
           if (dr.pair) mask_vals(zp, taup);
         }
+        if (dr.pair) {
 #pragma unroll
-        for (int k = 0; k < E::kVec; ++k) {
-          const df eq = acc_elem(zq[k], a.Chi, a.Clo, Kq, L.tab_hi, L.tab_lo);
-          Tq = df_add(Tq, eq);
-          if (!dr.pair) {
-            vq = df_add(vq, eq);
-            continue;
-          }
-          const df ep = acc_elem(zp[k], a.Chi, a.Clo, Kp, L.tab_hi, L.tab_lo);
-          Tp = df_add(Tp, ep);
-          const float x = __fmul_rn(eq.hi, Rq), y = __fmul_rn(ep.hi, Rp);
-          if (x > __fmul_rn(y, up1)) {
-            vq = df_add(vq, eq);
-            vp = df_add(vp, ep);
-          } else if (!(__fmul_rn(x, up1) <= y)) {
-            const int slot_i = atomicAdd(&st->namb, 1);
-            if (slot_i < kAmbCap) {
-              AmbEntry e;
-              e.v = (m.c0 + i) * E::kVec + k;
-              e.pad = 0;
-              e.qh = eq.hi;
-              e.ql = eq.lo;
-              e.ph = ep.hi;
-              e.pl = ep.lo;
-              st->amb[slot_i] = e;
+          for (int k = 0; k < E::kVec; ++k) {
+            df eq, ep;
+            lite_exp2x2(zq[k], zp[k], Lq, Lp, LC, L.tab2, eq, ep);
+            const uint64_t h = f2_pack(eq.hi, ep.hi), l = f2_pack(eq.lo, ep.lo);
+            const uint64_t sh = f2_add(h, l);
+            const uint64_t sl = f2_sub(l, f2_sub(sh, h));
+            acc2(Th, Tl, sh, sl);
+            float x, y;
+            f2_unpack(f2_mul(sh, r2), x, y);
+            const bool pos = x > __fmul_rn(y, up1);
+            if (pos) {
+              acc2(Vh, Vl, sh, sl);
+            } else if (!(__fmul_rn(x, up1) <= y)) {
+              const int slot_i = atomicAdd(&st->namb, 1);
+              if (slot_i < kAmbCap) {
+                float qh, ph, ql, pl;
+                f2_unpack(sh, qh, ph);
+                f2_unpack(sl, ql, pl);
+                AmbEntry e;
+                e.v = (m.c0 + i) * E::kVec + k;
+                e.pad = 0;
+                e.qh = qh;
+                e.ql = ql;
+                e.ph = ph;
+                e.pl = pl;
+                st->amb[slot_i] = e;
+              }
             }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < E::kVec; k += 2) {
+            df e0, e1;
+            lite_exp2x2(zq[k], zq[k + 1], Lq, Lq, LC, L.tab2, e0, e1);
+            const uint64_t h = f2_pack(e0.hi, e1.hi), l = f2_pack(e0.lo, e1.lo);
+            const uint64_t sh = f2_add(h, l);
+            const uint64_t sl = f2_sub(l, f2_sub(sh, h));
+            acc2(Th, Tl, sh, sl);
+            acc2(Vh, Vl, sh, sl);
           }
         }
       }
-      const df uq = df_warp_sum(vq);
-      const df uv = dr.pair ? df_warp_sum(vp) : df{0.f, 0.f};
+      if (!dr.pair) {
+        // both halves hold q terms: fold them into the first half
+        float h0, h1, l0, l1;
+        f2_unpack(Vh, h0, h1);
+        f2_unpack(Vl, l0, l1);
+        const df v = df_add(df{h0, l0}, df{h1, l1});
+        Vh = f2_pack(v.hi, 0.f);
+        Vl = f2_pack(v.lo, 0.f);
+      }
+      df_warp_sum2(Vh, Vl);
       if (lane == 0) {
-        units[(m.c0 - pv0 + i0) / 32] = make_float4(uq.hi, uq.lo, uv.hi, uv.lo);
-        Aq = df_add(Aq, uq);
-        Ap = df_add(Ap, uv);
+        float uqh, uph, uql, upl;
+        f2_unpack(Vh, uqh, uph);
+        f2_unpack(Vl, uql, upl);
+        units[(m.c0 - pv0 + i0) / 32] = make_float4(uqh, uql, uph, upl);
+        Aq = df_add(Aq, df{uqh, uql});
+        Ap = df_add(Ap, df{uph, upl});
       }
     }
     release_stage(L.ring, it);
@@ -1646,12 +1766,22 @@ __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uin
       break;
     }
   }
-  Tq = df_warp_sum(Tq);
-  Tp = df_warp_sum(Tp);
+  if (!dr.pair) {
+    float h0, h1, l0, l1;
+    f2_unpack(Th, h0, h1);
+    f2_unpack(Tl, l0, l1);
+    const df v = df_add(df{h0, l0}, df{h1, l1});
+    Th = f2_pack(v.hi, 0.f);
+    Tl = f2_pack(v.lo, 0.f);
+  }
+  df_warp_sum2(Th, Tl);
   if (lane == 0) {
+    float tqh, tph, tql, tpl;
+    f2_unpack(Th, tqh, tph);
+    f2_unpack(Tl, tql, tpl);
     df* w = reinterpret_cast<df*>(slot + 16);
-    w[warp] = Tq;
-    w[kCW + warp] = Tp;
+    w[warp] = df{tqh, tql};
+    w[kCW + warp] = df{tph, tpl};
     w[2 * kCW + warp] = Aq;
     w[3 * kCW + warp] = Ap;
   }
@@ -1740,13 +1870,14 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
     __syncwarp();
     return;
   }
-  // Error bound: per token, relative error below acc_rho for e_q / S_q and
-  // e_p / S_p (exponential, argument, normaliser and reciprocal), whatever
-  // the order of the pair-arithmetic sums and products; summed with weights
-  // q and p (total 1 each, margin 10%). A token whose sign is undecidable
-  // within that error moves by at most its own error.
-  const float Eb = 1.1f * fmaxf(acc_rho(Kq), acc_rho(Kp)) * (dr.pair ? 2.0f : 1.0f) +
-                   1e-14f * Sr.hi + 1e-36f;
+  // Error bound: per token, relative error below kFrRho for e_q / S_q and
+  // e_p / S_p (FR's exponential in the term and in the normaliser, the pair
+  // sums and the reciprocal), whatever the order of the pair-arithmetic sums
+  // and products; summed with weights q and p (total 1 each, margin 10%). The
+  // walk of the final unit uses double-float terms, well inside the same
+  // bound. A token whose sign is undecidable within that error moves by at
+  // most its own error.
+  const float Eb = 1.1f * kFrRho * (dr.pair ? 2.0f : 1.0f) + 1e-14f * Sr.hi + 1e-36f;
   int token = -1;
   bool cert = false;
   {
@@ -1763,14 +1894,20 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
     ae.Kp = Kp;
     ae.Iq = Iq;
     ae.Ip = Ip;
-    ae.th = L.tab_hi;
-    ae.tl = L.tab_lo;
+    ae.tab = L.tab2;
     FrUnits fu{&a, b, namb, av, dr.pair, Iq, Ip, ad};
     token = search_draw<E>(a, b, ae, sl, df_mul_f(Sr, uK), Eb, cert, fu);
   }
-  const int fl = flags | (cert ? 0 : SPEC_ROW_UNCERTIFIED);
-  if (token < 0 && lane == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
-  write_outputs(a, b, dr.j, token, fl, token < 0, d);
+  if (token >= 0 && cert) {
+    write_outputs(a, b, dr.j, token, flags, false, d);
+    return;
+  }
+  // not settled within FR's bound: the double-float stages FA and FB
+  if (lane == 0) {
+    const int pb = piece_choice(a);
+    enqueue_row_stage(a.ws, kFA, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
+  }
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1781,10 +1918,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
   const Smem L = make_smem(smem_raw, 2 * K);
   ring_init(L.ring);
   handoff_init(L.ho);
-  for (int i = threadIdx.x; i < 256; i += kThreads) {
-    L.tab_hi[i] = kExp2Tab.hi[i];
-    L.tab_lo[i] = kExp2Tab.lo[i];
-  }
+  for (int i = threadIdx.x; i < 256; i += kThreads)
+    L.tab2[i] = make_float2(kExp2Tab.hi[i], kExp2Tab.lo[i]);
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* h = a.ws.hdr();
