@@ -339,17 +339,19 @@ __device__ __forceinline__ bool claim_stage(const Ring& ring, uint32_t it) {
   return true;
 }
 
-// Producer: streams the rows of one task (rows[] are row base pointers).
+// Producer: streams the rows of one task (row(r) is the base pointer of the
+// task's row r, computed on demand: an array of pointers would live in local
+// memory, one L2 round trip per stage on the producer's critical path).
 // `paired` (two rows read element by element together) puts chunk k of both
 // rows in one stage, row 0 in the first half and row 1 in the second, so a
 // stage is self-contained and the ring keeps kStages pairs in flight.
 // `after_first` runs once the first stage is issued: the producer fetches its
 // next task there, so the fetch's memory round trips overlap the streaming
 // instead of leaving the ring to drain between tasks.
-template <class AfterFirst>
+template <class RowFn, class AfterFirst>
 __device__ inline bool produce_task(const Ring& ring, uint32_t& it, uint32_t& nt, const QTask& t,
-                                    const char* const* rows, int nrows, bool paired, int v0,
-                                    int v1, AfterFirst&& after_first) {
+                                    RowFn&& row, int nrows, bool paired, int v0, int v1,
+                                    AfterFirst&& after_first) {
   // The table entry of task nt is reused by task nt + kStages; it is written
   // only once the task's first stage is claimed, i.e. after every consumer
   // warp released the stage kStages earlier and so has read the entry of every
@@ -381,11 +383,11 @@ __device__ inline bool produce_task(const Ring& ring, uint32_t& it, uint32_t& nt
     uint8_t* dst = ring.buf + size_t(stage) * kChunk;
     if (paired) {
       mbar_arrive_expect_tx(&ring.full[stage], 2u * bytes);
-      bulk_g2s(dst, rows[0] + size_t(c0) * 16, bytes, &ring.full[stage]);
-      bulk_g2s(dst + kChunk / 2, rows[1] + size_t(c0) * 16, bytes, &ring.full[stage]);
+      bulk_g2s(dst, row(0) + size_t(c0) * 16, bytes, &ring.full[stage]);
+      bulk_g2s(dst + kChunk / 2, row(1) + size_t(c0) * 16, bytes, &ring.full[stage]);
     } else {
       mbar_arrive_expect_tx(&ring.full[stage], bytes);
-      bulk_g2s(dst, rows[r] + size_t(c0) * 16, bytes, &ring.full[stage]);
+      bulk_g2s(dst, row(r) + size_t(c0) * 16, bytes, &ring.full[stage]);
     }
     if (q == 0) after_first();
   }

@@ -377,16 +377,12 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
         const T* tgt = static_cast<const T*>(a.target) + size_t(t.b) * (K + 1) * a.V;
         int v0, v1;
         slice_range(a.nvec, a.S, t.s, v0, v1);
-        const char* rows[kMaxK + 2];
-        int nrows = 0;
-        if (t.type == kG1) {
-          for (int i = 0; i < R; ++i)
-            rows[nrows++] = reinterpret_cast<const char*>(tgt + size_t(i) * a.V);
-        } else {
-          rows[nrows++] = reinterpret_cast<const char*>(tgt + size_t(K) * a.V);
-        }
+        // G1: target rows 0..R-1; GB: target row K
+        const int nrows = (t.type == kG1) ? R : 1;
+        const int r0 = (t.type == kG1) ? 0 : K;
+        auto row = [&](int r) { return reinterpret_cast<const char*>(tgt + size_t(r0 + r) * a.V); };
         auto prefetch = [&]() { fx.prepare(a.ws); };
-        if (!produce_task(L.ring, it, nt, t, rows, nrows, false, v0, v1, prefetch)) break;
+        if (!produce_task(L.ring, it, nt, t, row, nrows, false, v0, v1, prefetch)) break;
       }
       produce_end(L.ring, it);
     }

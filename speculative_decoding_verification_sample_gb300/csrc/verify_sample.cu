@@ -161,7 +161,6 @@ struct Fin {  // finisher-private scratch: statistics of the 2K rows of a P1
   df rowS[2 * kMaxK];
   df rowInv[2 * kMaxK];
   int rowOK[2 * kMaxK];
-  float4 item[256];  // slice partials being combined
 };
 
 struct Smem {
@@ -485,6 +484,54 @@ struct AccEntries {
   }
 };
 
+// FR's terms (lite_exp2x2, relative error < kLiteExpRelErr) normalised in
+// pair arithmetic: the walk of the final unit in FR's draw, consistent with
+// the unit sums of the FR pass.
+template <class E>
+struct LiteEntries {
+  const uint4* tq;
+  const uint4* tp;
+  bool pair;
+  LiteConsts LC;
+  LiteRow Lq, Lp;
+  df Iq, Ip;
+  const float2* tab;
+  float tauq = -INFINITY, taup = -INFINITY;
+  __device__ __forceinline__ df entries(int vi, df (&rd)[E::kVec]) const {
+    const uint4 vq = ldg_nc_v4(tq + vi);
+    const uint4 vp = pair ? ldg_nc_v4(tp + vi) : vq;
+    float zq[E::kVec], zp[E::kVec];
+    E::unpack(vq, zq);
+    if (pair) E::unpack(vp, zp);
+    if (E::kMask) {
+      mask_vals(zq, tauq);
+      if (pair) mask_vals(zp, taup);
+    }
+    df vs{0.f, 0.f};
+    if (pair) {
+#pragma unroll
+      for (int k = 0; k < E::kVec; ++k) {
+        df eq, ep;
+        lite_exp2x2(zq[k], zp[k], Lq, Lp, LC, tab, eq, ep);
+        df rk = df_sub(df_mul(eq, Iq), df_mul(ep, Ip));
+        if (!(rk.hi > 0.0f)) rk = {0.f, 0.f};
+        rd[k] = rk;
+        vs = df_add(vs, rk);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < E::kVec; k += 2) {
+        df e0, e1;
+        lite_exp2x2(zq[k], zq[k + 1], Lq, Lq, LC, tab, e0, e1);
+        rd[k] = df_mul(e0, Iq);
+        rd[k + 1] = df_mul(e1, Iq);
+        vs = df_add(df_add(vs, rd[k]), rd[k + 1]);
+      }
+    }
+    return vs;
+  }
+};
+
 // ------------------------------------------------------------------ helpers
 template <class E>
 struct RowPtrs {
@@ -574,39 +621,65 @@ __device__ __forceinline__ float* task_part(const SampleArgs& a, bool pieces, in
 // other CTAs (partials, unit sums, row state) is read through L2 (ld.cg).
 
 // Row statistics of rows [0, nrows) (float offset 4r of each slice's
-// partials: max, sum hi, sum lo, NaN seen) into the finisher scratch: the
-// partials of a group of rows are loaded by all lanes at once (one memory
-// round trip per group), then lane r combines row r from shared memory.
+// partials: max, sum hi, sum lo, NaN seen) into the finisher scratch. Rows
+// are taken up to 32 at a time; each row gets g lanes (g = 32 / rows, a
+// power of two), lane k of a row combines slices k, k + g, ... (all its
+// loads issued together: one memory round trip per group of rows), then the
+// row's lanes reduce with g / 2 .. 1 butterfly shuffles: few dependent steps
+// for any number of slices.
 __device__ void stats_rows(const SampleArgs& a, Fin& F, int b, int nrows) {
   const int lane = threadIdx.x & 31, S = a.S;
-  const int per_group = 256 / S > 0 ? 256 / S : 1;
-  for (int r0 = 0; r0 < nrows; r0 += per_group) {
-    const int rg = min(per_group, nrows - r0), items = rg * S;
-#pragma unroll 8
-    for (int i = lane; i < items; i += 32) {
-      const int r = r0 + i / S, sl = i % S;
-      F.item[i] = __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, sl) + 4 * r));
-    }
-    __syncwarp();
-    for (int rr = lane; rr < rg; rr += 32) {
-      const float4* it = F.item + rr * S;
-      float M = -INFINITY;
-      int bad = 0;
-      for (int sl = 0; sl < S; ++sl) {
-        M = fmaxf(M, it[sl].x);
-        bad |= __float_as_int(it[sl].w);
+  for (int r0 = 0; r0 < nrows; r0 += 32) {
+    const int rg = min(32, nrows - r0);
+    int g = 1;
+    while (g * 2 * rg <= 32) g *= 2;
+    const int rr = lane / g, k = lane % g, r = r0 + rr;
+    const bool live = rr < rg;
+    float4 it[4];
+    // up to 4 slices per lane are loaded at once; more (small g, many slices) loop
+    float M = -INFINITY;
+    int bad = 0;
+    for (int s0 = k; s0 < S; s0 += 4 * g) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int sl = s0 + q * g;
+        it[q] = (live && sl < S) ? __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, sl) + 4 * r))
+                                 : make_float4(-INFINITY, 0.f, 0.f, 0.f);
       }
-      const float Kc = offset_of(M, a.c);
-      df Ssum{0.f, 0.f};
-      for (int sl = 0; sl < S; ++sl) {
-        if (it[sl].y != 0.0f) {
-          const float sc = pow2i(__fsub_rn(offset_of(it[sl].x, a.c), Kc));
-          Ssum = df_add(Ssum, df{__fmul_rn(it[sl].y, sc), __fmul_rn(it[sl].z, sc)});
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        M = fmaxf(M, it[q].x);
+        bad |= __float_as_int(it[q].w);
+      }
+    }
+    for (int o = g / 2; o > 0; o >>= 1) {
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    const float Kc = offset_of(M, a.c);
+    df Ssum{0.f, 0.f};
+    for (int s0 = k; s0 < S; s0 += 4 * g) {
+      if (S > 4 * g) {  // more than one batch of slices per lane: load this batch again
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int sl = s0 + q * g;
+          it[q] = (live && sl < S)
+                      ? __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, sl) + 4 * r))
+                      : make_float4(-INFINITY, 0.f, 0.f, 0.f);
         }
       }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (it[q].y != 0.0f) {
+          const float sc = pow2i(__fsub_rn(offset_of(it[q].x, a.c), Kc));
+          Ssum = df_add(Ssum, df{__fmul_rn(it[q].y, sc), __fmul_rn(it[q].z, sc)});
+        }
+      }
+    }
+    for (int o = g / 2; o > 0; o >>= 1) Ssum = df_add(Ssum, df_shfl_xor(Ssum, o));
+    if (live && k == 0) {
       const bool ok = !bad && isfinite(M) && fabsf(Kc) < kMaxOffset && Ssum.hi > 0.0f &&
                       isfinite(Ssum.hi);
-      const int r = r0 + rr;
       F.rowKc[r] = Kc;
       F.rowS[r] = Ssum;
       F.rowInv[r] = ok ? df_recip(Ssum) : df{0.f, 0.f};
@@ -996,9 +1069,22 @@ __device__ int search_draw(const SampleArgs& a, int b, const Entries& ent, const
     const int ub = (v0 - pv0) / 32;
     int us = -1;
     df ubase = pre_s, ubase_s = pre_s;
-    for (int u0 = 0; u0 < nu && us < 0; u0 += 32) {
+    // the unit sums of up to kPre passes are loaded together (one memory
+    // round trip), then scanned pass by pass
+    constexpr int kPre = 2;
+    for (int g0 = 0; g0 < nu && us < 0; g0 += 32 * kPre) {
+     df xs[kPre];
+#pragma unroll
+     for (int p = 0; p < kPre; ++p) {
+       const int u = g0 + 32 * p + lane;
+       xs[p] = units_src.get(ps, ub + u, u < nu);
+     }
+#pragma unroll
+     for (int p = 0; p < kPre; ++p) {
+      const int u0 = g0 + 32 * p;
+      if (u0 >= nu || us >= 0) break;
       const int u = u0 + lane;
-      const df x = units_src.get(ps, ub + u, u < nu);
+      const df x = xs[p];
       df inc = x;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -1019,6 +1105,7 @@ __device__ int search_draw(const SampleArgs& a, int b, const Entries& ent, const
         us = -(u0 + l) - 2;
       }
       ubase = df_add(ubase, df_shfl(inc, 31));
+     }
     }
     if (us < -1) us = -us - 2;
     if (us >= 0) {
@@ -1874,29 +1961,27 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
   // e_p / S_p (FR's exponential in the term and in the normaliser, the pair
   // sums and the reciprocal), whatever the order of the pair-arithmetic sums
   // and products; summed with weights q and p (total 1 each, margin 10%). The
-  // walk of the final unit uses double-float terms, well inside the same
-  // bound. A token whose sign is undecidable within that error moves by at
-  // most its own error.
+  // walk of the final unit recomputes its terms the same way. A token whose
+  // sign is undecidable within that error moves by at most its own error.
   const float Eb = 1.1f * kFrRho * (dr.pair ? 2.0f : 1.0f) + 1e-14f * Sr.hi + 1e-36f;
   int token = -1;
   bool cert = false;
   {
     const RowPtrs<E> rp = row_ptrs<E>(a, b);
-    AccEntries<E> ae;
-    ae.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
-    ae.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
-    ae.pair = dr.pair;
-    ae.tauq = thr_of(a, b, true, dr.j);
-    ae.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
-    ae.Chi = a.Chi;
-    ae.Clo = a.Clo;
-    ae.Kq = Kq;
-    ae.Kp = Kp;
-    ae.Iq = Iq;
-    ae.Ip = Ip;
-    ae.tab = L.tab2;
+    LiteEntries<E> le;
+    le.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
+    le.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
+    le.pair = dr.pair;
+    le.tauq = thr_of(a, b, true, dr.j);
+    le.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
+    le.LC = lite_consts(a.Chi, a.Clo);
+    le.Lq = lite_row(Kq, a.Chi);
+    le.Lp = dr.pair ? lite_row(Kp, a.Chi) : le.Lq;
+    le.Iq = Iq;
+    le.Ip = Ip;
+    le.tab = L.tab2;
     FrUnits fu{&a, b, namb, av, dr.pair, Iq, Ip, ad};
-    token = search_draw<E>(a, b, ae, sl, df_mul_f(Sr, uK), Eb, cert, fu);
+    token = search_draw<E>(a, b, le, sl, df_mul_f(Sr, uK), Eb, cert, fu);
   }
   if (token >= 0 && cert) {
     write_outputs(a, b, dr.j, token, flags, false, d);
@@ -1908,6 +1993,37 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
     enqueue_row_stage(a.ws, kFA, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
   }
   __syncwarp();
+}
+
+// Logit rows a task streams: their number, whether they are read element by
+// element in pairs, and (task_row) the base pointer of row r.
+__device__ inline int task_nrows(const SampleArgs& a, const QTask& t, bool& paired) {
+  paired = false;
+  if (t.type == kP1) return 2 * a.K;
+  if (t.type == kBS) return 1;
+  if (t.type == kAR) return 2;
+  const DrawRows dr = draw_rows(a.K, t.aux);
+  paired = dr.pair && t.type != kFA;
+  return dr.pair ? 2 : 1;
+}
+template <class E>
+__device__ inline const char* task_row(const SampleArgs& a, const QTask& t, int r) {
+  const RowPtrs<E> rp = row_ptrs<E>(a, t.b);
+  int i;
+  bool tgt = true;
+  if (t.type == kP1) {  // target i = row 2i, draft i = row 2i + 1
+    i = r >> 1;
+    tgt = (r & 1) == 0;
+  } else if (t.type == kBS) {
+    i = a.K;
+  } else if (t.type == kAR) {
+    i = t.aux & 0xff;
+    tgt = r == 0;
+  } else {
+    i = draw_rows(a.K, t.aux).j;
+    tgt = r == 0;
+  }
+  return reinterpret_cast<const char*>(tgt ? rp.tgt + size_t(i) * a.V : rp.drf + size_t(i) * a.V);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -1937,32 +2053,13 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
           continue;
         }
         idle_t0 = 0;
-        const RowPtrs<E> rp = row_ptrs<E>(a, t.b);
         int v0, v1, ps, pv0;
         task_range(a, is_piece(t), t.s, v0, v1, ps, pv0);
-        const char* rows[2 * kMaxK];
-        int nrows = 0;
-        bool paired = false;
-        if (t.type == kP1) {
-          for (int i = 0; i < K; ++i) {
-            rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(i) * a.V);
-            rows[nrows++] = reinterpret_cast<const char*>(rp.drf + size_t(i) * a.V);
-          }
-        } else if (t.type == kBS) {
-          rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(K) * a.V);
-        } else if (t.type == kAR) {
-          rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(t.aux & 0xff) * a.V);
-          rows[nrows++] = reinterpret_cast<const char*>(rp.drf + size_t(t.aux & 0xff) * a.V);
-        } else {
-          const DrawRows dr = draw_rows(K, t.aux);
-          rows[nrows++] = reinterpret_cast<const char*>(rp.tgt + size_t(dr.j) * a.V);
-          if (dr.pair) {
-            rows[nrows++] = reinterpret_cast<const char*>(rp.drf + size_t(dr.j) * a.V);
-            paired = (t.type != kFA);
-          }
-        }
+        bool paired;
+        const int nrows = task_nrows(a, t, paired);
+        auto row = [&](int r) { return task_row<E>(a, t, r); };
         auto prefetch = [&]() { fx.prepare(a.ws); };
-        if (!produce_task(L.ring, it, nt, t, rows, nrows, paired, v0, v1, prefetch)) break;
+        if (!produce_task(L.ring, it, nt, t, row, nrows, paired, v0, v1, prefetch)) break;
       }
       produce_end(L.ring, it);
     }
