@@ -22,7 +22,9 @@
 //       rows 0..K-1, which needs no statistics stage; per 32-vector unit
 //       sums kept in the workspace; finish: locate u_K * total mass
 //       slice -> unit -> entry, certify
-//   FR  (rare) one double-float pass over the draw's rows: their row sums
+//   FR  one pass over the draw's rows with a lighter exponential (relative
+//       error < 1e-9; FD: the same pass in double-float, for the draws FR
+//       cannot settle): their row sums
 //       S_q, S_p and, per unit, the sums of e_q and e_p over the tokens whose
 //       residual is positive. The sign of q - p = e_q/S_q - e_p/S_p is
 //       decided from the fp32 normalisers with a proven margin; the few
@@ -32,16 +34,18 @@
 //   FA, FB (fallback when the list overflows) double-float row sums, then
 //       the double-float residual and unit sums
 // Only row j of the draft/target pair is ever re-read for the draw. The rare
-// stages AR, FR, FA and FB are cut finer (each slice into M pieces) so that a
-// refined row's compute-heavy passes spread over more CTAs.
+// stages AR, FR, FD, FA and FB are cut finer (each slice into M pieces) so
+// that a refined row's compute-heavy passes spread over more CTAs.
 //
 // Arithmetic. No fp64 arithmetic (GB300 runs fp64 at a small fraction of its
 // fp32 rate): logits are widened to fp32, exponentials use the MUFU exp2 with
 // an integer offset ceil(max * log2(e)/T), and sums a decision depends on are
 // float pairs (df.cuh). A decision is taken from the fp32 path only when the
 // uniform is farther from the threshold than twice a proven bound on that
-// path's error; otherwise the AR / FA / FB stages recompute it with
-// double-float exponentials (relative error < 4e-12 per term) and the row is
+// path's error; otherwise the FR stage recomputes it with a lighter
+// exponential (relative error < 1e-9 per term) and, if that is not enough,
+// the AR / FD / FA / FB stages with double-float exponentials (relative
+// error < 4e-12 per term); the row is
 // flagged in row_info. The output equals an exact-arithmetic evaluation except
 // for rows flagged SPEC_ROW_UNCERTIFIED.
 #include <cuda_runtime.h>
@@ -61,7 +65,7 @@
 namespace sv {
 namespace {
 
-enum TaskType { kP1 = 1, kBS = 2, kSW = 3, kFA = 4, kFB = 5, kAR = 6, kFR = 7 };
+enum TaskType { kP1 = 1, kBS = 2, kSW = 3, kFA = 4, kFB = 5, kAR = 6, kFR = 7, kFD = 8 };
 enum { kAccept = 0, kReject = 1, kAmbiguous = 2, kInvalid = 3 };
 constexpr int kModeResidual = 0, kModeQ = 1;  // draw modes (task aux bits 8+)
 constexpr int kFinWarp = kCW + 1;             // warp index of the finisher
@@ -570,7 +574,7 @@ constexpr int kPieceBit = 1 << 9;
 constexpr int kRawBit = 1 << 10;
 
 __device__ __forceinline__ bool is_piece(const QTask& t) {
-  return (t.type == kAR || t.type == kFA || t.type == kFB || t.type == kFR) &&
+  return (t.type == kAR || t.type == kFA || t.type == kFB || t.type == kFR || t.type == kFD) &&
          (t.aux & kPieceBit);
 }
 
@@ -1251,9 +1255,9 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
     st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
     const int pb = piece_choice(a);
     // FR's exponential needs offsets within kLiteMaxOffset; beyond, the
-    // double-float stages FA and FB refine the draw
+    // double-float pass FD refines the draw
     const bool lite = fabsf(Kq) <= kLiteMaxOffset && (!dr.pair || fabsf(Kp) <= kLiteMaxOffset);
-    enqueue_row_stage(a.ws, lite ? kFR : kFA, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
+    enqueue_row_stage(a.ws, lite ? kFR : kFD, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
   }
   __syncwarp();
 }
@@ -1428,7 +1432,7 @@ __device__ void combine_task(const SampleArgs& a, const QTask& t, const uint8_t*
       o[1] = s0.lo;
       o[2] = s1.hi;
       o[3] = s1.lo;
-    } else if (t.type == kFR) {
+    } else if (t.type == kFR || t.type == kFD) {
       const df* w = reinterpret_cast<const df*>(slot + 16);
       df x[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
       for (int q = 0; q < kCW; ++q)
@@ -1738,13 +1742,15 @@ __device__ __forceinline__ void df_warp_sum2(uint64_t& H, uint64_t& Lo) {
 }
 
 // FR: one pass over the draw's rows (see the header) with the lighter
-// exponential (lite_exp2x2, relative error < kLiteExpRelErr) on packed pairs.
+// exponential (lite_exp2x2, relative error < kLiteExpRelErr) on packed pairs;
+// FD (kDf): the same pass with the double-float exponential (df_exp2,
+// relative error < 4e-13), for the rows FR leaves undecided.
 // Per unit the pair sums of e_q and e_p over the tokens with a certainly
 // positive residual; per task the row sums and the unit sums' totals;
 // tokens inside the sign test's margin go to the row's list. Each term is
 // first normalised to a pair (s, e) with |e| <= u |s| (FastTwoSum), so the
 // accumulations keep the error bound of acc2.
-template <class E>
+template <class E, bool kDf>
 __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot,
                            const QTask& t) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1786,7 +1792,12 @@ __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uin
 #pragma unroll
           for (int k = 0; k < E::kVec; ++k) {
             df eq, ep;
-            lite_exp2x2(zq[k], zp[k], Lq, Lp, LC, L.tab2, eq, ep);
+            if (kDf) {
+              eq = acc_elem(zq[k], a.Chi, a.Clo, Kq, L.tab2);
+              ep = acc_elem(zp[k], a.Chi, a.Clo, Kp, L.tab2);
+            } else {
+              lite_exp2x2(zq[k], zp[k], Lq, Lp, LC, L.tab2, eq, ep);
+            }
             const uint64_t h = f2_pack(eq.hi, ep.hi), l = f2_pack(eq.lo, ep.lo);
             const uint64_t sh = f2_add(h, l);
             const uint64_t sl = f2_sub(l, f2_sub(sh, h));
@@ -1817,7 +1828,12 @@ __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uin
 #pragma unroll
           for (int k = 0; k < E::kVec; k += 2) {
             df e0, e1;
-            lite_exp2x2(zq[k], zq[k + 1], Lq, Lq, LC, L.tab2, e0, e1);
+            if (kDf) {
+              e0 = acc_elem(zq[k], a.Chi, a.Clo, Kq, L.tab2);
+              e1 = acc_elem(zq[k + 1], a.Chi, a.Clo, Kq, L.tab2);
+            } else {
+              lite_exp2x2(zq[k], zq[k + 1], Lq, Lq, LC, L.tab2, e0, e1);
+            }
             const uint64_t h = f2_pack(e0.hi, e1.hi), l = f2_pack(e0.lo, e1.lo);
             const uint64_t sh = f2_add(h, l);
             const uint64_t sl = f2_sub(l, f2_sub(sh, h));
@@ -1875,9 +1891,10 @@ __device__ bool consume_fr(const SampleArgs& a, const Smem& L, uint32_t& it, uin
   return ok;
 }
 
-// FR complete: accurate normalisers, the ambiguous tokens decided exactly,
-// residual unit sums and the certified search (or the FA / FB fallback).
-template <class E>
+// FR / FD complete: accurate normalisers, the ambiguous tokens decided
+// exactly, residual unit sums and the certified search; a draw FR leaves
+// undecided goes to FD, a list overflow (or a degenerate row) to FA / FB.
+template <class E, bool kDf>
 __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
   const int lane = threadIdx.x & 31;
   RowState* st = row_state(a, b);
@@ -1949,10 +1966,10 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
   if (!(Sr.hi > 0.0f) && dr.pair) {
     // zero residual mass: the draw uses q_j itself
     if (lane == 0) {
-      st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;
-      st->namb = 0;
+      st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;  // (a q-only pass keeps no list of tokens)
       const int pb = piece_choice(a);
-      enqueue_row_stage(a.ws, kFR, b, stage_tasks(a, pb), dr.j | (kModeQ << 8) | pb);
+      enqueue_row_stage(a.ws, kDf ? kFD : kFR, b, stage_tasks(a, pb),
+                        dr.j | (kModeQ << 8) | pb);
     }
     __syncwarp();
     return;
@@ -1963,34 +1980,55 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
   // and products; summed with weights q and p (total 1 each, margin 10%). The
   // walk of the final unit recomputes its terms the same way. A token whose
   // sign is undecidable within that error moves by at most its own error.
-  const float Eb = 1.1f * kFrRho * (dr.pair ? 2.0f : 1.0f) + 1e-14f * Sr.hi + 1e-36f;
+  const float rho = kDf ? fmaxf(acc_rho(Kq), acc_rho(Kp)) : kFrRho;
+  const float Eb = 1.1f * rho * (dr.pair ? 2.0f : 1.0f) + 1e-14f * Sr.hi + 1e-36f;
   int token = -1;
   bool cert = false;
   {
     const RowPtrs<E> rp = row_ptrs<E>(a, b);
-    LiteEntries<E> le;
-    le.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
-    le.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
-    le.pair = dr.pair;
-    le.tauq = thr_of(a, b, true, dr.j);
-    le.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
-    le.LC = lite_consts(a.Chi, a.Clo);
-    le.Lq = lite_row(Kq, a.Chi);
-    le.Lp = dr.pair ? lite_row(Kp, a.Chi) : le.Lq;
-    le.Iq = Iq;
-    le.Ip = Ip;
-    le.tab = L.tab2;
     FrUnits fu{&a, b, namb, av, dr.pair, Iq, Ip, ad};
-    token = search_draw<E>(a, b, le, sl, df_mul_f(Sr, uK), Eb, cert, fu);
+    if (kDf) {
+      AccEntries<E> ae;
+      ae.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
+      ae.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
+      ae.pair = dr.pair;
+      ae.tauq = thr_of(a, b, true, dr.j);
+      ae.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
+      ae.Chi = a.Chi;
+      ae.Clo = a.Clo;
+      ae.Kq = Kq;
+      ae.Kp = Kp;
+      ae.Iq = Iq;
+      ae.Ip = Ip;
+      ae.tab = L.tab2;
+      token = search_draw<E>(a, b, ae, sl, df_mul_f(Sr, uK), Eb, cert, fu);
+    } else {
+      LiteEntries<E> le;
+      le.tq = reinterpret_cast<const uint4*>(rp.tgt + size_t(dr.j) * a.V);
+      le.tp = dr.pair ? reinterpret_cast<const uint4*>(rp.drf + size_t(dr.j) * a.V) : nullptr;
+      le.pair = dr.pair;
+      le.tauq = thr_of(a, b, true, dr.j);
+      le.taup = dr.pair ? thr_of(a, b, false, dr.j) : -INFINITY;
+      le.LC = lite_consts(a.Chi, a.Clo);
+      le.Lq = lite_row(Kq, a.Chi);
+      le.Lp = dr.pair ? lite_row(Kp, a.Chi) : le.Lq;
+      le.Iq = Iq;
+      le.Ip = Ip;
+      le.tab = L.tab2;
+      token = search_draw<E>(a, b, le, sl, df_mul_f(Sr, uK), Eb, cert, fu);
+    }
   }
-  if (token >= 0 && cert) {
-    write_outputs(a, b, dr.j, token, flags, false, d);
+  if (kDf || (token >= 0 && cert)) {
+    // FD's bound is the final word: a draw even FD leaves undecided is flagged
+    const int fl = flags | (cert ? 0 : SPEC_ROW_UNCERTIFIED);
+    if (token < 0 && lane == 0 && a.err) atomicOr(a.err, SPEC_DERR_LOGITS);
+    write_outputs(a, b, dr.j, token, fl, token < 0, d);
     return;
   }
-  // not settled within FR's bound: the double-float stages FA and FB
+  // not settled within FR's bound: one double-float pass of the same kind (FD)
   if (lane == 0) {
     const int pb = piece_choice(a);
-    enqueue_row_stage(a.ws, kFA, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
+    enqueue_row_stage(a.ws, kFD, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
   }
   __syncwarp();
 }
@@ -2086,7 +2124,10 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
               finish_fa(a, t.b, t.aux);
               break;
             case kFR:
-              finish_fr<E>(a, L, t.b, t.aux);
+              finish_fr<E, false>(a, L, t.b, t.aux);
+              break;
+            case kFD:
+              finish_fr<E, true>(a, L, t.b, t.aux);
               break;
             default:
               finish_fb<E>(a, L, t.b, t.aux);
@@ -2113,7 +2154,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
       if (t.type == kP1 || t.type == kBS) ok = consume_stats<E>(a, L, it, slot, t);
       else if (t.type == kSW) ok = consume_sw<E>(a, L, it, slot, t);
       else if (t.type == kFA || t.type == kAR) ok = consume_rowsums<E>(a, L, it, slot, t);
-      else if (t.type == kFR) ok = consume_fr<E>(a, L, it, slot, t);
+      else if (t.type == kFR) ok = consume_fr<E, false>(a, L, it, slot, t);
+      else if (t.type == kFD) ok = consume_fr<E, true>(a, L, it, slot, t);
       else ok = consume_fb<E>(a, L, it, slot, t);
       handoff_post(L.ho, n);
       if (!ok) {
@@ -2162,9 +2204,9 @@ WsLayout sample_layout(int B, int K, int V, int dtype) {
   const int ustride = 2 * ((maxslice + 31) / 32) + 2;
   int part = (8 * K > 8) ? 8 * K : 8;  // P1: 4 floats for each of the 2K rows; FR: 8
   if (part < 8 * M) part = 8 * M;      // a row's S blocks hold its R = S M piece partials
-  // queued tasks per row: BS, SW (S each); FR twice (zero residual), FA, FB
-  // twice, AR up to K times (R = S M each)
-  return ws_layout(B, S, part, ustride, (6 + K) * M, int(sizeof(RowState)));
+  // queued tasks per row: BS, SW (S each); FR and FD twice each (zero
+  // residual), FA, FB twice, AR up to K times (R = S M each)
+  return ws_layout(B, S, part, ustride, (8 + K) * M, int(sizeof(RowState)));
 }
 
 }  // namespace
