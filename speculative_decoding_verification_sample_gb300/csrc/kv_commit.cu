@@ -29,6 +29,7 @@
 
 #include "../../include/specverify.h"
 #include "launch.h"
+#include "launch_util.cuh"
 #include "ptx.cuh"
 
 namespace sv {
@@ -134,6 +135,8 @@ __global__ void __launch_bounds__(kPlanThreads) kv_plan_kernel(const KvArgs a) {
   __shared__ int sh[96];
   __shared__ int s_err, s_need, s_push;
   const int tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();  // the verification that produced num_accepted
   if (tid == 0) {
     s_err = 0;
     s_need = 0;
@@ -217,6 +220,8 @@ __global__ void __launch_bounds__(kCopyThreads) kv_copy_kernel(const KvArgs a) {
   // one CTA per (row, kept position): every SM takes a share of the slots,
   // whatever the rows' accepted lengths
   const int b = blockIdx.x / (a.K + 1), s = blockIdx.x % (a.K + 1);
+  pdl_trigger();
+  pdl_wait();  // the plan
   if (*a.status != 0) return;
   const int n = a.na[b];
   if (s > n) return;
@@ -256,6 +261,7 @@ __global__ void __launch_bounds__(kCopyThreads) kv_copy_kernel(const KvArgs a) {
 // copy CTAs read both, so they change only once all have run).
 __global__ void __launch_bounds__(256) kv_finish_kernel(const KvArgs a) {
   const int b = blockIdx.x * 256 + threadIdx.x;
+  pdl_wait();  // every copy
   if (b >= a.B || *a.status != 0) return;
   a.sl[b] = a.sl[b] + a.na[b] + 1;
   for (int i = 0; i < a.P; ++i) a.pb[size_t(b) * a.P + i] = -1;
@@ -302,6 +308,8 @@ __global__ void __launch_bounds__(kPlanThreads) kv_truncate_kernel(const TruncAr
   __shared__ int sh[96];
   __shared__ int s_err, s_push;
   const int tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();  // the verification that produced num_accepted
   if (tid == 0) {
     s_err = 0;
     s_push = 0;
@@ -349,8 +357,8 @@ __global__ void __launch_bounds__(kPlanThreads) kv_truncate_kernel(const TruncAr
 int launch_kv_truncate(const KvTruncLaunch& k) {
   TruncArgs a{k.block_table, k.seq_lens, k.num_accepted, k.num_blocks, k.block_size, k.B, k.K,
               k.max_blocks, k.free_stack, k.free_top, k.status};
-  kv_truncate_kernel<<<1, kPlanThreads, 0, static_cast<cudaStream_t>(k.stream)>>>(a);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+  return launch_pdl(kv_truncate_kernel, dim3(1), dim3(kPlanThreads), 0,
+                    static_cast<cudaStream_t>(k.stream), a);
 }
 
 int launch_kv_commit(const KvLaunch& k) {
@@ -376,13 +384,13 @@ int launch_kv_commit(const KvLaunch& k) {
   a.smap = k.slot_map;
   a.slot_bytes = int64_t(k.num_kv_heads) * k.head_dim * k.elem_bytes;
   cudaStream_t st = static_cast<cudaStream_t>(k.stream);
-  kv_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ECUDA;
-  kv_copy_kernel<<<k.B * (k.K + 1), kCopyThreads, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ECUDA;
-  kv_finish_kernel<<<(k.B + 255) / 256, 256, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ECUDA;
-  return SPEC_OK;
+  // each launch starts while its predecessor finishes and waits for it
+  // (programmatic dependent launch), so the three hide each other's launch gaps
+  if (launch_pdl(kv_plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, a) != SPEC_OK)
+    return SPEC_ECUDA;
+  if (launch_pdl(kv_copy_kernel, dim3(k.B * (k.K + 1)), dim3(kCopyThreads), 0, st, a) != SPEC_OK)
+    return SPEC_ECUDA;
+  return launch_pdl(kv_finish_kernel, dim3((k.B + 255) / 256), dim3(256), 0, st, a);
 }
 
 }  // namespace sv

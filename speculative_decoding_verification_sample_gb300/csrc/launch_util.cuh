@@ -10,6 +10,42 @@
 
 namespace sv {
 
+// Launch with programmatic stream serialization (see pdl_wait): the kernel
+// may start while its predecessor on the stream finishes, and waits for it
+// with pdl_wait() before touching that predecessor's results.
+template <class Kern, class... Args>
+int launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, args...) != cudaSuccess) return SPEC_ECUDA;
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
+// Zeroes n 16-byte words of the workspace (the per-launch counters and work
+// queue) ahead of a verification launch, which starts early and waits for it
+// (programmatic dependent launch) instead of following a host memset.
+static __global__ void zero_words_kernel(uint4* p, size_t n) {
+  pdl_trigger();
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += size_t(gridDim.x) * blockDim.x)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+inline int zero_workspace(void* ws, size_t bytes, cudaStream_t st) {
+  const size_t n = (bytes + 15) / 16;  // the zeroed regions are 256-byte aligned and padded
+  const int grid = int((n + 255) / 256 < 512 ? (n + 255) / 256 : 512);
+  zero_words_kernel<<<grid > 0 ? grid : 1, 256, 0, st>>>(static_cast<uint4*>(ws), n);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+}
+
 // Dataflow launch: one grid of persistent CTAs, as many as are co-resident
 // (occupancy query, cached per kernel and shared-memory size); the kernels
 // fetch their work from the workspace counters.
@@ -50,8 +86,7 @@ int launch_dataflow(Kern kern, const Args& args, size_t smem, cudaStream_t st) {
     const int g = std::atoi(env);
     if (g > 0 && g < grid) grid = g;
   }
-  kern<<<grid, kThreads, smem, st>>>(args);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ECUDA;
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, st, args);
 }
 
 }  // namespace sv

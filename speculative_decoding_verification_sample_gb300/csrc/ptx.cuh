@@ -89,6 +89,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// ----------------------------------------------------------------- dependent launches
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor on the stream has finished;
+// pdl_wait() returns once the predecessor has completed and its memory
+// operations are visible (a hardware dependency wait), and pdl_trigger()
+// lets this kernel's own successor start early. Without the launch
+// attribute both return at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- bulk copy
 // 1-D bulk async copy global -> this CTA's shared memory; completion (bytes)
 // is signalled on `bar`. Addresses 16-byte aligned, size a multiple of 16.

@@ -358,6 +358,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
   ring_init(L.ring);
   handoff_init(L.ho);
   __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // the workspace zeroing launched just before
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* h = a.ws.hdr();
 
@@ -484,7 +486,7 @@ int launch_verify_greedy(const GreedyLaunch& g) {
   a.parents = g.parents;
   a.out_slots = g.out_slots;
   cudaStream_t st = static_cast<cudaStream_t>(g.stream);
-  if (cudaMemsetAsync(g.workspace, 0, wl.zero_bytes, st) != cudaSuccess) return SPEC_ECUDA;
+  if (zero_workspace(g.workspace, wl.zero_bytes, st) != SPEC_OK) return SPEC_ECUDA;
   const size_t smem = greedy_smem_bytes(rows_of(a));
   if (g.dtype == SPEC_BF16) return launch_dataflow(verify_greedy_kernel<EBf16>, a, smem, st);
   return launch_dataflow(verify_greedy_kernel<EF32>, a, smem, st);

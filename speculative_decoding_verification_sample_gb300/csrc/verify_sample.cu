@@ -2075,6 +2075,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
   for (int i = threadIdx.x; i < 256; i += kThreads)
     L.tab2[i] = make_float2(kExp2Tab.hi[i], kExp2Tab.lo[i]);
   __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // the workspace zeroing launched just before
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WsHeader* h = a.ws.hdr();
 
@@ -2256,7 +2258,7 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.thr_d = s.thr_d;
   a.masked = (s.thr_t || s.thr_d) ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(s.stream);
-  if (cudaMemsetAsync(s.workspace, 0, wl.zero_bytes, st) != cudaSuccess) return SPEC_ECUDA;
+  if (zero_workspace(s.workspace, wl.zero_bytes, st) != SPEC_OK) return SPEC_ECUDA;
   const size_t smem = sample_smem_bytes(2 * s.K);
   if (a.masked) {
     if (s.dtype == SPEC_BF16)
