@@ -55,9 +55,10 @@ struct EBf16 {
     __nv_bfloat162 m = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
     return max_nan(__low2float(m), __high2float(m));
   }
-  __device__ static __forceinline__ float load(const T* p, int64_t i) {
-    return __uint_as_float(static_cast<uint32_t>(p[i]) << 16);
+  __device__ static __forceinline__ float cvt(T x) {
+    return __uint_as_float(static_cast<uint32_t>(x) << 16);
   }
+  __device__ static __forceinline__ float load(const T* p, int64_t i) { return cvt(p[i]); }
 };
 
 // fp32 logits: 4 values per 16-byte vector.
@@ -75,6 +76,7 @@ struct EF32 {
           d = __uint_as_float(v.w);
     return max_nan(max_nan(a, b), max_nan(c, d));
   }
+  __device__ static __forceinline__ float cvt(T x) { return x; }
   __device__ static __forceinline__ float load(const T* p, int64_t i) { return p[i]; }
 };
 

@@ -36,15 +36,19 @@ namespace sv {
 // persistent CTA gets about four (kTargetTasks), and row slices of at most
 // four ring stages; otherwise as few as possible, since every task and every
 // row slice costs fixed work (a fetch, a hand-off, an arrival, per-row warp
-// reductions). Slices keep at least 64 vectors; at most kMaxSlices (two
-// warp-wide scans in the draw).
+// reductions). Small batches (B <= kSmallBatch) take one task per CTA
+// instead: their streaming is short next to the latency of the stages after
+// it, and one wave lets every row reach those stages at the same time.
+// Slices keep at least 64 vectors; at most kMaxSlices (two warp-wide scans
+// in the draw).
 constexpr int kMaxSlices = 64;
 constexpr int kTargetTasks = 1216;  // four per CTA of a 152-SM GB300 at two CTAs per SM
+constexpr int kSmallBatch = 16;
 
 __host__ __device__ inline int slices_for(int nvec, int B) {
   const int per = 4 * (kChunk / 16);
   int s = (nvec + per - 1) / per;
-  int par = (kTargetTasks + B - 1) / B;
+  int par = B <= kSmallBatch ? kTargetTasks / 4 / B : (kTargetTasks + B - 1) / B;
   const int cap = nvec / 64 > 1 ? nvec / 64 : 1;
   if (par > cap) par = cap;
   if (s < par) s = par;
@@ -83,6 +87,7 @@ __device__ __forceinline__ QTask unpack_task(uint64_t w) {
 struct WsLayout {
   size_t header, row_cnt, entries, part, units, rowstate, total, zero_bytes;
   int B, S, qcap, part_floats, ustride, rowstate_bytes;
+  int kp = 1;  // first-stage tasks per (row, slice): 1, or one per draft position
 };
 
 __host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) / 256 * 256; }
@@ -164,29 +169,45 @@ __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
 }
 
 // ------------------------------------------------------------------ queue
-// Appends the n tasks (type, b, s = 0..n-1, aux); called by one lane. A
-// fence between the caller's earlier writes (row state) and the entries,
-// paired with the fence the reader issues after seeing an entry, makes those
-// writes visible to the task. A queue overflow (more later-stage tasks than
-// the layout provides) aborts the launch.
+// Appends the n tasks (type, b, s = 0..n-1, aux); called by all 32 lanes of
+// a warp, with lane 0's arguments. Lane 0 reserves the entries, then every
+// lane fences and writes its share of them: __syncwarp orders the lanes'
+// earlier writes (row state) before each lane's fence, and that fence,
+// paired with the one the reader issues after seeing an entry, makes them
+// visible to the task. A queue overflow (more later-stage tasks than the
+// layout provides) aborts the launch.
 __device__ inline void enqueue_row_stage(const Ws& ws, int type, int b, int n, int aux) {
-  const uint32_t base = atomicAdd(&ws.hdr()->dq_tail, uint32_t(n));
-  __threadfence();  // the caller's writes before any entry (the reader fences after its load)
+  const int lane = threadIdx.x & 31;
+  type = __shfl_sync(0xffffffffu, type, 0);
+  b = __shfl_sync(0xffffffffu, b, 0);
+  n = __shfl_sync(0xffffffffu, n, 0);
+  aux = __shfl_sync(0xffffffffu, aux, 0);
+  __syncwarp();
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(&ws.hdr()->dq_tail, uint32_t(n));
+  __threadfence();
+  base = __shfl_sync(0xffffffffu, base, 0);
   if (base + uint32_t(n) > uint32_t(ws.L.qcap)) {
-    atomicExch(&ws.hdr()->abort, 1u);
+    if (lane == 0) atomicExch(&ws.hdr()->abort, 1u);
     return;
   }
   uint64_t* e = ws.entries();
-  for (int s = 0; s < n; ++s) st_relaxed_u64(&e[base + s], pack_task(type, b, s, aux));
+  for (int s = lane; s < n; s += 32) st_relaxed_u64(&e[base + s], pack_task(type, b, s, aux));
 }
 
-__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
   uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void fence_acq_rel_gpu() {
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+// Atomic add with acquire and release semantics at GPU scope: the caller's
+// earlier writes (and those ordered before them) are visible to whoever
+// acquires the counter after it, and this thread sees what earlier adders
+// released.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_u32(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
 // The producer's task source. Queued tasks are claimed by ticket: every
@@ -201,7 +222,8 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 // ticket's entry and reserves the next first-stage task, all without waiting;
 // next(), called at the task boundary, uses what prepare() found. Only when
 // nothing was prepared does next() wait on memory itself. Entries are read
-// with relaxed loads and acquired with a fence once seen.
+// with acquire loads, so the row state written before an entry is visible
+// once the entry is seen.
 struct Fetcher {
   static constexpr uint32_t kNone = 0xffffffffu;
   int64_t ticket = -1;   // held queue ticket
@@ -212,17 +234,17 @@ struct Fetcher {
   __device__ __forceinline__ void prepare(const Ws& ws) {
     WsHeader* h = ws.hdr();
     if (ticket < 0) ticket = int64_t(atomicAdd(&h->dq_head, 1u));
-    else if (word == 0 && ticket < int64_t(ws.L.qcap)) word = ld_relaxed_u64(&ws.entries()[ticket]);
+    else if (word == 0 && ticket < int64_t(ws.L.qcap)) word = ld_acquire_u64(&ws.entries()[ticket]);
     if (kres == kNone && first_left) kres = atomicAdd(&h->p1_next, 1u);
   }
 
   // 1: task in t; 0: nothing runnable now; the caller backs off and retries.
   __device__ __forceinline__ int next(const Ws& ws, int first_type, QTask& t) {
     WsHeader* h = ws.hdr();
-    const uint32_t total = uint32_t(ws.L.B) * uint32_t(ws.L.S);
+    const uint32_t per = uint32_t(ws.L.S) * uint32_t(ws.L.kp);  // first-stage tasks per row
+    const uint32_t total = uint32_t(ws.L.B) * per;
     for (int pass = 0; pass < 2; ++pass) {
       if (ticket >= 0 && word != 0) {
-        fence_acq_rel_gpu();
         t = unpack_task(word);
         ticket = -1;
         word = 0;
@@ -232,7 +254,8 @@ struct Fetcher {
         const uint32_t k = kres;
         kres = kNone;
         if (k < total) {
-          t = QTask{first_type, int(k / ws.L.S), int(k % ws.L.S), 0};
+          // row-major, then slice, then (kp > 1) position
+          t = QTask{first_type, int(k / per), int((k % per) / ws.L.kp), int(k % ws.L.kp)};
           return 1;
         }
         first_left = false;
@@ -240,7 +263,7 @@ struct Fetcher {
       if (pass == 1) break;
       // nothing prepared: fetch now
       if (ticket < 0) ticket = int64_t(atomicAdd(&h->dq_head, 1u));
-      if (ticket < int64_t(ws.L.qcap)) word = ld_relaxed_u64(&ws.entries()[ticket]);
+      if (ticket < int64_t(ws.L.qcap)) word = ld_acquire_u64(&ws.entries()[ticket]);
       if (word == 0 && first_left) kres = atomicAdd(&h->p1_next, 1u);
     }
     return 0;
@@ -491,18 +514,21 @@ __device__ inline void finisher_loop(const Ws& ws, const Handoff& ho, volatile i
       t.aux = __shfl_sync(0xffffffffu, mine.aux, k);
       combine(t, ho.slot(n + k));
     }
+    // __syncwarp orders every lane's partial writes before each lane's
+    // arrival, whose release makes them visible to the row's last arriver;
+    // its acquire (then __syncwarp for the other lanes) makes every task's
+    // partials visible to the continuation
     __syncwarp();
-    __threadfence();
     if (lane == 0)
       for (int k = 0; k < cnt; ++k) mbar_arrive(&ho.freed[(n + k) % kSlots]);
     int last = 0;
     if (lane < cnt && mine.b != ws.stall_row) {
-      const uint32_t old = atomicAdd(&ws.row_cnt()[mine.b], 1u);
+      const uint32_t old = atom_add_acq_rel_u32(&ws.row_cnt()[mine.b], 1u);
       last = (old == uint32_t(expect(mine)) - 1);  // tasks in the row's stage
       if (last) ws.row_cnt()[mine.b] = 0;  // the row's next stage counts from zero
     }
     unsigned lm = __ballot_sync(0xffffffffu, last);
-    if (lm) __threadfence();
+    if (lm) __syncwarp();
     while (lm) {
       const int k = __ffs(int(lm)) - 1;
       lm &= lm - 1;

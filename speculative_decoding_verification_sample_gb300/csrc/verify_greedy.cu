@@ -273,8 +273,7 @@ __device__ void finish_g1(const GreedyArgs& a, const Smem& L, int b) {
     write_row(a, b, n, __shfl_sync(0xffffffffu, g, n), false, 0);
     return;
   }
-  if (lane == 0) enqueue_row_stage(a.ws, kGB, b, a.S, K);
-  __syncwarp();
+  enqueue_row_stage(a.ws, kGB, b, a.S, K);
 }
 
 // GB complete: the bonus token is the argmax of target row K.

@@ -97,6 +97,10 @@ struct SampleArgs {
   const float* thr_t;            // optional [B, K + 1] target-row logit thresholds
   const float* thr_d;            // optional [B, K] draft-row logit thresholds
   int masked;                    // either is given
+  // Small batches: one first-stage task per (slice, draft position), which
+  // covers target and draft row i of the slice, so that the first pass
+  // spreads over every CTA
+  int p1sub;
   Ws ws;
 };
 
@@ -581,11 +585,21 @@ __device__ __forceinline__ bool is_piece(const QTask& t) {
 // kPieceBit if the next rare stage of a row should run on pieces.
 __device__ __forceinline__ int piece_choice(const SampleArgs& a) {
   if (a.M == 1) return 0;
-  return ld_volatile_u32(&a.ws.hdr()->p1_next) >= uint32_t(a.B) * uint32_t(a.S) ? kPieceBit : 0;
+  return ld_volatile_u32(&a.ws.hdr()->p1_next) >=
+                 uint32_t(a.B) * uint32_t(a.S) * uint32_t(a.p1sub ? a.K : 1)
+             ? kPieceBit
+             : 0;
 }
 
 __device__ __forceinline__ int stage_tasks(const SampleArgs& a, int piece_bit) {
   return piece_bit ? a.R : a.S;
+}
+
+// Queues a rare stage of row b (all lanes; lane 0's arguments), on slices or
+// pieces as piece_choice decides.
+__device__ __forceinline__ void enqueue_rare(const SampleArgs& a, int type, int b, int aux) {
+  const int pb = __shfl_sync(0xffffffffu, (threadIdx.x & 31) == 0 ? piece_choice(a) : 0, 0);
+  enqueue_row_stage(a.ws, type, b, stage_tasks(a, pb), aux | pb);
 }
 
 // Vector range [v0, v1) of the task's part of the row: slice s, or for the
@@ -627,10 +641,13 @@ __device__ __forceinline__ float* task_part(const SampleArgs& a, bool pieces, in
 // Row statistics of rows [0, nrows) (float offset 4r of each slice's
 // partials: max, sum hi, sum lo, NaN seen) into the finisher scratch. Rows
 // are taken up to 32 at a time; each row gets g lanes (g = 32 / rows, a
-// power of two), lane k of a row combines slices k, k + g, ... (all its
-// loads issued together: one memory round trip per group of rows), then the
-// row's lanes reduce with g / 2 .. 1 butterfly shuffles: few dependent steps
-// for any number of slices.
+// power of two), lane k of a row combines slices k, k + g, ... in batches of
+// kStatBatch loads issued together (one memory round trip per batch), keeping
+// a running offset: a larger maximum rescales the running sum by the power of
+// two between the offsets, which is exact, so the sum equals the one taken
+// at the final offset term by term (up to terms below 2^-126 of the
+// largest). The row's lanes then merge with g / 2 .. 1 butterfly shuffles.
+constexpr int kStatBatch = 8;
 __device__ void stats_rows(const SampleArgs& a, Fin& F, int b, int nrows) {
   const int lane = threadIdx.x & 31, S = a.S;
   for (int r0 = 0; r0 < nrows; r0 += 32) {
@@ -639,21 +656,36 @@ __device__ void stats_rows(const SampleArgs& a, Fin& F, int b, int nrows) {
     while (g * 2 * rg <= 32) g *= 2;
     const int rr = lane / g, k = lane % g, r = r0 + rr;
     const bool live = rr < rg;
-    float4 it[4];
-    // up to 4 slices per lane are loaded at once; more (small g, many slices) loop
-    float M = -INFINITY;
+    float M = -INFINITY, Kr = -INFINITY;  // running maximum and its offset
+    df Ssum{0.f, 0.f};                    // at offset Kr
     int bad = 0;
-    for (int s0 = k; s0 < S; s0 += 4 * g) {
+    for (int s0 = k; s0 < S; s0 += kStatBatch * g) {
+      float4 it[kStatBatch];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kStatBatch; ++q) {
         const int sl = s0 + q * g;
         it[q] = (live && sl < S) ? __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, sl) + 4 * r))
                                  : make_float4(-INFINITY, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kStatBatch; ++q) {
         M = fmaxf(M, it[q].x);
         bad |= __float_as_int(it[q].w);
+      }
+      const float Kn = offset_of(M, a.c);
+      if (Kn > Kr) {
+        if (Ssum.hi != 0.0f) {
+          const float sc = pow2i(__fsub_rn(Kr, Kn));
+          Ssum = df{__fmul_rn(Ssum.hi, sc), __fmul_rn(Ssum.lo, sc)};
+        }
+        Kr = Kn;
+      }
+#pragma unroll
+      for (int q = 0; q < kStatBatch; ++q) {
+        if (it[q].y != 0.0f) {
+          const float sc = pow2i(__fsub_rn(offset_of(it[q].x, a.c), Kr));
+          Ssum = df_add(Ssum, df{__fmul_rn(it[q].y, sc), __fmul_rn(it[q].z, sc)});
+        }
       }
     }
     for (int o = g / 2; o > 0; o >>= 1) {
@@ -661,24 +693,9 @@ __device__ void stats_rows(const SampleArgs& a, Fin& F, int b, int nrows) {
       bad |= __shfl_xor_sync(0xffffffffu, bad, o);
     }
     const float Kc = offset_of(M, a.c);
-    df Ssum{0.f, 0.f};
-    for (int s0 = k; s0 < S; s0 += 4 * g) {
-      if (S > 4 * g) {  // more than one batch of slices per lane: load this batch again
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int sl = s0 + q * g;
-          it[q] = (live && sl < S)
-                      ? __ldcg(reinterpret_cast<const float4*>(a.ws.part(b, sl) + 4 * r))
-                      : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (it[q].y != 0.0f) {
-          const float sc = pow2i(__fsub_rn(offset_of(it[q].x, a.c), Kc));
-          Ssum = df_add(Ssum, df{__fmul_rn(it[q].y, sc), __fmul_rn(it[q].z, sc)});
-        }
-      }
+    if (Ssum.hi != 0.0f) {  // to the row's offset (Kr <= Kc, both finite here)
+      const float sc = pow2i(__fsub_rn(Kr, Kc));
+      Ssum = df{__fmul_rn(Ssum.hi, sc), __fmul_rn(Ssum.lo, sc)};
     }
     for (int o = g / 2; o > 0; o >>= 1) Ssum = df_add(Ssum, df_shfl_xor(Ssum, o));
     if (live && k == 0) {
@@ -772,14 +789,13 @@ __device__ void start_draw(const SampleArgs& a, int b, int j, int flags, float K
       st->Rq = Rq;
       st->Kp = Kp;
       st->Rp = Rp;
-      enqueue_row_stage(a.ws, kSW, b, a.S, j | (kModeResidual << 8));
     } else {
       st->Kq = Kg;
       st->Rq = 1.0f;  // the raw sweep sums e, not q
-      enqueue_row_stage(a.ws, kSW, b, a.S, a.K | (kModeQ << 8) | kRawBit);
     }
   }
-  __syncwarp();
+  enqueue_row_stage(a.ws, kSW, b, a.S,
+                    j < a.K ? (j | (kModeResidual << 8)) : (a.K | (kModeQ << 8) | kRawBit));
 }
 
 // Continues the accept tests from position i0 given the test states (lane i
@@ -808,17 +824,14 @@ __device__ void continue_tests(const SampleArgs& a, int b, int i0, int flags, in
     return;
   }
   // ambiguous: double-float sums of target and draft row i (AR stage)
-  if (lane == 0) {
-    row_state(a, b)->flags = flags | SPEC_ROW_ACCEPT_REFINED;
-    const int pb = piece_choice(a);
-    enqueue_row_stage(a.ws, kAR, b, stage_tasks(a, pb), i | pb);
-  }
-  __syncwarp();
+  if (lane == 0) row_state(a, b)->flags = flags | SPEC_ROW_ACCEPT_REFINED;
+  enqueue_rare(a, kAR, b, i);
 }
 
 // P1 complete: statistics of the 2K rows, accept tests, first rejection.
-// Memory round trips: the draft tokens, uniforms and slice partials load
-// together, then the logits at the draft tokens.
+// Memory round trips: the draft tokens and uniforms; then the logits at the
+// draft tokens together with the first batch of slice partials; then any
+// further batches of partials.
 template <class E>
 __device__ void finish_p1(const SampleArgs& a, const Smem& L, int b) {
   const int lane = threadIdx.x & 31, K = a.K, V = a.V;
@@ -827,16 +840,19 @@ __device__ void finish_p1(const SampleArgs& a, const Smem& L, int b) {
   const RowPtrs<E> rp = row_ptrs<E>(a, b);
   const int d = load_tokens(a, b);
   const float u = lane < K ? a.uniforms[size_t(b) * (K + 1) + lane] : 1.0f;
-  stats_rows(a, F, b, 2 * K);
   const bool badtok_lane = lane < K && (d < 0 || d >= V);
-  float zt = 0.f, zd = 0.f;
+  // raw elements: converted only after the statistics, so that nothing
+  // waits for these loads before the partials' loads are issued
+  typename E::T rt{}, rd{};
   if (lane < K && !badtok_lane) {
-    zt = E::load(rp.tgt + size_t(lane) * V, d);
-    zd = E::load(rp.drf + size_t(lane) * V, d);
-    if (E::kMask) {
-      if (!(zt >= thr_of(a, b, true, lane))) zt = -INFINITY;
-      if (!(zd >= thr_of(a, b, false, lane))) zd = -INFINITY;
-    }
+    rt = rp.tgt[size_t(lane) * V + d];
+    rd = rp.drf[size_t(lane) * V + d];
+  }
+  stats_rows(a, F, b, 2 * K);
+  float zt = E::cvt(rt), zd = E::cvt(rd);
+  if (E::kMask && lane < K && !badtok_lane) {
+    if (!(zt >= thr_of(a, b, true, lane))) zt = -INFINITY;
+    if (!(zd >= thr_of(a, b, false, lane))) zd = -INFINITY;
   }
   for (int r = lane; r < 2 * K; r += 32) {
     st->rK[r] = F.rowKc[r];
@@ -971,9 +987,8 @@ __device__ void finish_bs(const SampleArgs& a, const Smem& L, int b) {
   if (lane == 0) {
     st->Kq = F.rowKc[0];
     st->Rq = F.rowInv[0].hi;
-    enqueue_row_stage(a.ws, kSW, b, a.S, a.K | (kModeQ << 8));
   }
-  __syncwarp();
+  enqueue_row_stage(a.ws, kSW, b, a.S, a.K | (kModeQ << 8));
 }
 
 // The segment sums of a draw stage (slices after SW, pieces after FB), lanes
@@ -1186,8 +1201,7 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
     // finite): the statistics stage, then the normalised draw. Below 2^100
     // every exponent argument is below 100, inside the range over which the
     // ex2 bound is measured, and the sweep's sum of q|x| stays finite.
-    if (lane == 0) enqueue_row_stage(a.ws, kBS, b, a.S, a.K | (kModeQ << 8));
-    __syncwarp();
+    enqueue_row_stage(a.ws, kBS, b, a.S, a.K | (kModeQ << 8));
     return;
   }
   // Error bound (probability units) of the fp32 sweep. Per term, relative:
@@ -1253,13 +1267,11 @@ __device__ void finish_sw(const SampleArgs& a, int b, int aux) {
     st->amb_delta = 1.05f * (eps(sl.f2) + eps(sl.f3)) + 4.0f * kU;
     st->namb = 0;
     st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
-    const int pb = piece_choice(a);
-    // FR's exponential needs offsets within kLiteMaxOffset; beyond, the
-    // double-float pass FD refines the draw
-    const bool lite = fabsf(Kq) <= kLiteMaxOffset && (!dr.pair || fabsf(Kp) <= kLiteMaxOffset);
-    enqueue_row_stage(a.ws, lite ? kFR : kFD, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
   }
-  __syncwarp();
+  // FR's exponential needs offsets within kLiteMaxOffset; beyond, the
+  // double-float pass FD refines the draw
+  const bool lite = fabsf(Kq) <= kLiteMaxOffset && (!dr.pair || fabsf(Kp) <= kLiteMaxOffset);
+  enqueue_rare(a, lite ? kFR : kFD, b, aux & ~kPieceBit);
 }
 
 // Element index (token) of an ambiguous FR entry -> its slice or piece.
@@ -1321,10 +1333,8 @@ __device__ void finish_fa(const SampleArgs& a, int b, int aux) {
       st->Ip_hi = I1.hi;
       st->Ip_lo = I1.lo;
     }
-    const int pb = piece_choice(a);
-    enqueue_row_stage(a.ws, kFB, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
   }
-  __syncwarp();
+  enqueue_rare(a, kFB, b, aux & ~kPieceBit);
 }
 
 // FB complete: certified double-float draw (or the zero-residual rerun on q_j).
@@ -1344,12 +1354,8 @@ __device__ void finish_fb(const SampleArgs& a, const Smem& L, int b, int aux) {
   const float Eb = fmaxf(acc_rho(Kq), acc_rho(Kp)) * (sl.f2 + sl.f3) + 1e-14f * Sr.hi + 1e-36f;
   if (!(Sr.hi > 0.0f) && dr.pair) {
     // zero residual mass: the draw uses q_j itself
-    if (lane == 0) {
-      st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;
-      const int pb = piece_choice(a);
-      enqueue_row_stage(a.ws, kFB, b, stage_tasks(a, pb), dr.j | (kModeQ << 8) | pb);
-    }
-    __syncwarp();
+    if (lane == 0) st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;
+    enqueue_rare(a, kFB, b, dr.j | (kModeQ << 8));
     return;
   }
   int token = -1;
@@ -1382,7 +1388,10 @@ __device__ void combine_task(const SampleArgs& a, const QTask& t, const uint8_t*
   const int lane = threadIdx.x & 31;
   float* o = task_part(a, is_piece(t), t.b, t.s);
   if (t.type == kP1 || t.type == kBS) {
-    const int R = 2 * a.K, nrows = (t.type == kP1) ? 2 * a.K : 1;
+    // a per-position first-stage task covers rows 2 aux and 2 aux + 1
+    const bool sub = a.p1sub && t.type == kP1;
+    const int R = sub ? 2 : 2 * a.K, nrows = (t.type == kP1) ? R : 1;
+    if (sub) o += 8 * t.aux;
     const float* w = reinterpret_cast<const float*>(slot + 16);
     const int* wb = reinterpret_cast<const int*>(w + 2 * R * kCW);
     for (int r = lane; r < nrows; r += 32) {
@@ -1469,22 +1478,31 @@ template <class E>
 __device__ bool consume_stats(const SampleArgs& a, const Smem& L, uint32_t& it, uint8_t* slot,
                               const QTask& t) {
   const int tid = threadIdx.x;
+  // rows per task: 2K (P1), 2 (P1 per position aux, small batches), 1 (BS)
+  const bool sub = a.p1sub && t.type == kP1;
+  const int R = sub ? 2 : 2 * a.K;
+  const int pos0 = sub ? t.aux : 0;
   StatOp<E> op;
   op.c = a.c;
   op.tau = -INFINITY;
   op.begin();
+  // P1 rows: target i = 2i, draft i = 2i + 1; BS: target row K
+  auto tau_of = [&](int r) {
+    return (t.type == kBS) ? thr_of(a, t.b, true, a.K)
+                           : thr_of(a, t.b, (r & 1) == 0, pos0 + (r >> 1));
+  };
   for (;;) {
     const ChunkMeta m = L.ring.meta[it % kStages];
-    // P1 rows: target i = 2i, draft i = 2i + 1; BS: target row K
-    if (E::kMask)
-      op.tau = (t.type == kBS) ? thr_of(a, t.b, true, a.K) : thr_of(a, t.b, (m.r & 1) == 0, m.r >> 1);
-    op.chunk(stage_data(L.ring, it), m.c1 - m.c0, tid);
+    const uint4* buf = stage_data(L.ring, it);
+    const int cnt = m.c1 - m.c0;
+    if (E::kMask) op.tau = tau_of(m.r);
+    op.chunk(buf, cnt, tid);
     release_stage(L.ring, it);
-    ++it;
     if (m.last_k) {
-      op.end_row(slot, 2 * a.K, m.r);
+      op.end_row(slot, R, m.r);
       op.begin();
     }
+    ++it;
     if (m.last) return true;
     if (!wait_stage(L.ring, it)) return false;
   }
@@ -1925,11 +1943,7 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
   const int namb = dr.pair ? __ldcg(&st->namb) : 0;
   if (!(Sq.hi > 0.0f) || (dr.pair && !(Sp.hi > 0.0f)) || namb > kAmbCap) {
     // list overflow (or a degenerate row): the two-pass FA / FB path
-    if (lane == 0) {
-      const int pb = piece_choice(a);
-      enqueue_row_stage(a.ws, kFA, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
-    }
-    __syncwarp();
+    enqueue_rare(a, kFA, b, aux & ~kPieceBit);
     return;
   }
   const df Iq = df_recip(Sq), Ip = dr.pair ? df_recip(Sp) : df{0.f, 0.f};
@@ -1965,13 +1979,8 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
   const df Sr = sl.total;
   if (!(Sr.hi > 0.0f) && dr.pair) {
     // zero residual mass: the draw uses q_j itself
-    if (lane == 0) {
-      st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;  // (a q-only pass keeps no list of tokens)
-      const int pb = piece_choice(a);
-      enqueue_row_stage(a.ws, kDf ? kFD : kFR, b, stage_tasks(a, pb),
-                        dr.j | (kModeQ << 8) | pb);
-    }
-    __syncwarp();
+    if (lane == 0) st->flags = flags | SPEC_ROW_ZERO_RESIDUAL;  // (a q-only pass keeps no list of tokens)
+    enqueue_rare(a, kDf ? kFD : kFR, b, dr.j | (kModeQ << 8));
     return;
   }
   // Error bound: per token, relative error below kFrRho for e_q / S_q and
@@ -2026,18 +2035,14 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
     return;
   }
   // not settled within FR's bound: one double-float pass of the same kind (FD)
-  if (lane == 0) {
-    const int pb = piece_choice(a);
-    enqueue_row_stage(a.ws, kFD, b, stage_tasks(a, pb), (aux & ~kPieceBit) | pb);
-  }
-  __syncwarp();
+  enqueue_rare(a, kFD, b, aux & ~kPieceBit);
 }
 
 // Logit rows a task streams: their number, whether they are read element by
 // element in pairs, and (task_row) the base pointer of row r.
 __device__ inline int task_nrows(const SampleArgs& a, const QTask& t, bool& paired) {
   paired = false;
-  if (t.type == kP1) return 2 * a.K;
+  if (t.type == kP1) return a.p1sub ? 2 : 2 * a.K;
   if (t.type == kBS) return 1;
   if (t.type == kAR) return 2;
   const DrawRows dr = draw_rows(a.K, t.aux);
@@ -2050,7 +2055,7 @@ __device__ inline const char* task_row(const SampleArgs& a, const QTask& t, int 
   int i;
   bool tgt = true;
   if (t.type == kP1) {  // target i = row 2i, draft i = row 2i + 1
-    i = r >> 1;
+    i = (a.p1sub ? t.aux : 0) + (r >> 1);
     tgt = (r & 1) == 0;
   } else if (t.type == kBS) {
     i = a.K;
@@ -2136,7 +2141,9 @@ __global__ void __launch_bounds__(kThreads, 2) verify_sample_kernel(const Sample
               break;
           }
         },
-        [&](const QTask& t) { return is_piece(t) ? a.R : a.S; });
+        [&](const QTask& t) {
+          return is_piece(t) ? a.R : (t.type == kP1 && a.p1sub) ? a.S * a.K : a.S;
+        });
   } else {
     // ------------------------------------------------ consumers
     const int tid = threadIdx.x;
@@ -2208,7 +2215,11 @@ WsLayout sample_layout(int B, int K, int V, int dtype) {
   if (part < 8 * M) part = 8 * M;      // a row's S blocks hold its R = S M piece partials
   // queued tasks per row: BS, SW (S each); FR and FD twice each (zero
   // residual), FA, FB twice, AR up to K times (R = S M each)
-  return ws_layout(B, S, part, ustride, (8 + K) * M, int(sizeof(RowState)));
+  WsLayout w = ws_layout(B, S, part, ustride, (8 + K) * M, int(sizeof(RowState)));
+  // one first-stage task per (slice, position) when that still fits one
+  // task per persistent CTA
+  if (B * S * K <= kTargetTasks / 4) w.kp = K;
+  return w;
 }
 
 }  // namespace
@@ -2234,6 +2245,7 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.R = a.S * a.M;
   a.ws.base = static_cast<uint8_t*>(s.workspace);
   a.ws.L = wl;
+  a.p1sub = wl.kp > 1 ? 1 : 0;
   set_test_knobs(a.ws);
   const double C = 1.4426950408889634073599246810018921 / double(s.temperature);  // log2(e)/T
   a.c = float(C);
