@@ -430,42 +430,50 @@ SWEEP = dict(B=(1, 8, 64, 256, 1024), K=(2, 4, 8), V=(32000, 128256, 151936), T=
 def sweep_cell(torch, sv, B, K, V, T, reps, flush, peak, peak_kind):
     """One cell of the sweep: 3 warm-up launches, then `reps` launches timed with
     CUDA events around each one and a write of `flush` (larger than L2) between
-    them; the median launch with its algorithmic bytes against the peak."""
+    them; the median launch with its algorithmic bytes against the peak. Small
+    batches rotate over several input batches (a single row's draw path, and so
+    its time, depends on its draws)."""
     import numpy as np
-    bt = gen_batch(torch, 7 + B + K, T if T > 0 else 1.0, B=B, K=K, V=V)
+    nb = 8 if B <= 8 else 4 if B <= 64 else 1
+    bts = [gen_batch(torch, 7 + B + K + 1000 * i, T if T > 0 else 1.0, B=B, K=K, V=V)
+           for i in range(nb)]
     out = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
     n = torch.empty((B,), dtype=torch.int32, device="cuda")
     if T > 0:
-        def call():
+        def call(bt):
             sv.spec_verify_sample(bt["target"], bt["draft"], bt["tokens"], bt["uniforms"], T,
                                   out, n)
     else:
-        def call():
+        def call(bt):
             sv.spec_verify_greedy(bt["target"], bt["tokens"], out, n)
-    for _ in range(3):
-        call()
-    torch.cuda.synchronize()
-    na = n.cpu().numpy()
+    nas = []
+    for bt in bts:
+        call(bt)
+        torch.cuda.synchronize()
+        nas.append(n.cpu().numpy().copy())
     ts = []
-    for _ in range(reps):
+    for r in range(reps):
         flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        call()
+        call(bts[r % nb])
         e1.record()
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
     ms = float(np.median(ts))
-    alg = algorithmic_verify_bytes(na, K, V) if T > 0 else greedy_verify_bytes(na, K, V)
+    na = np.concatenate(nas)
+    bpb = (algorithmic_verify_bytes if T > 0 else greedy_verify_bytes)
+    alg = float(np.mean([bpb(x, K, V) for x in nas]))
     gbs = alg / (ms / 1e3) / 1e9
     cell = {"sweep": {"B": B, "K": K, "V": V, "T": T, "mode": "sample" if T > 0 else "greedy"},
             "us": ms * 1e3, "positions_per_s": B * K / (ms / 1e3), "algorithmic_bytes": alg,
             "gbs": gbs, "frac": gbs / peak, "peak_kind": peak_kind,
             "mean_accepted": float(na.mean())}
     if T > 0:
-        cell["sequential_frac"] = sequential_verify_bytes(na, K, V) / (ms / 1e3) / 1e9 / peak
-    del bt
+        seq = float(np.mean([sequential_verify_bytes(x, K, V) for x in nas]))
+        cell["sequential_frac"] = seq / (ms / 1e3) / 1e9 / peak
+    del bts
     torch.cuda.empty_cache()
     return cell
 
@@ -708,7 +716,8 @@ def main():
                          "algorithmic_bytes_per_launch": alg, "avg_launch_ms": v_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (4 if a.mode == "step" else 1) * a.steps,  # verify (+ kv plan, copy, finish)
+            # workspace zeroing + verify (+ kv plan, copy, finish) per step
+            "gpu_launches": (5 if a.mode == "step" else 2) * a.steps,
             "clocks": clk,
             "extra": {"verify_ms": v_ms, "kv_commit_and_table_restore_ms": ms_per_step - v_ms,
                       "kv_commit_inplace_us": (inplace_kv_us(torch, sv, na_list[0][0])

@@ -100,8 +100,10 @@ extern "C" {
 /* ---- per-row diagnostic bits written to row_info[b] (optional) ---- */
 #define SPEC_ROW_ACCEPT_REFINED 1 /* an accept test fell inside the fp32 error bound and was
                                      decided by the double-float path */
-#define SPEC_ROW_SAMPLE_REFINED 2 /* the final draw fell inside the fp32 error bound and was
-                                     decided by the double-float path */
+#define SPEC_ROW_SAMPLE_REFINED 2 /* the final draw fell inside the error bound of its first
+                                     pass (the fp32 sweep; for batches of 4 to 16 rows, a
+                                     residual draw's first pass is the accurate lite pass)
+                                     and was decided by a more accurate one */
 #define SPEC_ROW_UNCERTIFIED 4    /* the double-float path could not certify its decision either
                                      (its result is still returned) */
 #define SPEC_ROW_ZERO_RESIDUAL 8  /* the residual mass was exactly zero; q_j was used */

@@ -20,7 +20,10 @@
 //                    pass"), for every layer and both K and V planes, to
 //                    logical positions L..L+n;
 //   kv_finish_kernel one thread per row: sets the new length and clears the
-//                    provisional entries.
+//                    provisional entries. It starts once every copy CTA has
+//                    read the tables (programmatic dependent launch), runs
+//                    beside the copies and ends by waiting for them, so that
+//                    work after it on the stream sees them.
 // Only the accepted bytes move: 2 * (n + 1) * layers * heads * head_dim * elem
 // bytes read and written per row.
 #include <cuda_runtime.h>
@@ -58,6 +61,20 @@ __device__ __forceinline__ int kept_slot(const KvArgs& a, int b, int s) {
 }
 
 __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// Adds v (ors when `bits`) into a shared word: one atomic per warp (the warp
+// reduces first), not one per thread, which would serialise on the word.
+__device__ __forceinline__ void block_add(int* word, int v, bool bits = false) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const int y = __shfl_xor_sync(0xffffffffu, v, o);
+    v = bits ? (v | y) : (v + y);
+  }
+  if ((threadIdx.x & 31) == 0 && v != 0) {
+    if (bits) atomicOr(word, v);
+    else atomicAdd(word, v);
+  }
+}
 
 // Block-wide exclusive scan of one int per thread (kPlanThreads threads).
 __device__ int block_excl_scan(int v, int* sh, int& total) {
@@ -143,17 +160,21 @@ __global__ void __launch_bounds__(kPlanThreads) kv_plan_kernel(const KvArgs a) {
     s_push = 0;
   }
   __syncthreads();
-  // 1. validation and totals
-  int e = 0, need_sum = 0, push_sum = 0;
+  // 1. validation and totals; with one row per thread (B <= kPlanThreads) the
+  // row's counts stay in registers for the pops and pushes below
+  const bool one = a.B <= kPlanThreads;
+  int e = 0, need_sum = 0, push_sum = 0, my_need = 0, my_np = 0;
   for (int b = tid; b < a.B; b += kPlanThreads) {
     int need, np;
     e |= validate_row(a, b, need, np);
     need_sum += need;
     push_sum += np;
+    my_need = need;
+    my_np = np;
   }
-  atomicOr(&s_err, e);
-  atomicAdd(&s_need, need_sum);
-  atomicAdd(&s_push, push_sum);
+  block_add(&s_err, e, true);
+  block_add(&s_need, need_sum);
+  block_add(&s_push, push_sum);
   __syncthreads();
   const int top = *a.ftop;
   int err = s_err;
@@ -167,7 +188,7 @@ __global__ void __launch_bounds__(kPlanThreads) kv_plan_kernel(const KvArgs a) {
       const int x = a.fs[i];
       if (x < 0 || x >= a.NB) pe = 1;
     }
-    if (pe) atomicOr(&s_err, SPEC_DERR_BAD_BLOCK);
+    block_add(&s_err, pe ? SPEC_DERR_BAD_BLOCK : 0, true);
     __syncthreads();
     err |= s_err;
   }
@@ -179,8 +200,11 @@ __global__ void __launch_bounds__(kPlanThreads) kv_plan_kernel(const KvArgs a) {
   int carry = 0;
   for (int b0 = 0; b0 < a.B; b0 += kPlanThreads) {
     const int b = b0 + tid;
-    int need = 0, np = 0;
-    if (b < a.B) validate_row(a, b, need, np);
+    int need = my_need, np = 0;
+    if (!one) {
+      need = 0;
+      if (b < a.B) validate_row(a, b, need, np);
+    }
     int chunk_total;
     const int pre = block_excl_scan(need, sh, chunk_total) + carry;
     if (b < a.B) {
@@ -196,9 +220,12 @@ __global__ void __launch_bounds__(kPlanThreads) kv_plan_kernel(const KvArgs a) {
   carry = 0;
   for (int b0 = 0; b0 < a.B; b0 += kPlanThreads) {
     const int b = b0 + tid;
-    int np = 0;
-    if (b < a.B)
-      for (int k = 0; k < a.P; ++k) np += a.pb[size_t(b) * a.P + k] >= 0;
+    int np = my_np;
+    if (!one) {
+      np = 0;
+      if (b < a.B)
+        for (int k = 0; k < a.P; ++k) np += a.pb[size_t(b) * a.P + k] >= 0;
+    }
     int chunk_total;
     const int pre = block_excl_scan(np, sh, chunk_total) + carry;
     if (b < a.B) {
@@ -220,7 +247,6 @@ __global__ void __launch_bounds__(kCopyThreads) kv_copy_kernel(const KvArgs a) {
   // one CTA per (row, kept position): every SM takes a share of the slots,
   // whatever the rows' accepted lengths
   const int b = blockIdx.x / (a.K + 1), s = blockIdx.x % (a.K + 1);
-  pdl_trigger();
   pdl_wait();  // the plan
   if (*a.status != 0) return;
   const int n = a.na[b];
@@ -234,6 +260,11 @@ __global__ void __launch_bounds__(kCopyThreads) kv_copy_kernel(const KvArgs a) {
   const int db = a.bt[size_t(b) * a.MB + pos / a.bs];
   const uint8_t* src = a.pool + int64_t(sb) * block_stride + int64_t(x % a.bs) * a.slot_bytes;
   uint8_t* dst = a.pool + int64_t(db) * block_stride + int64_t(pos % a.bs) * a.slot_bytes;
+  // A barrier that takes the read values as operands: every table read of
+  // the CTA has returned before the trigger lets the finish change the
+  // tables. (The plan validated these ids; the test cannot fail.)
+  if (__syncthreads_or(sb < 0 || db < 0 || L < 0 || x < 0)) return;
+  pdl_trigger();
   const int vpu = int(a.slot_bytes / 16);  // 16-byte vectors per (layer, plane)
   const int total = 2 * a.NL * vpu;
   const int64_t plane_stride = int64_t(a.bs) * a.slot_bytes;
@@ -257,14 +288,17 @@ __global__ void __launch_bounds__(kCopyThreads) kv_copy_kernel(const KvArgs a) {
   }
 }
 
-// After every copy: the new lengths and the cleared provisional entries (the
-// copy CTAs read both, so they change only once all have run).
+// The new lengths and the cleared provisional entries (the copy CTAs read
+// both, so they change only once every copy CTA has read them).
 __global__ void __launch_bounds__(256) kv_finish_kernel(const KvArgs a) {
   const int b = blockIdx.x * 256 + threadIdx.x;
-  pdl_wait();  // every copy
-  if (b >= a.B || *a.status != 0) return;
-  a.sl[b] = a.sl[b] + a.na[b] + 1;
-  for (int i = 0; i < a.P; ++i) a.pb[size_t(b) * a.P + i] = -1;
+  // every copy CTA has read the tables (they trigger after their reads); the
+  // plan, which they waited for, is complete
+  if (b < a.B && *a.status == 0) {
+    a.sl[b] = a.sl[b] + a.na[b] + 1;
+    for (int i = 0; i < a.P; ++i) a.pb[size_t(b) * a.P + i] = -1;
+  }
+  pdl_wait();  // every copy: work after this launch on the stream sees them
 }
 
 // ------------------------------------------------------------------ in place
@@ -321,8 +355,8 @@ __global__ void __launch_bounds__(kPlanThreads) kv_truncate_kernel(const TruncAr
     e |= validate_trunc_row(a, b, nl, f, en);
     push_sum += en - f;
   }
-  atomicOr(&s_err, e);
-  atomicAdd(&s_push, push_sum);
+  block_add(&s_err, e, true);
+  block_add(&s_push, push_sum);
   __syncthreads();
   const int top = *a.ftop;
   int err = s_err;

@@ -101,6 +101,12 @@ struct SampleArgs {
   // covers target and draft row i of the slice, so that the first pass
   // spreads over every CTA
   int p1sub;
+  // Small batches (4 to 16 rows): a residual draw starts with FR (the
+  // accurate lite pass) instead of the fp32 sweep, which leaves about a
+  // third of these draws undecided at T = 1, so that some row of the batch
+  // almost surely needs the extra stage; with one to three rows the cheaper
+  // sweep first is faster on average
+  int direct_fr;
   Ws ws;
 };
 
@@ -782,6 +788,8 @@ __device__ void start_draw(const SampleArgs& a, int b, int j, int flags, float K
     __syncwarp();  // orders finish_p1's stores of the row offsets
     Kg = warp_max_f(lane < a.K ? __ldcg(&st->rK[2 * lane]) : -INFINITY);
   }
+  const bool fr = j < a.K && a.direct_fr && fabsf(Kq) <= kLiteMaxOffset &&
+                  fabsf(Kp) <= kLiteMaxOffset;
   if (lane == 0) {
     st->flags = flags;
     if (j < a.K) {
@@ -793,6 +801,19 @@ __device__ void start_draw(const SampleArgs& a, int b, int j, int flags, float K
       st->Kq = Kg;
       st->Rq = 1.0f;  // the raw sweep sums e, not q
     }
+    if (fr) {
+      // FR's sign-test margin as after the sweep (finish_sw), with the sums
+      // q|x| and p|x| bounded by xbar instead of measured
+      const float eps = a.bd.ex2 + a.bd.gamma1 +
+                        2.0f * kLn2f * kU * (1.01f * a.bd.xbar + 0.5f * kQmax) + 4.0f * kU +
+                        float(kLiteExpRelErr);
+      st->amb_delta = 1.05f * 2.0f * eps + 4.0f * kU;
+      st->namb = 0;
+    }
+  }
+  if (fr) {
+    enqueue_rare(a, kFR, b, j | (kModeResidual << 8));
+    return;
   }
   enqueue_row_stage(a.ws, kSW, b, a.S,
                     j < a.K ? (j | (kModeResidual << 8)) : (a.K | (kModeQ << 8) | kRawBit));
@@ -2035,6 +2056,7 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
     return;
   }
   // not settled within FR's bound: one double-float pass of the same kind (FD)
+  if (lane == 0) st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
   enqueue_rare(a, kFD, b, aux & ~kPieceBit);
 }
 
@@ -2246,6 +2268,7 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.ws.base = static_cast<uint8_t*>(s.workspace);
   a.ws.L = wl;
   a.p1sub = wl.kp > 1 ? 1 : 0;
+  a.direct_fr = (s.B >= 4 && s.B <= kSmallBatch) ? 1 : 0;
   set_test_knobs(a.ws);
   const double C = 1.4426950408889634073599246810018921 / double(s.temperature);  // log2(e)/T
   a.c = float(C);
