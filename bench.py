@@ -50,9 +50,15 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--temperature", type=float, default=WORKLOAD["T"])
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--mode", default="step", choices=["step", "verify", "greedy"],
+    p.add_argument("--mode", default="step", choices=["step", "verify", "greedy", "filter"],
                    help="step: verify + KV commit (the benchmark); verify / greedy: that kernel "
-                        "alone on the same logits, no KV pool (small footprint, for profiling)")
+                        "alone on the same logits, no KV pool (small footprint, for profiling); "
+                        "filter: the top-k / top-p thresholds of one batch alone")
+    p.add_argument("--kv-prefix", default=None,
+                   help="LO,HI: committed prefix lengths U[LO, HI] of the KV case (default: the "
+                        "workload's); short prefixes shrink the paged pool (profiling)")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the extra measurements after the timed step (profiling)")
     p.add_argument("--batches", type=int, default=3, help="input batches to rotate over")
     p.add_argument("--sweep", action="store_true",
                    help="time the verify launch over the B x K x V x T grid (one JSON line per cell)")
@@ -66,12 +72,13 @@ def dist_env():
     return rank, world, local
 
 
-def workload_name(T):
+def workload_name(T, prefix=None):
     w = WORKLOAD
+    lo, hi = prefix or (w["prefix_lo"], w["prefix_hi"])
     return (f"sampling verify + paged-KV commit: B={w['B']}, K={w['K']}, V={w['V']} bf16 logits, "
             f"T={T}, draft = target + N(0, {w['sigma']}^2), target ~ N(0, {w['target_std']}^2); "
             f"KV {w['kv_layers']}L x {w['kv_heads']}H x {w['head_dim']}D bf16, block "
-            f"{w['block_size']}, prefix U[{w['prefix_lo']}, {w['prefix_hi']}]")
+            f"{w['block_size']}, prefix U[{lo}, {hi}]")
 
 
 # ------------------------------------------------------------------ inputs
@@ -95,12 +102,13 @@ def gen_batch(torch, seed, T, B=None, K=None, V=None):
     return dict(target=zt.contiguous(), draft=zd.contiguous(), tokens=tok.contiguous(), uniforms=u)
 
 
-def kv_state(torch, na):
+def kv_state(torch, na, prefix=None):
     import numpy as np
     import synth
     w = WORKLOAD
-    c = synth.kv_case(w["B"], w["K"], block_size=w["block_size"], prefix_lo=w["prefix_lo"],
-                      prefix_hi=w["prefix_hi"], num_accepted=na, seed=44)
+    lo, hi = prefix or (w["prefix_lo"], w["prefix_hi"])
+    c = synth.kv_case(w["B"], w["K"], block_size=w["block_size"], prefix_lo=lo,
+                      prefix_hi=hi, num_accepted=na, seed=44)
     # the tables a commit changes live in one buffer, restored by one copy per step
     host = dict(bt=c.block_table, sl=c.seq_lens, pb=c.prov_blocks, fs=c.free_stack,
                 ft=[c.free_top])
@@ -577,6 +585,12 @@ def main():
     stream = torch.cuda.current_stream()
     nb = max(1, a.batches)
     batches = [gen_batch(torch, 1000 * rank + i, T) for i in range(nb)]
+    if a.mode == "filter":
+        if rank == 0:
+            r = filter_stats(torch, sv, batches[0], T, peaks()[0], reps=max(1, a.steps))
+            print(json.dumps({"mode": "filter", "config": {"workload": workload_name(T)}, **r}))
+        return
+    prefix = tuple(int(x) for x in a.kv_prefix.split(",")) if a.kv_prefix else None
     out = torch.empty((B, K + 1), dtype=torch.int32, device="cuda")
     n = torch.empty((B,), dtype=torch.int32, device="cuda")
     info = torch.empty((B,), dtype=torch.int32, device="cuda")
@@ -588,7 +602,7 @@ def main():
         torch.cuda.synchronize()
         na_list.append((n.cpu().numpy().copy(), info.cpu().numpy().copy()))
     if a.mode == "step":
-        kc, kd, saved, pool = kv_state(torch, np.max([x[0] for x in na_list], axis=0))
+        kc, kd, saved, pool = kv_state(torch, np.max([x[0] for x in na_list], axis=0), prefix)
 
     def step(i, ev=None):
         bt = batches[i % nb]
@@ -703,7 +717,8 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
             "warmup": max(3, a.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": workload_name(T), "global_batch": world * B, "B_per_gpu": B,
+            "config": {"workload": workload_name(T, prefix), "global_batch": world * B,
+                       "B_per_gpu": B,
                        "K": K, "V": V, "logits_dtype": "bf16", "temperature": T,
                        "parallelism": f"replicas x{world} (batch rows sharded, no collective)",
                        "mode": a.mode,
@@ -720,16 +735,7 @@ def main():
             "gpu_launches": (5 if a.mode == "step" else 2) * a.steps,
             "clocks": clk,
             "extra": {"verify_ms": v_ms, "kv_commit_and_table_restore_ms": ms_per_step - v_ms,
-                      "kv_commit_inplace_us": (inplace_kv_us(torch, sv, na_list[0][0])
-                                               if a.mode == "step" else None),
-                      "tree_greedy": (tree_greedy_stats(torch, sv, peak)
-                                      if a.mode == "step" else None),
-                      "top_k_top_p": (filter_stats(torch, sv, batches[0], T, peak)
-                                      if a.mode == "step" else None),
-                      "greedy": (greedy_stats(torch, sv, batches, peak)
-                                 if a.mode == "step" else None),
-                      "sweep_small": (sweep_small(torch, sv, peak, peak_kind)
-                                      if a.mode == "step" else None),
+                      **extras(a, torch, sv, batches, na_list, T, peak, peak_kind),
                       "kv_bytes_per_step": kvb, "refined_row_fraction": refined,
                       "mean_accepted": float(np.mean([x[0].mean() for x in na_list])),
                       "hbm_frac_of_nominal_8TBs": achieved / 8000.0,
@@ -740,6 +746,17 @@ def main():
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def extras(a, torch, sv, batches, na_list, T, peak, peak_kind):
+    """The extra measurements after the timed step (step mode)."""
+    if a.mode != "step" or a.no_extras:
+        return {}
+    return {"kv_commit_inplace_us": inplace_kv_us(torch, sv, na_list[0][0]),
+            "tree_greedy": tree_greedy_stats(torch, sv, peak),
+            "top_k_top_p": filter_stats(torch, sv, batches[0], T, peak),
+            "greedy": greedy_stats(torch, sv, batches, peak),
+            "sweep_small": sweep_small(torch, sv, peak, peak_kind)}
 
 
 def max_over_ranks(x, device=None):
