@@ -2055,8 +2055,12 @@ __device__ void finish_fr(const SampleArgs& a, const Smem& L, int b, int aux) {
     write_outputs(a, b, dr.j, token, fl, token < 0, d);
     return;
   }
-  // not settled within FR's bound: one double-float pass of the same kind (FD)
-  if (lane == 0) st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
+  // not settled within FR's bound: one double-float pass of the same kind
+  // (FD), which rebuilds the list of undecided tokens from its own values
+  if (lane == 0) {
+    st->flags = flags | SPEC_ROW_SAMPLE_REFINED;
+    st->namb = 0;
+  }
   enqueue_rare(a, kFD, b, aux & ~kPieceBit);
 }
 
