@@ -273,7 +273,13 @@ size_t spec_verify_greedy_noalloc_max_bytes(void);
  * spec_verify_workspace_bytes - size of the device workspace that
  * spec_verify_sample and spec_verify_greedy need for (B, K, V, dtype), and
  * spec_verify_tree_greedy for K = N; 0 for arguments those calls would reject.
- * One workspace serves all three calls.
+ * One workspace serves all three calls. The size follows the work split, which
+ * depends on B (batches of at most 16 rows split each row finer) and on the
+ * test knob SPECVERIFY_SMALL_BATCH=0 or 1 (read from the environment here and
+ * at every verify launch; it forces the small-batch split, per-position
+ * first-stage tasks and residual draws starting at the refinement pass off or
+ * on whatever B is, so that tests run both dispatches; the results are the
+ * same either way). Query the size under the same setting as the launch.
  */
 size_t spec_verify_workspace_bytes(int B, int K, int V, int dtype);
 

@@ -45,10 +45,16 @@ constexpr int kMaxSlices = 64;
 constexpr int kTargetTasks = 1216;  // four per CTA of a 152-SM GB300 at two CTAs per SM
 constexpr int kSmallBatch = 16;
 
-__host__ __device__ inline int slices_for(int nvec, int B) {
+// Small-batch dispatch: knob -1 decides by the batch size (B <= kSmallBatch);
+// 0 or 1 force it off or on (see small_batch_knob).
+__host__ __device__ inline bool small_batch(int B, int knob) {
+  return knob < 0 ? B <= kSmallBatch : knob != 0;
+}
+
+__host__ __device__ inline int slices_for(int nvec, int B, bool small) {
   const int per = 4 * (kChunk / 16);
   int s = (nvec + per - 1) / per;
-  int par = B <= kSmallBatch ? kTargetTasks / 4 / B : (kTargetTasks + B - 1) / B;
+  int par = small ? kTargetTasks / 4 / B : (kTargetTasks + B - 1) / B;
   const int cap = nvec / 64 > 1 ? nvec / 64 : 1;
   if (par > cap) par = cap;
   if (s < par) s = par;
@@ -158,6 +164,20 @@ __host__ inline void set_test_knobs(Ws& ws) {
     const long long v = std::strtoll(e, nullptr, 10);
     if (v > 0 && uint64_t(v) < kWaitNs) ws.idle_ns = uint64_t(v);
   }
+}
+
+// Dispatch test knob, read from the environment by every layout and launch:
+// SPECVERIFY_SMALL_BATCH=0 or 1 forces the small-batch choices (slicing,
+// per-position first-stage tasks, the residual draw starting at the lite
+// refinement pass) off or on whatever the batch size, so that the parity
+// tests run both dispatches on the same inputs. Unset (or any other value):
+// decided by the batch size.
+__host__ inline int small_batch_knob() {
+  if (const char* e = std::getenv("SPECVERIFY_SMALL_BATCH")) {
+    if (e[0] == '0' && e[1] == 0) return 0;
+    if (e[0] == '1' && e[1] == 0) return 1;
+  }
+  return -1;
 }
 
 // ------------------------------------------------------------------ memory helpers

@@ -2232,7 +2232,8 @@ int pieces_per_slice(int nvec, int S) {
 WsLayout sample_layout(int B, int K, int V, int dtype) {
   const int kvec = (dtype == SPEC_BF16) ? 8 : 4;
   const int nvec = V / kvec;
-  const int S = slices_for(nvec, B);
+  const bool small = small_batch(B, small_batch_knob());
+  const int S = slices_for(nvec, B, small);
   const int M = pieces_per_slice(nvec, S);
   const int maxslice = (nvec + S - 1) / S;
   // unit slots (float2) per slice: FR keeps two pairs per unit (float4)
@@ -2242,9 +2243,9 @@ WsLayout sample_layout(int B, int K, int V, int dtype) {
   // queued tasks per row: BS, SW (S each); FR and FD twice each (zero
   // residual), FA, FB twice, AR up to K times (R = S M each)
   WsLayout w = ws_layout(B, S, part, ustride, (8 + K) * M, int(sizeof(RowState)));
-  // one first-stage task per (slice, position) when that still fits one
-  // task per persistent CTA
-  if (B * S * K <= kTargetTasks / 4) w.kp = K;
+  // small batches: one first-stage task per (slice, position) when that
+  // still fits one task per persistent CTA
+  if (small && B * S * K <= kTargetTasks / 4) w.kp = K;
   return w;
 }
 
@@ -2272,7 +2273,8 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.ws.base = static_cast<uint8_t*>(s.workspace);
   a.ws.L = wl;
   a.p1sub = wl.kp > 1 ? 1 : 0;
-  a.direct_fr = (s.B >= 4 && s.B <= kSmallBatch) ? 1 : 0;
+  const int knob = small_batch_knob();
+  a.direct_fr = knob >= 0 ? knob : (s.B >= 4 && s.B <= kSmallBatch) ? 1 : 0;
   set_test_knobs(a.ws);
   const double C = 1.4426950408889634073599246810018921 / double(s.temperature);  // log2(e)/T
   a.c = float(C);
