@@ -64,3 +64,34 @@ def test_greedy_both_dispatches(sv, monkeypatch, B, K):
         assert g["err"] == 0, knob
         assert np.array_equal(g["num_accepted"], o["num_accepted"]), knob
         assert np.array_equal(g["out_tokens"], o["out_tokens"]), knob
+
+
+@pytest.mark.parametrize("B,K,V,T,k,p", [(1, 4, 4096, 1.0, 50, 0.9), (8, 4, 4096, 0.7, 20, 1.0),
+                                         (8, 4, 32000, 1.0, 0, 0.8)])
+def test_filtered_both_dispatches(sv, monkeypatch, B, K, V, T, k, p):
+    """Top-k / top-p thresholds (tokens below a row's threshold are -inf in
+    every stage) on small batches, whose first stage runs per position (B = 1)
+    and whose residual draws start at the refinement pass (B = 8)."""
+    import torch
+    c = synth.sampling_case(B, K, V, temperature=T, target_std=3.0, draft_noise_std=0.8,
+                            seed=900 + 10 * B + k)
+    dev = gh.dev_case(c)
+    tt = torch.empty((B, K + 1), dtype=torch.float32, device="cuda")
+    td = torch.empty((B, K), dtype=torch.float32, device="cuda")
+    sv.spec_filter_thresholds(dev["target"], T, k, p, tt)
+    sv.spec_filter_thresholds(dev["draft"], T, k, p, td)
+    torch.cuda.synchronize()
+    pf = float(np.float32(p))
+    zt = c.target_values().astype(np.float64)
+    zd = c.draft_values().astype(np.float64)
+    ot, od = oracle.filter_thresholds(zt, T, k, pf), oracle.filter_thresholds(zd, T, k, pf)
+    assert np.array_equal(tt.cpu().numpy(), ot) and np.array_equal(td.cpu().numpy(), od)
+    o = oracle.verify_sample(oracle.apply_threshold(zt, ot), oracle.apply_threshold(zd, od),
+                             c.tokens, c.uniforms, T)
+    res = _runs(sv, monkeypatch,
+                lambda: gh.run_sample(sv, c, dev, target_threshold=tt, draft_threshold=td))
+    for knob, g in res.items():
+        assert g["err"] == 0, knob
+        gh.assert_sample_parity(g, o, label=f"filtered B={B} k={k} p={p} knob={knob}")
+    for knob in ("0", "1"):
+        assert np.array_equal(res[knob]["out_tokens"], res[None]["out_tokens"]), knob
