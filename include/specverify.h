@@ -255,7 +255,7 @@ int spec_filter_thresholds(const void* logits, int R, int V, int dtype, float te
  *   Arguments, outputs and errors: as spec_verify_greedy, without workspace.
  *   Returns SPEC_ENOTSUP when the step needs more scratch than the built-in
  *   array holds (spec_verify_workspace_bytes(B, K, V, dtype) > 4 MiB; e.g.
- *   B = 256, K = 4, V = 151936 bf16 needs about 3.1 MiB; B = 1024 steps with
+ *   B = 256, K = 4, V = 151936 bf16 needs about 3.0 MiB; B = 1024 steps with
  *   V >= 128256 need 9.8 to 12.4 MiB and are refused), SPEC_ECUDA when the
  *   array's address cannot be obtained.
  *   The scratch's counters and queue are cleared on `stream` at every call.

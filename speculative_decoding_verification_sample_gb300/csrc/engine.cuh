@@ -33,16 +33,19 @@ namespace sv {
 
 // ------------------------------------------------------------------ slicing
 // Vocabulary slices per batch row. Enough first-stage tasks that every
-// persistent CTA gets about four (kTargetTasks), and row slices of at most
-// four ring stages; otherwise as few as possible, since every task and every
-// row slice costs fixed work (a fetch, a hand-off, an arrival, per-row warp
-// reductions). Small batches (B <= kSmallBatch) take one task per CTA
-// instead: their streaming is short next to the latency of the stages after
-// it, and one wave lets every row reach those stages at the same time.
-// Slices keep at least 64 vectors; at most kMaxSlices (two warp-wide scans
-// in the draw).
+// persistent CTA gets a few (`target` tasks per launch: about two per CTA for
+// the sampling kernel, four for the greedy one, each measured best on its
+// own stage mix), and row slices of at most four ring stages; otherwise as
+// few as possible, since every task and every row slice costs fixed work (a
+// fetch, a hand-off, an arrival, per-row warp reductions). Small batches
+// (B <= kSmallBatch) take one task per CTA instead (kOneWave): their
+// streaming is short next to the latency of the stages after it, and one
+// wave lets every row reach those stages at the same time. Slices keep at
+// least 64 vectors; at most kMaxSlices (two warp-wide scans in the draw).
 constexpr int kMaxSlices = 64;
-constexpr int kTargetTasks = 1216;  // four per CTA of a 152-SM GB300 at two CTAs per SM
+constexpr int kOneWave = 304;             // persistent CTAs of a 152-SM GB300 at two per SM
+constexpr int kSampleTasks = 2 * kOneWave;
+constexpr int kGreedyTasks = 4 * kOneWave;
 constexpr int kSmallBatch = 16;
 
 // Small-batch dispatch: knob -1 decides by the batch size (B <= kSmallBatch);
@@ -51,10 +54,10 @@ __host__ __device__ inline bool small_batch(int B, int knob) {
   return knob < 0 ? B <= kSmallBatch : knob != 0;
 }
 
-__host__ __device__ inline int slices_for(int nvec, int B, bool small) {
+__host__ __device__ inline int slices_for(int nvec, int B, bool small, int target) {
   const int per = 4 * (kChunk / 16);
   int s = (nvec + per - 1) / per;
-  int par = small ? kTargetTasks / 4 / B : (kTargetTasks + B - 1) / B;
+  int par = small ? kOneWave / B : (target + B - 1) / B;
   const int cap = nvec / 64 > 1 ? nvec / 64 : 1;
   if (par > cap) par = cap;
   if (s < par) s = par;

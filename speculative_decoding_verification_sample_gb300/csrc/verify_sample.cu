@@ -2233,7 +2233,7 @@ WsLayout sample_layout(int B, int K, int V, int dtype) {
   const int kvec = (dtype == SPEC_BF16) ? 8 : 4;
   const int nvec = V / kvec;
   const bool small = small_batch(B, small_batch_knob());
-  const int S = slices_for(nvec, B, small);
+  const int S = slices_for(nvec, B, small, kSampleTasks);
   const int M = pieces_per_slice(nvec, S);
   const int maxslice = (nvec + S - 1) / S;
   // unit slots (float2) per slice: FR keeps two pairs per unit (float4)
@@ -2245,7 +2245,7 @@ WsLayout sample_layout(int B, int K, int V, int dtype) {
   WsLayout w = ws_layout(B, S, part, ustride, (8 + K) * M, int(sizeof(RowState)));
   // small batches: one first-stage task per (slice, position) when that
   // still fits one task per persistent CTA
-  if (small && B * S * K <= kTargetTasks / 4) w.kp = K;
+  if (small && B * S * K <= kOneWave) w.kp = K;
   return w;
 }
 
