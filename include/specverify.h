@@ -101,7 +101,7 @@ extern "C" {
 #define SPEC_ROW_ACCEPT_REFINED 1 /* an accept test fell inside the fp32 error bound and was
                                      decided by the double-float path */
 #define SPEC_ROW_SAMPLE_REFINED 2 /* the final draw fell inside the error bound of its first
-                                     pass (the fp32 sweep; for batches of 4 to 16 rows, a
+                                     pass (the fp32 sweep; for batches of 4 to 48 rows, a
                                      residual draw's first pass is the accurate lite pass)
                                      and was decided by a more accurate one */
 #define SPEC_ROW_UNCERTIFIED 4    /* the double-float path could not certify its decision either
@@ -274,7 +274,8 @@ size_t spec_verify_greedy_noalloc_max_bytes(void);
  * spec_verify_sample and spec_verify_greedy need for (B, K, V, dtype), and
  * spec_verify_tree_greedy for K = N; 0 for arguments those calls would reject.
  * One workspace serves all three calls. The size follows the work split, which
- * depends on B (batches of at most 16 rows split each row finer) and on the
+ * depends on B (batches of at most 48 rows for sampling, 16 for greedy, split
+ * each row finer) and on the
  * test knob SPECVERIFY_SMALL_BATCH=0 or 1 (read from the environment here and
  * at every verify launch; it forces the small-batch split, per-position
  * first-stage tasks and residual draws starting at the refinement pass off or

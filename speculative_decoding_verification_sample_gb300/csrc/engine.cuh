@@ -38,20 +38,23 @@ namespace sv {
 // own stage mix), and row slices of at most four ring stages; otherwise as
 // few as possible, since every task and every row slice costs fixed work (a
 // fetch, a hand-off, an arrival, per-row warp reductions). Small batches
-// (B <= kSmallBatch) take one task per CTA instead (kOneWave): their
-// streaming is short next to the latency of the stages after it, and one
-// wave lets every row reach those stages at the same time. Slices keep at
-// least 64 vectors; at most kMaxSlices (two warp-wide scans in the draw).
+// (up to kSampleSmallBatch rows for the sampling kernel, kGreedySmallBatch
+// for the greedy one, each measured) take one task per CTA instead
+// (kOneWave): their streaming is short next to the latency of the stages
+// after it, and one wave lets every row reach those stages at the same time.
+// Slices keep at least 64 vectors; at most kMaxSlices (two warp-wide scans
+// in the draw).
 constexpr int kMaxSlices = 64;
 constexpr int kOneWave = 304;             // persistent CTAs of a 152-SM GB300 at two per SM
 constexpr int kSampleTasks = 2 * kOneWave;
 constexpr int kGreedyTasks = 4 * kOneWave;
-constexpr int kSmallBatch = 16;
+constexpr int kSampleSmallBatch = 48;
+constexpr int kGreedySmallBatch = 16;
 
-// Small-batch dispatch: knob -1 decides by the batch size (B <= kSmallBatch);
-// 0 or 1 force it off or on (see small_batch_knob).
-__host__ __device__ inline bool small_batch(int B, int knob) {
-  return knob < 0 ? B <= kSmallBatch : knob != 0;
+// Small-batch dispatch: knob -1 decides by the batch size (B <= limit); 0 or
+// 1 force it off or on (see small_batch_knob).
+__host__ __device__ inline bool small_batch(int B, int knob, int limit) {
+  return knob < 0 ? B <= limit : knob != 0;
 }
 
 __host__ __device__ inline int slices_for(int nvec, int B, bool small, int target) {

@@ -455,7 +455,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_greedy_kernel(const Greedy
 WsLayout greedy_layout(int B, int K, int V, int dtype) {
   const int kvec = (dtype == SPEC_BF16) ? 8 : 4;
   const int nvec = V / kvec;
-  return ws_layout(B, slices_for(nvec, B, small_batch(B, small_batch_knob()), kGreedyTasks),
+  return ws_layout(B, slices_for(nvec, B, small_batch(B, small_batch_knob(), kGreedySmallBatch),
+                                         kGreedyTasks),
                    2 * K + 2, 1, 2, 16);
 }
 

@@ -101,7 +101,7 @@ struct SampleArgs {
   // covers target and draft row i of the slice, so that the first pass
   // spreads over every CTA
   int p1sub;
-  // Small batches (4 to 16 rows): a residual draw starts with FR (the
+  // Small batches (4 to 48 rows): a residual draw starts with FR (the
   // accurate lite pass) instead of the fp32 sweep, which leaves about a
   // third of these draws undecided at T = 1, so that some row of the batch
   // almost surely needs the extra stage; with one to three rows the cheaper
@@ -2232,7 +2232,7 @@ int pieces_per_slice(int nvec, int S) {
 WsLayout sample_layout(int B, int K, int V, int dtype) {
   const int kvec = (dtype == SPEC_BF16) ? 8 : 4;
   const int nvec = V / kvec;
-  const bool small = small_batch(B, small_batch_knob());
+  const bool small = small_batch(B, small_batch_knob(), kSampleSmallBatch);
   const int S = slices_for(nvec, B, small, kSampleTasks);
   const int M = pieces_per_slice(nvec, S);
   const int maxslice = (nvec + S - 1) / S;
@@ -2274,7 +2274,7 @@ int launch_verify_sample(const SampleLaunch& s) {
   a.ws.L = wl;
   a.p1sub = wl.kp > 1 ? 1 : 0;
   const int knob = small_batch_knob();
-  a.direct_fr = knob >= 0 ? knob : (s.B >= 4 && s.B <= kSmallBatch) ? 1 : 0;
+  a.direct_fr = knob >= 0 ? knob : (s.B >= 4 && s.B <= kSampleSmallBatch) ? 1 : 0;
   set_test_knobs(a.ws);
   const double C = 1.4426950408889634073599246810018921 / double(s.temperature);  // log2(e)/T
   a.c = float(C);

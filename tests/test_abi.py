@@ -47,15 +47,16 @@ def test_binding_refuses_cpu_tensors():
 def test_small_batch_knob_changes_the_split(monkeypatch):
     """SPECVERIFY_SMALL_BATCH (host logic, no GPU needed): the workspace size
     follows the work split, so forcing the small-batch dispatch off for B = 8
-    (38 slices a row by default, 64 without) or on for B = 24 (51 slices a row
-    by default, 12 with) changes it; any value but 0 or 1 leaves the default."""
+    (38 slices a row by default, 64 without) or on for B = 64 (10 and 19
+    slices a row by default for sampling and greedy, 4 with) changes it; any
+    value but 0 or 1 leaves the default."""
     import speculative_decoding_verification_sample_gb300 as sv
     ws = lambda B: sv.spec_verify_workspace_bytes(B, 4, 151936, sv.SPEC_BF16)  # noqa: E731
     monkeypatch.delenv("SPECVERIFY_SMALL_BATCH", raising=False)
-    d8, d24 = ws(8), ws(24)
+    d8, d64 = ws(8), ws(64)
     monkeypatch.setenv("SPECVERIFY_SMALL_BATCH", "0")
-    assert ws(8) > d8 and ws(24) == d24
+    assert ws(8) > d8 and ws(64) == d64
     monkeypatch.setenv("SPECVERIFY_SMALL_BATCH", "1")
-    assert ws(8) == d8 and ws(24) < d24
+    assert ws(8) == d8 and ws(64) < d64
     monkeypatch.setenv("SPECVERIFY_SMALL_BATCH", "2")
-    assert ws(8) == d8 and ws(24) == d24
+    assert ws(8) == d8 and ws(64) == d64

@@ -1,9 +1,9 @@
 """The small-batch dispatch forced both ways (-m gpu).
 
-Batches of at most 16 rows take a different work split (one first-stage task
-per persistent CTA, per-position first-stage tasks for one row) and, from 4
-rows, start residual draws with the accurate refinement pass instead of the
-fp32 sweep. The test knob SPECVERIFY_SMALL_BATCH forces those choices off (0)
+Sampling batches of at most 48 rows (greedy: 16) take a different work
+split (one first-stage task per persistent CTA, per-position first-stage
+tasks for one row) and, from 4 rows, start residual draws with the accurate
+refinement pass instead of the fp32 sweep. The test knob SPECVERIFY_SMALL_BATCH forces those choices off (0)
 or on (1) whatever the batch size. Every case here runs three times on the
 same inputs (default, off, on): each run must match the oracle, and the three
 runs must agree exactly, since every decision is certified (a row flagged
@@ -38,7 +38,8 @@ def _runs(sv, monkeypatch, run):
 
 @pytest.mark.parametrize("B,K,V,T", [(1, 4, 32000, 1.0), (3, 4, 32000, 1.0), (8, 4, 32000, 1.0),
                                      (8, 8, 151936, 0.6), (24, 4, 32000, 1.0),
-                                     (16, 2, 151936, 1.0)])
+                                     (16, 2, 151936, 1.0), (40, 4, 32000, 1.0),
+                                     (64, 4, 32000, 0.6)])
 def test_sampling_both_dispatches(sv, monkeypatch, B, K, V, T):
     c = synth.sampling_case(B, K, V, temperature=T, target_std=3.0, draft_noise_std=0.5,
                             seed=700 + 10 * B + K)
