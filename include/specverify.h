@@ -274,7 +274,7 @@ size_t spec_verify_greedy_noalloc_max_bytes(void);
  * spec_verify_sample and spec_verify_greedy need for (B, K, V, dtype), and
  * spec_verify_tree_greedy for K = N; 0 for arguments those calls would reject.
  * One workspace serves all three calls. The size follows the work split, which
- * depends on B (batches of at most 48 rows for sampling, 16 for greedy, split
+ * depends on B (batches of at most 48 rows for sampling, 64 for greedy, split
  * each row finer) and on the
  * test knob SPECVERIFY_SMALL_BATCH=0 or 1 (read from the environment here and
  * at every verify launch; it forces the small-batch split, per-position

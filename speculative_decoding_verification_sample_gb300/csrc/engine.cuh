@@ -49,7 +49,7 @@ constexpr int kOneWave = 304;             // persistent CTAs of a 152-SM GB300 a
 constexpr int kSampleTasks = 2 * kOneWave;
 constexpr int kGreedyTasks = 4 * kOneWave;
 constexpr int kSampleSmallBatch = 48;
-constexpr int kGreedySmallBatch = 16;
+constexpr int kGreedySmallBatch = 64;
 
 // Small-batch dispatch: knob -1 decides by the batch size (B <= limit); 0 or
 // 1 force it off or on (see small_batch_knob).

@@ -1,6 +1,6 @@
 """The small-batch dispatch forced both ways (-m gpu).
 
-Sampling batches of at most 48 rows (greedy: 16) take a different work
+Sampling batches of at most 48 rows (greedy: 64) take a different work
 split (one first-stage task per persistent CTA, per-position first-stage
 tasks for one row) and, from 4 rows, start residual draws with the accurate
 refinement pass instead of the fp32 sweep. The test knob SPECVERIFY_SMALL_BATCH forces those choices off (0)
@@ -55,7 +55,7 @@ def test_sampling_both_dispatches(sv, monkeypatch, B, K, V, T):
         assert np.array_equal(res[knob]["num_accepted"], res[None]["num_accepted"]), knob
 
 
-@pytest.mark.parametrize("B,K", [(1, 4), (8, 4), (24, 2)])
+@pytest.mark.parametrize("B,K", [(1, 4), (8, 4), (24, 2), (48, 4), (96, 4)])
 def test_greedy_both_dispatches(sv, monkeypatch, B, K):
     c = synth.greedy_case(B, K, 151936, alpha=0.8, seed=800 + 10 * B + K)
     o = oracle.verify_greedy(c.target_values(), c.tokens)
