@@ -38,3 +38,18 @@ def test_greedy_and_kv_bytes():
 
 def test_job_rate_counts_every_rank():
     assert bench.job_rate(4, 256, 4, 0.5) == 4 * bench.job_rate(1, 256, 4, 0.5)
+
+
+def test_profiling_options(monkeypatch):
+    """The small-footprint options the committed ncu summaries were taken with:
+    short KV prefixes are named in the workload string, and the filter-only
+    mode and the no-extras switch parse."""
+    import sys
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--kv-prefix", "16,64", "--no-extras", "--steps", "3"])
+    a = bench.parse()
+    assert a.kv_prefix == "16,64" and a.no_extras and a.mode == "step"
+    assert "prefix U[16, 64]" in bench.workload_name(1.0, (16, 64))
+    assert "prefix U[512, 4096]" in bench.workload_name(1.0)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--mode", "filter"])
+    assert bench.parse().mode == "filter"
+
