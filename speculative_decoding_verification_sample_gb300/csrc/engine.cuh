@@ -511,11 +511,11 @@ __device__ __forceinline__ void handoff_post(const Handoff& h, uint32_t n) {
 // The finisher warp's loop. It takes the finished tasks in order, in batches
 // of those already complete: per batch it combines each task's per-warp
 // partials into the task's slice partials (`combine(t, slot)`, plain stores),
-// issues one fence, frees the slots, arrives on every task's row counter
-// (lanes in parallel, one atomicAdd each), and then runs the continuation
-// (`cont(t)`) of every row whose stage that arrival completed (`expect(t)`:
-// the number of tasks of t's stage). One memory round trip per batch instead
-// of two per task.
+// frees the slots, arrives on every task's row counter (lanes in parallel,
+// one acq_rel atomic add each, which publishes the partials without a
+// separate fence), and then runs the continuation (`cont(t)`) of every row
+// whose stage that arrival completed (`expect(t)`: the number of tasks of t's
+// stage). One memory round trip per batch.
 template <class Combine, class Continue, class Expect>
 __device__ inline void finisher_loop(const Ws& ws, const Handoff& ho, volatile int* abort,
                                      Combine&& combine, Continue&& cont, Expect&& expect) {

@@ -12,8 +12,8 @@
 // concurrent callers to race on. Nothing is allocated: no cudaMalloc, no
 // cudaFree, no library routine that allocates. Of the scratch, the header,
 // row counters and work queue must start at zero for every launch;
-// spec_verify_greedy clears them itself with cudaMemsetAsync on the caller's
-// stream, so no state carries over between calls.
+// spec_verify_greedy clears them itself with a small zeroing kernel on the
+// caller's stream, so no state carries over between calls.
 //
 // All calls on one device share the one scratch: two calls whose launches
 // can overlap on the device (different streams without ordering, several

@@ -102,10 +102,10 @@ struct SampleArgs {
   // spreads over every CTA
   int p1sub;
   // Small batches (4 to 48 rows): a residual draw starts with FR (the
-  // accurate lite pass) instead of the fp32 sweep, which leaves about a
-  // third of these draws undecided at T = 1, so that some row of the batch
-  // almost surely needs the extra stage; with one to three rows the cheaper
-  // sweep first is faster on average
+  // accurate lite pass) instead of the fp32 sweep, which leaves nearly half
+  // of these draws undecided at T = 1, so that some row of the batch almost
+  // surely needs the extra stage; with one to three rows the cheaper sweep
+  // first is faster on average
   int direct_fr;
   Ws ws;
 };
