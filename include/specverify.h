@@ -147,8 +147,11 @@ extern "C" {
  * u[i] < min(1, q_i(d_i)/p_i(d_i)); at the first rejection j the token is the
  * smallest v with u[K] * sum(r) < sum_{w<=v} r_w for r = max(0, q_j - p_j) (r = q_j if
  * that sum is 0); if all K are accepted the same draw is made from q_K. Every
- * decision is certified against a proven error bound of the fp32 arithmetic; the
- * rare decisions inside the bound are recomputed in double-float arithmetic.
+ * decision is certified against a proven error bound of the arithmetic that took
+ * it: the fp32 first pass, then for the decisions inside its bound a pass in pair
+ * (double-float) arithmetic with a lighter exponential (relative error < 1e-9),
+ * then, for what that leaves undecided, the full double-float pass (< 4e-13).
+ * Batches of 4 to 48 rows start residual draws at the pair-arithmetic pass.
  * Logit arrays must be 16-byte aligned and V * sizeof(dtype) a multiple of 16.
  * workspace / workspace_bytes: see the conventions above (SPEC_EINVAL if too small).
  */
